@@ -1,0 +1,488 @@
+#!/usr/bin/env python3
+"""Benchmark of the tensor/sequence-parallel MLP block on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--config NAME] [--mode fused|partials]
+
+One step = forward + backward of the block (every hot-path kernel: dim-0
+all-gather of X, fc1 + GeLU/SwiGLU, fc2 + shard sum / reduce-scatter, dZ
+all-gather and X re-gather, fc2 input gradient + act', both weight gradients,
+fc1 input gradient + reduce-scatter) through the C ABI on one synthetic batch.
+Default workload: the 22B-width TP+SP MLP, [s,b,h] = [4096,1,6144], f = 24576,
+tp = 8 logical shards, SP on, bf16.  Prints ONE JSON line (rank 0).
+
+With --gpus N > 1 (launched by torch.distributed.run) every rank runs an
+independent replica of the block on its own GPU (the tensor shards are logical
+partitions inside one GPU, so there is no cross-GPU exchange): weak scaling,
+value = all ranks' FLOPs / max-over-ranks time.
+
+--impl reference times the CPU oracle (NumPy fp64) on a bounded token sample of
+the same workload, on the host cores, with the same metric and unit.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "TP/SP MLP fwd+bwd TFLOP/s on 1 GB300 and % of dense BF16 peak"
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="w22b_tpsp8_bf16")
+    ap.add_argument("--mode", choices=["fused", "partials"], default="fused")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args(argv)
+
+
+# ---------------------------------------------------------------- helpers
+
+
+def workload_desc(cfg) -> dict:
+    names = {
+        "tiny_tp2_f32": "tiny TP MLP",
+        "tpsp4_bf16": "TP+SP MLP",
+        "w8p3b_tp8_f16": "8.3B-width TP MLP",
+        "w22b_tpsp8_bf16": "22B-width TP+SP MLP",
+        "llama70b_swiglu_tpsp8_bf16": "Llama-70B-like SwiGLU TP+SP MLP",
+    }
+    return {
+        "workload": f"{names.get(cfg.name, cfg.name)} [s,b,h]=[{cfg.s},{cfg.b},{cfg.h}] "
+                    f"{'F' if cfg.act == 'swiglu' else 'f'}={cfg.f} tp={cfg.tp} SP {'on' if cfg.sp else 'off'} "
+                    f"{cfg.dtype} {cfg.act}, fwd+bwd",
+        "name": cfg.name,
+        "s": cfg.s, "b": cfg.b, "h": cfg.h, "f": cfg.f, "tp": cfg.tp, "sp": cfg.sp, "act": cfg.act,
+    }
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "sp_partitioned_transformer_gb300", "csrc")
+    for f in ("gemm_tc.cu", "common.cuh"):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(config_name: str, mode: str):
+    """DRAM bytes per launch of the GEMM kernel from the committed ncu summary, if it
+    was taken on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "gemm_dram_traffic.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+    except (OSError, ValueError):
+        return None
+    if d.get("kernel_source_sha256_16") != kernel_source_hash():
+        return None
+    ent = d.get("per_step", {}).get(f"{config_name}/{mode}")
+    return ent
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the GPU is loaded."""
+
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_id: str):
+        self.proc = None
+        self.path = None
+        try:
+            import tempfile
+
+            fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={','.join(self.FIELDS)}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", gpu_id], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as fh:
+            for line in fh:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) == len(self.FIELDS):
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(r[0]) for r in rows if num(r[0]) is not None]
+        mx = [num(r[1]) for r in rows if num(r[1]) is not None]
+        power = [num(r[2]) for r in rows if num(r[2]) is not None]
+        reasons = set()
+        for r in rows:
+            for name, val in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"), r[4:]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        # samples under load: SM clock well above idle
+        loaded = [v for v in sm if v >= 0.5 * (max(mx) if mx else 0)] or sm
+        return {
+            "sm_mhz": statistics.median(loaded) if loaded else None,
+            "sm_max_mhz": max(mx) if mx else None,
+            "reasons": sorted(reasons),
+            "samples": len(rows),
+            "power_w_max": max(power) if power else None,
+        }
+
+
+def gpu_uuid(dev) -> str:
+    import torch
+
+    try:
+        u = torch.cuda.get_device_properties(dev).uuid
+        s = str(u)
+        return s if s.startswith("GPU-") else f"GPU-{s}"
+    except Exception:  # noqa: BLE001
+        return str(dev)
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+
+
+def oracle_sample(cfg, inputs, target_s: float, max_tokens: int | None = None):
+    """Time the fp64 oracle's fwd+bwd on the first M' tokens (full weights); M' is
+    sized so one run takes about target_s.  Returns (flops/s, seconds, tokens, setup)."""
+    import numpy as np
+
+    import oracle as O
+
+    W1 = inputs["W1"].double().numpy()
+    W2 = inputs["W2"].double().numpy()
+    X = O.flatten_sbh(inputs["X"].double().numpy())
+    dZ = O.flatten_sbh(inputs["dZ"].double().numpy())
+    M = X.shape[0]
+    cap = min(M, max_tokens or M)
+
+    def run(mt):
+        t0 = time.perf_counter()
+        O.mlp_backward(X[:mt], W1, W2, dZ[:mt], cfg.act)
+        return time.perf_counter() - t0
+
+    probe = min(32, cap)
+    t_probe = run(probe)
+    mt = probe
+    if t_probe < target_s:
+        mt = int(min(cap, max(probe, probe * target_s / max(t_probe, 1e-3))))
+        mt = max(probe, (mt // 32) * 32) if mt >= 32 else mt
+    per = {"tokens": mt}
+    del np
+    return run, mt, per
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def flops_for_tokens(cfg, tokens: int) -> float:
+    return float(cfg.with_(s=tokens, b=1).flops_fwd_bwd())
+
+
+# ---------------------------------------------------------------- reference arm
+
+
+def run_reference(args) -> int:
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return 0
+    from synthetic import CONFIGS, block_inputs
+
+    cfg = CONFIGS[args.config]
+    inputs = block_inputs(cfg)
+    # each step a bounded sample so that the whole run stays within a few minutes
+    per_step_s = max(0.2, min(3.0, 150.0 / max(1, args.steps + args.warmup)))
+    run, mt, _ = oracle_sample(cfg, inputs, per_step_s)
+    for _ in range(args.warmup):
+        run(mt)
+    times = [run(mt) for _ in range(args.steps)]
+    t = sum(times) / len(times)
+    value = flops_for_tokens(cfg, mt) / t / 1e12
+    sample = (f"first {mt} of {cfg.M} tokens of the workload, full weights; fp64 NumPy oracle fwd+bwd "
+              f"(12·M'·h·f FLOPs)" if cfg.act != "swiglu" else
+              f"first {mt} of {cfg.M} tokens of the workload, full weights; fp64 NumPy oracle fwd+bwd (18·M'·h·F FLOPs)")
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": t * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": workload_desc(cfg),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- our arm
+
+
+def run_ours(args) -> int:
+    import torch
+    import torch.distributed as dist
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != args.gpus and args.gpus != 1:
+        print(f"warning: --gpus {args.gpus} but WORLD_SIZE={world}", file=sys.stderr)
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        dist.init_process_group(backend="nccl", device_id=torch.device("cuda", local_rank))
+
+    from sp_partitioned_transformer_gb300 import build as _build
+
+    _build.build()
+    import sp_partitioned_transformer_gb300 as tpmlp
+    from synthetic import CONFIGS, ELEM_BYTES, block_inputs
+
+    tpmlp.load()
+    cfg = CONFIGS[args.config]
+    dt = cfg.torch_dtype
+    inputs = block_inputs(cfg)
+    dev = torch.device("cuda", local_rank)
+    W1 = inputs["W1"].to(dev)
+    W2 = inputs["W2"].to(dev)
+    X = inputs["X"].to(dev)
+    dZ = inputs["dZ"].to(dev)
+    x = [c.contiguous() for c in X.chunk(cfg.tp)] if cfg.sp else X
+    dz = [c.contiguous() for c in dZ.chunk(cfg.tp)] if cfg.sp else dZ
+    blk = tpmlp.MLPBlock(cfg.s, cfg.b, cfg.h, cfg.f, cfg.tp, cfg.sp, dt, cfg.act, args.mode, device=dev)
+    fw = blk.alloc_forward()
+    bw = blk.alloc_backward()
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        blk.forward(x, W1, W2, out=fw, stream=stream)
+        blk.backward(x, W1, W2, fw, dz, out=bw, stream=stream)
+
+    def barrier():
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    clocks = ClockSampler(gpu_uuid(local_rank)) if rank == 0 else None
+    for _ in range(max(3, args.warmup)):
+        step()
+    barrier()
+    tpmlp.profile_start()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    barrier()
+    prof = tpmlp.profile_stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    status = tpmlp.device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status}: {tpmlp.last_error()}")
+    ms_t = torch.tensor([ms], device=dev)
+    if world > 1:
+        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
+    ms_max = float(ms_t.item())
+    flops = float(cfg.flops_fwd_bwd())
+    value = world * flops / (ms_max / 1e3) / 1e12
+
+    # ------------------------------------------------ end to end through the public API
+    e2e = None
+    if not args.no_e2e:
+        pin = lambda t: t.cpu().pin_memory()  # noqa: E731
+        xh = [pin(c) for c in x] if cfg.sp else [pin(x)]
+        dzh = [pin(c) for c in dz] if cfg.sp else [pin(dz)]
+        xd = x if cfg.sp else [x]
+        dzd = dz if cfg.sp else [dz]
+        zd = fw["z"] if cfg.sp else [fw["z"]]
+        dxd = bw["dx"] if cfg.sp else [bw["dx"]]
+        zh = [torch.empty_like(t, device="cpu").pin_memory() for t in zd]
+        dxh = [torch.empty_like(t, device="cpu").pin_memory() for t in dxd]
+        h2d = sum(t.numel() * t.element_size() for t in xh + dzh)
+        d2h = sum(t.numel() * t.element_size() for t in zh + dxh)
+
+        def step_e2e():
+            for d_, h_ in zip(xd, xh):
+                d_.copy_(h_, non_blocking=True)
+            for d_, h_ in zip(dzd, dzh):
+                d_.copy_(h_, non_blocking=True)
+            step()
+            for h_, d_ in zip(zh, zd):
+                h_.copy_(d_, non_blocking=True)
+            for h_, d_ in zip(dxh, dxd):
+                h_.copy_(d_, non_blocking=True)
+
+        for _ in range(max(3, args.warmup)):
+            step_e2e()
+        barrier()
+        e0.record(stream)
+        n_e2e = max(3, args.steps // 2)
+        for _ in range(n_e2e):
+            step_e2e()
+        e1.record(stream)
+        barrier()
+        ms_e2e = e0.elapsed_time(e1) / n_e2e
+        t = torch.tensor([ms_e2e], device=dev)
+        if world > 1:
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e = {"value": world * flops / (float(t.item()) / 1e3) / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": float(t.item())}
+
+    clock_info = clocks.stop() if clocks is not None else None
+
+    if rank != 0:
+        if world > 1:
+            dist.barrier()
+            dist.destroy_process_group()
+        return 0
+
+    # ------------------------------------------------ roofline of the dominant kernel
+    peaks, peak_src = load_peaks()
+    g = prof["gemm_tc"] if prof["gemm_tc"]["launches"] else prof["gemm_f32"]
+    launches_total = sum(v["launches"] for v in prof.values())
+    per_kernel = {}
+    for k, v in prof.items():
+        if v["launches"]:
+            unit = "TFLOP/s" if k.startswith("gemm") else "GB/s"
+            rate = v["work"] / (v["ms"] / 1e3) / (1e12 if unit == "TFLOP/s" else 1e9)
+            per_kernel[k] = {"launches_per_step": v["launches"] / args.steps, "ms_per_step": v["ms"] / args.steps,
+                             "achieved": rate, "unit": unit,
+                             "share_of_step": v["ms"] / args.steps / ms}
+    peak = peaks.get("bf16_tflops_sustained") or FALLBACK_PEAKS["bf16_tflops_sustained"]
+    achieved = g["work"] / (g["ms"] / 1e3) / 1e12 if g["ms"] > 0 else None
+    traffic = ncu_traffic(cfg.name, args.mode)
+    roofline = {
+        "bound": "tensor",
+        "kernel": "tpmlp::tc::gemm_kernel (tcgen05, all six GEMMs of the step)",
+        "achieved": achieved,
+        "peak": peak,
+        "peak_source": f"{peak_src} bf16_tflops_sustained (dense BF16; fp16 has the same tensor rate)",
+        "unit": "TFLOP/s",
+        "frac": (achieved / peak) if achieved else None,
+        "traffic": traffic.get("dram_bytes_per_launch") if traffic else None,
+        "flops_per_launch": g["work"] / max(1, g["launches"]),
+        "avg_launch_ms": g["ms"] / max(1, g["launches"]),
+        "frac_of_burst_peak": (achieved / peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])) if achieved else None,
+        "per_kernel": per_kernel,
+    }
+    if "copy_dim0" in per_kernel:
+        hbm = peaks.get("hbm_gbs") or FALLBACK_PEAKS["hbm_gbs"]
+        roofline["per_kernel"]["copy_dim0"]["frac_of_hbm"] = per_kernel["copy_dim0"]["achieved"] / hbm
+    if "shard_sum" in per_kernel:
+        hbm = peaks.get("hbm_gbs") or FALLBACK_PEAKS["hbm_gbs"]
+        roofline["per_kernel"]["shard_sum"]["frac_of_hbm"] = per_kernel["shard_sum"]["achieved"] / hbm
+
+    # ------------------------------------------------ CPU oracle baseline (rank 0, N = 1)
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        run, mt, _ = oracle_sample(cfg, inputs, args.cpu_seconds)
+        t_cpu = run(mt)
+        cpu = {"value": flops_for_tokens(cfg, mt) / t_cpu / 1e12, "unit": UNIT, "cores": cpu_cores(),
+               "kind": "oracle",
+               "sample": f"first {mt} of {cfg.M} tokens, full weights, fp64 NumPy fwd+bwd, one run of {t_cpu:.1f} s"}
+
+    ebytes = ELEM_BYTES[cfg.dtype]
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_max,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": cfg.dtype,
+        "data": "synthetic",
+        "config": {**workload_desc(cfg), "reduce": args.mode,
+                   "l2": f"inputs larger than L2: W1 and W2 are {cfg.fc1_rows * cfg.h * ebytes / 1e6:.0f} and "
+                         f"{cfg.h * cfg.f * ebytes / 1e6:.0f} MB, no flush",
+                   "flops_per_step": flops,
+                   "replicas": world},
+        "frac_of_dense_bf16_peak": {"sustained": value / world / peak,
+                                    "burst": value / world / peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]),
+                                    "peak_source": peak_src},
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches_total,
+        "clocks": clock_info,
+        "kernel_source_sha256_16": kernel_source_hash(),
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None) -> int:
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,76 @@
+// Host-side internal interface between the C ABI (api.cu) and the kernel
+// launchers (copy_kernels.cu, gemm_tc.cu, gemm_simt.cu).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+#include <vector>
+
+#include "common.cuh"
+
+namespace tpmlp {
+
+// Sets the thread-local message returned by tpmlp_last_error(); returns `code`.
+int set_error(int code, const std::string& msg);
+
+// Per-device state (SM count, address of the device status word, timeout).
+struct DeviceInfo {
+  int device = -1;
+  int num_sms = 0;
+  unsigned* status = nullptr;  // device address of the status word
+  size_t max_smem_optin = 0;
+};
+// Returns TPMLP_OK and fills `info` for the current device.
+int current_device(DeviceInfo** info);
+uint64_t wait_timeout_ns();
+
+// One K segment of a GEMM: A rows/cols starting at `a`, B at `b`, K extent k.
+// All segments of one output partial accumulate into the same accumulator in
+// the order they are listed.
+struct GemmSeg {
+  const void* a;
+  const void* b;
+  int64_t k;
+  int part;
+};
+
+// C[m, n] = Σ_segments Σ_k A(m, k)·B(n, k), then an epilogue.
+//   A(m, k) = a[m·lda + k] (K-major) or a[k·lda + m] (MN-major); likewise B.
+// For SwiGLU fc1 (swiglu_up_row > 0) the logical N is F and the B rows of the
+// up half are at swiglu_up_row + n; the accumulator tile pairs each gate column
+// with its up column.
+struct GemmDesc {
+  int dtype = DT_BF16;
+  int64_t M = 0, N = 0;
+  bool a_mn = false, b_mn = false;
+  int64_t lda = 0, ldb = 0;
+  int64_t b_rows = 0;         // B extent along N (rows of the weight), for the TMA map
+  int64_t swiglu_up_row = 0;  // > 0: SwiGLU fc1 pairing
+  int nparts = 1;
+  std::vector<GemmSeg> segs;
+  EpiParams epi{};
+};
+
+int launch_gemm_tc(const GemmDesc& g, cudaStream_t st);
+int launch_gemm_simt(const GemmDesc& g, cudaStream_t st);
+
+// dim-0 movement: dst[j][0:bytes) = src[j][0:bytes) for j < n (one launch).
+int launch_copy_chunks(const void* const* src, void* const* dst, int n, int64_t bytes,
+                       cudaStream_t st);
+
+// out = fixed-order float32 sum of tp partials [tp][n], rounded to dtype; if
+// scatter, element e goes to out[e / chunk][e % chunk], else out[0][e].
+int launch_shard_sum(const float* partials, int tp, int64_t n, int dtype, int scatter,
+                     int64_t chunk, void* const* out, cudaStream_t st);
+
+int launch_wait_selftest(unsigned* status, uint64_t timeout_ns, cudaStream_t st);
+
+// Launch accounting (tpmlp_profile_start/stop): bracket one kernel launch with
+// CUDA events on its stream.  prof_begin returns -1 when accounting is off.
+enum ProfKind : int { PROF_GEMM_TC = 0, PROF_GEMM_SIMT = 1, PROF_COPY = 2, PROF_SHARD_SUM = 3 };
+int prof_begin(int kind, cudaStream_t st);
+void prof_end(int handle, double work, cudaStream_t st);
+
+}  // namespace tpmlp

@@ -1,0 +1,125 @@
+"""C-ABI checks that need no GPU: the library builds and loads, exports every
+function include/tpmlp.h declares, and rejects bad arguments on the host before
+anything is launched (no compute call is made here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "tpmlp.h")
+
+INVALID, NOT_DIV, UNSUP, WORKSPACE = -1, -2, -3, -4
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from sp_partitioned_transformer_gb300 import build
+
+    build.build()
+    import sp_partitioned_transformer_gb300 as tpmlp
+
+    return tpmlp.load()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*[\w\s\*]+?\b(tpmlp_\w+)\s*\(", src, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("tpmlp_forward", "tpmlp_backward", "tpmlp_split_dim0", "tpmlp_gather_dim0",
+              "tpmlp_reduce_scatter_dim0", "tpmlp_workspace_size", "tpmlp_last_error"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+    assert lib.tpmlp_abi_version() == 1
+
+
+def _ws(lib, *a):
+    return lib.tpmlp_workspace_size(*a)
+
+
+def test_workspace_size_formula(lib):
+    # [s,b,h] = [512,4,1024], f=4096, tp=4, SP, bf16: gathered X and dZ, each M·h·2 bytes
+    M, h = 512 * 4, 1024
+    assert _ws(lib, 512, 4, 1024, 4096, 4, 1, 2, 0, 1) == 2 * M * h * 2
+    # + tp float32 partials in PARTIALS mode
+    assert _ws(lib, 512, 4, 1024, 4096, 4, 1, 2, 0, 0) == 2 * M * h * 2 + 4 * M * h * 4
+    # SP off, fused: no workspace
+    assert _ws(lib, 1024, 8, 3072, 12288, 8, 0, 1, 0, 1) == 0
+    # invalid -> 0 with a message
+    assert _ws(lib, 16, 2, 64, 250, 4, 0, 0, 0, 1) == 0
+    assert b"divisible" in lib.tpmlp_last_error()
+
+
+def _vp(*vals):
+    return (ctypes.c_void_p * len(vals))(*vals)
+
+
+FAKE = 0x10000  # never dereferenced: every case below fails validation first
+
+
+def _fwd(lib, s=16, b=2, h=64, f=256, tp=2, sp=0, dt=2, act=0, mode=1, x=None, w1=FAKE, w2=FAKE, u=FAKE,
+         y=FAKE, z=None, ws=None, ws_bytes=0):
+    n = tp if sp else 1
+    x = x if x is not None else _vp(*([FAKE] * n))
+    z = z if z is not None else _vp(*([FAKE] * n))
+    return lib.tpmlp_forward(s, b, h, f, tp, sp, dt, act, mode, x, w1, w2, u, y, z, ws, ws_bytes, None)
+
+
+def test_forward_rejects_bad_arguments_on_the_host(lib):
+    assert _fwd(lib, f=250, tp=4) == NOT_DIV  # f % tp
+    assert _fwd(lib, s=15, tp=2, sp=1) == NOT_DIV  # s % tp under SP
+    assert b"First dimension" in lib.tpmlp_last_error()
+    assert _fwd(lib, tp=0) == INVALID
+    assert _fwd(lib, tp=65) == INVALID
+    assert _fwd(lib, dt=7) == INVALID
+    assert _fwd(lib, act=9) == INVALID
+    assert _fwd(lib, mode=5) == INVALID
+    assert _fwd(lib, h=0) == INVALID
+    assert _fwd(lib, s=-1) == INVALID
+    assert _fwd(lib, w1=None) == INVALID
+    assert _fwd(lib, z=_vp(None)) == INVALID
+    assert _fwd(lib, h=60) == UNSUP  # tensor-core path: h % 8
+    assert _fwd(lib, f=2 * 12, tp=2) == UNSUP  # f/tp = 12, not a multiple of 8
+    assert _fwd(lib, w2=FAKE + 2) == UNSUP  # 16-byte alignment of the tensor-core path
+    assert _fwd(lib, dt=0, w2=FAKE + 2) == INVALID  # float32 path wants 4-byte alignment
+    # SP needs workspace for the gathered input
+    assert _fwd(lib, sp=1, ws=None, ws_bytes=0) == WORKSPACE
+    assert _fwd(lib, sp=1, ws=FAKE, ws_bytes=100) == WORKSPACE
+    assert b"workspace" in lib.tpmlp_last_error()
+    assert _fwd(lib, mode=0, ws=FAKE + 16, ws_bytes=1 << 30) == UNSUP  # ws must be 256-byte aligned
+
+
+def test_backward_and_dim0_ops_reject_bad_arguments(lib):
+    vp1 = _vp(FAKE)
+    rc = lib.tpmlp_backward(16, 2, 64, 256, 2, 0, 2, 0, 1, vp1, FAKE, FAKE, FAKE, FAKE, vp1, _vp(None), FAKE,
+                            FAKE, FAKE, None, 0, None)
+    assert rc == INVALID
+    rc = lib.tpmlp_backward(16, 2, 64, 256, 3, 0, 2, 0, 1, vp1, FAKE, FAKE, FAKE, FAKE, vp1, vp1, FAKE, FAKE,
+                            FAKE, None, 0, None)
+    assert rc == NOT_DIV
+    assert lib.tpmlp_split_dim0(FAKE, _vp(FAKE, FAKE, FAKE), 10, 1, 8, 3, 2, None) == NOT_DIV
+    assert lib.tpmlp_gather_dim0(_vp(FAKE, None), FAKE, 10, 1, 8, 2, 2, None) == INVALID
+    assert lib.tpmlp_reduce_scatter_dim0(FAKE, _vp(FAKE), 10, 1, 8, 3, 1, 2, None) == NOT_DIV
+    assert lib.tpmlp_reduce_scatter_dim0(FAKE, _vp(FAKE), 10, 1, 8, 3, 2, 2, None) == INVALID
+    assert lib.tpmlp_wait_timeout_selftest(0, None) == INVALID
+
+
+def test_binding_refuses_to_run_without_the_library(tmp_path):
+    import sp_partitioned_transformer_gb300 as tpmlp
+
+    saved = tpmlp._lib
+    tpmlp._lib = None
+    try:
+        with pytest.raises(ImportError):
+            tpmlp.load(str(tmp_path / "missing.so"))
+    finally:
+        tpmlp._lib = saved
