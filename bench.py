@@ -469,6 +469,8 @@ def run_ours(args) -> int:
         "gpu_launches": launches_total,
         "clocks": clock_info,
         "kernel_source_sha256_16": kernel_source_hash(),
+        "device": {"name": torch.cuda.get_device_name(dev),
+                   "sms": torch.cuda.get_device_properties(dev).multi_processor_count},
     }
     print(json.dumps(line), flush=True)
     if world > 1:
