@@ -183,6 +183,39 @@ int tpmlp_gather_dim0(const void* const* shards, void* full, int64_t s, int64_t 
 int tpmlp_reduce_scatter_dim0(const float* partials, void* const* out, int64_t s, int64_t b,
                               int64_t h, int tp, int scatter, int dtype, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * tpmlp_forward_noalloc — tpmlp_forward for callers that cannot supply a
+ * device workspace.  (The pages have no counterpart; this is a library
+ * convenience.)
+ *
+ * Who needs it: code whose GPU memory belongs to a memory manager that does not
+ * let it allocate where it calls the block, and latency-critical loops that
+ * must not pay cudaMalloc's implicit device-wide synchronisation.  Arguments
+ * and results are those of tpmlp_forward without ws / ws_bytes; the caller
+ * still passes every input and output buffer.
+ *
+ * Scratch: a fixed array of TPMLP_NOALLOC_SCRATCH_BYTES (64 MiB) compiled into
+ * the library as device memory.  Every GPU that loads the library holds it
+ * until the process exits.  The call allocates nothing (no cudaMalloc,
+ * cudaFree or allocating library routine).
+ *   - Sizes whose workspace (tpmlp_workspace_size) exceeds the scratch are
+ *     rejected with TPMLP_ERR_WORKSPACE and a message giving both sizes; use
+ *     tpmlp_forward with a caller workspace for those.
+ *   - The first call on each device looks up the scratch array's device
+ *     address (cudaGetSymbolAddress) with that device current; make that first
+ *     call before any stream capture on the device.
+ *   - All calls share the one array and it keeps the last call's contents.
+ *     Nothing in it needs to start at zero (each call writes every scratch
+ *     byte it reads).  Calls that can overlap on the GPU — on different
+ *     streams, or from several host threads — race on the scratch; serialise
+ *     them (one stream) or use tpmlp_forward with separate workspaces.
+ * ------------------------------------------------------------------------- */
+#define TPMLP_NOALLOC_SCRATCH_BYTES (64ull << 20)
+
+int tpmlp_forward_noalloc(int64_t s, int64_t b, int64_t h, int64_t f, int tp, int sp, int dtype,
+                          int act, int mode, const void* const* x, const void* w1,
+                          const void* w2, void* u, void* y, void* const* z, void* stream);
+
 /* Thread-local description of the last non-OK status returned on this thread. */
 const char* tpmlp_last_error(void);
 

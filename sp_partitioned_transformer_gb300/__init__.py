@@ -31,6 +31,8 @@ __all__ = [
     "MODE",
     "workspace_size",
     "forward",
+    "forward_noalloc",
+    "NOALLOC_SCRATCH_BYTES",
     "backward",
     "split_dim0",
     "gather_dim0",
@@ -121,6 +123,9 @@ def load(path: str | None = None):
     lib.tpmlp_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
     lib.tpmlp_wait_timeout_selftest.restype = i32
     lib.tpmlp_wait_timeout_selftest.argtypes = [ctypes.c_uint64, vp]
+    lib.tpmlp_forward_noalloc.restype = i32
+    lib.tpmlp_forward_noalloc.argtypes = [i64, i64, i64, i64, i32, i32, i32, i32, i32,
+                                          vpp, vp, vp, vp, vp, vpp, vp]
     lib.tpmlp_profile_start.restype = i32
     lib.tpmlp_profile_start.argtypes = []
     lib.tpmlp_profile_stop.restype = i32
@@ -192,6 +197,20 @@ def forward(x, w1, w2, u, y, z, *, s, b, h, f, tp, sp, act="gelu", mode="fused",
         0 if workspace is None or isinstance(workspace, int) else workspace.numel() * workspace.element_size())
     rc = load().tpmlp_forward(s, b, h, f, tp, int(sp), dt, ACT[act], MODE[mode], _ptrs(x), _ptr(w1), _ptr(w2),
                               _ptr(u), _ptr(y), _ptrs(z), _ptr(workspace), ws_bytes, _stream(stream))
+    _check(rc)
+
+
+NOALLOC_SCRATCH_BYTES = 64 << 20
+
+
+def forward_noalloc(x, w1, w2, u, y, z, *, s, b, h, f, tp, sp, act="gelu", mode="fused", dtype=None,
+                    stream=None) -> None:
+    """The forward without a caller workspace: the library's built-in 64 MiB
+    scratch is used instead (for callers that cannot allocate device memory where
+    they call the block).  Calls share that scratch: do not overlap them on the GPU."""
+    dt = _dtype_code(dtype if dtype is not None else w1.dtype)
+    rc = load().tpmlp_forward_noalloc(s, b, h, f, tp, int(sp), dt, ACT[act], MODE[mode], _ptrs(x), _ptr(w1),
+                                      _ptr(w2), _ptr(u), _ptr(y), _ptrs(z), _stream(stream))
     _check(rc)
 
 

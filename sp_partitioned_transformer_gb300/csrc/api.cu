@@ -280,6 +280,16 @@ int row_parallel_and_reduce(const Block& k, bool is_dgrad, const void* a_act, co
 }
 
 }  // namespace
+
+int forward_workspace_bytes(int64_t s, int64_t b, int64_t h, int64_t f, int tp, int sp, int dtype, int act,
+                            int mode, size_t* bytes) {
+  Block k;
+  const int rc = check_block(s, b, h, f, tp, sp, dtype, act, mode, &k);
+  if (rc != TPMLP_OK) return rc;
+  *bytes = ws_layout(k).total;
+  return TPMLP_OK;
+}
+
 }  // namespace tpmlp
 
 using namespace tpmlp;

@@ -53,6 +53,10 @@ struct GemmDesc {
   EpiParams epi{};
 };
 
+// Validates tpmlp_forward's size arguments and returns the workspace it needs.
+int forward_workspace_bytes(int64_t s, int64_t b, int64_t h, int64_t f, int tp, int sp, int dtype, int act,
+                            int mode, size_t* bytes);
+
 int launch_gemm_tc(const GemmDesc& g, cudaStream_t st);
 int launch_gemm_simt(const GemmDesc& g, cudaStream_t st);
 
