@@ -129,44 +129,6 @@ __device__ __forceinline__ void epi_chunk(const Params& p, int64_t m, int64_t n0
     }
     return;
   }
-  // EPI_DACT
-  if (e.act == ACT_SWIGLU) {
-    // dY chunk -> dG = dY·Up·silu'(G), dUp = dY·silu(G); G, Up from the saved U.
-    const T* ug = static_cast<const T*>(e.aux) + m * e.ldaux + n0;
-    const T* uu = ug + e.swiglu_F;
-    T* dg = static_cast<T*>(e.out) + m * e.ldo + n0;
-    T* du = dg + e.swiglu_F;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      if (n0 + 8 * j < N) {
-        float g[8], up[8], rg[8], ru[8];
-        unpack8<DT>(*reinterpret_cast<const uint4*>(ug + 8 * j), g);
-        unpack8<DT>(*reinterpret_cast<const uint4*>(uu + 8 * j), up);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float s = sigmoid_f<false>(g[i]);
-          const float dy = v[8 * j + i];
-          rg[i] = dy * up[i] * (s * (1.0f + g[i] * (1.0f - s)));
-          ru[i] = dy * (g[i] * s);
-        }
-        *reinterpret_cast<uint4*>(dg + 8 * j) = pack8<DT>(rg);
-        *reinterpret_cast<uint4*>(du + 8 * j) = pack8<DT>(ru);
-      }
-    }
-    return;
-  }
-  const T* u = static_cast<const T*>(e.aux) + m * e.ldaux + n0;
-  T* du = static_cast<T*>(e.out) + m * e.ldo + n0;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    if (n0 + 8 * j < N) {
-      float uf[8], d[8];
-      unpack8<DT>(*reinterpret_cast<const uint4*>(u + 8 * j), uf);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) d[i] = v[8 * j + i] * act_grad<false>(e.act, uf[i]);
-      *reinterpret_cast<uint4*>(du + 8 * j) = pack8<DT>(d);
-    }
-  }
 }
 
 // SwiGLU fc1: 32 gate and the matching 32 up columns of one row.
@@ -191,6 +153,112 @@ __device__ __forceinline__ void epi_swiglu_fwd(const Params& p, int64_t m, int64
       *reinterpret_cast<uint4*>(uu + 8 * j) = pack8<DT>(up + 8 * j);
       *reinterpret_cast<uint4*>(y + 8 * j) = pack8<DT>(a);
     }
+  }
+}
+
+// fc2 input gradient epilogue for 8 columns: dU = act'(U) ⊙ dY.  SwiGLU:
+// dG = dY·Up·silu'(G) and dUp = dY·silu(G), written to dU's gate and up halves.
+template <int DT>
+__device__ __forceinline__ void epi_dact8(const EpiParams& e, int64_t m, int64_t n, const float* dy, uint4 u_raw,
+                                          uint4 up_raw) {
+  using T = typename Storage<DT>::T;
+  float u[8], r[8];
+  unpack8<DT>(u_raw, u);
+  T* out = static_cast<T*>(e.out) + m * e.ldo + n;
+  if (e.act == ACT_SWIGLU) {
+    float up[8], r2[8];
+    unpack8<DT>(up_raw, up);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float sg = sigmoid_f<false>(u[i]);
+      r[i] = dy[i] * up[i] * (sg * (1.0f + u[i] * (1.0f - sg)));
+      r2[i] = dy[i] * (u[i] * sg);
+    }
+    *reinterpret_cast<uint4*>(out) = pack8<DT>(r);
+    *reinterpret_cast<uint4*>(out + e.swiglu_F) = pack8<DT>(r2);
+    return;
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) r[i] = dy[i] * act_grad<false>(e.act, u[i]);
+  *reinterpret_cast<uint4*>(out) = pack8<DT>(r);
+}
+
+// L2 prefetch of the saved U row segment a fc2-input-gradient tile will read,
+// issued before the epilogue waits for the accumulator.
+template <int TN>
+__device__ __forceinline__ void epi_prefetch_aux(const Params& p, int64_t m, int nb, int elem_bytes) {
+  const EpiParams& e = p.epi;
+  if (e.kind != EPI_DACT || m >= p.M) return;
+  const char* row = static_cast<const char*>(e.aux) + (m * e.ldaux + static_cast<int64_t>(nb) * TN) * elem_bytes;
+  const int64_t left = (p.N - static_cast<int64_t>(nb) * TN) * elem_bytes;
+#pragma unroll
+  for (int b = 0; b < TN * 2 / 128; ++b) {
+    if (b * 128 < left) {
+      prefetch_l2(row + b * 128);
+      if (e.act == ACT_SWIGLU) prefetch_l2(row + e.swiglu_F * elem_bytes + b * 128);
+    }
+  }
+}
+
+// Drains one 128-row × BN-column accumulator (this warp's 32 lanes = rows)
+// from tensor memory and runs the epilogue.  All 32 lanes execute the
+// tcgen05.ld instructions; rows past M only skip their stores.
+template <int DT, int TN>
+__device__ __forceinline__ void epilogue_tile(const Params& p, uint32_t trow, int64_t m, bool row_ok, int nb,
+                                              int part) {
+  const EpiParams& e = p.epi;
+  if (p.swiglu_up_row > 0) {
+#pragma unroll 1
+    for (int c = 0; c < TN / 64; ++c) {
+      float g[32], up[32];
+      tmem_ld32(trow + c * 32, g);
+      tmem_ld32(trow + TN / 2 + c * 32, up);
+      if (row_ok) epi_swiglu_fwd<DT>(p, m, static_cast<int64_t>(nb) * (TN / 2) + c * 32, g, up);
+    }
+    return;
+  }
+  if (e.kind == EPI_DACT) {
+    using T = typename Storage<DT>::T;
+    const bool swi = e.act == ACT_SWIGLU;
+    const T* urow = static_cast<const T*>(e.aux) + m * e.ldaux;
+    const int64_t nbase = static_cast<int64_t>(nb) * TN;
+    uint4 cur[4], curup[4], nxt[4], nxtup[4];
+    auto load = [&](int c, uint4* dst, uint4* dstup) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int64_t n = nbase + c * 32 + 8 * j;
+        if (row_ok && n < p.N) {
+          dst[j] = ldg_nc_v4(urow + n);
+          if (swi) dstup[j] = ldg_nc_v4(urow + e.swiglu_F + n);
+        }
+      }
+    };
+    load(0, cur, curup);
+#pragma unroll 1
+    for (int c = 0; c < TN / 32; ++c) {
+      if (c + 1 < TN / 32) load(c + 1, nxt, nxtup);  // one chunk ahead
+      float v[32];
+      tmem_ld32(trow + c * 32, v);
+      if (row_ok) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int64_t n = nbase + c * 32 + 8 * j;
+          if (n < p.N) epi_dact8<DT>(e, m, n, v + 8 * j, cur[j], curup[j]);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        cur[j] = nxt[j];
+        curup[j] = nxtup[j];
+      }
+    }
+    return;
+  }
+#pragma unroll 1
+  for (int c = 0; c < TN / 32; ++c) {
+    float v[32];
+    tmem_ld32(trow + c * 32, v);
+    if (row_ok) epi_chunk<DT>(p, m, static_cast<int64_t>(nb) * TN + c * 32, v, p.part_base + part);
   }
 }
 
@@ -362,35 +430,20 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
   } else if (warp >= 4) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quarter accessible to this warp
-    const bool swiglu_fwd = p.swiglu_up_row > 0;
     int it = 0;
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++it) {
       int part, mb, nb;
       decode_tile(t, p, part, mb, nb);
       const int acc = it & 1;
       const uint32_t acc_phase = static_cast<uint32_t>(it >> 1) & 1u;
+      const int64_t m = static_cast<int64_t>(mb) * BM + q * 32 + lane;
+      const bool row_ok = m < p.M;
+      epi_prefetch_aux<BN>(p, m, nb, DT == DT_F32 ? 4 : 2);
       const bool ok = mbar_wait_bounded(tfull0 + 8u * acc, acc_phase, abort_flag, p.status, p.timeout_ns);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
-      const int64_t m = static_cast<int64_t>(mb) * BM + q * 32 + lane;
-      const bool row_ok = m < p.M;
       const uint32_t trow = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
-      if (swiglu_fwd) {
-#pragma unroll 1
-        for (int c = 0; c < BN / 64; ++c) {
-          float g[32], up[32];
-          tmem_ld32(trow + c * 32, g);
-          tmem_ld32(trow + BN / 2 + c * 32, up);
-          if (row_ok) epi_swiglu_fwd<DT>(p, m, static_cast<int64_t>(nb) * (BN / 2) + c * 32, g, up);
-        }
-      } else {
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          float v[32];
-          tmem_ld32(trow + c * 32, v);
-          if (row_ok) epi_chunk<DT>(p, m, static_cast<int64_t>(nb) * BN + c * 32, v, p.part_base + part);
-        }
-      }
+      epilogue_tile<DT, BN>(p, trow, m, row_ok, nb, part);
       tc_fence_before();
       mbar_arrive(tempty0 + 8u * acc);
     }
@@ -401,6 +454,235 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
   if (warp == 2) {
     tc_fence_after();
     tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------- 2-SM kernel
+// A CTA pair (cluster of 2) computes one 256×256 tile with tcgen05.mma
+// .cta_group::2 (M = 256, N = 256, K = 16), issued by the even CTA.  Each CTA
+// loads only its half of A (128 rows) and its half of B (128 rows of the
+// 256-wide N tile) — half the L2→SM traffic per FLOP of the 1-SM kernel — into
+// a 6-stage ring of 32 KB stages; both CTAs' TMA copies complete on the even
+// CTA's "full" barrier, and the MMA commits are multicast to both CTAs' "empty"
+// and "accumulator full" barriers.  Each CTA's tensor memory holds its 128 rows
+// of both 256-column accumulators; both epilogues release an accumulator by
+// arriving on the even CTA's "accumulator empty" barrier.
+constexpr int PAIR_STAGES = 6;
+constexpr int HALF_M = BM;      // rows of A per CTA
+constexpr int PA_BYTES = HALF_M * BK * 2;  // 16 KB
+constexpr int PB_BYTES = 128 * BK * 2;     // 16 KB: room for up to 128 B rows per CTA
+constexpr int PSTAGE_BYTES = PA_BYTES + PB_BYTES;
+constexpr int PAIR_NUM_BARS = 2 * PAIR_STAGES + 5;
+constexpr size_t PAIR_SMEM_BYTES = 1024 + static_cast<size_t>(PAIR_STAGES) * PSTAGE_BYTES + 256;
+
+// TN: N extent of the pair's tile; each CTA holds TN/2 rows of B.
+template <int DT, bool A_MN, bool B_MN, int TN>
+__global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_constant__ Params p) {
+  constexpr int HALF_N = TN / 2;
+  // bytes of one stage (both CTAs): A halves + B halves; an MN-major B half is
+  // two 64-column boxes even when TN/2 = 96
+  constexpr uint32_t CTA_STAGE_TX = PA_BYTES + (B_MN ? 2 * MN_BOX_BYTES : HALF_N * BK * 2);
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  uint8_t* smem_a = smem;
+  uint8_t* smem_b = smem + PAIR_STAGES * PA_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + PAIR_STAGES * PSTAGE_BYTES);
+  const uint32_t full0 = smem_u32(bars);
+  const uint32_t empty0 = smem_u32(bars + PAIR_STAGES);
+  const uint32_t tfull0 = smem_u32(bars + 2 * PAIR_STAGES);
+  const uint32_t tempty0 = smem_u32(bars + 2 * PAIR_STAGES + 2);
+  const uint32_t drain_bar = smem_u32(bars + 2 * PAIR_STAGES + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + PAIR_NUM_BARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();  // 0: issues the pair's MMAs
+  const bool leader = rank == 0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < PAIR_STAGES; ++s) {
+      mbar_init(full0 + 8u * s, 1);
+      mbar_init(empty0 + 8u * s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull0 + 8u * a, 1);
+      mbar_init(tempty0 + 8u * a, 8);  // 4 epilogue warps in each of the 2 CTAs
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 2) {
+    tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync_all();  // both CTAs' barriers exist before any cross-CTA signal
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int cluster_id = static_cast<int>(blockIdx.x >> 1);
+  const int nclusters = static_cast<int>(gridDim.x >> 1);
+  const int num_tiles = p.mt * p.nt * p.nparts;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer (both CTAs)
+    if (lane == 0) {
+      for (int s = p.seg_begin[0]; s < p.seg_begin[p.nparts]; ++s) {
+        tma_prefetch_map(&p.maps[p.segs[s].map_a]);
+        tma_prefetch_map(&p.maps[p.segs[s].map_b]);
+      }
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_mask = 0, issued_phase = 0;
+      bool ok = true;
+      for (int t = cluster_id; ok && t < num_tiles; t += nclusters) {
+        int part, mb, nb;
+        decode_tile(t, p, part, mb, nb);
+        const int m_off = mb * (2 * HALF_M) + static_cast<int>(rank) * HALF_M;
+        int n_row;  // first B row (K-major) / column (MN-major) this CTA loads
+        if (p.swiglu_up_row > 0)
+          n_row = (leader ? 0 : p.swiglu_up_row) + nb * HALF_N;  // gate half / up half
+        else
+          n_row = nb * TN + static_cast<int>(rank) * HALF_N;
+        for (int si = p.seg_begin[part]; ok && si < p.seg_begin[part + 1]; ++si) {
+          const Seg sg = p.segs[si];
+          const CUtensorMap* ma = &p.maps[sg.map_a];
+          const CUtensorMap* mbp = &p.maps[sg.map_b];
+          const int nkb = (sg.k_len + BK - 1) / BK;
+          for (int kb = 0; kb < nkb; ++kb) {
+            if (!mbar_wait_bounded(empty0 + 8u * stage, phase ^ 1u, abort_flag, p.status, p.timeout_ns)) {
+              ok = false;
+              break;
+            }
+            const uint32_t fb_local = full0 + 8u * stage;
+            const uint32_t fb = mapa_shared(fb_local, 0);  // the even CTA's barrier
+            if (leader) mbar_arrive_expect_tx(fb_local, 2 * CTA_STAGE_TX);
+            const uint32_t sa = smem_u32(smem_a + stage * PA_BYTES);
+            const uint32_t sb = smem_u32(smem_b + stage * PB_BYTES);
+            const int k0 = kb * BK;
+            if constexpr (!A_MN) {
+              tma_load_2d_pair(sa, ma, fb, k0, m_off);
+            } else {
+              tma_load_2d_pair(sa, ma, fb, m_off, k0);
+              tma_load_2d_pair(sa + MN_BOX_BYTES, ma, fb, m_off + 64, k0);
+            }
+            if constexpr (!B_MN) {
+              tma_load_2d_pair(sb, mbp, fb, k0, n_row);
+            } else {
+              tma_load_2d_pair(sb, mbp, fb, n_row, k0);
+              tma_load_2d_pair(sb + MN_BOX_BYTES, mbp, fb, n_row + 64, k0);
+            }
+            issued_mask |= 1u << stage;
+            issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+            if (++stage == PAIR_STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+      }
+      if (!ok) {
+        // Let copies in flight land before the CTA exits.  The even CTA can watch
+        // its full barriers; the odd CTA's copies complete there too, so it waits
+        // a fixed time instead.
+        if (leader) {
+          for (int s = 0; s < PAIR_STAGES; ++s)
+            if ((issued_mask >> s) & 1u)
+              (void)mbar_wait_bounded(full0 + 8u * s, (issued_phase >> s) & 1u, nullptr, nullptr, p.timeout_ns);
+        } else {
+          const uint64_t t0 = globaltimer_ns();
+          while (globaltimer_ns() - t0 < 2000000ull) __nanosleep(1000);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (even CTA)
+    if (lane == 0 && leader) {
+      constexpr uint32_t idesc = make_idesc_f16(DT == DT_BF16, A_MN, B_MN, 2 * HALF_M, TN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int it = 0;
+      bool ok = true;
+      for (int t = cluster_id; ok && t < num_tiles; t += nclusters, ++it) {
+        int part, mb, nb;
+        decode_tile(t, p, part, mb, nb);
+        const int acc = it & 1;
+        const uint32_t acc_phase = static_cast<uint32_t>(it >> 1) & 1u;
+        if (!mbar_wait_bounded(tempty0 + 8u * acc, acc_phase ^ 1u, abort_flag, p.status, p.timeout_ns)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        uint32_t accumulate = 0;
+        for (int si = p.seg_begin[part]; ok && si < p.seg_begin[part + 1]; ++si) {
+          const int nkb = (p.segs[si].k_len + BK - 1) / BK;
+          for (int kb = 0; kb < nkb; ++kb) {
+            if (!mbar_wait_bounded(full0 + 8u * stage, phase, abort_flag, p.status, p.timeout_ns)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t sa = smem_u32(smem_a + stage * PA_BYTES);
+            const uint32_t sb = smem_u32(smem_b + stage * PB_BYTES);
+#pragma unroll
+            for (int ks = 0; ks < BK / UMMA_K; ++ks) {
+              const uint64_t ad = A_MN ? make_sdesc_sw128(sa + ks * 2048u, MN_BOX_BYTES, 1024u)
+                                       : make_sdesc_sw128(sa + ks * 32u, 16u, 1024u);
+              const uint64_t bd = B_MN ? make_sdesc_sw128(sb + ks * 2048u, MN_BOX_BYTES, 1024u)
+                                       : make_sdesc_sw128(sb + ks * 32u, 16u, 1024u);
+              tc_mma_f16_pair(d_tmem, ad, bd, idesc, accumulate);
+              accumulate = 1u;
+            }
+            tc_commit_pair_mc(empty0 + 8u * stage, 0x3);  // frees the stage in both CTAs
+            if (++stage == PAIR_STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+        if (!ok) break;
+        tc_commit_pair_mc(tfull0 + 8u * acc, 0x3);  // both CTAs' accumulator halves ready
+      }
+      if (!ok) {
+        tc_commit_pair_mc(drain_bar, 0x1);
+        (void)mbar_wait_bounded(drain_bar, 0u, nullptr, nullptr, p.timeout_ns);
+      }
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    const int q = warp & 3;
+    const uint32_t tempty_leader = mapa_shared(tempty0, 0);
+    int it = 0;
+    for (int t = cluster_id; t < num_tiles; t += nclusters, ++it) {
+      int part, mb, nb;
+      decode_tile(t, p, part, mb, nb);
+      const int acc = it & 1;
+      const uint32_t acc_phase = static_cast<uint32_t>(it >> 1) & 1u;
+      const int64_t m = static_cast<int64_t>(mb) * (2 * HALF_M) + static_cast<int64_t>(rank) * HALF_M + q * 32 + lane;
+      const bool row_ok = m < p.M;
+      epi_prefetch_aux<TN>(p, m, nb, DT == DT_F32 ? 4 : 2);
+      const bool ok = mbar_wait_bounded(tfull0 + 8u * acc, acc_phase, abort_flag, p.status, p.timeout_ns);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      const uint32_t trow = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
+      epilogue_tile<DT, TN>(p, trow, m, row_ok, nb, part);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(tempty_leader + 8u * acc);
+    }
+  }
+
+  tc_fence_before();
+  cluster_sync_all();  // the pair's MMAs and cross-CTA arrivals are all done
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, TMEM_COLS);
   }
 }
 
@@ -439,32 +721,83 @@ static int make_map(CUtensorMap* m, int dtype, const void* base, int64_t inner, 
   return TPMLP_OK;
 }
 
-template <int DT, bool A_MN, bool B_MN>
-static int launch_one(const Params& p, int grid, cudaStream_t st, const DeviceInfo& dev) {
+template <int DT, bool A_MN, bool B_MN, int TN>
+static int launch_one(const Params& p, int64_t tiles, bool pair, cudaStream_t st, const DeviceInfo& dev) {
   static std::mutex mu;
-  static bool attr_set[64] = {};
+  static bool attr_set[64][2] = {};
+  static int max_clusters[64] = {};
+  auto* k1 = gemm_kernel<DT, A_MN, B_MN>;
+  auto* k2 = gemm_pair_kernel<DT, A_MN, B_MN, TN>;
+  int clusters = 0;
   {
     std::lock_guard<std::mutex> lk(mu);
-    if (dev.device >= 0 && dev.device < 64 && !attr_set[dev.device]) {
-      const cudaError_t e = cudaFuncSetAttribute(gemm_kernel<DT, A_MN, B_MN>,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 static_cast<int>(SMEM_BYTES));
+    const int d = (dev.device >= 0 && dev.device < 64) ? dev.device : 0;
+    if (!attr_set[d][pair]) {
+      const cudaError_t e =
+          pair ? cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(PAIR_SMEM_BYTES))
+               : cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(SMEM_BYTES));
       if (e != cudaSuccess) return set_error(TPMLP_ERR_CUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
-      attr_set[dev.device] = true;
+      if (pair) {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(2 * static_cast<unsigned>(std::max(1, dev.num_sms / 2)));
+        cfg.blockDim = dim3(THREADS);
+        cfg.dynamicSmemBytes = PAIR_SMEM_BYTES;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        const cudaError_t e2 = cudaOccupancyMaxActiveClusters(&n, k2, &cfg);
+        if (e2 != cudaSuccess || n <= 0)
+          return set_error(TPMLP_ERR_CUDA, std::string("cudaOccupancyMaxActiveClusters: ") + cudaGetErrorString(e2));
+        max_clusters[d] = n;
+      }
+      attr_set[d][pair] = true;
     }
+    clusters = max_clusters[d];
   }
-  gemm_kernel<DT, A_MN, B_MN><<<grid, THREADS, SMEM_BYTES, st>>>(p);
+  if (!pair) {
+    const int grid = static_cast<int>(std::min<int64_t>(tiles, dev.num_sms));
+    k1<<<grid, THREADS, SMEM_BYTES, st>>>(p);
+  } else {
+    const int nclusters = static_cast<int>(std::min<int64_t>(tiles, clusters));
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * static_cast<unsigned>(nclusters));
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = PAIR_SMEM_BYTES;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, k2, p);
+    if (e != cudaSuccess) return set_error(TPMLP_ERR_CUDA, std::string("2-SM GEMM launch: ") + cudaGetErrorString(e));
+  }
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return set_error(TPMLP_ERR_CUDA, std::string("tensor-core GEMM launch: ") + cudaGetErrorString(e));
   return TPMLP_OK;
 }
 
-template <int DT>
-static int dispatch(const Params& p, int grid, cudaStream_t st, const DeviceInfo& dev, bool a_mn, bool b_mn) {
-  if (!a_mn && !b_mn) return launch_one<DT, false, false>(p, grid, st, dev);
-  if (!a_mn && b_mn) return launch_one<DT, false, true>(p, grid, st, dev);
-  if (a_mn && b_mn) return launch_one<DT, true, true>(p, grid, st, dev);
+template <int DT, int TN>
+static int dispatch_tn(const Params& p, int64_t tiles, bool pair, cudaStream_t st, const DeviceInfo& dev, bool a_mn,
+                       bool b_mn) {
+  if (!a_mn && !b_mn) return launch_one<DT, false, false, TN>(p, tiles, pair, st, dev);
+  if (!a_mn && b_mn) return launch_one<DT, false, true, TN>(p, tiles, pair, st, dev);
+  if (a_mn && b_mn) return launch_one<DT, true, true, TN>(p, tiles, pair, st, dev);
   return set_error(TPMLP_ERR_UNSUPPORTED, "MN-major A with K-major B is not instantiated");
+}
+
+template <int DT>
+static int dispatch(const Params& p, int64_t tiles, bool pair, int tn, cudaStream_t st, const DeviceInfo& dev,
+                    bool a_mn, bool b_mn) {
+  (void)tn;
+  return dispatch_tn<DT, BN>(p, tiles, pair, st, dev, a_mn, b_mn);
 }
 
 }  // namespace tc
@@ -479,12 +812,17 @@ int launch_gemm_tc(const GemmDesc& g, cudaStream_t st) {
   const bool swiglu = g.swiglu_up_row > 0;
   if (swiglu && (g.a_mn || g.b_mn)) return set_error(TPMLP_ERR_UNSUPPORTED, "SwiGLU pairing needs K-major operands");
 
+  // CTA pairs (256-row tiles) whenever there is more than one 128-row block.
+  const bool pair = g.M > BM;
+  // N tile of the pair kernel.  (A 192-wide variant that trims the last wave of
+  // N = h GEMMs measured slower per tile than it saved, so one width is used.)
+  const int tn = BN;
   Params p;
   memset(&p, 0, sizeof(p));
   p.M = static_cast<int32_t>(g.M);
   p.N = static_cast<int32_t>(g.N);
-  p.mt = static_cast<int32_t>((g.M + BM - 1) / BM);
-  const int tile_n = swiglu ? BN / 2 : BN;
+  p.mt = static_cast<int32_t>((g.M + (pair ? 2 * BM : BM) - 1) / (pair ? 2 * BM : BM));
+  const int tile_n = swiglu ? tn / 2 : tn;
   p.nt = static_cast<int32_t>((g.N + tile_n - 1) / tile_n);
   p.swiglu_up_row = static_cast<int32_t>(g.swiglu_up_row);
   p.status = dev->status;
@@ -521,7 +859,8 @@ int launch_gemm_tc(const GemmDesc& g, cudaStream_t st) {
           rc = make_map(&p.maps[d.map_a], g.dtype, s.a, g.M, s.k, g.lda, 64, BK);
         if (rc != TPMLP_OK) return rc;
         if (!g.b_mn)
-          rc = make_map(&p.maps[d.map_b], g.dtype, s.b, s.k, g.b_rows, g.ldb, BK, swiglu ? BN / 2 : BN);
+          rc = make_map(&p.maps[d.map_b], g.dtype, s.b, s.k, g.b_rows, g.ldb, BK,
+                        static_cast<uint32_t>(pair ? tn / 2 : (swiglu ? BN / 2 : BN)));
         else
           rc = make_map(&p.maps[d.map_b], g.dtype, s.b, g.N, s.k, g.ldb, 64, BK);
         if (rc != TPMLP_OK) return rc;
@@ -534,15 +873,14 @@ int launch_gemm_tc(const GemmDesc& g, cudaStream_t st) {
     p.nparts = nparts;
     const int64_t tiles = static_cast<int64_t>(p.mt) * p.nt * nparts;
     if (tiles >= (1ll << 31)) return set_error(TPMLP_ERR_UNSUPPORTED, "too many tiles");
-    const int grid = static_cast<int>(std::min<int64_t>(tiles, dev->num_sms));
     double ksum = 0.0;
     for (int c = 0; c < nsegs; ++c) ksum += static_cast<double>(p.segs[c].k_len);
     const double work = 2.0 * static_cast<double>(g.M) * static_cast<double>(swiglu ? 2 * g.N : g.N) * ksum;
     const int ph = prof_begin(PROF_GEMM_TC, st);
     if (g.dtype == DT_BF16)
-      rc = dispatch<DT_BF16>(p, grid, st, *dev, g.a_mn, g.b_mn);
+      rc = dispatch<DT_BF16>(p, tiles, pair, tn, st, *dev, g.a_mn, g.b_mn);
     else
-      rc = dispatch<DT_F16>(p, grid, st, *dev, g.a_mn, g.b_mn);
+      rc = dispatch<DT_F16>(p, tiles, pair, tn, st, *dev, g.a_mn, g.b_mn);
     prof_end(ph, work, st);
     if (rc != TPMLP_OK) return rc;
     seg_i += nsegs;
