@@ -151,6 +151,26 @@ int tpmlp_backward(int64_t s, int64_t b, int64_t h, int64_t f, int tp, int sp, i
                    void* dw1, void* dw2, void* du, void* ws, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * tpmlp_backward_main_grad — tpmlp_backward with the weight gradients
+ * accumulated into float32 master-gradient buffers, Megatron's
+ * gradient_accumulation_fusion ("Tensor Parallelism（TP）与 Sequence Parallelism
+ * （SP）", §这组文档怎么读, the ColumnParallelLinear/RowParallelLinear row:
+ * gradient_accumulation_fusion, main_grad):
+ *   main_grad_w1 [f,h] (SwiGLU [2F,h]) float32  += dW1   (input and output)
+ *   main_grad_w2 [h,f]                 float32  += dW2   (input and output)
+ * Each weight-gradient GEMM keeps its float32 accumulator and adds it to
+ * main_grad in its epilogue (one float32 add per element, no rounding to the
+ * storage type first), so gradients of several micro-batches sum in float32.
+ * Every other argument, output and rule is that of tpmlp_backward; the two
+ * main_grad buffers must be 16-byte aligned.  s = 0 leaves them unchanged.
+ * ------------------------------------------------------------------------- */
+int tpmlp_backward_main_grad(int64_t s, int64_t b, int64_t h, int64_t f, int tp, int sp, int dtype,
+                             int act, int mode, const void* const* x, const void* w1,
+                             const void* w2, const void* u, const void* y, const void* const* dz,
+                             void* const* dx, float* main_grad_w1, float* main_grad_w2, void* du,
+                             void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
  * tpmlp_split_dim0 — shard i := full[i·s/tp : (i+1)·s/tp] (each [s/tp,b,h]);
  * an exact copy ("Tensor Parallelism（TP）与 Sequence Parallelism（SP）", §1:
  * the split takes a contiguous slice of the outermost dimension).
@@ -216,6 +236,55 @@ int tpmlp_forward_noalloc(int64_t s, int64_t b, int64_t h, int64_t f, int tp, in
                           int act, int mode, const void* const* x, const void* w1,
                           const void* w2, void* u, void* y, void* const* z, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * The sequence-parallel region around the block ("Sequence Parallel 与 Context
+ * Parallel", §SP：all-gather 进、reduce-scatter 出: LayerNorm → fc1 → act → fc2 →
+ * dropout, LayerNorm and dropout on the [s/tp, b, h] sequence chunks).  Every
+ * tensor argument below is a HOST array of tp device pointers to the chunks
+ * [s/tp, b, h] (row m of the full sequence is chunk m / (s/tp·b)); tp = 1 works
+ * on an unsplit tensor.  s % tp != 0 -> TPMLP_ERR_NOT_DIVISIBLE.
+ *
+ * tpmlp_sp_layernorm_forward — y = (x − μ)/√(σ² + eps)·γ + β per token over h
+ * (σ² without Bessel's correction).  gamma, beta [h] in dtype; mean, rstd [s·b]
+ * float32 outputs kept for the backward.  The y chunks are what tpmlp_forward
+ * takes as its x chunks: its fc1 reads them in place.
+ * ------------------------------------------------------------------------- */
+int tpmlp_sp_layernorm_forward(const void* const* x, const void* gamma, const void* beta, float eps,
+                               void* const* y, float* mean, float* rstd, int64_t s, int64_t b,
+                               int64_t h, int tp, int dtype, void* stream);
+
+/* Bytes of float32 workspace tpmlp_sp_layernorm_backward needs (2·⌈s·b/128⌉·h·4). */
+size_t tpmlp_sp_layernorm_backward_workspace(int64_t s, int64_t b, int64_t h);
+
+/* ---------------------------------------------------------------------------
+ * tpmlp_sp_layernorm_backward — given dy = ∂L/∂y:
+ *   dx = rstd·(g − mean_h(g) − x̂·mean_h(g·x̂)),  g = dy·γ, x̂ = (x − μ)·rstd;
+ *   written to dx (accumulate = 0) or added to it (accumulate = 1: dx holds the
+ *   residual branch's gradient on entry);
+ *   dgamma[h] = Σ_tokens dy·x̂, dbeta[h] = Σ_tokens dy (float32, overwritten;
+ *   partial sums over 128-token blocks added in a fixed order: deterministic).
+ * ws: tpmlp_sp_layernorm_backward_workspace() bytes, 16-byte aligned.
+ * ------------------------------------------------------------------------- */
+int tpmlp_sp_layernorm_backward(const void* const* x, const void* gamma, const float* mean,
+                                const float* rstd, const void* const* dy, void* const* dx,
+                                int accumulate, float* dgamma, float* dbeta, void* ws,
+                                size_t ws_bytes, int64_t s, int64_t b, int64_t h, int tp, int dtype,
+                                void* stream);
+
+/* ---------------------------------------------------------------------------
+ * tpmlp_sp_residual_dropout_forward — out = r + keep·z/(1 − p) on the chunks
+ * after the reduce-scatter; keep: tp chunks of s/tp·b·h bytes, 0 = dropped,
+ * nonzero = kept (the caller draws the mask); 0 <= p < 1.
+ * tpmlp_sp_residual_dropout_backward — dz = keep·dout/(1 − p); the residual
+ * branch's gradient is dout itself.
+ * ------------------------------------------------------------------------- */
+int tpmlp_sp_residual_dropout_forward(const void* const* r, const void* const* z,
+                                      const uint8_t* const* keep, float p, void* const* out,
+                                      int64_t s, int64_t b, int64_t h, int tp, int dtype, void* stream);
+int tpmlp_sp_residual_dropout_backward(const void* const* dout, const uint8_t* const* keep, float p,
+                                       void* const* dz, int64_t s, int64_t b, int64_t h, int tp,
+                                       int dtype, void* stream);
+
 /* Thread-local description of the last non-OK status returned on this thread. */
 const char* tpmlp_last_error(void);
 
@@ -249,10 +318,12 @@ int tpmlp_wait_timeout_selftest(uint64_t timeout_ns, void* stream);
  *   kind 1  float32 CUDA-core GEMM work = 2·M·N·K FLOPs
  *   kind 2  dim-0 chunk copy      work = bytes read + bytes written
  *   kind 3  shard sum             work = tp·n·4 bytes read + n·elem bytes written
+ *   kind 4  SP-region kernels     work = bytes read + bytes written (LayerNorm,
+ *                                 dropout + residual)
  * tpmlp_profile_stop() synchronises the recorded events and fills `out`
  * (out may be NULL to discard).  Recording stays off unless started.
  * ------------------------------------------------------------------------- */
-#define TPMLP_PROFILE_KINDS 4
+#define TPMLP_PROFILE_KINDS 5
 typedef struct tpmlp_profile {
   int launches[TPMLP_PROFILE_KINDS];
   double ms[TPMLP_PROFILE_KINDS];

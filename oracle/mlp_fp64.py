@@ -71,6 +71,10 @@ __all__ = [
     "bf16_bits_to_f32",
     "round_to_storage",
     "sampled_reference",
+    "layernorm_forward",
+    "layernorm_backward",
+    "residual_dropout_forward",
+    "residual_dropout_backward",
 ]
 
 # --------------------------------------------------------------------------
@@ -496,3 +500,54 @@ def sampled_reference(X, W1, W2, dZ, act, rows, feats, chunk=4096):
     dW2_cols = dZf.T @ Yc
     return {"Z_rows": Zr, "dX_rows": dXr, "dW1_rows": dW1_rows, "dW1_row_index": w1_rows,
             "dW2_cols": dW2_cols}
+
+
+# --------------------------------------------------------------------------
+# Sequence-parallel region around the block ("Sequence Parallel 与 Context
+# Parallel", §SP：all-gather 进、reduce-scatter 出: LayerNorm and dropout run on the
+# sequence chunks [s/tp, b, h]; "tensor-parallel-megatron" reading, SP section:
+# LayerNorm, dropout and the residual are split along the sequence).  All of it
+# is token-wise, so the oracle works on full [M, h] tensors; chunking does not
+# change a value.  Reading: the LayerNorm is the standard one over h with affine
+# gamma, beta and variance without Bessel's correction; dropout scales kept
+# values by 1/(1-p) ("inverted" dropout) and its keep-mask is an input.
+# --------------------------------------------------------------------------
+
+
+def layernorm_forward(X, gamma, beta, eps):
+    """y = (x − μ)/√(σ² + eps)·γ + β per row, μ and σ² over the last axis."""
+    X = np.asarray(X, dtype=np.float64)
+    mu = X.mean(axis=-1, keepdims=True)
+    var = ((X - mu) ** 2).mean(axis=-1, keepdims=True)
+    rstd = 1.0 / np.sqrt(var + eps)
+    xhat = (X - mu) * rstd
+    return {"Y": xhat * np.asarray(gamma, dtype=np.float64) + np.asarray(beta, dtype=np.float64),
+            "mean": mu[..., 0], "rstd": rstd[..., 0]}
+
+
+def layernorm_backward(X, gamma, dY, eps):
+    """Gradients of layernorm_forward: dX, dγ = Σ_rows dY·x̂, dβ = Σ_rows dY.
+
+    dX = rstd·(g − mean(g) − x̂·mean(g·x̂)) with g = dY·γ (the gradient through the
+    mean and the variance written out)."""
+    X = np.asarray(X, dtype=np.float64)
+    dY = np.asarray(dY, dtype=np.float64)
+    gamma = np.asarray(gamma, dtype=np.float64)
+    fw = layernorm_forward(X, gamma, np.zeros_like(gamma), eps)
+    rstd = fw["rstd"][..., None]
+    xhat = (X - fw["mean"][..., None]) * rstd
+    g = dY * gamma
+    dX = rstd * (g - g.mean(axis=-1, keepdims=True) - xhat * (g * xhat).mean(axis=-1, keepdims=True))
+    rows = dY.reshape(-1, dY.shape[-1])
+    return {"dX": dX, "dgamma": (rows * xhat.reshape(rows.shape)).sum(axis=0), "dbeta": rows.sum(axis=0)}
+
+
+def residual_dropout_forward(R, Z, keep, p):
+    """out = R + keep·Z/(1 − p); keep ∈ {0, 1} is drawn by the caller."""
+    return np.asarray(R, dtype=np.float64) + np.asarray(keep, dtype=np.float64) * np.asarray(Z, dtype=np.float64) / (1.0 - p)
+
+
+def residual_dropout_backward(dOut, keep, p):
+    """dR = dOut (identity branch), dZ = keep·dOut/(1 − p)."""
+    dOut = np.asarray(dOut, dtype=np.float64)
+    return {"dR": dOut.copy(), "dZ": np.asarray(keep, dtype=np.float64) * dOut / (1.0 - p)}

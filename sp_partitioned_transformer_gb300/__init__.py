@@ -34,6 +34,7 @@ __all__ = [
     "forward_noalloc",
     "NOALLOC_SCRATCH_BYTES",
     "backward",
+    "backward_main_grad",
     "split_dim0",
     "gather_dim0",
     "reduce_scatter_dim0",
@@ -42,6 +43,11 @@ __all__ = [
     "set_wait_timeout_ns",
     "wait_timeout_selftest",
     "abi_version",
+    "sp_layernorm_forward",
+    "sp_layernorm_backward",
+    "sp_layernorm_backward_workspace",
+    "sp_residual_dropout_forward",
+    "sp_residual_dropout_backward",
     "profile_start",
     "profile_stop",
     "PROFILE_KINDS",
@@ -65,13 +71,13 @@ DTYPE_NAMES = {"f32": 0, "f16": 1, "bf16": 2}
 ACT = {"gelu": 0, "swiglu": 1, "identity": 2, "relu": 3}
 MODE = {"partials": 0, "fused": 1}
 
-PROFILE_KINDS = ("gemm_tc", "gemm_f32", "copy_dim0", "shard_sum")
+PROFILE_KINDS = ("gemm_tc", "gemm_f32", "copy_dim0", "shard_sum", "sp_region")
 
 _lib = None
 
 
 class _Profile(ctypes.Structure):
-    _fields_ = [("launches", ctypes.c_int * 4), ("ms", ctypes.c_double * 4), ("work", ctypes.c_double * 4)]
+    _fields_ = [("launches", ctypes.c_int * 5), ("ms", ctypes.c_double * 5), ("work", ctypes.c_double * 5)]
 
 
 class TpmlpError(RuntimeError):
@@ -111,6 +117,9 @@ def load(path: str | None = None):
     lib.tpmlp_backward.restype = i32
     lib.tpmlp_backward.argtypes = [i64, i64, i64, i64, i32, i32, i32, i32, i32,
                                    vpp, vp, vp, vp, vp, vpp, vpp, vp, vp, vp, vp, sz, vp]
+    lib.tpmlp_backward_main_grad.restype = i32
+    lib.tpmlp_backward_main_grad.argtypes = [i64, i64, i64, i64, i32, i32, i32, i32, i32,
+                                             vpp, vp, vp, vp, vp, vpp, vpp, vp, vp, vp, vp, sz, vp]
     lib.tpmlp_split_dim0.restype = i32
     lib.tpmlp_split_dim0.argtypes = [vp, vpp, i64, i64, i64, i32, i32, vp]
     lib.tpmlp_gather_dim0.restype = i32
@@ -126,6 +135,18 @@ def load(path: str | None = None):
     lib.tpmlp_forward_noalloc.restype = i32
     lib.tpmlp_forward_noalloc.argtypes = [i64, i64, i64, i64, i32, i32, i32, i32, i32,
                                           vpp, vp, vp, vp, vp, vpp, vp]
+    f32 = ctypes.c_float
+    lib.tpmlp_sp_layernorm_forward.restype = i32
+    lib.tpmlp_sp_layernorm_forward.argtypes = [vpp, vp, vp, f32, vpp, vp, vp, i64, i64, i64, i32, i32, vp]
+    lib.tpmlp_sp_layernorm_backward_workspace.restype = sz
+    lib.tpmlp_sp_layernorm_backward_workspace.argtypes = [i64, i64, i64]
+    lib.tpmlp_sp_layernorm_backward.restype = i32
+    lib.tpmlp_sp_layernorm_backward.argtypes = [vpp, vp, vp, vp, vpp, vpp, i32, vp, vp, vp, sz, i64, i64, i64, i32,
+                                                i32, vp]
+    lib.tpmlp_sp_residual_dropout_forward.restype = i32
+    lib.tpmlp_sp_residual_dropout_forward.argtypes = [vpp, vpp, vpp, f32, vpp, i64, i64, i64, i32, i32, vp]
+    lib.tpmlp_sp_residual_dropout_backward.restype = i32
+    lib.tpmlp_sp_residual_dropout_backward.argtypes = [vpp, vpp, f32, vpp, i64, i64, i64, i32, i32, vp]
     lib.tpmlp_profile_start.restype = i32
     lib.tpmlp_profile_start.argtypes = []
     lib.tpmlp_profile_stop.restype = i32
@@ -226,6 +247,19 @@ def backward(x, w1, w2, u, y, dz, dx, dw1, dw2, du, *, s, b, h, f, tp, sp, act="
     _check(rc)
 
 
+def backward_main_grad(x, w1, w2, u, y, dz, dx, main_grad_w1, main_grad_w2, du, *, s, b, h, f, tp, sp,
+                       act="gelu", mode="fused", workspace=None, workspace_bytes=None, dtype=None,
+                       stream=None) -> None:
+    """tpmlp_backward with the weight gradients added into float32 main_grad buffers."""
+    dt = _dtype_code(dtype if dtype is not None else w1.dtype)
+    ws_bytes = workspace_bytes if workspace_bytes is not None else (
+        0 if workspace is None or isinstance(workspace, int) else workspace.numel() * workspace.element_size())
+    rc = load().tpmlp_backward_main_grad(s, b, h, f, tp, int(sp), dt, ACT[act], MODE[mode], _ptrs(x), _ptr(w1),
+                                         _ptr(w2), _ptr(u), _ptr(y), _ptrs(dz), _ptrs(dx), _ptr(main_grad_w1),
+                                         _ptr(main_grad_w2), _ptr(du), _ptr(workspace), ws_bytes, _stream(stream))
+    _check(rc)
+
+
 def split_dim0(full, shards, *, s, b, h, tp, dtype=None, stream=None) -> None:
     dt = _dtype_code(dtype if dtype is not None else full.dtype)
     _check(load().tpmlp_split_dim0(_ptr(full), _ptrs(shards), s, b, h, tp, dt, _stream(stream)))
@@ -254,6 +288,49 @@ def set_wait_timeout_ns(ns: int) -> None:
 
 def wait_timeout_selftest(timeout_ns: int, stream=None) -> None:
     _check(load().tpmlp_wait_timeout_selftest(int(timeout_ns), _stream(stream)))
+
+
+def _as_list(t):
+    return list(t) if isinstance(t, (list, tuple)) else [t]
+
+
+def sp_layernorm_forward(x, gamma, beta, eps, y, mean, rstd, *, s, b, h, tp, dtype=None, stream=None) -> None:
+    """LayerNorm over h on the SP chunks (lists of tp [s/tp,b,h] tensors, or one tensor with tp=1)."""
+    xs, ys = _as_list(x), _as_list(y)
+    dt = _dtype_code(dtype if dtype is not None else xs[0].dtype)
+    _check(load().tpmlp_sp_layernorm_forward(_ptrs(xs), _ptr(gamma), _ptr(beta), float(eps), _ptrs(ys), _ptr(mean),
+                                             _ptr(rstd), s, b, h, tp, dt, _stream(stream)))
+
+
+def sp_layernorm_backward_workspace(s, b, h) -> int:
+    return int(load().tpmlp_sp_layernorm_backward_workspace(s, b, h))
+
+
+def sp_layernorm_backward(x, gamma, mean, rstd, dy, dx, dgamma, dbeta, *, s, b, h, tp, accumulate=False,
+                          workspace=None, dtype=None, stream=None) -> None:
+    xs, dys, dxs = _as_list(x), _as_list(dy), _as_list(dx)
+    dt = _dtype_code(dtype if dtype is not None else xs[0].dtype)
+    need = sp_layernorm_backward_workspace(s, b, h)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=xs[0].device)
+    _check(load().tpmlp_sp_layernorm_backward(_ptrs(xs), _ptr(gamma), _ptr(mean), _ptr(rstd), _ptrs(dys),
+                                              _ptrs(dxs), int(accumulate), _ptr(dgamma), _ptr(dbeta),
+                                              _ptr(workspace), workspace.numel() * workspace.element_size(), s, b, h,
+                                              tp, dt, _stream(stream)))
+
+
+def sp_residual_dropout_forward(r, z, keep, p, out, *, s, b, h, tp, dtype=None, stream=None) -> None:
+    rs = _as_list(r)
+    dt = _dtype_code(dtype if dtype is not None else rs[0].dtype)
+    _check(load().tpmlp_sp_residual_dropout_forward(_ptrs(rs), _ptrs(_as_list(z)), _ptrs(_as_list(keep)), float(p),
+                                                    _ptrs(_as_list(out)), s, b, h, tp, dt, _stream(stream)))
+
+
+def sp_residual_dropout_backward(dout, keep, p, dz, *, s, b, h, tp, dtype=None, stream=None) -> None:
+    ds = _as_list(dout)
+    dt = _dtype_code(dtype if dtype is not None else ds[0].dtype)
+    _check(load().tpmlp_sp_residual_dropout_backward(_ptrs(ds), _ptrs(_as_list(keep)), float(p), _ptrs(_as_list(dz)),
+                                                     s, b, h, tp, dt, _stream(stream)))
 
 
 def profile_start() -> None:
@@ -326,6 +403,13 @@ class MLPBlock:
     def forward(self, x, w1, w2, out=None, stream=None):
         out = out or self.alloc_forward()
         forward(x, w1, w2, out["u"], out["y"], out["z"], stream=stream, **self._kw())
+        return out
+
+    def backward_main_grad(self, x, w1, w2, fwd, dz, main_grad_w1, main_grad_w2, out=None, stream=None):
+        """Backward whose weight gradients are added into float32 main_grad buffers."""
+        out = out or self.alloc_backward()
+        backward_main_grad(x, w1, w2, fwd["u"], fwd["y"], dz, out["dx"], main_grad_w1, main_grad_w2, out["du"],
+                           stream=stream, **self._kw())
         return out
 
     def backward(self, x, w1, w2, fwd, dz, out=None, stream=None):

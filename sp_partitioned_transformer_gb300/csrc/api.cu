@@ -118,14 +118,24 @@ struct WsLayout {
   size_t x_off, dz_off, p_off, total;
 };
 
+// SP all-gather fused into the GEMMs' TMA loads: the tensor-core path reads the
+// sequence chunks in place when every chunk is a whole number of 128-row blocks
+// (fc1 and the fc2 input gradient pick a chunk's tensor map per row block; the
+// weight gradients take each chunk as its own K segment).  Otherwise the chunks
+// are first gathered into the workspace by the copy kernel.
+bool fused_gather(const Block& k) {
+  return k.sp && k.dtype != DT_F32 && k.tp <= 16 && ((k.s / k.tp) * k.b) % 128 == 0;
+}
+
 WsLayout ws_layout(const Block& k) {
   WsLayout L{};
   size_t off = 0;
   const size_t act_bytes = static_cast<size_t>(k.M) * k.h * k.e;
+  const bool gathered = k.sp && !fused_gather(k);
   L.x_off = off;
-  if (k.sp) off += align256(act_bytes);
+  if (gathered) off += align256(act_bytes);
   L.dz_off = off;
-  if (k.sp) off += align256(act_bytes);
+  if (gathered) off += align256(act_bytes);
   L.p_off = off;
   if (k.mode == TPMLP_REDUCE_PARTIALS) off += align256(static_cast<size_t>(k.tp) * k.M * k.h * 4);
   L.total = off;
@@ -214,10 +224,44 @@ int gather(const Block& k, const void* const* shards, void* full, cudaStream_t s
   return launch_copy_chunks(shards, dst, k.tp, bytes, st);
 }
 
+// g / f-backward over the float32 partials in the workspace: fixed-order shard
+// sum, rounded once, dim-0 chunks scattered to the SP buffers.
+int shard_sum_partials(const Block& k, void* const* out, void* ws, const WsLayout& L, cudaStream_t st) {
+  return launch_shard_sum(reinterpret_cast<const float*>(wb(ws) + L.p_off), k.tp, k.M * k.h, k.dtype, k.sp,
+                          (k.s / k.tp) * k.b * k.h, out, st);
+}
+
+// A second stream per device, forked from and joined back into the caller's
+// stream with events, so that the HBM-bound shard sum of dX runs alongside the
+// tensor-bound weight-gradient GEMMs (they are independent: the weight
+// gradients need no shard sum).
+struct SideStream {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+std::mutex g_side_mu;
+SideStream g_side[64];
+
+int side_stream_locked(SideStream** out) {
+  int d = 0;
+  cudaError_t e = cudaGetDevice(&d);
+  if (e != cudaSuccess || d < 0 || d >= 64) return set_error(TPMLP_ERR_CUDA, "cudaGetDevice failed");
+  SideStream& ss = g_side[d];
+  if (ss.stream == nullptr) {
+    e = cudaStreamCreateWithFlags(&ss.stream, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming);
+    if (e != cudaSuccess) return set_error(TPMLP_ERR_CUDA, std::string("side stream: ") + cudaGetErrorString(e));
+  }
+  *out = &ss;
+  return TPMLP_OK;
+}
+
 // fc2 forward (P_i = Y_i·B_i) or fc1 input gradient (G_i = dU_i·A_iᵀ) followed by g /
 // f-backward: either float32 partials + shard sum, or the fused K-concatenation.
 int row_parallel_and_reduce(const Block& k, bool is_dgrad, const void* a_act, const void* w,
-                            void* const* out, void* ws, const WsLayout& L, cudaStream_t st) {
+                            void* const* out, void* ws, const WsLayout& L, cudaStream_t st,
+                            bool defer_shard_sum = false) {
   const bool swiglu = k.act == ACT_SWIGLU;
   GemmDesc g;
   g.dtype = k.dtype;
@@ -259,9 +303,8 @@ int row_parallel_and_reduce(const Block& k, bool is_dgrad, const void* a_act, co
     g.epi.ldo = k.h;
     g.epi.part_stride = k.M * k.h;
     int rc = launch_gemm(g, st);
-    if (rc != TPMLP_OK) return rc;
-    return launch_shard_sum(reinterpret_cast<const float*>(wb(ws) + L.p_off), k.tp, k.M * k.h, k.dtype,
-                            k.sp, (k.s / k.tp) * k.b * k.h, out, st);
+    if (rc != TPMLP_OK || defer_shard_sum) return rc;
+    return shard_sum_partials(k, out, ws, L, st);
   }
   g.nparts = 1;
   g.segs.push_back(seg(0, k.f, 0));
@@ -293,6 +336,153 @@ int forward_workspace_bytes(int64_t s, int64_t b, int64_t h, int64_t f, int tp, 
 }  // namespace tpmlp
 
 using namespace tpmlp;
+
+// Backward pass.  main_grad: the weight gradients are added to float32
+// buffers (dw1, dw2 are float*) instead of overwriting storage-type ones.
+static int backward_impl(int64_t s, int64_t b, int64_t h, int64_t f, int tp, int sp, int dtype, int act, int mode,
+                         const void* const* x, const void* w1, const void* w2, const void* u, const void* y,
+                         const void* const* dz, void* const* dx, void* dw1, void* dw2, void* du, void* ws,
+                         size_t ws_bytes, void* stream, bool main_grad) {
+  Block k;
+  int rc = check_block(s, b, h, f, tp, sp, dtype, act, mode, &k);
+  if (rc != TPMLP_OK) return rc;
+  const int nio = sp ? tp : 1;
+  const size_t al = ptr_align(k);
+  if ((rc = check_ptrs(x, nio, al, "x")) || (rc = check_ptr(w1, al, "w1")) || (rc = check_ptr(w2, al, "w2")) ||
+      (rc = check_ptr(u, al, "u")) || (rc = check_ptr(y, al, "y")) || (rc = check_ptrs(dz, nio, al, "dz")) ||
+      (rc = check_ptrs(dx, nio, al, "dx")) || (rc = check_ptr(dw1, main_grad ? 16 : al, "dw1")) ||
+      (rc = check_ptr(dw2, main_grad ? 16 : al, "dw2")) ||
+      (rc = check_ptr(du, al, "du")))
+    return rc;
+  const WsLayout L = ws_layout(k);
+  if (L.total > 0) {
+    if (ws == nullptr || ws_bytes < L.total)
+      return set_error(TPMLP_ERR_WORKSPACE, "workspace needs " + std::to_string(L.total) + " bytes");
+    if ((rc = check_ptr(ws, 256, "ws"))) return rc;
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  DeviceInfo* dev = nullptr;
+  if ((rc = current_device(&dev))) return rc;
+  if (k.M == 0) {
+    // No tokens: the weight gradients are empty sums (nothing to add to main_grad).
+    if (main_grad) return TPMLP_OK;
+    cudaError_t e = cudaMemsetAsync(dw1, 0, static_cast<size_t>(k.n1) * h * k.e, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dw2, 0, static_cast<size_t>(h) * f * k.e, st);
+    if (e != cudaSuccess) return set_error(TPMLP_ERR_CUDA, std::string("cudaMemsetAsync: ") + cudaGetErrorString(e));
+    return TPMLP_OK;
+  }
+  // [SP] g backward = all-gather of dZ; re-gather of X for the weight gradient
+  // (both fused into the GEMMs' loads, or separate copies).
+  const bool fused_ag = fused_gather(k);
+  const int64_t rpc = sp ? (s / tp) * b : k.M;  // rows per sequence chunk
+  const void* dZ = dz[0];
+  const void* X = x[0];
+  if (sp && !fused_ag) {
+    if ((rc = gather(k, dz, wb(ws) + L.dz_off, st))) return rc;
+    if ((rc = gather(k, x, wb(ws) + L.x_off, st))) return rc;
+    dZ = wb(ws) + L.dz_off;
+    X = wb(ws) + L.x_off;
+  }
+  // fc2 input gradient with the activation derivative: dU = act'(U) ⊙ (dZ·W2).
+  {
+    GemmDesc g;
+    g.dtype = dtype;
+    g.M = k.M;
+    g.N = f;
+    g.a_mn = false;
+    g.b_mn = true;  // B(n, k) = W2[k, n]
+    g.lda = h;
+    g.ldb = f;
+    g.b_rows = h;
+    g.nparts = 1;
+    g.segs.push_back(GemmSeg{dZ, w2, h, 0});
+    if (fused_ag) {
+      g.a_chunks.assign(dz, dz + tp);
+      g.a_chunk_rows = rpc;
+    }
+    g.epi.kind = EPI_DACT;
+    g.epi.act = act;
+    g.epi.aux = u;
+    g.epi.ldaux = k.n1;
+    g.epi.out = du;
+    g.epi.ldo = k.n1;
+    g.epi.swiglu_F = act == ACT_SWIGLU ? f : 0;
+    if ((rc = launch_gemm(g, st))) return rc;
+  }
+  auto weight_gradients = [&]() -> int {
+    int rc2 = TPMLP_OK;
+    // fc2 weight gradient: dW2[i, j] = Σ_m dZ[m, i]·Y[m, j]  (dB = Yᵀ·dZ stored transposed).
+    {
+      GemmDesc g;
+      g.dtype = dtype;
+      g.M = h;
+      g.N = f;
+      g.a_mn = true;
+      g.b_mn = true;
+      g.lda = h;
+      g.ldb = f;
+      g.b_rows = f;
+      g.nparts = 1;
+      if (fused_ag) {
+        // K = tokens runs over the SP chunks in rank order: one K segment per chunk.
+        for (int j = 0; j < tp; ++j) g.segs.push_back(GemmSeg{dz[j], cb(y) + j * rpc * f * k.e, rpc, 0});
+      } else {
+        g.segs.push_back(GemmSeg{dZ, y, k.M, 0});
+      }
+      g.epi.kind = main_grad ? EPI_ACC_F32 : EPI_STORE;
+      g.epi.out = dw2;
+      g.epi.ldo = f;
+      if ((rc2 = launch_gemm(g, st))) return rc2;
+    }
+    // fc1 weight gradient: dW1[j, i] = Σ_m dU[m, j]·X[m, i]  (dA = Xᵀ·dU stored transposed).
+    {
+      GemmDesc g;
+      g.dtype = dtype;
+      g.M = k.n1;
+      g.N = h;
+      g.a_mn = true;
+      g.b_mn = true;
+      g.lda = k.n1;
+      g.ldb = h;
+      g.b_rows = h;
+      g.nparts = 1;
+      if (fused_ag) {
+        for (int j = 0; j < tp; ++j) g.segs.push_back(GemmSeg{cb(du) + j * rpc * k.n1 * k.e, x[j], rpc, 0});
+      } else {
+        g.segs.push_back(GemmSeg{du, X, k.M, 0});
+      }
+      g.epi.kind = main_grad ? EPI_ACC_F32 : EPI_STORE;
+      g.epi.out = dw1;
+      g.epi.ldo = h;
+      if ((rc2 = launch_gemm(g, st))) return rc2;
+    }
+
+    return rc2;
+  };
+  if (mode == TPMLP_REDUCE_PARTIALS) {
+    // fc1 input-gradient partials first; their shard sum (f backward) then runs
+    // on a side stream while the weight-gradient GEMMs run on the caller's.
+    if ((rc = row_parallel_and_reduce(k, true, du, w1, dx, ws, L, st, /*defer_shard_sum=*/true))) return rc;
+    std::lock_guard<std::mutex> lk(g_side_mu);
+    SideStream* ss = nullptr;
+    if ((rc = side_stream_locked(&ss))) return rc;
+    cudaError_t e = cudaEventRecord(ss->fork, st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(ss->stream, ss->fork, 0);
+    if (e != cudaSuccess) return set_error(TPMLP_ERR_CUDA, std::string("fork: ") + cudaGetErrorString(e));
+    rc = shard_sum_partials(k, dx, ws, L, ss->stream);
+    e = cudaEventRecord(ss->join, ss->stream);
+    const int rcw = weight_gradients();
+    const cudaError_t e2 = cudaStreamWaitEvent(st, ss->join, 0);  // join, whatever happened above
+    if (rc != TPMLP_OK) return rc;
+    if (rcw != TPMLP_OK) return rcw;
+    if (e != cudaSuccess || e2 != cudaSuccess)
+      return set_error(TPMLP_ERR_CUDA, std::string("join: ") + cudaGetErrorString(e != cudaSuccess ? e : e2));
+    return TPMLP_OK;
+  }
+  if ((rc = weight_gradients())) return rc;
+  // fc1 input gradient + f backward (all-reduce / reduce-scatter).
+  return row_parallel_and_reduce(k, true, du, w1, dx, ws, L, st);
+}
 
 extern "C" {
 
@@ -359,9 +549,11 @@ int tpmlp_forward(int64_t s, int64_t b, int64_t h, int64_t f, int tp, int sp, in
   if ((rc = current_device(&dev))) return rc;
   if (k.M == 0) return TPMLP_OK;
 
-  // [SP] f -> all-gather of the input chunks along dim 0.
+  // [SP] f -> all-gather of the input chunks along dim 0 (fused into fc1's loads,
+  // or a separate copy).
+  const bool fused_ag = fused_gather(k);
   const void* X = x[0];
-  if (sp) {
+  if (sp && !fused_ag) {
     if ((rc = gather(k, x, wb(ws) + L.x_off, st))) return rc;
     X = wb(ws) + L.x_off;
   }
@@ -378,6 +570,10 @@ int tpmlp_forward(int64_t s, int64_t b, int64_t h, int64_t f, int tp, int sp, in
   g1.swiglu_up_row = act == ACT_SWIGLU ? f : 0;
   g1.nparts = 1;
   g1.segs.push_back(GemmSeg{X, w1, h, 0});
+  if (fused_ag) {
+    g1.a_chunks.assign(x, x + tp);
+    g1.a_chunk_rows = (s / tp) * b;
+  }
   g1.epi.kind = EPI_ACT;
   g1.epi.act = act;
   g1.epi.out = u;
@@ -394,101 +590,16 @@ int tpmlp_backward(int64_t s, int64_t b, int64_t h, int64_t f, int tp, int sp, i
                    const void* const* x, const void* w1, const void* w2, const void* u, const void* y,
                    const void* const* dz, void* const* dx, void* dw1, void* dw2, void* du, void* ws,
                    size_t ws_bytes, void* stream) {
-  Block k;
-  int rc = check_block(s, b, h, f, tp, sp, dtype, act, mode, &k);
-  if (rc != TPMLP_OK) return rc;
-  const int nio = sp ? tp : 1;
-  const size_t al = ptr_align(k);
-  if ((rc = check_ptrs(x, nio, al, "x")) || (rc = check_ptr(w1, al, "w1")) || (rc = check_ptr(w2, al, "w2")) ||
-      (rc = check_ptr(u, al, "u")) || (rc = check_ptr(y, al, "y")) || (rc = check_ptrs(dz, nio, al, "dz")) ||
-      (rc = check_ptrs(dx, nio, al, "dx")) || (rc = check_ptr(dw1, al, "dw1")) || (rc = check_ptr(dw2, al, "dw2")) ||
-      (rc = check_ptr(du, al, "du")))
-    return rc;
-  const WsLayout L = ws_layout(k);
-  if (L.total > 0) {
-    if (ws == nullptr || ws_bytes < L.total)
-      return set_error(TPMLP_ERR_WORKSPACE, "workspace needs " + std::to_string(L.total) + " bytes");
-    if ((rc = check_ptr(ws, 256, "ws"))) return rc;
-  }
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  DeviceInfo* dev = nullptr;
-  if ((rc = current_device(&dev))) return rc;
-  if (k.M == 0) {
-    // No tokens: the weight gradients are empty sums.
-    cudaError_t e = cudaMemsetAsync(dw1, 0, static_cast<size_t>(k.n1) * h * k.e, st);
-    if (e == cudaSuccess) e = cudaMemsetAsync(dw2, 0, static_cast<size_t>(h) * f * k.e, st);
-    if (e != cudaSuccess) return set_error(TPMLP_ERR_CUDA, std::string("cudaMemsetAsync: ") + cudaGetErrorString(e));
-    return TPMLP_OK;
-  }
-  // [SP] g backward = all-gather of dZ; re-gather of X for the weight gradient.
-  const void* dZ = dz[0];
-  const void* X = x[0];
-  if (sp) {
-    if ((rc = gather(k, dz, wb(ws) + L.dz_off, st))) return rc;
-    if ((rc = gather(k, x, wb(ws) + L.x_off, st))) return rc;
-    dZ = wb(ws) + L.dz_off;
-    X = wb(ws) + L.x_off;
-  }
-  // fc2 input gradient with the activation derivative: dU = act'(U) ⊙ (dZ·W2).
-  {
-    GemmDesc g;
-    g.dtype = dtype;
-    g.M = k.M;
-    g.N = f;
-    g.a_mn = false;
-    g.b_mn = true;  // B(n, k) = W2[k, n]
-    g.lda = h;
-    g.ldb = f;
-    g.b_rows = h;
-    g.nparts = 1;
-    g.segs.push_back(GemmSeg{dZ, w2, h, 0});
-    g.epi.kind = EPI_DACT;
-    g.epi.act = act;
-    g.epi.aux = u;
-    g.epi.ldaux = k.n1;
-    g.epi.out = du;
-    g.epi.ldo = k.n1;
-    g.epi.swiglu_F = act == ACT_SWIGLU ? f : 0;
-    if ((rc = launch_gemm(g, st))) return rc;
-  }
-  // fc2 weight gradient: dW2[i, j] = Σ_m dZ[m, i]·Y[m, j]  (dB = Yᵀ·dZ stored transposed).
-  {
-    GemmDesc g;
-    g.dtype = dtype;
-    g.M = h;
-    g.N = f;
-    g.a_mn = true;
-    g.b_mn = true;
-    g.lda = h;
-    g.ldb = f;
-    g.b_rows = f;
-    g.nparts = 1;
-    g.segs.push_back(GemmSeg{dZ, y, k.M, 0});
-    g.epi.kind = EPI_STORE;
-    g.epi.out = dw2;
-    g.epi.ldo = f;
-    if ((rc = launch_gemm(g, st))) return rc;
-  }
-  // fc1 weight gradient: dW1[j, i] = Σ_m dU[m, j]·X[m, i]  (dA = Xᵀ·dU stored transposed).
-  {
-    GemmDesc g;
-    g.dtype = dtype;
-    g.M = k.n1;
-    g.N = h;
-    g.a_mn = true;
-    g.b_mn = true;
-    g.lda = k.n1;
-    g.ldb = h;
-    g.b_rows = h;
-    g.nparts = 1;
-    g.segs.push_back(GemmSeg{du, X, k.M, 0});
-    g.epi.kind = EPI_STORE;
-    g.epi.out = dw1;
-    g.epi.ldo = h;
-    if ((rc = launch_gemm(g, st))) return rc;
-  }
-  // fc1 input gradient + f backward (all-reduce / reduce-scatter).
-  return row_parallel_and_reduce(k, true, du, w1, dx, ws, L, st);
+  return backward_impl(s, b, h, f, tp, sp, dtype, act, mode, x, w1, w2, u, y, dz, dx, dw1, dw2, du, ws, ws_bytes,
+                       stream, false);
+}
+
+int tpmlp_backward_main_grad(int64_t s, int64_t b, int64_t h, int64_t f, int tp, int sp, int dtype, int act,
+                             int mode, const void* const* x, const void* w1, const void* w2, const void* u,
+                             const void* y, const void* const* dz, void* const* dx, float* main_grad_w1,
+                             float* main_grad_w2, void* du, void* ws, size_t ws_bytes, void* stream) {
+  return backward_impl(s, b, h, f, tp, sp, dtype, act, mode, x, w1, w2, u, y, dz, dx, main_grad_w1, main_grad_w2,
+                       du, ws, ws_bytes, stream, true);
 }
 
 int tpmlp_split_dim0(const void* full, void* const* shards, int64_t s, int64_t b, int64_t h, int tp, int dtype,

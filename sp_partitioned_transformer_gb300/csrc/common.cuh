@@ -29,7 +29,8 @@ enum EpiKind : int {
   EPI_STORE = 0,  // out[m,n] = C (storage type); optional SP dim-0 scatter of rows
   EPI_F32 = 1,    // out[part][m][n] = C in float32 (one partial sum per tensor shard)
   EPI_ACT = 2,    // out = U = C, out2 = Y = act(C)        (fc1 forward)
-  EPI_DACT = 3    // out = dU = act'(aux = U) ⊙ C           (fc2 input gradient)
+  EPI_DACT = 3,   // out = dU = act'(aux = U) ⊙ C           (fc2 input gradient)
+  EPI_ACC_F32 = 4 // out[m,n] += C in float32 (weight gradient into a float32 main_grad)
 };
 
 struct EpiParams {

@@ -37,6 +37,9 @@ __device__ __forceinline__ void epi_scalar(const Params& p, int64_t m, int64_t n
     case EPI_F32:
       static_cast<float*>(e.out)[static_cast<int64_t>(part) * e.part_stride + m * e.ldo + n] = v;
       return;
+    case EPI_ACC_F32:
+      static_cast<float*>(e.out)[m * e.ldo + n] += v;
+      return;
     case EPI_STORE: {
       float* row;
       if (e.scatter) {

@@ -67,7 +67,12 @@ struct Params {
   int32_t nparts;         // output partials handled by this launch
   int32_t part_base;      // index of this launch's first partial
   int32_t swiglu_up_row;  // > 0: SwiGLU fc1, B rows of the up half start here
-  int32_t pad0;
+  // > 0: a K-major A operand is split along M into chunks of this many rows,
+  // chunk j read through maps[seg.map_a + j] (the SP all-gather fused into the
+  // loads: every 128-row block lies inside one chunk).
+  int32_t a_chunk_rows;
+  int32_t a_nchunks;
+  int32_t pad1;
   unsigned* status;
   uint64_t timeout_ns;
   EpiParams epi;
@@ -93,6 +98,19 @@ __device__ __forceinline__ void epi_chunk(const Params& p, int64_t m, int64_t n0
   using T = typename Storage<DT>::T;
   const EpiParams& e = p.epi;
   const int64_t N = p.N;
+  if (e.kind == EPI_ACC_F32) {
+    float* o = static_cast<float*>(e.out) + m * e.ldo + n0;
+    float4 old[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (n0 + 4 * j < N) old[j] = reinterpret_cast<const float4*>(o)[j];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (n0 + 4 * j < N)
+        reinterpret_cast<float4*>(o)[j] = make_float4(old[j].x + v[4 * j], old[j].y + v[4 * j + 1],
+                                                      old[j].z + v[4 * j + 2], old[j].w + v[4 * j + 3]);
+    return;
+  }
   if (e.kind == EPI_F32) {
     float* o = static_cast<float*>(e.out) + static_cast<int64_t>(part) * e.part_stride + m * e.ldo + n0;
 #pragma unroll
@@ -188,7 +206,16 @@ __device__ __forceinline__ void epi_dact8(const EpiParams& e, int64_t m, int64_t
 template <int TN>
 __device__ __forceinline__ void epi_prefetch_aux(const Params& p, int64_t m, int nb, int elem_bytes) {
   const EpiParams& e = p.epi;
-  if (e.kind != EPI_DACT || m >= p.M) return;
+  if (m >= p.M) return;
+  if (e.kind == EPI_ACC_F32) {  // the float32 main_grad rows this tile will update
+    const char* row = static_cast<const char*>(e.out) + (m * e.ldo + static_cast<int64_t>(nb) * TN) * 4;
+    const int64_t left = (p.N - static_cast<int64_t>(nb) * TN) * 4;
+#pragma unroll
+    for (int b = 0; b < TN * 4 / 128; ++b)
+      if (b * 128 < left) prefetch_l2(row + b * 128);
+    return;
+  }
+  if (e.kind != EPI_DACT) return;
   const char* row = static_cast<const char*>(e.aux) + (m * e.ldaux + static_cast<int64_t>(nb) * TN) * elem_bytes;
   const int64_t left = (p.N - static_cast<int64_t>(nb) * TN) * elem_bytes;
 #pragma unroll
@@ -337,7 +364,14 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
             const uint32_t sb = smem_u32(smem_b + stage * B_BYTES);
             const int k0 = kb * BK;
             if constexpr (!A_MN) {
-              tma_load_2d(sa, ma, fb, k0, mb * BM);
+              if (p.a_chunk_rows > 0) {
+                // rows past M (last tile) read the last chunk out of range: zero fill
+                const int m_off = mb * BM;
+                const int j = min(m_off / p.a_chunk_rows, p.a_nchunks - 1);
+                tma_load_2d(sa, ma + j, fb, k0, m_off - j * p.a_chunk_rows);
+              } else {
+                tma_load_2d(sa, ma, fb, k0, mb * BM);
+              }
             } else {
               tma_load_2d(sa, ma, fb, mb * BM, k0);
               tma_load_2d(sa + MN_BOX_BYTES, ma, fb, mb * BM + 64, k0);
@@ -564,7 +598,12 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
             const uint32_t sb = smem_u32(smem_b + stage * PB_BYTES);
             const int k0 = kb * BK;
             if constexpr (!A_MN) {
-              tma_load_2d_pair(sa, ma, fb, k0, m_off);
+              if (p.a_chunk_rows > 0) {
+                // rows past M (last tile) read the last chunk out of range: zero fill
+                const int j = min(m_off / p.a_chunk_rows, p.a_nchunks - 1);
+                tma_load_2d_pair(sa, ma + j, fb, k0, m_off - j * p.a_chunk_rows);
+              } else
+                tma_load_2d_pair(sa, ma, fb, k0, m_off);
             } else {
               tma_load_2d_pair(sa, ma, fb, m_off, k0);
               tma_load_2d_pair(sa + MN_BOX_BYTES, ma, fb, m_off + 64, k0);
@@ -811,6 +850,10 @@ int launch_gemm_tc(const GemmDesc& g, cudaStream_t st) {
   if (g.M >= (1ll << 31) || g.N >= (1ll << 31)) return set_error(TPMLP_ERR_UNSUPPORTED, "GEMM extent >= 2^31");
   const bool swiglu = g.swiglu_up_row > 0;
   if (swiglu && (g.a_mn || g.b_mn)) return set_error(TPMLP_ERR_UNSUPPORTED, "SwiGLU pairing needs K-major operands");
+  const bool chunked = g.a_chunk_rows > 0;
+  if (chunked && (g.a_mn || g.a_chunk_rows % BM != 0 || g.a_chunks.empty() ||
+                  static_cast<int64_t>(g.a_chunks.size()) * g.a_chunk_rows != g.M))
+    return set_error(TPMLP_ERR_UNSUPPORTED, "chunked A needs K-major chunks of a multiple of 128 rows covering M");
 
   // CTA pairs (256-row tiles) whenever there is more than one 128-row block.
   const bool pair = g.M > BM;
@@ -825,6 +868,8 @@ int launch_gemm_tc(const GemmDesc& g, cudaStream_t st) {
   const int tile_n = swiglu ? tn / 2 : tn;
   p.nt = static_cast<int32_t>((g.N + tile_n - 1) / tile_n);
   p.swiglu_up_row = static_cast<int32_t>(g.swiglu_up_row);
+  p.a_chunk_rows = chunked ? static_cast<int32_t>(g.a_chunk_rows) : 0;
+  p.a_nchunks = chunked ? static_cast<int32_t>(g.a_chunks.size()) : 0;
   p.status = dev->status;
   p.timeout_ns = wait_timeout_ns();
   p.epi = g.epi;
@@ -834,7 +879,7 @@ int launch_gemm_tc(const GemmDesc& g, cudaStream_t st) {
   const int nseg = static_cast<int>(g.segs.size());
   int part = 0;
   while (part < g.nparts) {
-    int nparts = 0, nsegs = 0;
+    int nparts = 0, nsegs = 0, nmaps = 0;
     p.part_base = part;
     p.seg_begin[0] = 0;
     while (part < g.nparts && nparts < MAX_PARTS) {
@@ -845,24 +890,35 @@ int launch_gemm_tc(const GemmDesc& g, cudaStream_t st) {
         if (nparts == 0) return set_error(TPMLP_ERR_UNSUPPORTED, "too many K segments in one partial");
         break;
       }
+      const int chunks = chunked ? static_cast<int>(g.a_chunks.size()) : 1;
+      if (nmaps + cnt * (chunks + 1) > MAX_MAPS) {
+        if (nparts == 0) return set_error(TPMLP_ERR_UNSUPPORTED, "too many tensor maps in one partial");
+        break;
+      }
       for (int c = 0; c < cnt; ++c) {
         const GemmSeg& s = g.segs[seg_i + nsegs + c];
         if (s.k <= 0 || s.k >= (1ll << 31)) return set_error(TPMLP_ERR_INVALID_ARG, "bad K segment");
         const int idx = nsegs + c;
         Seg& d = p.segs[idx];
-        d.map_a = 2 * idx;
-        d.map_b = 2 * idx + 1;
         d.k_len = static_cast<int32_t>(s.k);
-        if (!g.a_mn)
-          rc = make_map(&p.maps[d.map_a], g.dtype, s.a, s.k, g.M, g.lda, BK, BM);
-        else
-          rc = make_map(&p.maps[d.map_a], g.dtype, s.a, g.M, s.k, g.lda, 64, BK);
+        d.map_a = nmaps;
+        if (chunked) {
+          for (int j = 0; j < chunks; ++j) {
+            rc = make_map(&p.maps[nmaps++], g.dtype, g.a_chunks[j], s.k, g.a_chunk_rows, g.lda, BK, BM);
+            if (rc != TPMLP_OK) return rc;
+          }
+        } else if (!g.a_mn) {
+          rc = make_map(&p.maps[nmaps++], g.dtype, s.a, s.k, g.M, g.lda, BK, BM);
+        } else {
+          rc = make_map(&p.maps[nmaps++], g.dtype, s.a, g.M, s.k, g.lda, 64, BK);
+        }
         if (rc != TPMLP_OK) return rc;
+        d.map_b = nmaps;
         if (!g.b_mn)
-          rc = make_map(&p.maps[d.map_b], g.dtype, s.b, s.k, g.b_rows, g.ldb, BK,
+          rc = make_map(&p.maps[nmaps++], g.dtype, s.b, s.k, g.b_rows, g.ldb, BK,
                         static_cast<uint32_t>(pair ? tn / 2 : (swiglu ? BN / 2 : BN)));
         else
-          rc = make_map(&p.maps[d.map_b], g.dtype, s.b, g.N, s.k, g.ldb, 64, BK);
+          rc = make_map(&p.maps[nmaps++], g.dtype, s.b, g.N, s.k, g.ldb, 64, BK);
         if (rc != TPMLP_OK) return rc;
       }
       nsegs += cnt;

@@ -50,6 +50,11 @@ struct GemmDesc {
   int64_t swiglu_up_row = 0;  // > 0: SwiGLU fc1 pairing
   int nparts = 1;
   std::vector<GemmSeg> segs;
+  // Optional: a K-major A split along M into equal chunks of a_chunk_rows rows
+  // (sequence-parallel chunks read in place: the all-gather fused into the GEMM).
+  // Tensor-core path only; the segments' `a` pointers are then ignored.
+  std::vector<const void*> a_chunks;
+  int64_t a_chunk_rows = 0;
   EpiParams epi{};
 };
 
@@ -71,9 +76,20 @@ int launch_shard_sum(const float* partials, int tp, int64_t n, int dtype, int sc
 
 int launch_wait_selftest(unsigned* status, uint64_t timeout_ns, cudaStream_t st);
 
+// Sequence-parallel region (sp_region.cu); x/y/dy/dx are nchunks chunk pointers
+// of rpc rows each (M = nchunks·rpc rows of h).
+int launch_ln_forward(const void* const* x, const void* gamma, const void* beta, float eps, void* const* y,
+                      float* mean, float* rstd, int64_t M, int64_t h, int64_t rpc, int nchunks, int dtype,
+                      cudaStream_t st);
+int launch_ln_backward(const void* const* x, const void* gamma, const float* mean, const float* rstd,
+                       const void* const* dy, void* const* dx, int accumulate, float* dgamma, float* dbeta,
+                       float* part, int64_t M, int64_t h, int64_t rpc, int nchunks, int dtype, cudaStream_t st);
+int launch_residual_dropout(bool forward, const void* const* r, const void* const* z, const uint8_t* const* keep,
+                            float p, void* const* out, int64_t n_chunk, int nchunks, int dtype, cudaStream_t st);
+
 // Launch accounting (tpmlp_profile_start/stop): bracket one kernel launch with
 // CUDA events on its stream.  prof_begin returns -1 when accounting is off.
-enum ProfKind : int { PROF_GEMM_TC = 0, PROF_GEMM_SIMT = 1, PROF_COPY = 2, PROF_SHARD_SUM = 3 };
+enum ProfKind : int { PROF_GEMM_TC = 0, PROF_GEMM_SIMT = 1, PROF_COPY = 2, PROF_SHARD_SUM = 3, PROF_SP_REGION = 4 };
 int prof_begin(int kind, cudaStream_t st);
 void prof_end(int handle, double work, cudaStream_t st);
 

@@ -118,3 +118,18 @@ def fp32_partials(tp: int, rows: int, cols: int, seed: int) -> torch.Tensor:
     """Random fp32 partial sums [tp, rows, cols] ~ N(0, 1) for the shard-sum kernels."""
     g = torch.Generator().manual_seed(seed)
     return torch.randn(tp, rows, cols, generator=g)
+
+
+def sp_region_inputs(s: int, b: int, h: int, p: float, seed: int, dtype: str = "bf16") -> dict[str, torch.Tensor]:
+    """Residual stream R [s,b,h] ~ N(0,1)·2 + 0.5, LayerNorm γ ~ 1 + N(0,0.1), β ~ N(0,0.1),
+    and a dropout keep-mask (uint8, 1 = kept with probability 1 - p) for the
+    sequence-parallel region around the block."""
+    g = torch.Generator().manual_seed(seed)
+    dt = TORCH_DTYPES[dtype]
+    return {
+        "R": (torch.randn(s, b, h, generator=g) * 2 + 0.5).to(dt),
+        "gamma": (1 + 0.1 * torch.randn(h, generator=g)).to(dt),
+        "beta": (0.1 * torch.randn(h, generator=g)).to(dt),
+        "keep": (torch.rand(s, b, h, generator=g) >= p).to(torch.uint8),
+        "dOut": torch.randn(s, b, h, generator=g).to(dt),
+    }

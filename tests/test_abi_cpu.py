@@ -47,11 +47,18 @@ def _ws(lib, *a):
 
 
 def test_workspace_size_formula(lib):
-    # [s,b,h] = [512,4,1024], f=4096, tp=4, SP, bf16: gathered X and dZ, each M·h·2 bytes
+    # [s,b,h] = [512,4,1024], f=4096, tp=4, SP, bf16: 512-row sequence chunks are read in
+    # place by the GEMMs (all-gather fused into the loads), so no gather buffers ...
     M, h = 512 * 4, 1024
-    assert _ws(lib, 512, 4, 1024, 4096, 4, 1, 2, 0, 1) == 2 * M * h * 2
-    # + tp float32 partials in PARTIALS mode
-    assert _ws(lib, 512, 4, 1024, 4096, 4, 1, 2, 0, 0) == 2 * M * h * 2 + 4 * M * h * 4
+    assert _ws(lib, 512, 4, 1024, 4096, 4, 1, 2, 0, 1) == 0
+    # ... and PARTIALS mode needs only the tp float32 partials
+    assert _ws(lib, 512, 4, 1024, 4096, 4, 1, 2, 0, 0) == 4 * M * h * 4
+    # 96-row chunks (not whole 128-row blocks): gathered X and dZ, each M·h·2 bytes
+    M2, h2 = 96 * 2, 136
+    g = ((M2 * h2 * 2 + 255) // 256) * 256
+    assert _ws(lib, 96, 2, 136, 272, 2, 1, 2, 0, 1) == 2 * g
+    # float32 path always gathers
+    assert _ws(lib, 512, 4, 1024, 4096, 4, 1, 0, 0, 1) == 2 * M * h * 4
     # SP off, fused: no workspace
     assert _ws(lib, 1024, 8, 3072, 12288, 8, 0, 1, 0, 1) == 0
     # invalid -> 0 with a message

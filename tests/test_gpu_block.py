@@ -70,17 +70,27 @@ def test_tensor_core_path_exact_on_integer_data(cuda_lib, dt, s, b, h, f, act, m
         assert np.array_equal(out[k], ref[k]), k
 
 
+# (s, b, h, f, tp): 64-row chunks -> the SP chunks are gathered by the copy kernel;
+# 128-row chunks -> the all-gather is fused into the GEMMs' loads; 3 chunks of 128
+# rows -> M = 384, so the last 256-row tile's second half starts past M.
+SP_SHAPES = [(128, 2, 256, 512, 4), (256, 2, 256, 512, 4), (192, 2, 256, 288, 3)]
+
+
 @pytest.mark.parametrize("dt", ["bf16", "f16", "f32"])
 @pytest.mark.parametrize("act", ["gelu", "swiglu"])
 @pytest.mark.parametrize("mode", ["fused", "partials"])
-def test_sp_on_and_off_are_bit_identical(cuda_lib, dt, act, mode):
-    """AG → block → RS equals block → all-reduce → split, bit for bit."""
-    cfg = _cfg(128, 2, 256, 512, 4, False, dt, act)
+@pytest.mark.parametrize("shape", SP_SHAPES, ids=["gathered", "fused-gather", "fused-gather-3chunks"])
+def test_sp_on_and_off_are_bit_identical(cuda_lib, dt, act, mode, shape):
+    """AG → block → RS equals block → all-reduce → split, bit for bit, whether the
+    all-gather is a separate copy or fused into the GEMM loads."""
+    s, b, h, f, tp = shape
+    cfg = _cfg(s, b, h, f, tp, False, dt, act)
     inp = block_inputs(cfg)
-    a = run_block(cuda_lib, inp, 128, 2, 256, 512, 4, False, act, mode, DT[dt])
-    c = run_block(cuda_lib, inp, 128, 2, 256, 512, 4, True, act, mode, DT[dt])
+    a = run_block(cuda_lib, inp, s, b, h, f, tp, False, act, mode, DT[dt])
+    c = run_block(cuda_lib, inp, s, b, h, f, tp, True, act, mode, DT[dt])
     for k in ("Z", "dX", "dW1", "dW2", "U", "Y", "dU"):
         assert np.array_equal(a[k], c[k]), k
+    assert_block_close(c, oracle_block(inp, act), DT[dt])
 
 
 @pytest.mark.parametrize("act", ["gelu", "swiglu"])

@@ -358,3 +358,79 @@ def test_sampled_reference_matches_full_oracle(act):
     np.testing.assert_allclose(s["dX_rows"], full["dX"][rows], rtol=1e-12, atol=1e-12)
     np.testing.assert_allclose(s["dW1_rows"], full["dW1"][s["dW1_row_index"]], rtol=1e-12, atol=1e-12)
     np.testing.assert_allclose(s["dW2_cols"], full["dW2"][:, feats], rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("act", ["gelu", "swiglu"])
+def test_weight_gradients_accumulate_over_micro_batches(act):
+    """Gradient accumulation (main_grad): the loss of two micro-batches is the sum of
+    their losses, so dW of the concatenated batch equals the sum of the two dW."""
+    rng = np.random.default_rng(12)
+    h, f = 8, 12
+    n1 = 2 * f if act == "swiglu" else f
+    W1 = rng.standard_normal((n1, h)) * 0.5
+    W2 = rng.standard_normal((h, f)) * 0.5
+    X1, X2 = rng.standard_normal((5, h)), rng.standard_normal((7, h))
+    dZ1, dZ2 = rng.standard_normal((5, h)), rng.standard_normal((7, h))
+    g1 = O.mlp_backward(X1, W1, W2, dZ1, act)
+    g2 = O.mlp_backward(X2, W1, W2, dZ2, act)
+    g = O.mlp_backward(np.vstack([X1, X2]), W1, W2, np.vstack([dZ1, dZ2]), act)
+    np.testing.assert_allclose(g1["dW1"] + g2["dW1"], g["dW1"], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(g1["dW2"] + g2["dW2"], g["dW2"], rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------- SP region: LayerNorm, dropout + residual
+
+
+def test_layernorm_forward_closed_forms():
+    rng = np.random.default_rng(13)
+    X = rng.standard_normal((6, 16)) * 3 + 1.5
+    out = O.layernorm_forward(X, np.ones(16), np.zeros(16), 0.0)
+    # normalised rows have mean 0 and (population) variance 1
+    np.testing.assert_allclose(out["Y"].mean(-1), 0, atol=1e-12)
+    np.testing.assert_allclose((out["Y"] ** 2).mean(-1), 1, atol=1e-12)
+    # affine part and statistics against numpy's own routines
+    g, b = rng.standard_normal(16), rng.standard_normal(16)
+    o2 = O.layernorm_forward(X, g, b, 1e-5)
+    np.testing.assert_allclose(o2["mean"], np.mean(X, -1), rtol=1e-14)
+    np.testing.assert_allclose(o2["rstd"], 1 / np.sqrt(np.var(X, -1) + 1e-5), rtol=1e-14)
+    # a constant row maps to beta (x − μ = 0)
+    c = O.layernorm_forward(np.full((1, 16), 7.0), g, b, 1e-5)
+    np.testing.assert_allclose(c["Y"][0], b, atol=1e-12)
+    # shift invariance
+    np.testing.assert_allclose(O.layernorm_forward(X + 10.0, g, b, 1e-5)["Y"], o2["Y"], atol=1e-9)
+
+
+def test_layernorm_backward_finite_differences():
+    rng = np.random.default_rng(14)
+    X = rng.standard_normal((3, 8))
+    g, b = rng.standard_normal(8), rng.standard_normal(8)
+    dY = rng.standard_normal((3, 8))
+    eps = 1e-3
+    gr = O.layernorm_backward(X, g, dY, eps)
+
+    def loss(X_, g_, b_):
+        return float(np.sum(O.layernorm_forward(X_, g_, b_, eps)["Y"] * dY))
+
+    h = 1e-6
+    for name, T, grad in (("X", X, gr["dX"]), ("g", g, gr["dgamma"]), ("b", b, gr["dbeta"])):
+        fd = np.zeros_like(T)
+        for idx in np.ndindex(*T.shape):
+            Tp, Tm = T.copy(), T.copy()
+            Tp[idx] += h
+            Tm[idx] -= h
+            args_p = {"X": X, "g": g, "b": b}
+            args_m = dict(args_p)
+            args_p[name], args_m[name] = Tp, Tm
+            fd[idx] = (loss(args_p["X"], args_p["g"], args_p["b"]) - loss(args_m["X"], args_m["g"], args_m["b"])) / (2 * h)
+        np.testing.assert_allclose(grad, fd, rtol=1e-6, atol=1e-7, err_msg=name)
+
+
+def test_residual_dropout_closed_forms():
+    R = np.array([[1.0, 2.0, 3.0, 4.0]])
+    Z = np.array([[10.0, 20.0, 30.0, 40.0]])
+    keep = np.array([[1, 0, 1, 0]])
+    out = O.residual_dropout_forward(R, Z, keep, 0.5)
+    assert np.array_equal(out, np.array([[21.0, 2.0, 63.0, 4.0]]))
+    assert np.array_equal(O.residual_dropout_forward(R, Z, np.ones_like(keep), 0.0), R + Z)
+    bw = O.residual_dropout_backward(np.ones((1, 4)), keep, 0.5)
+    assert np.array_equal(bw["dZ"], np.array([[2.0, 0.0, 2.0, 0.0]])) and np.array_equal(bw["dR"], np.ones((1, 4)))

@@ -18,7 +18,7 @@ from synthetic import CONFIGS, BlockConfig, block_inputs
 pytestmark = pytest.mark.gpu
 
 CASES = [
-    # TP+SP config, PARTIALS mode: gathered X and dZ regions + tp fp32 partials (≈42 MB of scratch)
+    # TP+SP config, PARTIALS mode: tp fp32 partials (≈34 MB of scratch)
     (CONFIGS["tpsp4_bf16"], "partials"),
     (CONFIGS["tpsp4_bf16"], "fused"),
     # SwiGLU with SP, ragged shapes, fp16
