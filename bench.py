@@ -50,6 +50,11 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--main-grad", action="store_true",
+                    help="weight gradients accumulated into float32 main_grad (gradient-accumulation fusion)")
+    ap.add_argument("--sp-region", action="store_true",
+                    help="time the whole SP sublayer: LayerNorm on the chunks -> block -> dropout + residual, "
+                         "and its backward (FLOPs counted are the block's)")
     return ap.parse_args(argv)
 
 
@@ -364,9 +369,56 @@ def run_ours(args) -> int:
     bw = blk.alloc_backward()
     stream = torch.cuda.current_stream(dev)
 
-    def step():
-        blk.forward(x, W1, W2, out=fw, stream=stream)
-        blk.backward(x, W1, W2, fw, dz, out=bw, stream=stream)
+    mg1 = mg2 = None
+    if args.main_grad:
+        mg1 = torch.zeros(cfg.fc1_rows, cfg.h, dtype=torch.float32, device=dev)
+        mg2 = torch.zeros(cfg.h, cfg.f, dtype=torch.float32, device=dev)
+
+    def block_step(xin, dzin):
+        blk.forward(xin, W1, W2, out=fw, stream=stream)
+        if args.main_grad:
+            blk.backward_main_grad(xin, W1, W2, fw, dzin, mg1, mg2, out=bw, stream=stream)
+        else:
+            blk.backward(xin, W1, W2, fw, dzin, out=bw, stream=stream)
+
+    if args.sp_region:
+        if not cfg.sp:
+            raise SystemExit("--sp-region needs an SP workload")
+        from synthetic import sp_region_inputs
+
+        reg = sp_region_inputs(cfg.s, cfg.b, cfg.h, 0.1, seed=cfg.seed + 1, dtype=cfg.dtype)
+        R = [c.contiguous() for c in reg["R"].to(dev).chunk(cfg.tp)]
+        keep = [c.contiguous() for c in reg["keep"].to(dev).chunk(cfg.tp)]
+        dOut = [c.contiguous() for c in reg["dOut"].to(dev).chunk(cfg.tp)]
+        gamma, beta = reg["gamma"].to(dev), reg["beta"].to(dev)
+        ln_out = [torch.empty_like(c) for c in R]
+        mean = torch.empty(cfg.M, device=dev)
+        rstd = torch.empty(cfg.M, device=dev)
+        out = [torch.empty_like(c) for c in R]
+        dZs = [torch.empty_like(c) for c in R]
+        dgam = torch.empty(cfg.h, device=dev)
+        dbet = torch.empty(cfg.h, device=dev)
+        ln_ws = torch.empty(max(16, tpmlp.sp_layernorm_backward_workspace(cfg.s, cfg.b, cfg.h)), dtype=torch.uint8,
+                            device=dev)
+        kw = dict(s=cfg.s, b=cfg.b, h=cfg.h, tp=cfg.tp, stream=stream)
+
+        def step():
+            tpmlp.sp_layernorm_forward(R, gamma, beta, 1e-5, ln_out, mean, rstd, **kw)
+            blk.forward(ln_out, W1, W2, out=fw, stream=stream)
+            tpmlp.sp_residual_dropout_forward(R, fw["z"], keep, 0.1, out, **kw)
+            tpmlp.sp_residual_dropout_backward(dOut, keep, 0.1, dZs, **kw)
+            if args.main_grad:
+                blk.backward_main_grad(ln_out, W1, W2, fw, dZs, mg1, mg2, out=bw, stream=stream)
+            else:
+                blk.backward(ln_out, W1, W2, fw, dZs, out=bw, stream=stream)
+            # dR = dOut (residual branch) + LayerNorm backward, accumulated in place into
+            # the incoming-gradient chunks as a training step would (their values drift
+            # from step to step; timing does not depend on values)
+            tpmlp.sp_layernorm_backward(R, gamma, mean, rstd, bw["dx"], dOut, dgam, dbet, accumulate=True,
+                                        workspace=ln_ws, **kw)
+    else:
+        def step():
+            block_step(x, dz)
 
     def barrier():
         torch.cuda.synchronize(dev)
@@ -400,7 +452,7 @@ def run_ours(args) -> int:
 
     # ------------------------------------------------ end to end through the public API
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not args.sp_region:
         pin = lambda t: t.cpu().pin_memory()  # noqa: E731
         xh = [pin(c) for c in x] if cfg.sp else [pin(x)]
         dzh = [pin(c) for c in dz] if cfg.sp else [pin(dz)]
@@ -512,6 +564,7 @@ def run_ours(args) -> int:
         "dtype": cfg.dtype,
         "data": "synthetic",
         "config": {**workload_desc(cfg), "reduce": args.mode,
+                   "variant": ("sp-sublayer " if args.sp_region else "") + ("main_grad" if args.main_grad else "block"),
                    "l2": f"inputs larger than L2: W1 and W2 are {cfg.fc1_rows * cfg.h * ebytes / 1e6:.0f} and "
                          f"{cfg.h * cfg.f * ebytes / 1e6:.0f} MB, no flush",
                    "flops_per_step": flops,
