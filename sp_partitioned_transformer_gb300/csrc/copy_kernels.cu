@@ -44,6 +44,47 @@ __global__ void __launch_bounds__(256) copy_chunks_kernel(ChunkPtrs p, int64_t n
   for (; i < nvec; i += stride) d[i] = __ldcs(s + i);
 }
 
+// TMA bulk copy: one thread per CTA streams 32 KB slabs global -> shared ->
+// global with cp.async.bulk (double-buffered, completion on an mbarrier for the
+// load, bulk-group accounting for the store).  Address generation is left to
+// the TMA unit; three such CTAs per SM keep enough bytes in flight.
+constexpr int BULK_SLAB = 32768;
+
+__global__ void __launch_bounds__(32) copy_chunks_bulk_kernel(ChunkPtrs p, int64_t bytes, int64_t slabs_per_chunk,
+                                                              int64_t total_slabs, unsigned* status,
+                                                              uint64_t timeout_ns) {
+  extern __shared__ __align__(128) uint8_t slab[];
+  __shared__ __align__(8) uint64_t bar[2];
+  if (threadIdx.x != 0) return;
+  mbar_init(smem_u32(&bar[0]), 1);
+  mbar_init(smem_u32(&bar[1]), 1);
+  fence_barrier_init();
+  uint32_t phase[2] = {0u, 0u};
+  int buf = 0;
+  for (int64_t t = blockIdx.x; t < total_slabs; t += gridDim.x) {
+    const int64_t j = t / slabs_per_chunk;
+    const int64_t off = (t - j * slabs_per_chunk) * BULK_SLAB;
+    const int64_t left = bytes - off;
+    const uint32_t len = static_cast<uint32_t>(left < BULK_SLAB ? left : BULK_SLAB);
+    const uint32_t s = smem_u32(slab + buf * BULK_SLAB);
+    const uint32_t b = smem_u32(&bar[buf]);
+    // the bulk store issued from this buffer two slabs ago has finished reading it
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+    mbar_arrive_expect_tx(b, len);
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(s),
+                 "l"(static_cast<const uint8_t*>(p.src[j]) + off), "r"(len), "r"(b)
+                 : "memory");
+    if (!mbar_wait_bounded(b, phase[buf], nullptr, status, timeout_ns)) break;
+    phase[buf] ^= 1u;
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(static_cast<uint8_t*>(p.dst[j]) + off),
+                 "r"(s), "r"(len)
+                 : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    buf ^= 1;
+  }
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 // Byte copy for sizes or addresses that are not even 4-byte aligned.
 __global__ void __launch_bounds__(256) copy_chunks_bytes(ChunkPtrs p, int64_t n) {
   const uint8_t* __restrict__ s = static_cast<const uint8_t*>(p.src[blockIdx.y]);
@@ -74,11 +115,23 @@ int launch_copy_chunks(const void* const* src, void* const* dst, int n, int64_t 
     p.dst[j] = dst[j];
     align_or |= reinterpret_cast<uintptr_t>(src[j]) | reinterpret_cast<uintptr_t>(dst[j]);
   }
+  DeviceInfo* dev = nullptr;
+  int rc = current_device(&dev);
+  if (rc != TPMLP_OK) return rc;
   const int ph = prof_begin(PROF_COPY, st);
   if ((align_or & 15u) == 0) {
-    const int64_t nvec = bytes / 16;
-    dim3 grid(grid_for(nvec, n, 256, 4), n);
-    copy_chunks_kernel<uint4><<<grid, 256, 0, st>>>(p, nvec);
+    // 16-byte aligned chunks: TMA bulk copies, 3 single-thread CTAs per SM
+    static bool attr_set[64] = {};
+    if (dev->device >= 0 && dev->device < 64 && !attr_set[dev->device]) {
+      const cudaError_t e = cudaFuncSetAttribute(copy_chunks_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 2 * BULK_SLAB);
+      if (e != cudaSuccess) return set_error(TPMLP_ERR_CUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
+      attr_set[dev->device] = true;
+    }
+    const int64_t spc = (bytes + BULK_SLAB - 1) / BULK_SLAB;
+    const int64_t total = spc * n;
+    const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(total, 3 * dev->num_sms)));
+    copy_chunks_bulk_kernel<<<grid, 32, 2 * BULK_SLAB, st>>>(p, bytes, spc, total, dev->status, wait_timeout_ns());
   } else if ((align_or & 3u) == 0) {
     const int64_t nvec = bytes / 4;
     dim3 grid(grid_for(nvec, n, 256, 4), n);

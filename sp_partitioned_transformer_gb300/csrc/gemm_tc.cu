@@ -98,19 +98,6 @@ __device__ __forceinline__ void epi_chunk(const Params& p, int64_t m, int64_t n0
   using T = typename Storage<DT>::T;
   const EpiParams& e = p.epi;
   const int64_t N = p.N;
-  if (e.kind == EPI_ACC_F32) {
-    float* o = static_cast<float*>(e.out) + m * e.ldo + n0;
-    float4 old[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-      if (n0 + 4 * j < N) old[j] = reinterpret_cast<const float4*>(o)[j];
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-      if (n0 + 4 * j < N)
-        reinterpret_cast<float4*>(o)[j] = make_float4(old[j].x + v[4 * j], old[j].y + v[4 * j + 1],
-                                                      old[j].z + v[4 * j + 2], old[j].w + v[4 * j + 3]);
-    return;
-  }
   if (e.kind == EPI_F32) {
     float* o = static_cast<float*>(e.out) + static_cast<int64_t>(part) * e.part_stride + m * e.ldo + n0;
 #pragma unroll
@@ -278,6 +265,40 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, uint32_t trow, in
         cur[j] = nxt[j];
         curup[j] = nxtup[j];
       }
+    }
+    return;
+  }
+  if (e.kind == EPI_ACC_F32) {
+    // main_grad += C: the float32 row segment of chunk c+1 is loaded while chunk
+    // c is added and stored (read-modify-write of the same elements by the same
+    // thread, so L2-coherent loads rather than the read-only path).
+    float* orow = static_cast<float*>(e.out) + m * e.ldo;
+    const int64_t nbase = static_cast<int64_t>(nb) * TN;
+    float4 cur[8], nxt[8];
+    auto load = [&](int c, float4* dst) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int64_t n = nbase + c * 32 + 4 * j;
+        if (row_ok && n < p.N) dst[j] = __ldcg(reinterpret_cast<const float4*>(orow + n));
+      }
+    };
+    load(0, cur);
+#pragma unroll 1
+    for (int c = 0; c < TN / 32; ++c) {
+      if (c + 1 < TN / 32) load(c + 1, nxt);
+      float v[32];
+      tmem_ld32(trow + c * 32, v);
+      if (row_ok) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int64_t n = nbase + c * 32 + 4 * j;
+          if (n < p.N)
+            *reinterpret_cast<float4*>(orow + n) =
+                make_float4(cur[j].x + v[4 * j], cur[j].y + v[4 * j + 1], cur[j].z + v[4 * j + 2], cur[j].w + v[4 * j + 3]);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) cur[j] = nxt[j];
     }
     return;
   }

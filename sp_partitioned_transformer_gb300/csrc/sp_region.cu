@@ -132,6 +132,200 @@ __global__ void __launch_bounds__(256) ln_fwd_kernel(ChunkSet cs, const void* __
   }
 }
 
+// ------------------------------------------------------------------ row-resident variants
+// One CTA of 256 threads per token row, the row held in registers (up to
+// RV vectors of 8 elements per thread: h <= 8192), block-wide reductions: every
+// load of the row is in flight at once and the row is read from HBM once.
+constexpr int RV = 4;
+
+__device__ __forceinline__ float block_sum(float v, float* red) {
+  v = warp_sum(v);
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();  // previous use of red[] finished
+  if (lane == 0) red[w] = v;
+  __syncthreads();
+  float t = lane < (blockDim.x >> 5) ? red[lane] : 0.0f;
+  return warp_sum(t);
+}
+
+// The row stays packed in its storage type (16 registers for 32 bf16 values per
+// thread) so that four or more CTAs fit per SM: enough bytes in flight.
+template <int DT>
+struct Packed8 {
+  uint4 w[DT == DT_F32 ? 2 : 1];
+  __device__ __forceinline__ void load(const void* p, int64_t i) {
+    if constexpr (DT == DT_F32) {
+      w[0] = *reinterpret_cast<const uint4*>(static_cast<const float*>(p) + i);
+      w[1] = *reinterpret_cast<const uint4*>(static_cast<const float*>(p) + i + 4);
+    } else {
+      w[0] = *reinterpret_cast<const uint4*>(static_cast<const typename Storage<DT>::T*>(p) + i);
+    }
+  }
+  __device__ __forceinline__ void unpack(float* v) const {
+    if constexpr (DT == DT_F32) {
+      memcpy(v, &w[0], 16);
+      memcpy(v + 4, &w[1], 16);
+    } else {
+      unpack8<DT>(w[0], v);
+    }
+  }
+};
+
+template <int DT>
+__global__ void __launch_bounds__(256, 4) ln_fwd_row_kernel(ChunkSet cs, const void* __restrict__ gamma,
+                                                            const void* __restrict__ beta, float eps,
+                                                            float* __restrict__ mean, float* __restrict__ rstd,
+                                                            int64_t h, int64_t rpc) {
+  __shared__ float red[8];
+  const int64_t m = blockIdx.x;
+  const int64_t j = m / rpc;
+  const int64_t off = (m - j * rpc) * h;
+  const void* x = cs.in[j];
+  void* y = cs.out[j];
+  const int nv = static_cast<int>(h / 8);
+  Packed8<DT> raw[RV];
+#pragma unroll
+  for (int k = 0; k < RV; ++k)
+    if (threadIdx.x + k * 256 < nv) raw[k].load(x, off + (threadIdx.x + k * 256) * 8);
+  float sum = 0.0f;
+#pragma unroll
+  for (int k = 0; k < RV; ++k)
+    if (threadIdx.x + k * 256 < nv) {
+      float v[8];
+      raw[k].unpack(v);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) sum += v[i];
+    }
+  const float inv_h = 1.0f / static_cast<float>(h);
+  const float mu = block_sum(sum, red) * inv_h;
+  float q = 0.0f;
+#pragma unroll
+  for (int k = 0; k < RV; ++k)
+    if (threadIdx.x + k * 256 < nv) {
+      float v[8];
+      raw[k].unpack(v);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) q += (v[i] - mu) * (v[i] - mu);
+    }
+  const float r = 1.0f / sqrtf(block_sum(q, red) * inv_h + eps);
+#pragma unroll
+  for (int k = 0; k < RV; ++k) {
+    const int vi = threadIdx.x + k * 256;
+    if (vi < nv) {
+      float v[8], g[8], b[8], o[8];
+      raw[k].unpack(v);
+      ld8<DT>(gamma, vi * 8, g);
+      ld8<DT>(beta, vi * 8, b);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) o[i] = (v[i] - mu) * r * g[i] + b[i];
+      st8<DT>(y, off + vi * 8, o);
+    }
+  }
+  if (threadIdx.x == 0) {
+    mean[m] = mu;
+    rstd[m] = r;
+  }
+}
+
+template <int DT>
+__global__ void __launch_bounds__(256, 3) ln_bwd_row_kernel(ChunkSet cs, const void* __restrict__ gamma,
+                                                            const float* __restrict__ mean,
+                                                            const float* __restrict__ rstd, int accumulate, int64_t h,
+                                                            int64_t rpc) {
+  __shared__ float red[8];
+  const int64_t m = blockIdx.x;
+  const int64_t j = m / rpc;
+  const int64_t off = (m - j * rpc) * h;
+  const void* x = cs.in[j];
+  const void* dy = cs.in2[j];
+  void* dx = cs.out[j];
+  const float mu = mean[m], r = rstd[m];
+  const int nv = static_cast<int>(h / 8);
+  Packed8<DT> rx[RV], rd[RV];
+#pragma unroll
+  for (int k = 0; k < RV; ++k)
+    if (threadIdx.x + k * 256 < nv) {
+      rx[k].load(x, off + (threadIdx.x + k * 256) * 8);
+      rd[k].load(dy, off + (threadIdx.x + k * 256) * 8);
+    }
+  float sg = 0.0f, sgx = 0.0f;
+#pragma unroll
+  for (int k = 0; k < RV; ++k) {
+    const int vi = threadIdx.x + k * 256;
+    if (vi < nv) {
+      float xv[8], d[8], g[8];
+      rx[k].unpack(xv);
+      rd[k].unpack(d);
+      ld8<DT>(gamma, vi * 8, g);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float gi = d[i] * g[i];
+        sg += gi;
+        sgx += gi * (xv[i] - mu) * r;
+      }
+    }
+  }
+  const float inv_h = 1.0f / static_cast<float>(h);
+  const float mg = block_sum(sg, red) * inv_h;
+  const float mgx = block_sum(sgx, red) * inv_h;
+#pragma unroll
+  for (int k = 0; k < RV; ++k) {
+    const int vi = threadIdx.x + k * 256;
+    if (vi < nv) {
+      float xv[8], d[8], g[8], o[8];
+      rx[k].unpack(xv);
+      rd[k].unpack(d);
+      ld8<DT>(gamma, vi * 8, g);
+      if (accumulate) ld8<DT>(dx, off + vi * 8, o);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float t = r * (d[i] * g[i] - mg - (xv[i] - mu) * r * mgx);
+        o[i] = accumulate ? o[i] + t : t;
+      }
+      st8<DT>(dx, off + vi * 8, o);
+    }
+  }
+}
+
+constexpr int VCOL_ROWS = 16;  // tokens per dγ/dβ partial in the vectorised column kernel
+
+// Eight consecutive columns per thread, VCOL_ROWS tokens per CTA row block; the
+// block's chunk is computed once when chunks are whole numbers of blocks.
+template <int DT>
+__global__ void __launch_bounds__(256) ln_bwd_cols_vec_kernel(ChunkSet cs, const float* __restrict__ mean,
+                                                              const float* __restrict__ rstd, float* __restrict__ part,
+                                                              int64_t M, int64_t h, int64_t rpc, int64_t nrb) {
+  const int64_t c = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 8;
+  const int64_t rb = blockIdx.y;
+  if (c >= h) return;
+  const int64_t m0 = rb * VCOL_ROWS, m1 = min(M, m0 + VCOL_ROWS);
+  const bool one_chunk = (rpc % VCOL_ROWS) == 0;
+  const int64_t j0 = m0 / rpc;
+  float ag[8], ab[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) ag[i] = ab[i] = 0.0f;
+#pragma unroll 4
+  for (int64_t m = m0; m < m1; ++m) {
+    const int64_t jj = one_chunk ? j0 : m / rpc;
+    const int64_t idx = (m - jj * rpc) * h + c;
+    float d[8], xv[8];
+    ld8<DT>(cs.in2[jj], idx, d);
+    ld8<DT>(cs.in[jj], idx, xv);
+    const float mu = mean[m], r = rstd[m];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      ag[i] += d[i] * (xv[i] - mu) * r;
+      ab[i] += d[i];
+    }
+  }
+  float* pg = part + rb * h + c;
+  float* pb = part + (nrb + rb) * h + c;
+  *reinterpret_cast<float4*>(pg) = make_float4(ag[0], ag[1], ag[2], ag[3]);
+  *reinterpret_cast<float4*>(pg + 4) = make_float4(ag[4], ag[5], ag[6], ag[7]);
+  *reinterpret_cast<float4*>(pb) = make_float4(ab[0], ab[1], ab[2], ab[3]);
+  *reinterpret_cast<float4*>(pb + 4) = make_float4(ab[4], ab[5], ab[6], ab[7]);
+}
+
 // ------------------------------------------------------------------ LN backward
 // cs.in = x chunks, cs.in2 = dy chunks, cs.out = dx chunks.
 template <int DT, bool VEC>
@@ -246,22 +440,37 @@ __global__ void __launch_bounds__(256) residual_dropout_kernel(ChunkSet cs, floa
 
 template <int DT, bool FWD>
 __global__ void __launch_bounds__(256) residual_dropout_vec8_kernel(ChunkSet cs, float scale, int64_t n_chunk) {
+  constexpr int U = 4;  // vectors of 8 elements in flight per thread
   const int j = blockIdx.y;
   const uint8_t* keep = static_cast<const uint8_t*>(cs.mask[j]);
+  const int64_t nvec = n_chunk / 8;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t v = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; v < n_chunk / 8; v += stride) {
-    const int64_t e = v * 8;
-    float z[8], r[8], o[8];
-    ld8<DT>(cs.in2[j], e, z);
-    if (FWD) ld8<DT>(cs.in[j], e, r);
-    const uint2 k8 = *reinterpret_cast<const uint2*>(keep + e);
-    const uint8_t* kb = reinterpret_cast<const uint8_t*>(&k8);
+  for (int64_t v0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; v0 < nvec; v0 += U * stride) {
+    float z[U][8], r[U][8];
+    uint2 k8[U];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float kz = kb[i] ? z[i] * scale : 0.0f;
-      o[i] = FWD ? r[i] + kz : kz;
+    for (int u = 0; u < U; ++u) {
+      const int64_t v = v0 + u * stride;
+      if (v < nvec) {
+        ld8<DT>(cs.in2[j], v * 8, z[u]);
+        if (FWD) ld8<DT>(cs.in[j], v * 8, r[u]);
+        k8[u] = *reinterpret_cast<const uint2*>(keep + v * 8);
+      }
     }
-    st8<DT>(cs.out[j], e, o);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t v = v0 + u * stride;
+      if (v < nvec) {
+        const uint8_t* kb = reinterpret_cast<const uint8_t*>(&k8[u]);
+        float o[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float kz = kb[i] ? z[u][i] * scale : 0.0f;
+          o[i] = FWD ? r[u][i] + kz : kz;
+        }
+        st8<DT>(cs.out[j], v * 8, o);
+      }
+    }
   }
 }
 
@@ -302,11 +511,18 @@ int launch_ln_forward(const void* const* x, const void* gamma, const void* beta,
                                   (8 * e)) == 0;
   const int grid = static_cast<int>((M + ROWS_PER_CTA - 1) / ROWS_PER_CTA);
   const int ph = prof_begin(PROF_SP_REGION, st);
+  if (vec && h <= 256 * 8 * RV) {
+    const unsigned rows = static_cast<unsigned>(M);
+    if (dtype == DT_F32) ln_fwd_row_kernel<DT_F32><<<rows, 256, 0, st>>>(cs, gamma, beta, eps, mean, rstd, h, rpc);
+    else if (dtype == DT_F16) ln_fwd_row_kernel<DT_F16><<<rows, 256, 0, st>>>(cs, gamma, beta, eps, mean, rstd, h, rpc);
+    else ln_fwd_row_kernel<DT_BF16><<<rows, 256, 0, st>>>(cs, gamma, beta, eps, mean, rstd, h, rpc);
+  } else {
 #define LNF(D, V) ln_fwd_kernel<D, V><<<grid, 256, 0, st>>>(cs, gamma, beta, eps, mean, rstd, M, h, rpc)
-  if (dtype == DT_F32) { if (vec) LNF(DT_F32, true); else LNF(DT_F32, false); }
-  else if (dtype == DT_F16) { if (vec) LNF(DT_F16, true); else LNF(DT_F16, false); }
-  else { if (vec) LNF(DT_BF16, true); else LNF(DT_BF16, false); }
+    if (dtype == DT_F32) { if (vec) LNF(DT_F32, true); else LNF(DT_F32, false); }
+    else if (dtype == DT_F16) { if (vec) LNF(DT_F16, true); else LNF(DT_F16, false); }
+    else { if (vec) LNF(DT_BF16, true); else LNF(DT_BF16, false); }
 #undef LNF
+  }
   prof_end(ph, static_cast<double>(M) * h * e * 2 + 8.0 * M, st);
   return check_launch("LayerNorm forward");
 }
@@ -331,22 +547,41 @@ int launch_ln_backward(const void* const* x, const void* gamma, const float* mea
                                    align_bits(const_cast<const void* const*>(dx), nchunks) |
                                    reinterpret_cast<uintptr_t>(gamma)) % (8 * e)) == 0;
   const int grid = static_cast<int>((M + ROWS_PER_CTA - 1) / ROWS_PER_CTA);
+  const bool row_resident = vec && h <= 256 * 8 * RV;
   int ph = prof_begin(PROF_SP_REGION, st);
+  if (row_resident) {
+    const unsigned rows = static_cast<unsigned>(M);
+    if (dtype == DT_F32) ln_bwd_row_kernel<DT_F32><<<rows, 256, 0, st>>>(cs, gamma, mean, rstd, accumulate, h, rpc);
+    else if (dtype == DT_F16) ln_bwd_row_kernel<DT_F16><<<rows, 256, 0, st>>>(cs, gamma, mean, rstd, accumulate, h, rpc);
+    else ln_bwd_row_kernel<DT_BF16><<<rows, 256, 0, st>>>(cs, gamma, mean, rstd, accumulate, h, rpc);
+  } else {
 #define LNB(D, V) ln_bwd_rows_kernel<D, V><<<grid, 256, 0, st>>>(cs, gamma, mean, rstd, accumulate, M, h, rpc)
-  if (dtype == DT_F32) { if (vec) LNB(DT_F32, true); else LNB(DT_F32, false); }
-  else if (dtype == DT_F16) { if (vec) LNB(DT_F16, true); else LNB(DT_F16, false); }
-  else { if (vec) LNB(DT_BF16, true); else LNB(DT_BF16, false); }
+    if (dtype == DT_F32) { if (vec) LNB(DT_F32, true); else LNB(DT_F32, false); }
+    else if (dtype == DT_F16) { if (vec) LNB(DT_F16, true); else LNB(DT_F16, false); }
+    else { if (vec) LNB(DT_BF16, true); else LNB(DT_BF16, false); }
 #undef LNB
+  }
   prof_end(ph, static_cast<double>(M) * h * e * (accumulate ? 4 : 3) + 8.0 * M, st);
   int rc = check_launch("LayerNorm backward (rows)");
   if (rc != TPMLP_OK) return rc;
-  dim3 g2(static_cast<unsigned>((h + 255) / 256), static_cast<unsigned>(nrb));
   ph = prof_begin(PROF_SP_REGION, st);
-  if (dtype == DT_F32) ln_bwd_cols_kernel<DT_F32><<<g2, 256, 0, st>>>(cs, mean, rstd, part, M, h, rpc, nrb);
-  else if (dtype == DT_F16) ln_bwd_cols_kernel<DT_F16><<<g2, 256, 0, st>>>(cs, mean, rstd, part, M, h, rpc, nrb);
-  else ln_bwd_cols_kernel<DT_BF16><<<g2, 256, 0, st>>>(cs, mean, rstd, part, M, h, rpc, nrb);
-  ln_bwd_reduce_kernel<<<static_cast<unsigned>((h + 255) / 256), 256, 0, st>>>(part, dgamma, dbeta, h, nrb);
-  prof_end(ph, static_cast<double>(M) * h * e * 2 + 16.0 * nrb * h, st);
+  if (vec) {
+    // vectorised column pass: 8 columns per thread, 32-token blocks
+    const int64_t nrb_v = (M + VCOL_ROWS - 1) / VCOL_ROWS;
+    dim3 g2(static_cast<unsigned>((h / 8 + 255) / 256), static_cast<unsigned>(nrb_v));
+    if (dtype == DT_F32) ln_bwd_cols_vec_kernel<DT_F32><<<g2, 256, 0, st>>>(cs, mean, rstd, part, M, h, rpc, nrb_v);
+    else if (dtype == DT_F16) ln_bwd_cols_vec_kernel<DT_F16><<<g2, 256, 0, st>>>(cs, mean, rstd, part, M, h, rpc, nrb_v);
+    else ln_bwd_cols_vec_kernel<DT_BF16><<<g2, 256, 0, st>>>(cs, mean, rstd, part, M, h, rpc, nrb_v);
+    ln_bwd_reduce_kernel<<<static_cast<unsigned>((h + 255) / 256), 256, 0, st>>>(part, dgamma, dbeta, h, nrb_v);
+    prof_end(ph, static_cast<double>(M) * h * e * 2 + 16.0 * nrb_v * h, st);
+  } else {
+    dim3 g2(static_cast<unsigned>((h + 255) / 256), static_cast<unsigned>(nrb));
+    if (dtype == DT_F32) ln_bwd_cols_kernel<DT_F32><<<g2, 256, 0, st>>>(cs, mean, rstd, part, M, h, rpc, nrb);
+    else if (dtype == DT_F16) ln_bwd_cols_kernel<DT_F16><<<g2, 256, 0, st>>>(cs, mean, rstd, part, M, h, rpc, nrb);
+    else ln_bwd_cols_kernel<DT_BF16><<<g2, 256, 0, st>>>(cs, mean, rstd, part, M, h, rpc, nrb);
+    ln_bwd_reduce_kernel<<<static_cast<unsigned>((h + 255) / 256), 256, 0, st>>>(part, dgamma, dbeta, h, nrb);
+    prof_end(ph, static_cast<double>(M) * h * e * 2 + 16.0 * nrb * h, st);
+  }
   return check_launch("LayerNorm backward (gamma, beta)");
 }
 
@@ -366,8 +601,9 @@ int launch_residual_dropout(bool forward, const void* const* r, const void* cons
   if (forward) al |= align_bits(r, nchunks);
   const bool vec = n_chunk % 8 == 0 && (al % (8 * e)) == 0 &&
                    (align_bits(reinterpret_cast<const void* const*>(keep), nchunks) % 8) == 0;
-  // about 8 CTAs per SM in total over the nchunks rows of the grid
-  const int per_chunk = std::max(1, grid_1d(vec ? n_chunk / 8 : n_chunk, 256) / nchunks);
+  // about 8 CTAs per SM in total over the nchunks rows of the grid (the vector
+  // kernel handles four 8-element vectors per thread per iteration)
+  const int per_chunk = std::max(1, grid_1d(vec ? n_chunk / 32 : n_chunk, 256) / nchunks);
   dim3 grid(static_cast<unsigned>(per_chunk), static_cast<unsigned>(nchunks));
   const int ph = prof_begin(PROF_SP_REGION, st);
 #define RD(D, F)                                                                        \
@@ -437,7 +673,7 @@ int tpmlp_sp_layernorm_forward(const void* const* x, const void* gamma, const vo
 
 size_t tpmlp_sp_layernorm_backward_workspace(int64_t s, int64_t b, int64_t h) {
   if (s < 0 || b < 0 || h <= 0) return 0;
-  const int64_t nrb = (s * b + 127) / 128;
+  const int64_t nrb = (s * b + 15) / 16;  // 16-token partial blocks (the 128-token variant needs less)
   return static_cast<size_t>(2 * nrb * h) * sizeof(float);
 }
 

@@ -22,7 +22,7 @@ def _flat(t):
 
 
 @pytest.mark.parametrize("dt", ["f32", "bf16", "f16"])
-@pytest.mark.parametrize("s,b,h,tp", [(64, 2, 136, 2), (9, 1, 5, 3), (512, 4, 1024, 4), (16, 2, 64, 1)])
+@pytest.mark.parametrize("s,b,h,tp", [(64, 2, 136, 2), (9, 1, 5, 3), (512, 4, 1024, 4), (16, 2, 64, 1), (24, 1, 64, 2)])
 def test_layernorm_forward_and_backward(cuda_lib, dt, s, b, h, tp):
     tpmlp = cuda_lib
     inp = sp_region_inputs(s, b, h, 0.1, seed=s + h, dtype=dt)
