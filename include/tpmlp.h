@@ -253,7 +253,7 @@ int tpmlp_sp_layernorm_forward(const void* const* x, const void* gamma, const vo
                                void* const* y, float* mean, float* rstd, int64_t s, int64_t b,
                                int64_t h, int tp, int dtype, void* stream);
 
-/* Bytes of float32 workspace tpmlp_sp_layernorm_backward needs (2·⌈s·b/16⌉·h·4). */
+/* Bytes of float32 workspace tpmlp_sp_layernorm_backward needs (2·⌈s·b/8⌉·h·4). */
 size_t tpmlp_sp_layernorm_backward_workspace(int64_t s, int64_t b, int64_t h);
 
 /* ---------------------------------------------------------------------------
@@ -262,7 +262,8 @@ size_t tpmlp_sp_layernorm_backward_workspace(int64_t s, int64_t b, int64_t h);
  *   written to dx (accumulate = 0) or added to it (accumulate = 1: dx holds the
  *   residual branch's gradient on entry);
  *   dgamma[h] = Σ_tokens dy·x̂, dbeta[h] = Σ_tokens dy (float32, overwritten;
- *   partial sums over 16- or 128-token blocks added in a fixed order: deterministic).
+ *   partial sums over fixed sets of tokens, added in a fixed order: the same
+ *   bits on every call with the same shapes on the same device).
  * ws: tpmlp_sp_layernorm_backward_workspace() bytes, 16-byte aligned.
  * ------------------------------------------------------------------------- */
 int tpmlp_sp_layernorm_backward(const void* const* x, const void* gamma, const float* mean,

@@ -56,12 +56,16 @@ int current_device(DeviceInfo** out) {
     if (e != cudaSuccess) return set_error(TPMLP_ERR_CUDA, std::string("cudaDeviceGetAttribute: ") + cudaGetErrorString(e));
     e = cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, d);
     if (e != cudaSuccess) return set_error(TPMLP_ERR_CUDA, std::string("cudaDeviceGetAttribute: ") + cudaGetErrorString(e));
+    int smem_sm = 0;
+    e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, d);
+    if (e != cudaSuccess) return set_error(TPMLP_ERR_CUDA, std::string("cudaDeviceGetAttribute: ") + cudaGetErrorString(e));
     void* addr = nullptr;
     e = cudaGetSymbolAddress(&addr, g_status_word);
     if (e != cudaSuccess) return set_error(TPMLP_ERR_CUDA, std::string("cudaGetSymbolAddress: ") + cudaGetErrorString(e));
     info.status = static_cast<unsigned*>(addr);
     info.num_sms = sms;
     info.max_smem_optin = static_cast<size_t>(smem);
+    info.smem_per_sm = static_cast<size_t>(smem_sm);
     info.device = d;
   }
   *out = &info;
@@ -74,6 +78,7 @@ struct ProfRec {
   int kind;
   int ev0, ev1;
   double work;
+  int kernels;
 };
 thread_local bool g_prof_on = false;
 thread_local std::vector<ProfRec> g_prof_recs;
@@ -89,13 +94,14 @@ int prof_begin(int kind, cudaStream_t st) {
     g_prof_events.push_back(e);
   }
   if (cudaEventRecord(g_prof_events[2 * n], st) != cudaSuccess) return -1;
-  g_prof_recs.push_back(ProfRec{kind, 2 * n, 2 * n + 1, 0.0});
+  g_prof_recs.push_back(ProfRec{kind, 2 * n, 2 * n + 1, 0.0, 1});
   return n;
 }
 
-void prof_end(int handle, double work, cudaStream_t st) {
+void prof_end(int handle, double work, cudaStream_t st, int kernels) {
   if (handle < 0 || handle >= static_cast<int>(g_prof_recs.size())) return;
   g_prof_recs[handle].work = work;
+  g_prof_recs[handle].kernels = kernels;
   cudaEventRecord(g_prof_events[g_prof_recs[handle].ev1], st);
 }
 
@@ -509,7 +515,7 @@ int tpmlp_profile_stop(tpmlp_profile* out) {
       rc = set_error(TPMLP_ERR_CUDA, std::string("profile events: ") + cudaGetErrorString(e));
       continue;
     }
-    acc.launches[r.kind] += 1;
+    acc.launches[r.kind] += r.kernels;
     acc.ms[r.kind] += ms;
     acc.work[r.kind] += r.work;
   }

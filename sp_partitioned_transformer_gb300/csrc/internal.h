@@ -21,6 +21,7 @@ struct DeviceInfo {
   int num_sms = 0;
   unsigned* status = nullptr;  // device address of the status word
   size_t max_smem_optin = 0;
+  size_t smem_per_sm = 0;  // shared memory of one SM (all resident CTAs)
 };
 // Returns TPMLP_OK and fills `info` for the current device.
 int current_device(DeviceInfo** info);
@@ -87,10 +88,11 @@ int launch_ln_backward(const void* const* x, const void* gamma, const float* mea
 int launch_residual_dropout(bool forward, const void* const* r, const void* const* z, const uint8_t* const* keep,
                             float p, void* const* out, int64_t n_chunk, int nchunks, int dtype, cudaStream_t st);
 
-// Launch accounting (tpmlp_profile_start/stop): bracket one kernel launch with
+// Launch accounting (tpmlp_profile_start/stop): bracket one or more kernel launches with
 // CUDA events on its stream.  prof_begin returns -1 when accounting is off.
 enum ProfKind : int { PROF_GEMM_TC = 0, PROF_GEMM_SIMT = 1, PROF_COPY = 2, PROF_SHARD_SUM = 3, PROF_SP_REGION = 4 };
 int prof_begin(int kind, cudaStream_t st);
-void prof_end(int handle, double work, cudaStream_t st);
+// `kernels` is the number of kernel launches the region enclosed.
+void prof_end(int handle, double work, cudaStream_t st, int kernels = 1);
 
 }  // namespace tpmlp

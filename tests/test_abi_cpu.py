@@ -46,6 +46,18 @@ def _ws(lib, *a):
     return lib.tpmlp_workspace_size(*a)
 
 
+def test_layernorm_backward_workspace_formula(lib):
+    """2·⌈s·b/8⌉·h float32 partial rows: room for one dγ and one dβ partial per
+    CTA of the streamed pass (at most one CTA per 8 tokens)."""
+    f = lib.tpmlp_sp_layernorm_backward_workspace
+    f.restype = ctypes.c_size_t
+    f.argtypes = [ctypes.c_int64] * 3
+    assert f(4096, 1, 6144) == 2 * 512 * 6144 * 4
+    assert f(9, 1, 5) == 2 * 2 * 5 * 4
+    assert f(0, 1, 64) == 0
+    assert f(-1, 1, 64) == 0
+
+
 def test_workspace_size_formula(lib):
     # [s,b,h] = [512,4,1024], f=4096, tp=4, SP, bf16: 512-row sequence chunks are read in
     # place by the GEMMs (all-gather fused into the loads), so no gather buffers ...

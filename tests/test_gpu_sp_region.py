@@ -21,8 +21,16 @@ def _flat(t):
     return to_np(t).reshape(-1, t.shape[-1])
 
 
+# Shapes: warp-per-row kernels (h < 1024, or rows not a whole number of
+# 8-element vectors) and the streamed kernels (h >= 1024) with 1..4 vectors per
+# thread, a ragged last vector column (h = 2056: 257 vectors), fewer rows than
+# CTAs, and the widest ring (h = 8192).
+LN_SHAPES = [(64, 2, 136, 2), (9, 1, 5, 3), (512, 4, 1024, 4), (16, 2, 64, 1), (24, 1, 64, 2),
+             (40, 2, 2056, 4), (48, 1, 6144, 2), (9, 1, 1032, 3), (24, 1, 8192, 3), (6, 1, 1030, 3)]
+
+
 @pytest.mark.parametrize("dt", ["f32", "bf16", "f16"])
-@pytest.mark.parametrize("s,b,h,tp", [(64, 2, 136, 2), (9, 1, 5, 3), (512, 4, 1024, 4), (16, 2, 64, 1), (24, 1, 64, 2)])
+@pytest.mark.parametrize("s,b,h,tp", LN_SHAPES)
 def test_layernorm_forward_and_backward(cuda_lib, dt, s, b, h, tp):
     tpmlp = cuda_lib
     inp = sp_region_inputs(s, b, h, 0.1, seed=s + h, dtype=dt)
@@ -133,3 +141,44 @@ def test_sp_mlp_sublayer_end_to_end(cuda_lib, act, mode):
     assert rel_err(to_np(bw["dw1"]), mb["dW1"]) <= tol
     assert rel_err(to_np(bw["dw2"]), mb["dW2"]) <= tol
     assert M == len(mean)
+
+
+def test_sp_region_at_the_22b_width(cuda_lib):
+    """LayerNorm forward/backward (accumulating into the residual gradient) and
+    dropout + residual on the [4096, 1, 6144] bf16 residual stream in 8 sequence
+    chunks — the shapes the benchmark's SP-region step runs — against the oracle,
+    every element."""
+    tpmlp = cuda_lib
+    s, b, h, tp, p = 4096, 1, 6144, 8, 0.1
+    inp = sp_region_inputs(s, b, h, p, seed=61)
+    Z = block_inputs(BlockConfig("z", s, b, h, 8 * tp, tp, True, "bf16", "gelu", seed=62))["X"]
+    dev = "cuda"
+    R = chunks(inp["R"].to(dev), tp)
+    gamma, beta = inp["gamma"].to(dev), inp["beta"].to(dev)
+    M = s * b
+    mean, rstd = torch.empty(M, device=dev), torch.empty(M, device=dev)
+    Y = [torch.empty_like(c) for c in R]
+    tpmlp.sp_layernorm_forward(R, gamma, beta, EPS, Y, mean, rstd, s=s, b=b, h=h, tp=tp)
+    dY = chunks(inp["dOut"].to(dev), tp)
+    dR = [torch.ones_like(c) for c in R]
+    dg, db = torch.empty(h, device=dev), torch.empty(h, device=dev)
+    tpmlp.sp_layernorm_backward(R, gamma, mean, rstd, dY, dR, dg, db, s=s, b=b, h=h, tp=tp, accumulate=True)
+    keep = chunks(inp["keep"].to(dev), tp)
+    out = [torch.empty_like(c) for c in R]
+    tpmlp.sp_residual_dropout_forward(R, chunks(Z.to(dev), tp), keep, p, out, s=s, b=b, h=h, tp=tp)
+    dz = [torch.empty_like(c) for c in R]
+    tpmlp.sp_residual_dropout_backward(dY, keep, p, dz, s=s, b=b, h=h, tp=tp)
+    torch.cuda.synchronize()
+    assert tpmlp.device_status() == 0
+    R64, g64 = _flat(inp["R"]), to_np(inp["gamma"])
+    ref = O.layernorm_forward(R64, g64, to_np(inp["beta"]), EPS)
+    assert rel_err(_flat(torch.cat(Y)), ref["Y"]) <= 2e-2
+    assert rel_err(to_np(mean), ref["mean"]) <= 1e-5
+    assert rel_err(to_np(rstd), ref["rstd"]) <= 1e-5
+    rb = O.layernorm_backward(R64, g64, _flat(inp["dOut"]), EPS)
+    assert rel_err(_flat(torch.cat(dR)), rb["dX"] + 1.0) <= 2e-2
+    assert rel_err(to_np(dg), rb["dgamma"]) <= 2e-2
+    assert rel_err(to_np(db), rb["dbeta"]) <= 2e-2
+    keep64 = _flat(inp["keep"])
+    assert rel_err(_flat(torch.cat(out)), O.residual_dropout_forward(R64, _flat(Z), keep64, p)) <= 2e-2
+    assert rel_err(_flat(torch.cat(dz)), O.residual_dropout_backward(_flat(inp["dOut"]), keep64, p)["dZ"]) <= 2e-2
