@@ -1,4 +1,4 @@
-"""CPU oracle of the tensor/sequence-parallel MLP block (TEST INFRASTRUCTURE ONLY).
+"""CPU oracle of the tensor/sequence-parallel MLP and attention blocks (TEST INFRASTRUCTURE ONLY).
 
 Plain NumPy float64 (plus a few float32 helpers where the method fixes float32
 arithmetic: the fixed-order shard sum and the final rounding).  Nothing here is
@@ -12,8 +12,10 @@ Pages followed (cited by title and section):
 * "tensor-parallel-megatron" visual reading (blog.vllbc.top)
 * "Sequence Parallel 与 Context Parallel" (blog.vllbc.top)
 
-Every function is pinned by a ``-m "not gpu"`` test (``tests/test_oracle_pins.py``)
+Every function is pinned by a ``-m "not gpu"`` test (``tests/test_oracle_pins.py``,
+``tests/test_oracle_attn_pins.py``)
 against something other than itself: values the pages print, closed forms,
 finite differences, brute-force loops or an independent library routine.
 """
 from .mlp_fp64 import *  # noqa: F401,F403
+from .attn_fp64 import *  # noqa: F401,F403

@@ -133,3 +133,67 @@ def sp_region_inputs(s: int, b: int, h: int, p: float, seed: int, dtype: str = "
         "keep": (torch.rand(s, b, h, generator=g) >= p).to(torch.uint8),
         "dOut": torch.randn(s, b, h, generator=g).to(dt),
     }
+
+
+@dataclass(frozen=True)
+class AttnConfig:
+    """One tensor-parallel self-attention workload: h = heads·128 (head width 128,
+    "Tensor Parallelism（TP）与 Sequence Parallelism（SP）", §6 numbers:
+    heads = 64, head_dim = 128 at H = 8192)."""
+
+    name: str
+    s: int
+    b: int
+    h: int
+    heads: int
+    tp: int
+    sp: bool
+    dtype: str
+    causal: bool
+    seed: int = 0
+
+    @property
+    def M(self) -> int:
+        return self.s * self.b
+
+    @property
+    def d(self) -> int:
+        return self.h // self.heads
+
+    @property
+    def torch_dtype(self) -> torch.dtype:
+        return TORCH_DTYPES[self.dtype]
+
+    def flops_fwd_bwd(self) -> int:
+        """Matmul FLOPs of one forward+backward, without recomputation.
+
+        Projections: QKV 2·M·h·3h and output 2·M·h·h forward, twice that backward
+        (input and weight gradients): 24·M·h².  Core per sequence and head: QKᵀ and
+        P·V forward (2·s²·d each), dV, dP, dQ, dK backward (2·s²·d each): 12·s²·d,
+        i.e. 12·b·s²·h over all heads — halved (to the visible pairs, ≈ s²/2) with
+        the causal mask."""
+        core = 12 * self.b * self.s * self.s * self.h
+        if self.causal:
+            core = 12 * self.b * (self.s * (self.s + 1) // 2) * self.h
+        return 24 * self.M * self.h * self.h + core
+
+    def with_(self, **kw) -> "AttnConfig":
+        return replace(self, **kw)
+
+
+ATTN_CONFIGS = {
+    "attn_tiny_tp2_bf16": AttnConfig("attn_tiny_tp2_bf16", 192, 2, 512, 4, 2, True, "bf16", False),
+    "llama70b_attn_tpsp8_bf16": AttnConfig("llama70b_attn_tpsp8_bf16", 4096, 1, 8192, 64, 8, True, "bf16", True),
+}
+
+
+def attn_inputs(cfg: AttnConfig, seed: int | None = None) -> dict[str, torch.Tensor]:
+    """CPU tensors X [s,b,h], Wqkv [3h,h], Wo [h,h], dZ [s,b,h] in cfg.dtype:
+    X, dZ ~ N(0, 1), weights ~ N(0, 0.02), drawn in that order from one generator."""
+    g = torch.Generator().manual_seed(cfg.seed if seed is None else seed)
+    dt = cfg.torch_dtype
+    X = torch.randn(cfg.s, cfg.b, cfg.h, generator=g)
+    Wqkv = torch.randn(3 * cfg.h, cfg.h, generator=g).mul_(0.02)
+    Wo = torch.randn(cfg.h, cfg.h, generator=g).mul_(0.02)
+    dZ = torch.randn(cfg.s, cfg.b, cfg.h, generator=g)
+    return {"X": X.to(dt), "Wqkv": Wqkv.to(dt), "Wo": Wo.to(dt), "dZ": dZ.to(dt)}
