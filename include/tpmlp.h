@@ -64,7 +64,7 @@
 extern "C" {
 #endif
 
-#define TPMLP_ABI_VERSION 1
+#define TPMLP_ABI_VERSION 2
 #define TPMLP_MAX_TP 64
 
 typedef enum tpmlp_status {
@@ -311,6 +311,52 @@ void tpmlp_set_wait_timeout_ns(uint64_t ns);
 int tpmlp_wait_timeout_selftest(uint64_t timeout_ns, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * Tensor-parallel self-attention block ("tensor-parallel-megatron" reading,
+ * attention section; "Tensor Parallelism（TP）与 Sequence Parallelism（SP）", §2
+ * "attention 的道理是一样的"): the fused QKV projection is column-parallel with
+ * whole heads per tensor shard, each head computes softmax(Q·Kᵀ/√d)·V on its
+ * shard, and the output projection is row-parallel with one reduction at the
+ * exit (g; the reduce-scatter under SP).  As in the MLP block the tp shards are
+ * partitions of one device's buffers and the shard sums are folded into the
+ * GEMM accumulators (the fused mode).
+ *
+ * Shapes: head width d = 128, so h = 128·heads; heads % tp == 0 (else
+ * TPMLP_ERR_NOT_DIVISIBLE), s % tp == 0 under SP; float16 or bfloat16 storage
+ * (float32 -> TPMLP_ERR_UNSUPPORTED); b < 65536, s ≤ 65535·128.  Activations
+ * are sequence-first [s, b, ·] (row m = t·b + bi); every pointer 16-byte aligned.
+ *   x      sp ? tp chunk pointers [s/tp, b, h] : one pointer [s, b, h]
+ *   wqkv   [3h, h]: rows 3·128·j … 3·128·j+383 are head j's q, k and v rows
+ *          (128 each); tensor shard i owns the contiguous rows of its heads
+ *   wo     [h, h]: shard i owns the columns of its heads
+ *   qkv    [s·b, 3h] output of the forward, input of the backward (head j's q,
+ *          k, v in columns 384·j …)
+ *   o      [s·b, h] attention output before the projection (head j in
+ *          columns 128·j …); forward output, backward input
+ *   lse    [b][heads][s_pad] float32, s_pad = s rounded up to a multiple of 128:
+ *          log2 Σ_u 2^(x_tu) of each query row's scaled scores
+ *          x = (q·k/√d)·log2(e); forward output, backward input
+ *   z, dz, dx  like x
+ *   dwqkv, dwo  weight gradients (overwritten), storage type
+ *   dqkv   [s·b, 3h], dout [s·b, h]: backward scratch and outputs (dQKV, dO)
+ * causal = 1 applies the decoder mask (key u visible to query t iff u ≤ t);
+ * causal = 0 is the unmasked formula.  ws: tpmlp_attn_workspace_size() bytes,
+ * 256-byte aligned (the forward needs it only under SP when the chunks of
+ * s/tp·b rows are not whole multiples of 128 rows; the backward always).
+ * Every on-chip wait is bounded (tpmlp_set_wait_timeout_ns): an expired wait
+ * is reported through tpmlp_device_status() as TPMLP_ERR_TIMEOUT.  Results
+ * are deterministic (no atomics).
+ * ------------------------------------------------------------------------- */
+size_t tpmlp_attn_workspace_size(int64_t s, int64_t b, int64_t h, int heads, int tp, int sp, int dtype);
+int tpmlp_attn_forward(int64_t s, int64_t b, int64_t h, int heads, int tp, int sp, int dtype, int causal,
+                       const void* const* x, const void* wqkv, const void* wo, void* qkv, void* o,
+                       float* lse, void* const* z, void* ws, size_t ws_bytes, void* stream);
+int tpmlp_attn_backward(int64_t s, int64_t b, int64_t h, int heads, int tp, int sp, int dtype, int causal,
+                        const void* const* x, const void* wqkv, const void* wo, const void* qkv,
+                        const void* o, const float* lse, const void* const* dz, void* const* dx,
+                        void* dwqkv, void* dwo, void* dqkv, void* dout, void* ws, size_t ws_bytes,
+                        void* stream);
+
+/* ---------------------------------------------------------------------------
  * Launch accounting (for benchmarks).  Between tpmlp_profile_start() and
  * tpmlp_profile_stop(), every kernel the library launches on this thread is
  * bracketed by two CUDA events recorded on its launching stream, and the
@@ -321,10 +367,14 @@ int tpmlp_wait_timeout_selftest(uint64_t timeout_ns, void* stream);
  *   kind 3  shard sum             work = tp·n·4 bytes read + n·elem bytes written
  *   kind 4  SP-region kernels     work = bytes read + bytes written (LayerNorm,
  *                                 dropout + residual)
+ *   kind 5  attention core        work = matmul FLOPs over the visible (query,
+ *                                 key) pairs: 4·pairs·128·heads·b forward,
+ *                                 8·pairs·128·heads·b backward (the recomputed
+ *                                 scores are not counted)
  * tpmlp_profile_stop() synchronises the recorded events and fills `out`
  * (out may be NULL to discard).  Recording stays off unless started.
  * ------------------------------------------------------------------------- */
-#define TPMLP_PROFILE_KINDS 5
+#define TPMLP_PROFILE_KINDS 6
 typedef struct tpmlp_profile {
   int launches[TPMLP_PROFILE_KINDS];
   double ms[TPMLP_PROFILE_KINDS];

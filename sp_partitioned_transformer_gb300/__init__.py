@@ -52,6 +52,10 @@ __all__ = [
     "profile_stop",
     "PROFILE_KINDS",
     "MLPBlock",
+    "attn_workspace_size",
+    "attn_forward",
+    "attn_backward",
+    "AttnBlock",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -71,13 +75,13 @@ DTYPE_NAMES = {"f32": 0, "f16": 1, "bf16": 2}
 ACT = {"gelu": 0, "swiglu": 1, "identity": 2, "relu": 3}
 MODE = {"partials": 0, "fused": 1}
 
-PROFILE_KINDS = ("gemm_tc", "gemm_f32", "copy_dim0", "shard_sum", "sp_region")
+PROFILE_KINDS = ("gemm_tc", "gemm_f32", "copy_dim0", "shard_sum", "sp_region", "attn_core")
 
 _lib = None
 
 
 class _Profile(ctypes.Structure):
-    _fields_ = [("launches", ctypes.c_int * 5), ("ms", ctypes.c_double * 5), ("work", ctypes.c_double * 5)]
+    _fields_ = [("launches", ctypes.c_int * 6), ("ms", ctypes.c_double * 6), ("work", ctypes.c_double * 6)]
 
 
 class TpmlpError(RuntimeError):
@@ -147,6 +151,14 @@ def load(path: str | None = None):
     lib.tpmlp_sp_residual_dropout_forward.argtypes = [vpp, vpp, vpp, f32, vpp, i64, i64, i64, i32, i32, vp]
     lib.tpmlp_sp_residual_dropout_backward.restype = i32
     lib.tpmlp_sp_residual_dropout_backward.argtypes = [vpp, vpp, f32, vpp, i64, i64, i64, i32, i32, vp]
+    lib.tpmlp_attn_workspace_size.restype = sz
+    lib.tpmlp_attn_workspace_size.argtypes = [i64, i64, i64, i32, i32, i32, i32]
+    lib.tpmlp_attn_forward.restype = i32
+    lib.tpmlp_attn_forward.argtypes = [i64, i64, i64, i32, i32, i32, i32, i32,
+                                       vpp, vp, vp, vp, vp, vp, vpp, vp, sz, vp]
+    lib.tpmlp_attn_backward.restype = i32
+    lib.tpmlp_attn_backward.argtypes = [i64, i64, i64, i32, i32, i32, i32, i32,
+                                        vpp, vp, vp, vp, vp, vp, vpp, vpp, vp, vp, vp, vp, vp, sz, vp]
     lib.tpmlp_profile_start.restype = i32
     lib.tpmlp_profile_start.argtypes = []
     lib.tpmlp_profile_stop.restype = i32
@@ -417,3 +429,70 @@ class MLPBlock:
         backward(x, w1, w2, fwd["u"], fwd["y"], dz, out["dx"], out["dw1"], out["dw2"], out["du"], stream=stream,
                  **self._kw())
         return out
+
+
+# ---------------------------------------------------------------- attention block
+
+
+def attn_workspace_size(s, b, h, heads, tp, sp, dtype) -> int:
+    return int(load().tpmlp_attn_workspace_size(s, b, h, heads, tp, int(bool(sp)), _dtype_code(dtype)))
+
+
+def attn_forward(x, wqkv, wo, qkv, o, lse, z, *, s, b, h, heads, tp, sp, causal, workspace=None, dtype=None,
+                 stream=None) -> None:
+    """tpmlp_attn_forward.  x, z: lists of tp chunks under sp, else single tensors."""
+    dt = _dtype_code(dtype if dtype is not None else wqkv.dtype)
+    _check(load().tpmlp_attn_forward(s, b, h, heads, tp, int(bool(sp)), dt, int(bool(causal)), _ptrs(x), _ptr(wqkv),
+                                     _ptr(wo), _ptr(qkv), _ptr(o), _ptr(lse), _ptrs(z), _ptr(workspace),
+                                     0 if workspace is None else workspace.numel() * workspace.element_size(),
+                                     _stream(stream)))
+
+
+def attn_backward(x, wqkv, wo, qkv, o, lse, dz, dx, dwqkv, dwo, dqkv, dout, *, s, b, h, heads, tp, sp, causal,
+                  workspace, dtype=None, stream=None) -> None:
+    """tpmlp_attn_backward.  x, dz, dx: lists of tp chunks under sp, else single tensors."""
+    dt = _dtype_code(dtype if dtype is not None else wqkv.dtype)
+    _check(load().tpmlp_attn_backward(s, b, h, heads, tp, int(bool(sp)), dt, int(bool(causal)), _ptrs(x),
+                                      _ptr(wqkv), _ptr(wo), _ptr(qkv), _ptr(o), _ptr(lse), _ptrs(dz), _ptrs(dx),
+                                      _ptr(dwqkv), _ptr(dwo), _ptr(dqkv), _ptr(dout), _ptr(workspace),
+                                      workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+class AttnBlock:
+    """One attention-block configuration; allocates outputs, saved activations and
+    workspace with torch.empty (the library itself allocates nothing)."""
+
+    def __init__(self, s, b, h, heads, tp, sp, dtype, causal, device="cuda"):
+        self.s, self.b, self.h, self.heads, self.tp, self.sp = s, b, h, heads, tp, bool(sp)
+        self.dtype, self.causal, self.device = dtype, bool(causal), device
+        self.M = s * b
+        self.s_pad = (s + 127) // 128 * 128
+        n = attn_workspace_size(s, b, h, heads, tp, sp, dtype)
+        self.ws = torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+
+    def _act(self):
+        if self.sp:
+            return [torch.empty(self.s // self.tp, self.b, self.h, dtype=self.dtype, device=self.device)
+                    for _ in range(self.tp)]
+        return torch.empty(self.s, self.b, self.h, dtype=self.dtype, device=self.device)
+
+    def _kw(self):
+        return dict(s=self.s, b=self.b, h=self.h, heads=self.heads, tp=self.tp, sp=self.sp, causal=self.causal)
+
+    def forward(self, x, wqkv, wo, stream=None):
+        qkv = torch.empty(self.M, 3 * self.h, dtype=self.dtype, device=self.device)
+        o = torch.empty(self.M, self.h, dtype=self.dtype, device=self.device)
+        lse = torch.empty(self.b, self.heads, self.s_pad, dtype=torch.float32, device=self.device)
+        z = self._act()
+        attn_forward(x, wqkv, wo, qkv, o, lse, z, workspace=self.ws, stream=stream, **self._kw())
+        return {"qkv": qkv, "o": o, "lse": lse, "z": z}
+
+    def backward(self, x, wqkv, wo, fw, dz, stream=None):
+        dx = self._act()
+        dwqkv = torch.empty(3 * self.h, self.h, dtype=self.dtype, device=self.device)
+        dwo = torch.empty(self.h, self.h, dtype=self.dtype, device=self.device)
+        dqkv = torch.empty(self.M, 3 * self.h, dtype=self.dtype, device=self.device)
+        dout = torch.empty(self.M, self.h, dtype=self.dtype, device=self.device)
+        attn_backward(x, wqkv, wo, fw["qkv"], fw["o"], fw["lse"], dz, dx, dwqkv, dwo, dqkv, dout,
+                      workspace=self.ws, stream=stream, **self._kw())
+        return {"dx": dx, "dwqkv": dwqkv, "dwo": dwo, "dqkv": dqkv, "dout": dout}

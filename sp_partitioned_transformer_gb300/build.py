@@ -24,7 +24,7 @@ BUILD_DIR = os.path.join(PKG, "_build")
 LIB_DIR = os.path.join(PKG, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libtpmlp.so")
 
-SOURCES = ["api.cu", "copy_kernels.cu", "gemm_tc.cu", "gemm_simt.cu", "noalloc.cu", "sp_region.cu"]
+SOURCES = ["api.cu", "attn.cu", "copy_kernels.cu", "gemm_tc.cu", "gemm_simt.cu", "noalloc.cu", "sp_region.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + [
     "-O3",

@@ -1,0 +1,1202 @@
+// Tensor-parallel self-attention block: fused QKV projection (column-parallel
+// by heads), per-head softmax(Q·Kᵀ/√d)·V, output projection (row-parallel, the
+// shard sum folded into the accumulator, the reduce-scatter into the epilogue),
+// and the backward ("tensor-parallel-megatron" reading, attention section: QKV
+// split by columns so each shard owns whole heads, softmax(QKᵀ/√d)V per head on
+// its own shard, output projection split by rows with one reduction at the
+// exit; "Tensor Parallelism（TP）与 Sequence Parallelism（SP）", §2 "attention 的
+// 道理是一样的").
+//
+// The projections run on the tcgen05 GEMM (gemm_tc.cu).  The attention core is
+// three tcgen05 kernels (head width 128, 16-bit storage, float32 accumulation in
+// tensor memory), each one CTA of 8 warps: warp 0 issues TMA loads, warp 1
+// issues the MMAs, warp 2 owns the tensor-memory allocation and warps 4–7 do the
+// element-wise work with one thread per row of the 128-row tile.
+//
+//   attn_fwd_kernel   per (128-query tile, head, sequence): S = Q·Kᵀ into one of
+//                     two TMEM buffers (the next S is computed while the softmax
+//                     works on this one), streaming softmax in base 2, P written
+//                     to shared memory as a 128-byte-swizzled operand, O += P·V in
+//                     TMEM, O rescaled in TMEM only when a warp's row maximum
+//                     moved; O and the row log-sum-exp (lse2) written at the end.
+//   attn_bwd_dkdv_kernel  per (128-key tile, head, sequence), over 64-query tiles:
+//                     Sᵀ = K·Qᵀ and dPᵀ = V·dOᵀ, Pᵀ = 2^(Sᵀ·c − lse2),
+//                     dSᵀ = Pᵀ ⊙ (dPᵀ − Δ), dV += Pᵀ·dO, dK += dSᵀ·Q.
+//   attn_bwd_dq_kernel    per (128-query tile, head, sequence), over 64-key tiles:
+//                     S, dP recomputed, dS as above, dQ += dS·K.
+//   attn_bwd_delta_kernel Δ = rowsum(dO ⊙ O) per query row and head.
+// No atomics anywhere: every output element is written by one CTA, so results
+// are the same bits on every run.
+#include <algorithm>
+#include <cmath>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "internal.h"
+
+namespace tpmlp {
+namespace attn {
+
+constexpr int HD = 128;  // head width (d)
+constexpr int ATT_THREADS = 256;
+constexpr uint32_t HALF_ROW_BYTES = 128;  // one 64-column half row of 16-bit elements
+
+// ---------------------------------------------------------------- device helpers
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int32_t c0,
+                                            int32_t c1, int32_t c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
+// A [rows × 128] tile of one head: two 64-column halves of rows × 128 bytes,
+// each 128-byte swizzled (what TMA writes with SWIZZLE_128B).
+__device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* map, uint32_t bar, int col, int bi,
+                                          int row0, int rows) {
+  tma_load_3d(dst, map, bar, col, bi, row0);
+  tma_load_3d(dst + static_cast<uint32_t>(rows) * HALF_ROW_BYTES, map, bar, col + 64, bi, row0);
+}
+
+// K-major operand descriptors (rows = M or N, the 16-element K step ks along the
+// columns): a [rows × 128] tile, and a [rows × 64] half.
+__device__ __forceinline__ uint64_t kmajor128(uint32_t base, int rows, int ks) {
+  return make_sdesc_sw128(base + static_cast<uint32_t>(ks >> 2) * rows * HALF_ROW_BYTES + (ks & 3) * 32u, 16u,
+                          1024u);
+}
+__device__ __forceinline__ uint64_t kmajor64(uint32_t base, int ks) {
+  return make_sdesc_sw128(base + ks * 32u, 16u, 1024u);
+}
+// MN-major operand descriptor of a [krows × 128] tile whose rows run along K and
+// whose 128 columns are M or N: K step ks = rows 16·ks … 16·ks+15; the second
+// 64-column half is krows·128 bytes further on.
+__device__ __forceinline__ uint64_t mnmajor128(uint32_t base, int krows, int ks) {
+  return make_sdesc_sw128(base + ks * 2048u, static_cast<uint32_t>(krows) * HALF_ROW_BYTES, 1024u);
+}
+
+// 16-byte chunk c (8 elements) of row r of a 128-byte-swizzled [rows × 64] half.
+__device__ __forceinline__ void st_swizzled(uint8_t* half, int r, int c, const uint4& v) {
+  *reinterpret_cast<uint4*>(half + r * HALF_ROW_BYTES + ((c ^ (r & 7)) << 4)) = v;
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+      "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+      "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Shared bookkeeping at the end of a dynamic shared-memory block.
+struct Tail {
+  uint64_t bars[24];
+  uint32_t tmem_slot;
+  int abort_flag;
+};
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* raw) {
+  const uint32_t a = smem_u32(raw);
+  return raw + ((1024u - (a & 1023u)) & 1023u);
+}
+
+struct AttnParams {
+  CUtensorMap qkv128;  // QKV [s][b][3h] as a 3-D tensor {3h, b, s}, box {64, 1, 128}
+  CUtensorMap qkv64;   // same tensor, box {64, 1, 64}
+  CUtensorMap do128;   // dO [s][b][h] as {h, b, s}, box {64, 1, 128}
+  CUtensorMap do64;    // box {64, 1, 64}
+  void* o;             // forward: O [M, h] output
+  float* lse;          // [b][heads][s_pad]: forward output, backward input
+  const float* delta;  // [b][heads][s_pad] (backward)
+  void* dqkv;          // backward: dQKV [M, 3h]
+  int s, b, h, heads, s_pad, causal;
+  float scale_log2;    // log2(e)/√d
+  float scale;         // 1/√d
+  unsigned* status;
+  uint64_t timeout_ns;
+};
+
+template <int DT>
+__device__ __forceinline__ void store_row_chunk(void* base, int64_t off, const float* v) {
+  *reinterpret_cast<uint4*>(static_cast<typename Storage<DT>::T*>(base) + off) = pack8<DT>(v);
+}
+
+// ================================================================== forward
+constexpr int F_BQ = 128, F_BK = 128;
+constexpr uint32_t F_TILE = 128 * 128 * 2;  // 32 KB
+constexpr uint32_t F_Q = 0, F_K0 = F_TILE, F_V0 = 3 * F_TILE, F_P = 5 * F_TILE, F_END = 6 * F_TILE;
+constexpr size_t F_SMEM = 1024 + F_END + sizeof(Tail);
+// barriers
+enum { FB_Q = 0, FB_KF = 1, FB_KE = 3, FB_VF = 5, FB_VE = 7, FB_SF = 9, FB_P = 11, FB_O = 12, FB_DRAIN = 13 };
+
+template <int DT>
+__global__ void __launch_bounds__(ATT_THREADS, 1) attn_fwd_kernel(const __grid_constant__ AttnParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  Tail* tail = reinterpret_cast<Tail*>(smem + F_END);
+  auto bar = [&](int i) { return smem_u32(&tail->bars[i]); };
+  volatile int* abort_flag = &tail->abort_flag;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // grid (heads, b, query tiles): the tile index varies slowest, so under the
+  // causal mask the longest tiles (the last ones) are dispatched first
+  const int ntq = (p.s + F_BQ - 1) / F_BQ;
+  const int qt = p.causal ? ntq - 1 - static_cast<int>(blockIdx.z) : static_cast<int>(blockIdx.z);
+  const int head = blockIdx.x, bi = blockIdx.y;
+  const int q0 = qt * F_BQ;
+  const int nkt = (p.s + F_BK - 1) / F_BK;
+  const int N = p.causal ? min(nkt, (q0 + F_BQ - 1) / F_BK + 1) : nkt;
+  const int colq = 3 * HD * head, colk = colq + HD, colv = colq + 2 * HD;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(FB_Q), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(FB_KF + i), 1);
+      mbar_init(bar(FB_KE + i), 1);
+      mbar_init(bar(FB_VF + i), 1);
+      mbar_init(bar(FB_VE + i), 1);
+      mbar_init(bar(FB_SF + i), 1);
+    }
+    mbar_init(bar(FB_P), 128);
+    mbar_init(bar(FB_O), 1);
+    mbar_init(bar(FB_DRAIN), 1);
+    tail->abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(smem_u32(&tail->tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tail->tmem_slot;
+  const uint32_t sQ = smem_u32(smem + F_Q), sP = smem_u32(smem + F_P);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_map(&p.qkv128);
+      uint32_t issued = 0;  // stages with copies that may still be in flight
+      mbar_arrive_expect_tx(bar(FB_Q), F_TILE);
+      load_tile(sQ, &p.qkv128, bar(FB_Q), colq, bi, q0, 128);
+      bool ok = true;
+      for (int n = 0; ok && n < N; ++n) {
+        const int st = n & 1;
+        const uint32_t par = ((n >> 1) & 1) ^ 1u;
+        if (!(ok = mbar_wait_bounded(bar(FB_KE + st), par, abort_flag, p.status, p.timeout_ns))) break;
+        mbar_arrive_expect_tx(bar(FB_KF + st), F_TILE);
+        load_tile(smem_u32(smem + F_K0 + st * F_TILE), &p.qkv128, bar(FB_KF + st), colk, bi, n * F_BK, 128);
+        if (!(ok = mbar_wait_bounded(bar(FB_VE + st), par, abort_flag, p.status, p.timeout_ns))) break;
+        mbar_arrive_expect_tx(bar(FB_VF + st), F_TILE);
+        load_tile(smem_u32(smem + F_V0 + st * F_TILE), &p.qkv128, bar(FB_VF + st), colv, bi, n * F_BK, 128);
+        issued = static_cast<uint32_t>(n + 1);
+      }
+      if (!ok) {
+        // let the copies already issued land before the CTA exits
+        (void)mbar_wait_bounded(bar(FB_Q), 0u, nullptr, nullptr, p.timeout_ns);
+        for (uint32_t n = issued > 2 ? issued - 2 : 0; n < issued; ++n) {
+          (void)mbar_wait_bounded(bar(FB_KF + (n & 1)), (n >> 1) & 1u, nullptr, nullptr, p.timeout_ns);
+          (void)mbar_wait_bounded(bar(FB_VF + (n & 1)), (n >> 1) & 1u, nullptr, nullptr, p.timeout_ns);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = make_idesc_f16(DT == DT_BF16, false, false, 128, F_BK);
+      constexpr uint32_t idesc_o = make_idesc_f16(DT == DT_BF16, false, true, 128, HD);
+      bool ok = mbar_wait_bounded(bar(FB_Q), 0u, abort_flag, p.status, p.timeout_ns);
+      auto issue_s = [&](int n) -> bool {
+        const int st = n & 1;
+        if (!mbar_wait_bounded(bar(FB_KF + st), (n >> 1) & 1u, abort_flag, p.status, p.timeout_ns)) return false;
+        tc_fence_after();
+        const uint32_t sK = smem_u32(smem + F_K0 + st * F_TILE);
+#pragma unroll
+        for (int ks = 0; ks < HD / 16; ++ks)
+          tc_mma_f16(tmem + st * F_BK, kmajor128(sQ, 128, ks), kmajor128(sK, 128, ks), idesc_s, ks > 0 ? 1u : 0u);
+        tc_commit(bar(FB_SF + st));
+        tc_commit(bar(FB_KE + st));
+        return true;
+      };
+      if (ok) tc_fence_after();
+      if (ok) ok = issue_s(0);
+      if (ok && N > 1) ok = issue_s(1);
+      for (int n = 0; ok && n < N; ++n) {
+        const int st = n & 1;
+        if (!(ok = mbar_wait_bounded(bar(FB_P), n & 1, abort_flag, p.status, p.timeout_ns))) break;
+        if (!(ok = mbar_wait_bounded(bar(FB_VF + st), (n >> 1) & 1u, abort_flag, p.status, p.timeout_ns))) break;
+        tc_fence_after();
+        const uint32_t sV = smem_u32(smem + F_V0 + st * F_TILE);
+#pragma unroll
+        for (int ks = 0; ks < F_BK / 16; ++ks)
+          tc_mma_f16(tmem + 256, kmajor128(sP, 128, ks), mnmajor128(sV, 128, ks), idesc_o,
+                     (n > 0 || ks > 0) ? 1u : 0u);
+        tc_commit(bar(FB_O));
+        tc_commit(bar(FB_VE + st));
+        if (n + 2 < N) ok = issue_s(n + 2);
+      }
+      if (!ok) {
+        tc_commit(bar(FB_DRAIN));
+        (void)mbar_wait_bounded(bar(FB_DRAIN), 0u, nullptr, nullptr, p.timeout_ns);
+      }
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    const int qw = warp & 3;
+    const int r = qw * 32 + lane;  // row of the tile = TMEM lane
+    const int q = q0 + r;
+    const uint32_t tl = tmem + (static_cast<uint32_t>(qw * 32) << 16);
+    float m = -INFINITY, l = 0.0f;
+    bool ok = true;
+    for (int n = 0; n < N; ++n) {
+      const int st = n & 1;
+      ok = mbar_wait_bounded(bar(FB_SF + st), (n >> 1) & 1u, abort_flag, p.status, p.timeout_ns);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      tc_fence_after();
+      float x[F_BK];
+#pragma unroll
+      for (int c = 0; c < F_BK / 32; ++c) tmem_ld32(tl + st * F_BK + c * 32, x + c * 32);
+      const int k0 = n * F_BK;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < F_BK; ++j) {
+        const int key = k0 + j;
+        const bool vis = key < p.s && (!p.causal || key <= q);
+        x[j] = vis ? x[j] * p.scale_log2 : -INFINITY;
+        mx = fmaxf(mx, x[j]);
+      }
+      const float m_new = fmaxf(m, mx);
+      const float m_use = m_new == -INFINITY ? 0.0f : m_new;
+      const float alpha = ex2(m - m_use);
+      float rs = 0.0f;
+#pragma unroll
+      for (int j = 0; j < F_BK; ++j) {
+        x[j] = ex2(x[j] - m_use);
+        rs += x[j];
+      }
+      l = l * alpha + rs;
+      m = m_new;
+      if (n > 0) {
+        // P·V of the previous tile has finished: P's buffer is free and O holds
+        // the sum so far, to be rescaled to the new maximum.
+        ok = mbar_wait_bounded(bar(FB_O), (n - 1) & 1, abort_flag, p.status, p.timeout_ns);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, alpha != 1.0f)) {
+#pragma unroll 1
+          for (int c = 0; c < HD / 32; ++c) {
+            float o[32];
+            tmem_ld32(tl + 256 + c * 32, o);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) o[j] *= alpha;
+            tmem_st32(tl + 256 + c * 32, o);
+          }
+          tmem_st_wait();
+        }
+      }
+      // P as the A operand of O += P·V: row r, keys along the columns.
+#pragma unroll
+      for (int c = 0; c < F_BK / 8; ++c)
+        st_swizzled(smem + F_P + (c >> 3) * (128 * HALF_ROW_BYTES), r, c & 7, pack8<DT>(x + c * 8));
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar(FB_P));
+    }
+    if (ok) {
+      ok = mbar_wait_bounded(bar(FB_O), (N - 1) & 1, abort_flag, p.status, p.timeout_ns);
+      ok = __all_sync(0xffffffffu, ok);
+    }
+    if (ok) {
+      tc_fence_after();
+      const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
+      const int64_t mrow = static_cast<int64_t>(q) * p.b + bi;
+#pragma unroll 1
+      for (int c = 0; c < HD / 32; ++c) {
+        float o[32];
+        tmem_ld32(tl + 256 + c * 32, o);
+        if (q < p.s) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) o[j] *= inv_l;
+#pragma unroll
+          for (int g = 0; g < 4; ++g)
+            store_row_chunk<DT>(p.o, mrow * p.h + head * HD + c * 32 + g * 8, o + g * 8);
+        }
+      }
+      // rows past s (the padded tail of the last tile) get 0: the backward reads whole tiles
+      p.lse[(static_cast<int64_t>(bi) * p.heads + head) * p.s_pad + q] = q < p.s ? m + __log2f(l) : 0.0f;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ================================================================== backward: Δ
+template <int DT>
+__global__ void __launch_bounds__(256) attn_bwd_delta_kernel(const void* __restrict__ dout,
+                                                             const void* __restrict__ o, float* __restrict__ delta,
+                                                             int s, int b, int h, int heads, int s_pad) {
+  // one warp per (token row, head); each lane takes 4 of the 128 columns
+  const int64_t wid = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const int64_t total = static_cast<int64_t>(s_pad) * b * heads;
+  if (wid >= total) return;
+  const int head = static_cast<int>(wid % heads);
+  const int64_t rest = wid / heads;
+  const int bi = static_cast<int>(rest % b);
+  const int q = static_cast<int>(rest / b);
+  float acc = 0.0f;
+  if (q < s) {
+    using T = typename Storage<DT>::T;
+    const int64_t off = (static_cast<int64_t>(q) * b + bi) * h + head * HD + lane * 4;
+    const uint2 a = *reinterpret_cast<const uint2*>(static_cast<const T*>(dout) + off);
+    const uint2 c = *reinterpret_cast<const uint2*>(static_cast<const T*>(o) + off);
+    const T* ta = reinterpret_cast<const T*>(&a);
+    const T* tc = reinterpret_cast<const T*>(&c);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc += Storage<DT>::to_f32(ta[i]) * Storage<DT>::to_f32(tc[i]);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (lane == 0) delta[(static_cast<int64_t>(bi) * heads + head) * s_pad + q] = acc;
+}
+
+// ================================================================== backward: dK, dV
+constexpr int KV_BK = 128, KV_BQ = 64, KV_ST = 3;
+constexpr uint32_t KV_TILE = 128 * 128 * 2;    // K or V tile, 32 KB
+constexpr uint32_t KV_QTILE = 64 * 128 * 2;    // Q or dO tile of 64 rows, 16 KB
+constexpr uint32_t KV_STAGE = 2 * KV_QTILE + 512;  // Q, dO, lse2[64], Δ[64]
+constexpr uint32_t KV_K = 0, KV_V = KV_TILE, KV_S0 = 2 * KV_TILE;
+constexpr uint32_t KV_PT = KV_S0 + KV_ST * ((KV_STAGE + 1023) & ~1023u);
+constexpr uint32_t KV_DST = KV_PT + 128 * HALF_ROW_BYTES;
+constexpr uint32_t KV_END = KV_DST + 128 * HALF_ROW_BYTES;
+constexpr uint32_t KV_STRIDE = (KV_STAGE + 1023) & ~1023u;
+constexpr size_t KV_SMEM = 1024 + KV_END + sizeof(Tail);
+enum { KB_KV = 0, KB_F = 1, KB_E = 4, KB_SF = 7, KB_P = 9, KB_MM = 10, KB_DRAIN = 11 };
+
+template <int DT>
+__global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dkdv_kernel(const __grid_constant__ AttnParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  Tail* tail = reinterpret_cast<Tail*>(smem + KV_END);
+  auto bar = [&](int i) { return smem_u32(&tail->bars[i]); };
+  volatile int* abort_flag = &tail->abort_flag;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // grid (heads, b, key tiles), the tile index slowest; under the causal mask the
+  // first key tiles see the most query tiles and are dispatched first
+  const int kt = static_cast<int>(blockIdx.z);
+  const int head = blockIdx.x, bi = blockIdx.y;
+  const int k0 = kt * KV_BK;
+  const int nqt = (p.s + KV_BQ - 1) / KV_BQ;
+  const int qt_first = p.causal ? k0 / KV_BQ : 0;
+  const int N = nqt - qt_first;
+  const int colq = 3 * HD * head, colk = colq + HD, colv = colq + 2 * HD;
+  const float* lse_row = p.lse + (static_cast<int64_t>(bi) * p.heads + head) * p.s_pad;
+  const float* delta_row = p.delta + (static_cast<int64_t>(bi) * p.heads + head) * p.s_pad;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(KB_KV), 1);
+    for (int i = 0; i < KV_ST; ++i) {
+      mbar_init(bar(KB_F + i), 1);
+      mbar_init(bar(KB_E + i), 1);
+    }
+    mbar_init(bar(KB_SF), 1);
+    mbar_init(bar(KB_SF + 1), 1);
+    mbar_init(bar(KB_P), 128);
+    mbar_init(bar(KB_MM), 1);
+    mbar_init(bar(KB_DRAIN), 1);
+    tail->abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(smem_u32(&tail->tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tail->tmem_slot;
+  // TMEM columns: Sᵀ[2] at 0 / 64, dPᵀ[2] at 128 / 192, dV at 256, dK at 384.
+  const uint32_t sK = smem_u32(smem + KV_K), sV = smem_u32(smem + KV_V);
+  const uint32_t sPT = smem_u32(smem + KV_PT), sDST = smem_u32(smem + KV_DST);
+  auto stage_base = [&](int st) { return smem + KV_S0 + st * KV_STRIDE; };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_map(&p.qkv128);
+      tma_prefetch_map(&p.qkv64);
+      tma_prefetch_map(&p.do64);
+      mbar_arrive_expect_tx(bar(KB_KV), 2 * KV_TILE);
+      load_tile(sK, &p.qkv128, bar(KB_KV), colk, bi, k0, 128);
+      load_tile(sV, &p.qkv128, bar(KB_KV), colv, bi, k0, 128);
+      bool ok = true;
+      int issued = 0;
+      for (int n = 0; ok && n < N; ++n) {
+        const int st = n % KV_ST;
+        const uint32_t par = ((n / KV_ST) & 1) ^ 1u;
+        if (!(ok = mbar_wait_bounded(bar(KB_E + st), par, abort_flag, p.status, p.timeout_ns))) break;
+        const int qq = (qt_first + n) * KV_BQ;
+        uint8_t* sb = stage_base(st);
+        const uint32_t f = bar(KB_F + st);
+        mbar_arrive_expect_tx(f, KV_STAGE);
+        load_tile(smem_u32(sb), &p.qkv64, f, colq, bi, qq, 64);
+        load_tile(smem_u32(sb + KV_QTILE), &p.do64, f, head * HD, bi, qq, 64);
+        bulk_load(smem_u32(sb + 2 * KV_QTILE), lse_row + qq, 256, f);
+        bulk_load(smem_u32(sb + 2 * KV_QTILE + 256), delta_row + qq, 256, f);
+        issued = n + 1;
+      }
+      if (!ok) {
+        (void)mbar_wait_bounded(bar(KB_KV), 0u, nullptr, nullptr, p.timeout_ns);
+        for (int n = issued > KV_ST ? issued - KV_ST : 0; n < issued; ++n)
+          (void)mbar_wait_bounded(bar(KB_F + n % KV_ST), (n / KV_ST) & 1u, nullptr, nullptr, p.timeout_ns);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = make_idesc_f16(DT == DT_BF16, false, false, 128, KV_BQ);
+      constexpr uint32_t idesc_acc = make_idesc_f16(DT == DT_BF16, false, true, 128, HD);
+      bool ok = mbar_wait_bounded(bar(KB_KV), 0u, abort_flag, p.status, p.timeout_ns);
+      auto issue_sdp = [&](int n) -> bool {
+        const int st = n % KV_ST, buf = n & 1;
+        if (!mbar_wait_bounded(bar(KB_F + st), (n / KV_ST) & 1u, abort_flag, p.status, p.timeout_ns)) return false;
+        tc_fence_after();
+        const uint32_t sQ = smem_u32(stage_base(st)), sDO = sQ + KV_QTILE;
+#pragma unroll
+        for (int ks = 0; ks < HD / 16; ++ks) {
+          tc_mma_f16(tmem + buf * 64, kmajor128(sK, 128, ks), kmajor128(sQ, 64, ks), idesc_s, ks > 0 ? 1u : 0u);
+          tc_mma_f16(tmem + 128 + buf * 64, kmajor128(sV, 128, ks), kmajor128(sDO, 64, ks), idesc_s,
+                     ks > 0 ? 1u : 0u);
+        }
+        tc_commit(bar(KB_SF + buf));
+        return true;
+      };
+      if (ok) tc_fence_after();
+      if (ok) ok = issue_sdp(0);
+      if (ok && N > 1) ok = issue_sdp(1);
+      for (int n = 0; ok && n < N; ++n) {
+        const int st = n % KV_ST;
+        if (!(ok = mbar_wait_bounded(bar(KB_P), n & 1, abort_flag, p.status, p.timeout_ns))) break;
+        tc_fence_after();
+        const uint32_t sQ = smem_u32(stage_base(st)), sDO = sQ + KV_QTILE;
+#pragma unroll
+        for (int ks = 0; ks < KV_BQ / 16; ++ks) {
+          tc_mma_f16(tmem + 256, kmajor64(sPT, ks), mnmajor128(sDO, KV_BQ, ks), idesc_acc,
+                     (n > 0 || ks > 0) ? 1u : 0u);
+          tc_mma_f16(tmem + 384, kmajor64(sDST, ks), mnmajor128(sQ, KV_BQ, ks), idesc_acc,
+                     (n > 0 || ks > 0) ? 1u : 0u);
+        }
+        tc_commit(bar(KB_MM));
+        tc_commit(bar(KB_E + st));
+        if (n + 2 < N) ok = issue_sdp(n + 2);
+      }
+      if (!ok) {
+        tc_commit(bar(KB_DRAIN));
+        (void)mbar_wait_bounded(bar(KB_DRAIN), 0u, nullptr, nullptr, p.timeout_ns);
+      }
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    const int qw = warp & 3;
+    const int r = qw * 32 + lane;
+    const int key = k0 + r;
+    const uint32_t tl = tmem + (static_cast<uint32_t>(qw * 32) << 16);
+    bool ok = true;
+    for (int n = 0; n < N; ++n) {
+      const int st = n % KV_ST, buf = n & 1;
+      ok = mbar_wait_bounded(bar(KB_SF + buf), (n >> 1) & 1u, abort_flag, p.status, p.timeout_ns);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      tc_fence_after();
+      float sv[KV_BQ], dp[KV_BQ];
+      tmem_ld32(tl + buf * 64, sv);
+      tmem_ld32(tl + buf * 64 + 32, sv + 32);
+      tmem_ld32(tl + 128 + buf * 64, dp);
+      tmem_ld32(tl + 128 + buf * 64 + 32, dp + 32);
+      const float* lse_s = reinterpret_cast<const float*>(stage_base(st) + 2 * KV_QTILE);
+      const float* del_s = lse_s + 64;
+      const int qq = (qt_first + n) * KV_BQ;
+#pragma unroll
+      for (int j = 0; j < KV_BQ; ++j) {
+        const int q = qq + j;
+        const bool vis = q < p.s && key < p.s && (!p.causal || key <= q);
+        const float pr = vis ? ex2(sv[j] * p.scale_log2 - lse_s[j]) : 0.0f;
+        dp[j] = pr * (dp[j] - del_s[j]);
+        sv[j] = pr;
+      }
+      if (n > 0) {
+        ok = mbar_wait_bounded(bar(KB_MM), (n - 1) & 1, abort_flag, p.status, p.timeout_ns);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      }
+#pragma unroll
+      for (int c = 0; c < KV_BQ / 8; ++c) {
+        st_swizzled(smem + KV_PT, r, c, pack8<DT>(sv + c * 8));
+        st_swizzled(smem + KV_DST, r, c, pack8<DT>(dp + c * 8));
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar(KB_P));
+    }
+    if (ok) {
+      ok = mbar_wait_bounded(bar(KB_MM), (N - 1) & 1, abort_flag, p.status, p.timeout_ns);
+      ok = __all_sync(0xffffffffu, ok);
+    }
+    if (ok) {
+      tc_fence_after();
+      const int64_t mrow = static_cast<int64_t>(key) * p.b + bi;
+      const int64_t ld = 3 * static_cast<int64_t>(p.h);
+#pragma unroll 1
+      for (int c = 0; c < HD / 32; ++c) {
+        float dv[32], dk[32];
+        tmem_ld32(tl + 256 + c * 32, dv);
+        tmem_ld32(tl + 384 + c * 32, dk);
+        if (key < p.s) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) dk[j] *= p.scale;
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            store_row_chunk<DT>(p.dqkv, mrow * ld + colv + c * 32 + g * 8, dv + g * 8);
+            store_row_chunk<DT>(p.dqkv, mrow * ld + colk + c * 32 + g * 8, dk + g * 8);
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ================================================================== backward: dQ
+constexpr int DQ_BQ = 128, DQ_BK = 64, DQ_ST = 3;
+constexpr uint32_t DQ_TILE = 128 * 128 * 2;   // Q or dO, 32 KB
+constexpr uint32_t DQ_KTILE = 64 * 128 * 2;   // K or V tile of 64 rows, 16 KB
+constexpr uint32_t DQ_STAGE = 2 * DQ_KTILE;   // K, V
+constexpr uint32_t DQ_Q = 0, DQ_DO = DQ_TILE, DQ_S0 = 2 * DQ_TILE;
+constexpr uint32_t DQ_DS = DQ_S0 + DQ_ST * DQ_STAGE;
+constexpr uint32_t DQ_END = DQ_DS + 128 * HALF_ROW_BYTES;
+constexpr size_t DQ_SMEM = 1024 + DQ_END + sizeof(Tail);
+enum { QB_QD = 0, QB_F = 1, QB_E = 4, QB_SF = 7, QB_P = 9, QB_MM = 10, QB_DRAIN = 11 };
+
+template <int DT>
+__global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dq_kernel(const __grid_constant__ AttnParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  Tail* tail = reinterpret_cast<Tail*>(smem + DQ_END);
+  auto bar = [&](int i) { return smem_u32(&tail->bars[i]); };
+  volatile int* abort_flag = &tail->abort_flag;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const int ntq = (p.s + DQ_BQ - 1) / DQ_BQ;
+  const int qt = p.causal ? ntq - 1 - static_cast<int>(blockIdx.z) : static_cast<int>(blockIdx.z);
+  const int head = blockIdx.x, bi = blockIdx.y;
+  const int q0 = qt * DQ_BQ;
+  const int nkt = (p.s + DQ_BK - 1) / DQ_BK;
+  const int N = p.causal ? min(nkt, (q0 + DQ_BQ - 1) / DQ_BK + 1) : nkt;
+  const int colq = 3 * HD * head, colk = colq + HD, colv = colq + 2 * HD;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(QB_QD), 1);
+    for (int i = 0; i < DQ_ST; ++i) {
+      mbar_init(bar(QB_F + i), 1);
+      mbar_init(bar(QB_E + i), 1);
+    }
+    mbar_init(bar(QB_SF), 1);
+    mbar_init(bar(QB_SF + 1), 1);
+    mbar_init(bar(QB_P), 128);
+    mbar_init(bar(QB_MM), 1);
+    mbar_init(bar(QB_DRAIN), 1);
+    tail->abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(smem_u32(&tail->tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tail->tmem_slot;
+  // TMEM columns: S[2] at 0 / 64, dP[2] at 128 / 192, dQ at 256.
+  const uint32_t sQ = smem_u32(smem + DQ_Q), sDO = smem_u32(smem + DQ_DO), sDS = smem_u32(smem + DQ_DS);
+  auto stage_addr = [&](int st) { return smem_u32(smem + DQ_S0 + st * DQ_STAGE); };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_map(&p.qkv128);
+      tma_prefetch_map(&p.qkv64);
+      tma_prefetch_map(&p.do128);
+      mbar_arrive_expect_tx(bar(QB_QD), 2 * DQ_TILE);
+      load_tile(sQ, &p.qkv128, bar(QB_QD), colq, bi, q0, 128);
+      load_tile(sDO, &p.do128, bar(QB_QD), head * HD, bi, q0, 128);
+      bool ok = true;
+      int issued = 0;
+      for (int n = 0; ok && n < N; ++n) {
+        const int st = n % DQ_ST;
+        const uint32_t par = ((n / DQ_ST) & 1) ^ 1u;
+        if (!(ok = mbar_wait_bounded(bar(QB_E + st), par, abort_flag, p.status, p.timeout_ns))) break;
+        const uint32_t f = bar(QB_F + st);
+        mbar_arrive_expect_tx(f, DQ_STAGE);
+        load_tile(stage_addr(st), &p.qkv64, f, colk, bi, n * DQ_BK, 64);
+        load_tile(stage_addr(st) + DQ_KTILE, &p.qkv64, f, colv, bi, n * DQ_BK, 64);
+        issued = n + 1;
+      }
+      if (!ok) {
+        (void)mbar_wait_bounded(bar(QB_QD), 0u, nullptr, nullptr, p.timeout_ns);
+        for (int n = issued > DQ_ST ? issued - DQ_ST : 0; n < issued; ++n)
+          (void)mbar_wait_bounded(bar(QB_F + n % DQ_ST), (n / DQ_ST) & 1u, nullptr, nullptr, p.timeout_ns);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = make_idesc_f16(DT == DT_BF16, false, false, 128, DQ_BK);
+      constexpr uint32_t idesc_acc = make_idesc_f16(DT == DT_BF16, false, true, 128, HD);
+      bool ok = mbar_wait_bounded(bar(QB_QD), 0u, abort_flag, p.status, p.timeout_ns);
+      auto issue_sdp = [&](int n) -> bool {
+        const int st = n % DQ_ST, buf = n & 1;
+        if (!mbar_wait_bounded(bar(QB_F + st), (n / DQ_ST) & 1u, abort_flag, p.status, p.timeout_ns)) return false;
+        tc_fence_after();
+        const uint32_t sKn = stage_addr(st), sVn = sKn + DQ_KTILE;
+#pragma unroll
+        for (int ks = 0; ks < HD / 16; ++ks) {
+          tc_mma_f16(tmem + buf * 64, kmajor128(sQ, 128, ks), kmajor128(sKn, 64, ks), idesc_s, ks > 0 ? 1u : 0u);
+          tc_mma_f16(tmem + 128 + buf * 64, kmajor128(sDO, 128, ks), kmajor128(sVn, 64, ks), idesc_s,
+                     ks > 0 ? 1u : 0u);
+        }
+        tc_commit(bar(QB_SF + buf));
+        return true;
+      };
+      if (ok) tc_fence_after();
+      if (ok) ok = issue_sdp(0);
+      if (ok && N > 1) ok = issue_sdp(1);
+      for (int n = 0; ok && n < N; ++n) {
+        const int st = n % DQ_ST;
+        if (!(ok = mbar_wait_bounded(bar(QB_P), n & 1, abort_flag, p.status, p.timeout_ns))) break;
+        tc_fence_after();
+        const uint32_t sKn = stage_addr(st);
+#pragma unroll
+        for (int ks = 0; ks < DQ_BK / 16; ++ks)
+          tc_mma_f16(tmem + 256, kmajor64(sDS, ks), mnmajor128(sKn, DQ_BK, ks), idesc_acc,
+                     (n > 0 || ks > 0) ? 1u : 0u);
+        tc_commit(bar(QB_MM));
+        tc_commit(bar(QB_E + st));
+        if (n + 2 < N) ok = issue_sdp(n + 2);
+      }
+      if (!ok) {
+        tc_commit(bar(QB_DRAIN));
+        (void)mbar_wait_bounded(bar(QB_DRAIN), 0u, nullptr, nullptr, p.timeout_ns);
+      }
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    const int qw = warp & 3;
+    const int r = qw * 32 + lane;
+    const int q = q0 + r;
+    const uint32_t tl = tmem + (static_cast<uint32_t>(qw * 32) << 16);
+    const int64_t sidx = (static_cast<int64_t>(bi) * p.heads + head) * p.s_pad + q;
+    const float lse_q = q < p.s ? p.lse[sidx] : 0.0f;
+    const float del_q = q < p.s ? p.delta[sidx] : 0.0f;
+    bool ok = true;
+    for (int n = 0; n < N; ++n) {
+      const int buf = n & 1;
+      ok = mbar_wait_bounded(bar(QB_SF + buf), (n >> 1) & 1u, abort_flag, p.status, p.timeout_ns);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      tc_fence_after();
+      float sv[DQ_BK], dp[DQ_BK];
+      tmem_ld32(tl + buf * 64, sv);
+      tmem_ld32(tl + buf * 64 + 32, sv + 32);
+      tmem_ld32(tl + 128 + buf * 64, dp);
+      tmem_ld32(tl + 128 + buf * 64 + 32, dp + 32);
+      const int kk = n * DQ_BK;
+#pragma unroll
+      for (int j = 0; j < DQ_BK; ++j) {
+        const int key = kk + j;
+        const bool vis = q < p.s && key < p.s && (!p.causal || key <= q);
+        const float pr = vis ? ex2(sv[j] * p.scale_log2 - lse_q) : 0.0f;
+        dp[j] = pr * (dp[j] - del_q);
+      }
+      if (n > 0) {
+        ok = mbar_wait_bounded(bar(QB_MM), (n - 1) & 1, abort_flag, p.status, p.timeout_ns);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      }
+#pragma unroll
+      for (int c = 0; c < DQ_BK / 8; ++c) st_swizzled(smem + DQ_DS, r, c, pack8<DT>(dp + c * 8));
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar(QB_P));
+    }
+    if (ok) {
+      ok = mbar_wait_bounded(bar(QB_MM), (N - 1) & 1, abort_flag, p.status, p.timeout_ns);
+      ok = __all_sync(0xffffffffu, ok);
+    }
+    if (ok) {
+      tc_fence_after();
+      const int64_t mrow = static_cast<int64_t>(q) * p.b + bi;
+      const int64_t ld = 3 * static_cast<int64_t>(p.h);
+#pragma unroll 1
+      for (int c = 0; c < HD / 32; ++c) {
+        float dq[32];
+        tmem_ld32(tl + 256 + c * 32, dq);
+        if (q < p.s) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) dq[j] *= p.scale;
+#pragma unroll
+          for (int g = 0; g < 4; ++g) store_row_chunk<DT>(p.dqkv, mrow * ld + colq + c * 32 + g * 8, dq + g * 8);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace attn
+}  // namespace tpmlp
+
+// ================================================================== host side
+namespace tpmlp {
+namespace attn {
+namespace {
+
+using EncodeFn = PFN_cuTensorMapEncodeTiled_v12000;
+
+EncodeFn get_encode() {
+  static EncodeFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(ptr);
+  });
+  return fn;
+}
+
+// 3-D map over a sequence-first [s][b][cols] activation: {cols, b, s}, box
+// {64, 1, rows}, 128-byte swizzle, zero fill past s.
+int make_map3(CUtensorMap* m, int dtype, const void* base, int64_t cols, int64_t b, int64_t s, uint32_t rows) {
+  EncodeFn enc = get_encode();
+  if (!enc) return set_error(TPMLP_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(b), static_cast<cuuint64_t>(s)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * 2, static_cast<cuuint64_t>(b * cols) * 2};
+  cuuint32_t box[3] = {64, 1, rows};
+  cuuint32_t es[3] = {1, 1, 1};
+  const CUresult r = enc(m, dtype == DT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                         3, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return set_error(TPMLP_ERR_CUDA, "cuTensorMapEncodeTiled (3-D) failed (code " + std::to_string(static_cast<int>(r)) + ")");
+  return TPMLP_OK;
+}
+
+struct Shape {
+  int64_t s, b, h;
+  int heads, tp, sp, dtype, causal;
+  int64_t M, s_pad, rpc;  // tokens, s rounded up to 128, rows per SP chunk
+  size_t e;
+  bool fused_ag;          // SP chunks read in place by the GEMMs
+};
+
+const uint8_t* cb(const void* p) { return static_cast<const uint8_t*>(p); }
+uint8_t* wb(void* p) { return static_cast<uint8_t*>(p); }
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+int check_shape(int64_t s, int64_t b, int64_t h, int heads, int tp, int sp, int dtype, int causal, Shape* out) {
+  if (s < 0 || b < 1 || h < 1) return set_error(TPMLP_ERR_INVALID_ARG, "s >= 0, b >= 1 and h >= 1 required");
+  if (heads < 1 || tp < 1 || tp > TPMLP_MAX_TP) return set_error(TPMLP_ERR_INVALID_ARG, "heads >= 1 and tp in [1, 64]");
+  if (sp != 0 && sp != 1) return set_error(TPMLP_ERR_INVALID_ARG, "sp must be 0 or 1");
+  if (causal != 0 && causal != 1) return set_error(TPMLP_ERR_INVALID_ARG, "causal must be 0 or 1");
+  if (dtype != DT_F16 && dtype != DT_BF16)
+    return set_error(TPMLP_ERR_UNSUPPORTED, "the attention block runs in float16 or bfloat16 storage");
+  if (h != static_cast<int64_t>(heads) * HD) return set_error(TPMLP_ERR_UNSUPPORTED, "head width must be 128 (h = 128·heads)");
+  if (heads % tp != 0) return set_error(TPMLP_ERR_NOT_DIVISIBLE, "the number of heads must be divisible by tensor parallel size");
+  if (sp && s % tp != 0)
+    return set_error(TPMLP_ERR_NOT_DIVISIBLE, "First dimension of the tensor should be divisible by tensor parallel size");
+  if (s > 65535ll * 128 || s * b >= (1ll << 31) || 3 * h >= (1ll << 31) || b >= 65536)
+    return set_error(TPMLP_ERR_UNSUPPORTED, "extent too large");
+  Shape k;
+  k.s = s;
+  k.b = b;
+  k.h = h;
+  k.heads = heads;
+  k.tp = tp;
+  k.sp = sp;
+  k.dtype = dtype;
+  k.causal = causal;
+  k.M = s * b;
+  k.s_pad = (s + 127) / 128 * 128;
+  k.rpc = sp ? (s / tp) * b : k.M;
+  k.e = 2;
+  k.fused_ag = sp && tp <= 16 && k.rpc % 128 == 0;
+  *out = k;
+  return TPMLP_OK;
+}
+
+// workspace: [X gathered | dZ gathered] when SP chunks are not read in place, then Δ.
+struct Ws {
+  size_t x_off, dz_off, delta_off, total;
+};
+Ws ws_layout(const Shape& k) {
+  Ws w{};
+  size_t off = 0;
+  const size_t act = static_cast<size_t>(k.M) * k.h * k.e;
+  const bool gathered = k.sp && !k.fused_ag;
+  w.x_off = off;
+  if (gathered) off += align256(act);
+  w.dz_off = off;
+  if (gathered) off += align256(act);
+  w.delta_off = off;
+  off += align256(static_cast<size_t>(k.b) * k.heads * k.s_pad * sizeof(float));
+  w.total = off;
+  return w;
+}
+
+int check_ptr(const void* p, size_t align, const char* name) {
+  if (p == nullptr) return set_error(TPMLP_ERR_INVALID_ARG, std::string(name) + " is NULL");
+  if (reinterpret_cast<uintptr_t>(p) % align != 0)
+    return set_error(TPMLP_ERR_UNSUPPORTED, std::string(name) + " must be 16-byte aligned");
+  return TPMLP_OK;
+}
+int check_ptrs(const void* const* a, int n, const char* name) {
+  if (a == nullptr) return set_error(TPMLP_ERR_INVALID_ARG, std::string(name) + " array is NULL");
+  for (int i = 0; i < n; ++i) {
+    int rc = check_ptr(a[i], 16, name);
+    if (rc) return rc;
+  }
+  return TPMLP_OK;
+}
+
+int gather_chunks(const Shape& k, const void* const* chunks, void* full, cudaStream_t st) {
+  void* dst[TPMLP_MAX_TP];
+  const size_t bytes = static_cast<size_t>(k.rpc) * k.h * k.e;
+  for (int j = 0; j < k.tp; ++j) dst[j] = wb(full) + j * bytes;
+  return launch_copy_chunks(chunks, dst, k.tp, static_cast<int64_t>(bytes), st);
+}
+
+int set_smem(const void* fn, size_t bytes) {
+  const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  if (e != cudaSuccess) return set_error(TPMLP_ERR_CUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
+  return TPMLP_OK;
+}
+
+int base_params(const Shape& k, AttnParams* p) {
+  DeviceInfo* dev = nullptr;
+  int rc = current_device(&dev);
+  if (rc) return rc;
+  memset(p, 0, sizeof(*p));
+  p->s = static_cast<int>(k.s);
+  p->b = static_cast<int>(k.b);
+  p->h = static_cast<int>(k.h);
+  p->heads = k.heads;
+  p->s_pad = static_cast<int>(k.s_pad);
+  p->causal = k.causal;
+  p->scale = 1.0f / std::sqrt(static_cast<float>(HD));
+  p->scale_log2 = 1.4426950408889634f / std::sqrt(static_cast<float>(HD));
+  p->status = dev->status;
+  p->timeout_ns = wait_timeout_ns();
+  return TPMLP_OK;
+}
+
+int launch_core_forward(const Shape& k, const void* qkv, void* o, float* lse, cudaStream_t st) {
+  AttnParams p;
+  int rc = base_params(k, &p);
+  if (rc) return rc;
+  if ((rc = make_map3(&p.qkv128, k.dtype, qkv, 3 * k.h, k.b, k.s, 128))) return rc;
+  p.o = o;
+  p.lse = lse;
+  const dim3 grid(static_cast<unsigned>(k.heads), static_cast<unsigned>(k.b), static_cast<unsigned>(k.s_pad / 128));
+  const void* fn = k.dtype == DT_BF16 ? reinterpret_cast<const void*>(attn_fwd_kernel<DT_BF16>)
+                                      : reinterpret_cast<const void*>(attn_fwd_kernel<DT_F16>);
+  if ((rc = set_smem(fn, F_SMEM))) return rc;
+  const int ph = prof_begin(PROF_ATTN, st);
+  if (k.dtype == DT_BF16) attn_fwd_kernel<DT_BF16><<<grid, ATT_THREADS, F_SMEM, st>>>(p);
+  else attn_fwd_kernel<DT_F16><<<grid, ATT_THREADS, F_SMEM, st>>>(p);
+  // QKᵀ and P·V over the visible (query, key) pairs
+  const double pairs = k.causal ? static_cast<double>(k.s) * (k.s + 1) / 2 : static_cast<double>(k.s) * k.s;
+  prof_end(ph, 4.0 * pairs * HD * k.heads * k.b, st);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return set_error(TPMLP_ERR_CUDA, std::string("attention forward launch: ") + cudaGetErrorString(e));
+  return TPMLP_OK;
+}
+
+int launch_core_backward(const Shape& k, const void* qkv, const void* o, const float* lse, const void* dout,
+                         float* delta, void* dqkv, cudaStream_t st) {
+  AttnParams p;
+  int rc = base_params(k, &p);
+  if (rc) return rc;
+  if ((rc = make_map3(&p.qkv128, k.dtype, qkv, 3 * k.h, k.b, k.s, 128)) ||
+      (rc = make_map3(&p.qkv64, k.dtype, qkv, 3 * k.h, k.b, k.s, 64)) ||
+      (rc = make_map3(&p.do128, k.dtype, dout, k.h, k.b, k.s, 128)) ||
+      (rc = make_map3(&p.do64, k.dtype, dout, k.h, k.b, k.s, 64)))
+    return rc;
+  p.lse = const_cast<float*>(lse);
+  p.delta = delta;
+  p.dqkv = dqkv;
+  const bool bf = k.dtype == DT_BF16;
+  const void* fkv = bf ? reinterpret_cast<const void*>(attn_bwd_dkdv_kernel<DT_BF16>)
+                       : reinterpret_cast<const void*>(attn_bwd_dkdv_kernel<DT_F16>);
+  const void* fq = bf ? reinterpret_cast<const void*>(attn_bwd_dq_kernel<DT_BF16>)
+                      : reinterpret_cast<const void*>(attn_bwd_dq_kernel<DT_F16>);
+  if ((rc = set_smem(fkv, KV_SMEM)) || (rc = set_smem(fq, DQ_SMEM))) return rc;
+  const int ph = prof_begin(PROF_ATTN, st);
+  const int64_t warps = k.s_pad * k.b * k.heads;
+  const unsigned gd = static_cast<unsigned>((warps * 32 + 255) / 256);
+  if (bf) attn_bwd_delta_kernel<DT_BF16><<<gd, 256, 0, st>>>(dout, o, delta, p.s, p.b, p.h, p.heads, p.s_pad);
+  else attn_bwd_delta_kernel<DT_F16><<<gd, 256, 0, st>>>(dout, o, delta, p.s, p.b, p.h, p.heads, p.s_pad);
+  const dim3 gkv(static_cast<unsigned>(k.heads), static_cast<unsigned>(k.b), static_cast<unsigned>(k.s_pad / 128));
+  if (bf) attn_bwd_dkdv_kernel<DT_BF16><<<gkv, ATT_THREADS, KV_SMEM, st>>>(p);
+  else attn_bwd_dkdv_kernel<DT_F16><<<gkv, ATT_THREADS, KV_SMEM, st>>>(p);
+  if (bf) attn_bwd_dq_kernel<DT_BF16><<<gkv, ATT_THREADS, DQ_SMEM, st>>>(p);
+  else attn_bwd_dq_kernel<DT_F16><<<gkv, ATT_THREADS, DQ_SMEM, st>>>(p);
+  // dV, dP, dQ, dK over the visible pairs (the recomputed S is not counted)
+  const double pairs = k.causal ? static_cast<double>(k.s) * (k.s + 1) / 2 : static_cast<double>(k.s) * k.s;
+  prof_end(ph, 8.0 * pairs * HD * k.heads * k.b, st, 3);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return set_error(TPMLP_ERR_CUDA, std::string("attention backward launch: ") + cudaGetErrorString(e));
+  return TPMLP_OK;
+}
+
+GemmDesc gemm(const Shape& k) {
+  GemmDesc g;
+  g.dtype = k.dtype;
+  g.nparts = 1;
+  return g;
+}
+
+void scatter_to(const Shape& k, void* const* out, GemmDesc* g) {
+  g->epi.kind = EPI_STORE;
+  g->epi.ldo = k.h;
+  if (k.sp) {
+    g->epi.scatter = 1;
+    g->epi.nshards = k.tp;
+    g->epi.rows_per_shard = k.rpc;
+    for (int j = 0; j < k.tp; ++j) g->epi.shard[j] = out[j];
+  } else {
+    g->epi.out = out[0];
+  }
+}
+
+}  // namespace
+}  // namespace attn
+}  // namespace tpmlp
+
+using namespace tpmlp;
+using namespace tpmlp::attn;
+
+extern "C" {
+
+size_t tpmlp_attn_workspace_size(int64_t s, int64_t b, int64_t h, int heads, int tp, int sp, int dtype) {
+  Shape k;
+  if (check_shape(s, b, h, heads, tp, sp, dtype, 0, &k) != TPMLP_OK) return 0;
+  return ws_layout(k).total;
+}
+
+int tpmlp_attn_forward(int64_t s, int64_t b, int64_t h, int heads, int tp, int sp, int dtype, int causal,
+                       const void* const* x, const void* wqkv, const void* wo, void* qkv, void* o, float* lse,
+                       void* const* z, void* ws, size_t ws_bytes, void* stream) {
+  Shape k;
+  int rc = check_shape(s, b, h, heads, tp, sp, dtype, causal, &k);
+  if (rc) return rc;
+  const int nio = sp ? tp : 1;
+  if ((rc = check_ptrs(x, nio, "x")) || (rc = check_ptr(wqkv, 16, "wqkv")) || (rc = check_ptr(wo, 16, "wo")) ||
+      (rc = check_ptr(qkv, 16, "qkv")) || (rc = check_ptr(o, 16, "o")) || (rc = check_ptr(lse, 16, "lse")) ||
+      (rc = check_ptrs(const_cast<const void* const*>(z), nio, "z")))
+    return rc;
+  const Ws W = ws_layout(k);
+  const bool gathered = k.sp && !k.fused_ag;
+  if (gathered) {
+    if (ws == nullptr || ws_bytes < W.total)
+      return set_error(TPMLP_ERR_WORKSPACE, "workspace needs " + std::to_string(W.total) + " bytes");
+    if ((rc = check_ptr(ws, 256, "ws"))) return rc;
+  }
+  if (k.M == 0) return TPMLP_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const void* X = x[0];
+  if (gathered) {
+    if ((rc = gather_chunks(k, x, wb(ws) + W.x_off, st))) return rc;
+    X = wb(ws) + W.x_off;
+  }
+  // QKV = X·Wqkvᵀ: column-parallel, every shard's heads in one launch.
+  {
+    GemmDesc g = gemm(k);
+    g.M = k.M;
+    g.N = 3 * h;
+    g.lda = h;
+    g.ldb = h;
+    g.b_rows = 3 * h;
+    g.segs.push_back(GemmSeg{X, wqkv, h, 0});
+    if (k.fused_ag) {
+      g.a_chunks.assign(x, x + tp);
+      g.a_chunk_rows = k.rpc;
+    }
+    g.epi.kind = EPI_STORE;
+    g.epi.out = qkv;
+    g.epi.ldo = 3 * h;
+    if ((rc = launch_gemm_tc(g, st))) return rc;
+  }
+  if ((rc = launch_core_forward(k, qkv, o, lse, st))) return rc;
+  // Z = Σ_i O_i·Wo_iᵀ: the shards' K ranges accumulate in order in one
+  // accumulator; under SP each row goes straight to its sequence chunk.
+  GemmDesc g = gemm(k);
+  g.M = k.M;
+  g.N = h;
+  g.lda = h;
+  g.ldb = h;
+  g.b_rows = h;
+  g.segs.push_back(GemmSeg{o, wo, h, 0});
+  scatter_to(k, z, &g);
+  return launch_gemm_tc(g, st);
+}
+
+int tpmlp_attn_backward(int64_t s, int64_t b, int64_t h, int heads, int tp, int sp, int dtype, int causal,
+                        const void* const* x, const void* wqkv, const void* wo, const void* qkv, const void* o,
+                        const float* lse, const void* const* dz, void* const* dx, void* dwqkv, void* dwo, void* dqkv,
+                        void* dout, void* ws, size_t ws_bytes, void* stream) {
+  Shape k;
+  int rc = check_shape(s, b, h, heads, tp, sp, dtype, causal, &k);
+  if (rc) return rc;
+  const int nio = sp ? tp : 1;
+  if ((rc = check_ptrs(x, nio, "x")) || (rc = check_ptr(wqkv, 16, "wqkv")) || (rc = check_ptr(wo, 16, "wo")) ||
+      (rc = check_ptr(qkv, 16, "qkv")) || (rc = check_ptr(o, 16, "o")) || (rc = check_ptr(lse, 16, "lse")) ||
+      (rc = check_ptrs(dz, nio, "dz")) || (rc = check_ptrs(const_cast<const void* const*>(dx), nio, "dx")) ||
+      (rc = check_ptr(dwqkv, 16, "dwqkv")) || (rc = check_ptr(dwo, 16, "dwo")) || (rc = check_ptr(dqkv, 16, "dqkv")) ||
+      (rc = check_ptr(dout, 16, "dout")))
+    return rc;
+  const Ws W = ws_layout(k);
+  if (ws == nullptr || ws_bytes < W.total)
+    return set_error(TPMLP_ERR_WORKSPACE, "workspace needs " + std::to_string(W.total) + " bytes");
+  if ((rc = check_ptr(ws, 256, "ws"))) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (k.M == 0) {
+    cudaError_t e = cudaMemsetAsync(dwqkv, 0, static_cast<size_t>(3 * h) * h * k.e, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dwo, 0, static_cast<size_t>(h) * h * k.e, st);
+    if (e != cudaSuccess) return set_error(TPMLP_ERR_CUDA, std::string("cudaMemsetAsync: ") + cudaGetErrorString(e));
+    return TPMLP_OK;
+  }
+  const bool gathered = k.sp && !k.fused_ag;
+  const void* X = x[0];
+  const void* dZ = dz[0];
+  if (gathered) {
+    if ((rc = gather_chunks(k, dz, wb(ws) + W.dz_off, st))) return rc;
+    if ((rc = gather_chunks(k, x, wb(ws) + W.x_off, st))) return rc;
+    dZ = wb(ws) + W.dz_off;
+    X = wb(ws) + W.x_off;
+  }
+  // dO = dZ·Wo (g's backward is the identity / the all-gather of dZ).
+  {
+    GemmDesc g = gemm(k);
+    g.M = k.M;
+    g.N = h;
+    g.b_mn = true;  // B(n, k) = Wo[k, n]
+    g.lda = h;
+    g.ldb = h;
+    g.b_rows = h;
+    g.segs.push_back(GemmSeg{dZ, wo, h, 0});
+    if (k.fused_ag) {
+      g.a_chunks.assign(dz, dz + tp);
+      g.a_chunk_rows = k.rpc;
+    }
+    g.epi.kind = EPI_STORE;
+    g.epi.out = dout;
+    g.epi.ldo = h;
+    if ((rc = launch_gemm_tc(g, st))) return rc;
+  }
+  // dWo = dZᵀ·O (each shard's column block of Wo from its heads' O).
+  {
+    GemmDesc g = gemm(k);
+    g.M = h;
+    g.N = h;
+    g.a_mn = true;
+    g.b_mn = true;
+    g.lda = h;
+    g.ldb = h;
+    g.b_rows = h;
+    if (k.fused_ag) {
+      for (int j = 0; j < tp; ++j) g.segs.push_back(GemmSeg{dz[j], cb(o) + j * k.rpc * h * k.e, k.rpc, 0});
+    } else {
+      g.segs.push_back(GemmSeg{dZ, o, k.M, 0});
+    }
+    g.epi.kind = EPI_STORE;
+    g.epi.out = dwo;
+    g.epi.ldo = h;
+    if ((rc = launch_gemm_tc(g, st))) return rc;
+  }
+  if ((rc = launch_core_backward(k, qkv, o, lse, dout, reinterpret_cast<float*>(wb(ws) + W.delta_off), dqkv, st)))
+    return rc;
+  // dWqkv = dQKVᵀ·X.
+  {
+    GemmDesc g = gemm(k);
+    g.M = 3 * h;
+    g.N = h;
+    g.a_mn = true;
+    g.b_mn = true;
+    g.lda = 3 * h;
+    g.ldb = h;
+    g.b_rows = h;
+    if (k.fused_ag) {
+      for (int j = 0; j < tp; ++j) g.segs.push_back(GemmSeg{cb(dqkv) + j * k.rpc * 3 * h * k.e, x[j], k.rpc, 0});
+    } else {
+      g.segs.push_back(GemmSeg{dqkv, X, k.M, 0});
+    }
+    g.epi.kind = EPI_STORE;
+    g.epi.out = dwqkv;
+    g.epi.ldo = h;
+    if ((rc = launch_gemm_tc(g, st))) return rc;
+  }
+  // dX = Σ_i dQKV_i·Wqkv_i (f's backward), shard sum folded into the accumulator.
+  GemmDesc g = gemm(k);
+  g.M = k.M;
+  g.N = h;
+  g.b_mn = true;  // B(n, k) = Wqkv[k, n]
+  g.lda = 3 * h;
+  g.ldb = h;
+  g.b_rows = 3 * h;
+  g.segs.push_back(GemmSeg{dqkv, wqkv, 3 * h, 0});
+  scatter_to(k, dx, &g);
+  return launch_gemm_tc(g, st);
+}
+
+}  // extern "C"

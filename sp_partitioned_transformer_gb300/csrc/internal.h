@@ -90,7 +90,14 @@ int launch_residual_dropout(bool forward, const void* const* r, const void* cons
 
 // Launch accounting (tpmlp_profile_start/stop): bracket one or more kernel launches with
 // CUDA events on its stream.  prof_begin returns -1 when accounting is off.
-enum ProfKind : int { PROF_GEMM_TC = 0, PROF_GEMM_SIMT = 1, PROF_COPY = 2, PROF_SHARD_SUM = 3, PROF_SP_REGION = 4 };
+enum ProfKind : int {
+  PROF_GEMM_TC = 0,
+  PROF_GEMM_SIMT = 1,
+  PROF_COPY = 2,
+  PROF_SHARD_SUM = 3,
+  PROF_SP_REGION = 4,
+  PROF_ATTN = 5
+};
 int prof_begin(int kind, cudaStream_t st);
 // `kernels` is the number of kernel launches the region enclosed.
 void prof_end(int handle, double work, cudaStream_t st, int kernels = 1);

@@ -39,7 +39,7 @@ def test_header_declares_the_boundary():
 def test_library_exports_every_declared_symbol(lib):
     missing = [n for n in declared_functions() if not hasattr(lib, n)]
     assert not missing, missing
-    assert lib.tpmlp_abi_version() == 1
+    assert lib.tpmlp_abi_version() == 2
 
 
 def _ws(lib, *a):
@@ -142,3 +142,46 @@ def test_binding_refuses_to_run_without_the_library(tmp_path):
             tpmlp.load(str(tmp_path / "missing.so"))
     finally:
         tpmlp._lib = saved
+
+
+def _attn_fwd(lib, s=256, b=1, h=256, heads=2, tp=2, sp=1, dt=2, causal=0, wqkv=FAKE, lse=FAKE, ws=None,
+              ws_bytes=0):
+    n = tp if sp else 1
+    x = _vp(*([FAKE] * n))
+    z = _vp(*([FAKE] * n))
+    f = lib.tpmlp_attn_forward
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_int64] * 3 + [ctypes.c_int] * 5 + [ctypes.c_void_p] * 7 + [ctypes.c_void_p,
+                                                                                       ctypes.c_size_t,
+                                                                                       ctypes.c_void_p]
+    return f(s, b, h, heads, tp, sp, dt, causal, x, wqkv, FAKE, FAKE, FAKE, lse, z, ws, ws_bytes, None)
+
+
+def test_attention_rejects_bad_arguments_on_the_host(lib):
+    assert _attn_fwd(lib, heads=3, h=384, tp=2) == NOT_DIV  # heads % tp
+    assert b"heads" in lib.tpmlp_last_error()
+    assert _attn_fwd(lib, s=255) == NOT_DIV  # s % tp under SP
+    assert _attn_fwd(lib, h=320) == UNSUP  # head width must be 128
+    assert _attn_fwd(lib, dt=0) == UNSUP  # float32 storage
+    assert _attn_fwd(lib, causal=2) == INVALID
+    assert _attn_fwd(lib, tp=0) == INVALID
+    assert _attn_fwd(lib, wqkv=None) == INVALID
+    assert _attn_fwd(lib, lse=FAKE + 4) == UNSUP  # 16-byte alignment
+    # 96-row chunks (s/tp·b = 96) are gathered through the workspace
+    assert _attn_fwd(lib, s=192, ws=None) == WORKSPACE
+    assert b"workspace" in lib.tpmlp_last_error()
+
+
+def test_attention_workspace_formula(lib):
+    f = lib.tpmlp_attn_workspace_size
+    f.restype = ctypes.c_size_t
+    f.argtypes = [ctypes.c_int64] * 3 + [ctypes.c_int] * 4
+
+    def a256(x):
+        return (x + 255) // 256 * 256
+
+    # 128-row chunks read in place: only Δ [b][heads][s_pad] float32
+    assert f(256, 1, 256, 2, 2, 1, 2) == a256(1 * 2 * 256 * 4)
+    # 96-row chunks: gathered X and dZ, then Δ (s_pad = 256)
+    assert f(192, 1, 256, 2, 2, 1, 2) == 2 * a256(192 * 256 * 2) + a256(2 * 256 * 4)
+    assert f(192, 1, 320, 2, 2, 1, 2) == 0  # invalid (h != 128·heads) -> 0

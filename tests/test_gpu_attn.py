@@ -1,0 +1,153 @@
+"""The tensor-parallel attention block on the GPU, through the C ABI, against the
+fp64 oracle (oracle/attn_fp64.py): Z, dX, dWqkv, dWo and the saved
+intermediates (QKV, O, lse2, dO, dQKV), both masks, both 16-bit storage types,
+SP chunks read in place (whole 128-row chunks) or gathered (ragged chunks),
+ragged sequence lengths, several sequences per batch, and bit-identical
+repeats.  Tolerance ‖GPU − oracle‖∞ / ‖oracle‖∞ ≤ 2e-2 per tensor."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from gpu_common import chunks, rel_err, to_np
+from synthetic import ATTN_CONFIGS, AttnConfig, attn_inputs
+
+pytestmark = pytest.mark.gpu
+
+TOL = 2e-2
+
+
+def _run(tpmlp, cfg, t=None):
+    t = t or attn_inputs(cfg)
+    dev = "cuda"
+    X, Wqkv, Wo, dZ = (t[k].to(dev) for k in ("X", "Wqkv", "Wo", "dZ"))
+    x = chunks(X, cfg.tp) if cfg.sp else X
+    dz = chunks(dZ, cfg.tp) if cfg.sp else dZ
+    blk = tpmlp.AttnBlock(cfg.s, cfg.b, cfg.h, cfg.heads, cfg.tp, cfg.sp, cfg.torch_dtype, cfg.causal)
+    fw = blk.forward(x, Wqkv, Wo)
+    bw = blk.backward(x, Wqkv, Wo, fw, dz)
+    torch.cuda.synchronize()
+    assert tpmlp.device_status() == 0, tpmlp.last_error()
+    cat = (lambda v: torch.cat(v)) if cfg.sp else (lambda v: v)
+    return t, blk, fw, bw, cat
+
+
+def _flat(a, M):
+    return np.asarray(a).reshape(M, -1)
+
+
+CASES = [
+    # name, s, b, h, heads, tp, sp, dtype, causal
+    AttnConfig("ag-gathered", 192, 2, 512, 4, 2, True, "bf16", False),
+    AttnConfig("ag-in-place-causal", 256, 1, 256, 2, 2, True, "bf16", True),
+    AttnConfig("no-sp-f16", 128, 1, 256, 2, 1, False, "f16", False),
+    AttnConfig("no-sp-f16-causal", 128, 2, 256, 2, 1, False, "f16", True),
+    AttnConfig("short-ragged", 100, 3, 256, 2, 1, False, "bf16", True),
+    AttnConfig("ragged-tiles", 320, 1, 512, 4, 4, True, "bf16", True),
+    AttnConfig("multi-tile-in-place", 1024, 1, 512, 4, 2, True, "bf16", False),
+]
+
+
+@pytest.mark.parametrize("cfg", CASES, ids=[c.name for c in CASES])
+def test_attention_block_matches_the_oracle(cuda_lib, cfg):
+    tpmlp = cuda_lib
+    t, blk, fw, bw, cat = _run(tpmlp, cfg)
+    M, s, b, heads = cfg.M, cfg.s, cfg.b, cfg.heads
+    X, Wqkv, Wo, dZ = (to_np(t[k]).reshape(-1, t[k].shape[-1]) for k in ("X", "Wqkv", "Wo", "dZ"))
+    ref = O.attn_forward(X, Wqkv, Wo, s, b, heads, cfg.causal)
+    assert rel_err(to_np(fw["qkv"]), ref["QKV"]) <= TOL
+    assert rel_err(to_np(fw["o"]), ref["O"]) <= TOL
+    lse = to_np(fw["lse"])[:, :, :s]
+    assert np.abs(lse - ref["lse2"]).max() <= 2e-2 * max(1.0, np.abs(ref["lse2"]).max())
+    assert rel_err(_flat(to_np(cat(fw["z"])), M), ref["Z"]) <= TOL
+    g = O.attn_backward(X, Wqkv, Wo, dZ, s, b, heads, cfg.causal)
+    assert rel_err(to_np(bw["dout"]), g["dO"]) <= TOL
+    assert rel_err(to_np(bw["dqkv"]), g["dQKV"]) <= TOL
+    assert rel_err(_flat(to_np(cat(bw["dx"])), M), g["dX"]) <= TOL
+    assert rel_err(to_np(bw["dwqkv"]), g["dWqkv"]) <= TOL
+    assert rel_err(to_np(bw["dwo"]), g["dWo"]) <= TOL
+
+
+def test_attention_core_alone_on_the_gpu_s_own_qkv(cuda_lib):
+    """The core's O, lse2 and dQ/dK/dV against the oracle's core evaluated on the
+    GPU's own (rounded) QKV and dO: isolates the flash kernels from the
+    projections."""
+    tpmlp = cuda_lib
+    cfg = AttnConfig("core", 384, 2, 512, 4, 2, True, "bf16", True)
+    t, blk, fw, bw, cat = _run(tpmlp, cfg)
+    Q, K, V = O.split_qkv(to_np(fw["qkv"]), cfg.heads)
+    core = O.attention_core_forward(Q, K, V, cfg.s, cfg.b, cfg.heads, True)
+    assert rel_err(to_np(fw["o"]), core["O"]) <= 1e-2
+    assert np.abs(to_np(fw["lse"])[:, :, :cfg.s] - core["lse2"]).max() <= 1e-3 * np.abs(core["lse2"]).max()
+    gc = O.attention_core_backward(Q, K, V, to_np(bw["dout"]), cfg.s, cfg.b, cfg.heads, True)
+    dq, dk, dv = O.split_qkv(to_np(bw["dqkv"]), cfg.heads)
+    assert rel_err(dq, gc["dQ"]) <= TOL
+    assert rel_err(dk, gc["dK"]) <= TOL
+    assert rel_err(dv, gc["dV"]) <= TOL
+
+
+def test_attention_is_deterministic(cuda_lib):
+    tpmlp = cuda_lib
+    cfg = AttnConfig("det", 256, 1, 512, 4, 2, True, "bf16", True)
+    t = attn_inputs(cfg)
+    _, _, fw1, bw1, cat = _run(tpmlp, cfg, t)
+    _, _, fw2, bw2, _ = _run(tpmlp, cfg, t)
+    assert torch.equal(cat(fw1["z"]), cat(fw2["z"]))
+    for k in ("dwqkv", "dwo", "dqkv"):
+        assert torch.equal(bw1[k], bw2[k]), k
+    assert torch.equal(cat(bw1["dx"]), cat(bw2["dx"]))
+
+
+def test_sp_on_equals_sp_off(cuda_lib):
+    """Reading the SP chunks in place (all-gather fused into the GEMM loads) and the
+    reduce-scatter fused into the epilogue give the SP-off block's bits."""
+    tpmlp = cuda_lib
+    on = AttnConfig("sp", 256, 2, 256, 2, 2, True, "bf16", False)
+    t = attn_inputs(on)
+    _, _, fa, ba, cat = _run(tpmlp, on, t)
+    _, _, fb, bb, _ = _run(tpmlp, on.with_(sp=False), t)
+    assert torch.equal(cat(fa["z"]), fb["z"])
+    assert torch.equal(cat(ba["dx"]), bb["dx"])
+    assert torch.equal(ba["dwqkv"], bb["dwqkv"]) and torch.equal(ba["dwo"], bb["dwo"])
+
+
+def test_llama70b_width_attention_sampled(cuda_lib):
+    """The benchmark's workload ([4096, 1, 8192], 64 heads of 128, tp 8, SP, causal,
+    bf16) at full size: the core of two heads (one in the first shard, one in the
+    last) against the oracle's core on the GPU's own QKV and dO, and the
+    projections on sampled rows."""
+    tpmlp = cuda_lib
+    cfg = ATTN_CONFIGS["llama70b_attn_tpsp8_bf16"]
+    t, blk, fw, bw, cat = _run(tpmlp, cfg)
+    s, b, d = cfg.s, cfg.b, cfg.d
+    qkv = to_np(fw["qkv"])
+    o = to_np(fw["o"])
+    do = to_np(bw["dout"])
+    dqkv = to_np(bw["dqkv"])
+    for j in (3, 60):
+        cols = slice(3 * d * j, 3 * d * (j + 1))
+        Q, K, V = O.split_qkv(qkv[:, cols], 1)
+        core = O.attention_core_forward(Q, K, V, s, b, 1, True)
+        assert rel_err(o[:, d * j:d * (j + 1)], core["O"]) <= 1e-2
+        gc = O.attention_core_backward(Q, K, V, do[:, d * j:d * (j + 1)], s, b, 1, True)
+        dq, dk, dv = O.split_qkv(dqkv[:, cols], 1)
+        assert rel_err(dq, gc["dQ"]) <= TOL
+        assert rel_err(dk, gc["dK"]) <= TOL
+        assert rel_err(dv, gc["dV"]) <= TOL
+    # projections on sampled rows, with the oracle's fp64 products of the GPU's inputs
+    rows = np.array([0, 1, 511, 512, 2047, 4095])
+    X = to_np(t["X"]).reshape(-1, cfg.h)
+    Wqkv, Wo = to_np(t["Wqkv"]), to_np(t["Wo"])
+    assert rel_err(qkv[rows], X[rows] @ Wqkv.T) <= TOL
+    z = to_np(cat(fw["z"])).reshape(-1, cfg.h)
+    assert rel_err(z[rows], o[rows] @ Wo.T) <= TOL
+    dZ = to_np(t["dZ"]).reshape(-1, cfg.h)
+    assert rel_err(do[rows], dZ[rows] @ Wo) <= TOL
+    dx = to_np(cat(bw["dx"])).reshape(-1, cfg.h)
+    assert rel_err(dx[rows], dqkv[rows] @ Wqkv) <= TOL
+    feats = np.array([0, 127, 4096, 8191])
+    dwo = to_np(bw["dwo"])
+    assert rel_err(dwo[feats], dZ[:, feats].T @ o) <= TOL
+    dwqkv = to_np(bw["dwqkv"])
+    qrows = np.array([0, 383, 12288, 24575])
+    assert rel_err(dwqkv[qrows], dqkv[:, qrows].T @ X) <= TOL
