@@ -18,6 +18,11 @@ value = all ranks' FLOPs / max-over-ranks time.
 
 --impl reference times the CPU oracle (NumPy fp64) on a bounded token sample of
 the same workload, on the host cores, with the same metric and unit.
+
+--block attention times the tensor-parallel self-attention block instead
+(QKV projection, per-head attention core, output projection, and the
+backward) on the Llama-70B width ([4096,1,8192], 64 heads of 128, tp = 8, SP,
+causal, bf16) or another --config from synthetic.ATTN_CONFIGS.
 """
 from __future__ import annotations
 
@@ -53,6 +58,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-dim0", action="store_true", help="skip the stand-alone dim-0 kernel measurement")
     ap.add_argument("--main-grad", action="store_true",
                     help="weight gradients accumulated into float32 main_grad (gradient-accumulation fusion)")
+    ap.add_argument("--block", choices=["mlp", "attention"], default="mlp")
     ap.add_argument("--sp-region", action="store_true",
                     help="time the whole SP sublayer: LayerNorm on the chunks -> block -> dropout + residual, "
                          "and its backward (FLOPs counted are the block's)")
@@ -546,7 +552,7 @@ def run_ours(args) -> int:
     per_kernel = {}
     for k, v in prof.items():
         if v["launches"]:
-            unit = "TFLOP/s" if k.startswith("gemm") else "GB/s"
+            unit = "TFLOP/s" if k.startswith("gemm") or k == "attn_core" else "GB/s"
             rate = v["work"] / (v["ms"] / 1e3) / (1e12 if unit == "TFLOP/s" else 1e9)
             per_kernel[k] = {"launches_per_step": v["launches"] / args.steps, "ms_per_step": v["ms"] / args.steps,
                              "achieved": rate, "unit": unit,
@@ -630,10 +636,106 @@ def run_ours(args) -> int:
     return 0
 
 
+def run_attention(args) -> int:
+    """Forward + backward of the tensor-parallel attention block through the C ABI."""
+    import torch
+
+    from sp_partitioned_transformer_gb300 import build as _build
+
+    _build.build()
+    import sp_partitioned_transformer_gb300 as tpmlp
+    from synthetic import ATTN_CONFIGS, attn_inputs
+
+    tpmlp.load()
+    name = args.config if args.config in ATTN_CONFIGS else "llama70b_attn_tpsp8_bf16"
+    cfg = ATTN_CONFIGS[name]
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    t = attn_inputs(cfg)
+    X, Wqkv, Wo, dZ = (t[k].to(dev) for k in ("X", "Wqkv", "Wo", "dZ"))
+    x = [c.contiguous() for c in X.chunk(cfg.tp)] if cfg.sp else X
+    dz = [c.contiguous() for c in dZ.chunk(cfg.tp)] if cfg.sp else dZ
+    blk = tpmlp.AttnBlock(cfg.s, cfg.b, cfg.h, cfg.heads, cfg.tp, cfg.sp, cfg.torch_dtype, cfg.causal, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    fw = blk.forward(x, Wqkv, Wo, stream=stream)
+    bw = blk.backward(x, Wqkv, Wo, fw, dz, stream=stream)
+    kw = dict(s=cfg.s, b=cfg.b, h=cfg.h, heads=cfg.heads, tp=cfg.tp, sp=cfg.sp, causal=cfg.causal,
+              workspace=blk.ws, stream=stream)
+
+    def step():
+        tpmlp.attn_forward(x, Wqkv, Wo, fw["qkv"], fw["o"], fw["lse"], fw["z"], **kw)
+        tpmlp.attn_backward(x, Wqkv, Wo, fw["qkv"], fw["o"], fw["lse"], dz, bw["dx"], bw["dwqkv"], bw["dwo"],
+                            bw["dqkv"], bw["dout"], **kw)
+
+    clocks = ClockSampler(gpu_uuid(0))
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    tpmlp.profile_start()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    prof = tpmlp.profile_stop()
+    clock_info = clocks.stop()
+    if tpmlp.device_status() != 0:
+        raise RuntimeError(f"device status {tpmlp.device_status()}: {tpmlp.last_error()}")
+    ms = e0.elapsed_time(e1) / args.steps
+    flops = float(cfg.flops_fwd_bwd())
+    peaks, peak_src = load_peaks()
+    peak = peaks.get("bf16_tflops_sustained") or FALLBACK_PEAKS["bf16_tflops_sustained"]
+    per_kernel = {}
+    for k, v in prof.items():
+        if v["launches"]:
+            tf = k.startswith("gemm") or k == "attn_core"
+            rate = v["work"] / (v["ms"] / 1e3) / (1e12 if tf else 1e9)
+            per_kernel[k] = {"launches_per_step": v["launches"] / args.steps, "ms_per_step": v["ms"] / args.steps,
+                             "achieved": rate, "unit": "TFLOP/s" if tf else "GB/s",
+                             "share_of_step": v["ms"] / args.steps / ms}
+    a = prof["attn_core"]
+    achieved = a["work"] / (a["ms"] / 1e3) / 1e12
+    line = {
+        "metric": "TP/SP attention block fwd+bwd TFLOP/s on 1 GB300 and % of dense BF16 peak",
+        "value": flops / (ms / 1e3) / 1e12,
+        "unit": UNIT,
+        "n_gpus": 1,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": cfg.dtype,
+        "data": "synthetic",
+        "config": {"workload": f"TP self-attention [s,b,h]=[{cfg.s},{cfg.b},{cfg.h}] {cfg.heads} heads of {cfg.d} "
+                               f"tp={cfg.tp} SP {'on' if cfg.sp else 'off'} {'causal' if cfg.causal else 'unmasked'} "
+                               f"{cfg.dtype}, fwd+bwd",
+                   "name": cfg.name, "flops_per_step": flops,
+                   "flops_note": "24·M·h² projections + 12·b·h·(visible query-key pairs) core, no recomputation",
+                   "l2": f"inputs larger than L2: Wqkv is {3 * cfg.h * cfg.h * 2 / 1e6:.0f} MB, no flush"},
+        "frac_of_dense_bf16_peak": {"sustained": flops / (ms / 1e3) / 1e12 / peak, "peak_source": peak_src},
+        "roofline": {"bound": "tensor", "kernel": "tpmlp::attn core (attn_fwd_kernel, attn_bwd_dkdv_kernel, "
+                                                  "attn_bwd_dq_kernel, attn_bwd_delta_kernel)",
+                     "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                     "peak_source": f"{peak_src} bf16_tflops_sustained", "traffic": None, "per_kernel": per_kernel},
+        "gpu_launches": sum(v["launches"] for v in prof.values()),
+        "clocks": clock_info,
+        "device": {"name": torch.cuda.get_device_name(dev),
+                   "sms": torch.cuda.get_device_properties(dev).multi_processor_count},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None) -> int:
     args = parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
+    if args.block == "attention":
+        return run_attention(args)
     return run_ours(args)
 
 

@@ -39,7 +39,8 @@ namespace tpmlp {
 namespace attn {
 
 constexpr int HD = 128;  // head width (d)
-constexpr int ATT_THREADS = 256;
+constexpr int ATT_THREADS = 384;  // warps 0-3: TMA, MMA, TMEM, idle; warps 4-11: two compute groups
+constexpr int COMPUTE_THREADS = 256;
 constexpr uint32_t HALF_ROW_BYTES = 128;  // one 64-column half row of 16-bit elements
 
 // ---------------------------------------------------------------- device helpers
@@ -153,10 +154,12 @@ __device__ __forceinline__ void store_row_chunk(void* base, int64_t off, const f
 // ================================================================== forward
 constexpr int F_BQ = 128, F_BK = 128;
 constexpr uint32_t F_TILE = 128 * 128 * 2;  // 32 KB
-constexpr uint32_t F_Q = 0, F_K0 = F_TILE, F_V0 = 3 * F_TILE, F_P = 5 * F_TILE, F_END = 6 * F_TILE;
+constexpr uint32_t F_Q = 0, F_K0 = F_TILE, F_V0 = 3 * F_TILE, F_P = 5 * F_TILE;
+constexpr uint32_t F_RED = 6 * F_TILE;                 // [2 parities][2 groups][128 rows] float
+constexpr uint32_t F_END = F_RED + 2 * 2 * 128 * 4;
 constexpr size_t F_SMEM = 1024 + F_END + sizeof(Tail);
 // barriers
-enum { FB_Q = 0, FB_KF = 1, FB_KE = 3, FB_VF = 5, FB_VE = 7, FB_SF = 9, FB_P = 11, FB_O = 12, FB_DRAIN = 13 };
+enum { FB_Q = 0, FB_KF = 1, FB_KE = 3, FB_VF = 5, FB_VE = 7, FB_SF = 9, FB_P = 11, FB_O = 12, FB_DRAIN = 13, FB_RED = 14 };
 
 template <int DT>
 __global__ void __launch_bounds__(ATT_THREADS, 1) attn_fwd_kernel(const __grid_constant__ AttnParams p) {
@@ -186,9 +189,11 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_fwd_kernel(const __grid_c
       mbar_init(bar(FB_VE + i), 1);
       mbar_init(bar(FB_SF + i), 1);
     }
-    mbar_init(bar(FB_P), 128);
+    mbar_init(bar(FB_P), COMPUTE_THREADS);
     mbar_init(bar(FB_O), 1);
     mbar_init(bar(FB_DRAIN), 1);
+    mbar_init(bar(FB_RED), COMPUTE_THREADS);
+    mbar_init(bar(FB_RED + 1), COMPUTE_THREADS);
     tail->abort_flag = 0;
     fence_barrier_init();
   }
@@ -271,39 +276,57 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_fwd_kernel(const __grid_c
     }
     __syncwarp();
   } else if (warp >= 4) {
+    // Two groups of four warps; group g takes columns [64g, 64g+64) of every S
+    // tile and of O, for the 128 rows (one per thread, = TMEM lane).  The row
+    // maximum is combined across the groups through shared memory and an
+    // mbarrier; each group keeps its own partial row sum until the end.
+    const int g = (warp - 4) >> 2;
     const int qw = warp & 3;
-    const int r = qw * 32 + lane;  // row of the tile = TMEM lane
+    const int r = qw * 32 + lane;
     const int q = q0 + r;
     const uint32_t tl = tmem + (static_cast<uint32_t>(qw * 32) << 16);
-    float m = -INFINITY, l = 0.0f;
+    float* red = reinterpret_cast<float*>(smem + F_RED);
+    const float c = p.scale_log2;
+    float m = -INFINITY, l = 0.0f;  // running maximum of the raw scores; this group's partial sum
     bool ok = true;
     for (int n = 0; n < N; ++n) {
       const int st = n & 1;
       ok = mbar_wait_bounded(bar(FB_SF + st), (n >> 1) & 1u, abort_flag, p.status, p.timeout_ns);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
-      float x[F_BK];
+      float x[64];
+      tmem_ld32(tl + st * F_BK + g * 64, x);
+      tmem_ld32(tl + st * F_BK + g * 64 + 32, x + 32);
+      const int kb = n * F_BK + g * 64;
+      // only tiles reaching past s or across the diagonal need the mask
+      if (n * F_BK + F_BK > p.s || (p.causal && n * F_BK + F_BK - 1 > q0)) {
 #pragma unroll
-      for (int c = 0; c < F_BK / 32; ++c) tmem_ld32(tl + st * F_BK + c * 32, x + c * 32);
-      const int k0 = n * F_BK;
-      float mx = -INFINITY;
-#pragma unroll
-      for (int j = 0; j < F_BK; ++j) {
-        const int key = k0 + j;
-        const bool vis = key < p.s && (!p.causal || key <= q);
-        x[j] = vis ? x[j] * p.scale_log2 : -INFINITY;
-        mx = fmaxf(mx, x[j]);
+        for (int j = 0; j < 64; ++j) {
+          const int key = kb + j;
+          if (!(key < p.s && (!p.causal || key <= q))) x[j] = -INFINITY;
+        }
       }
+      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int j = 0; j < 64; ++j) m4[j & 3] = fmaxf(m4[j & 3], x[j]);
+      float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+      const int rb = n & 1;
+      red[(rb * 2 + g) * 128 + r] = mx;
+      mbar_arrive(bar(FB_RED + rb));
+      ok = mbar_wait_bounded(bar(FB_RED + rb), (n >> 1) & 1u, abort_flag, p.status, p.timeout_ns);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      mx = fmaxf(mx, red[(rb * 2 + (g ^ 1)) * 128 + r]);
       const float m_new = fmaxf(m, mx);
       const float m_use = m_new == -INFINITY ? 0.0f : m_new;
-      const float alpha = ex2(m - m_use);
-      float rs = 0.0f;
+      const float mc = m_use * c;
+      const float alpha = ex2((m - m_use) * c);
+      float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-      for (int j = 0; j < F_BK; ++j) {
-        x[j] = ex2(x[j] - m_use);
-        rs += x[j];
+      for (int j = 0; j < 64; ++j) {
+        x[j] = ex2(fmaf(x[j], c, -mc));
+        s4[j & 3] += x[j];
       }
-      l = l * alpha + rs;
+      l = l * alpha + ((s4[0] + s4[1]) + (s4[2] + s4[3]));
       m = m_new;
       if (n > 0) {
         // P·V of the previous tile has finished: P's buffer is free and O holds
@@ -313,20 +336,20 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_fwd_kernel(const __grid_c
         tc_fence_after();
         if (__any_sync(0xffffffffu, alpha != 1.0f)) {
 #pragma unroll 1
-          for (int c = 0; c < HD / 32; ++c) {
+          for (int cc = 0; cc < 2; ++cc) {
             float o[32];
-            tmem_ld32(tl + 256 + c * 32, o);
+            const uint32_t ta = tl + 256 + g * 64 + cc * 32;
+            tmem_ld32(ta, o);
 #pragma unroll
             for (int j = 0; j < 32; ++j) o[j] *= alpha;
-            tmem_st32(tl + 256 + c * 32, o);
+            tmem_st32(ta, o);
           }
           tmem_st_wait();
         }
       }
-      // P as the A operand of O += P·V: row r, keys along the columns.
+      // P as the A operand of O += P·V: row r, keys [64g, 64g+64) = half g.
 #pragma unroll
-      for (int c = 0; c < F_BK / 8; ++c)
-        st_swizzled(smem + F_P + (c >> 3) * (128 * HALF_ROW_BYTES), r, c & 7, pack8<DT>(x + c * 8));
+      for (int cc = 0; cc < 8; ++cc) st_swizzled(smem + F_P + g * (128 * HALF_ROW_BYTES), r, cc, pack8<DT>(x + cc * 8));
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar(FB_P));
@@ -336,23 +359,33 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_fwd_kernel(const __grid_c
       ok = __all_sync(0xffffffffu, ok);
     }
     if (ok) {
+      // the two groups' partial sums (exchange slot of iteration N)
+      const int rb = N & 1;
+      red[(rb * 2 + g) * 128 + r] = l;
+      mbar_arrive(bar(FB_RED + rb));
+      ok = mbar_wait_bounded(bar(FB_RED + rb), (N >> 1) & 1u, abort_flag, p.status, p.timeout_ns);
+      ok = __all_sync(0xffffffffu, ok);
+      if (ok) l += red[(rb * 2 + (g ^ 1)) * 128 + r];
+    }
+    if (ok) {
       tc_fence_after();
       const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
       const int64_t mrow = static_cast<int64_t>(q) * p.b + bi;
 #pragma unroll 1
-      for (int c = 0; c < HD / 32; ++c) {
+      for (int cc = 0; cc < 2; ++cc) {
         float o[32];
-        tmem_ld32(tl + 256 + c * 32, o);
+        tmem_ld32(tl + 256 + g * 64 + cc * 32, o);
         if (q < p.s) {
 #pragma unroll
           for (int j = 0; j < 32; ++j) o[j] *= inv_l;
 #pragma unroll
-          for (int g = 0; g < 4; ++g)
-            store_row_chunk<DT>(p.o, mrow * p.h + head * HD + c * 32 + g * 8, o + g * 8);
+          for (int k4 = 0; k4 < 4; ++k4)
+            store_row_chunk<DT>(p.o, mrow * p.h + head * HD + g * 64 + cc * 32 + k4 * 8, o + k4 * 8);
         }
       }
       // rows past s (the padded tail of the last tile) get 0: the backward reads whole tiles
-      p.lse[(static_cast<int64_t>(bi) * p.heads + head) * p.s_pad + q] = q < p.s ? m + __log2f(l) : 0.0f;
+      if (g == 0)
+        p.lse[(static_cast<int64_t>(bi) * p.heads + head) * p.s_pad + q] = q < p.s ? m * c + __log2f(l) : 0.0f;
     }
   }
   tc_fence_before();
@@ -435,7 +468,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dkdv_kernel(const __g
     }
     mbar_init(bar(KB_SF), 1);
     mbar_init(bar(KB_SF + 1), 1);
-    mbar_init(bar(KB_P), 128);
+    mbar_init(bar(KB_P), COMPUTE_THREADS);
     mbar_init(bar(KB_MM), 1);
     mbar_init(bar(KB_DRAIN), 1);
     tail->abort_flag = 0;
@@ -530,30 +563,45 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dkdv_kernel(const __g
     }
     __syncwarp();
   } else if (warp >= 4) {
+    // Two groups of four warps; group g takes query columns [32g, 32g+32) of
+    // every 64-query tile and columns [64g, 64g+64) of dV and dK.
+    const int g = (warp - 4) >> 2;
     const int qw = warp & 3;
     const int r = qw * 32 + lane;
     const int key = k0 + r;
     const uint32_t tl = tmem + (static_cast<uint32_t>(qw * 32) << 16);
+    const float c = p.scale_log2;
     bool ok = true;
     for (int n = 0; n < N; ++n) {
       const int st = n % KV_ST, buf = n & 1;
       ok = mbar_wait_bounded(bar(KB_SF + buf), (n >> 1) & 1u, abort_flag, p.status, p.timeout_ns);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
-      float sv[KV_BQ], dp[KV_BQ];
-      tmem_ld32(tl + buf * 64, sv);
-      tmem_ld32(tl + buf * 64 + 32, sv + 32);
-      tmem_ld32(tl + 128 + buf * 64, dp);
-      tmem_ld32(tl + 128 + buf * 64 + 32, dp + 32);
-      const float* lse_s = reinterpret_cast<const float*>(stage_base(st) + 2 * KV_QTILE);
-      const float* del_s = lse_s + 64;
-      const int qq = (qt_first + n) * KV_BQ;
+      float sv[32], dp[32];
+      tmem_ld32(tl + buf * 64 + g * 32, sv);
+      tmem_ld32(tl + 128 + buf * 64 + g * 32, dp);
+      const float4* lse4 = reinterpret_cast<const float4*>(stage_base(st) + 2 * KV_QTILE) + g * 8;
+      const float4* del4 = lse4 + 16;
+      const int qq = (qt_first + n) * KV_BQ + g * 32;
+      const bool masked = qq + 32 > p.s || k0 + KV_BK > p.s || (p.causal && k0 + KV_BK - 1 > qq);
+      float lj[32], dj[32];
 #pragma unroll
-      for (int j = 0; j < KV_BQ; ++j) {
-        const int q = qq + j;
-        const bool vis = q < p.s && key < p.s && (!p.causal || key <= q);
-        const float pr = vis ? ex2(sv[j] * p.scale_log2 - lse_s[j]) : 0.0f;
-        dp[j] = pr * (dp[j] - del_s[j]);
+      for (int j4 = 0; j4 < 8; ++j4) {
+        const float4 lv = lse4[j4], dv = del4[j4];
+        lj[4 * j4] = lv.x; lj[4 * j4 + 1] = lv.y; lj[4 * j4 + 2] = lv.z; lj[4 * j4 + 3] = lv.w;
+        dj[4 * j4] = dv.x; dj[4 * j4 + 1] = dv.y; dj[4 * j4 + 2] = dv.z; dj[4 * j4 + 3] = dv.w;
+      }
+      if (masked) {  // tiles at the diagonal or past s: zero the invisible pairs first
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int q = qq + j;
+          if (!(q < p.s && key < p.s && (!p.causal || key <= q))) sv[j] = -INFINITY;
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float pr = ex2(fmaf(sv[j], c, -lj[j]));
+        dp[j] = pr * (dp[j] - dj[j]);
         sv[j] = pr;
       }
       if (n > 0) {
@@ -561,9 +609,9 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dkdv_kernel(const __g
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       }
 #pragma unroll
-      for (int c = 0; c < KV_BQ / 8; ++c) {
-        st_swizzled(smem + KV_PT, r, c, pack8<DT>(sv + c * 8));
-        st_swizzled(smem + KV_DST, r, c, pack8<DT>(dp + c * 8));
+      for (int cc = 0; cc < 4; ++cc) {
+        st_swizzled(smem + KV_PT, r, g * 4 + cc, pack8<DT>(sv + cc * 8));
+        st_swizzled(smem + KV_DST, r, g * 4 + cc, pack8<DT>(dp + cc * 8));
       }
       fence_proxy_async_smem();
       tc_fence_before();
@@ -578,17 +626,18 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dkdv_kernel(const __g
       const int64_t mrow = static_cast<int64_t>(key) * p.b + bi;
       const int64_t ld = 3 * static_cast<int64_t>(p.h);
 #pragma unroll 1
-      for (int c = 0; c < HD / 32; ++c) {
+      for (int cc = 0; cc < 2; ++cc) {
+        const int col = g * 64 + cc * 32;
         float dv[32], dk[32];
-        tmem_ld32(tl + 256 + c * 32, dv);
-        tmem_ld32(tl + 384 + c * 32, dk);
+        tmem_ld32(tl + 256 + col, dv);
+        tmem_ld32(tl + 384 + col, dk);
         if (key < p.s) {
 #pragma unroll
           for (int j = 0; j < 32; ++j) dk[j] *= p.scale;
 #pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            store_row_chunk<DT>(p.dqkv, mrow * ld + colv + c * 32 + g * 8, dv + g * 8);
-            store_row_chunk<DT>(p.dqkv, mrow * ld + colk + c * 32 + g * 8, dk + g * 8);
+          for (int k4 = 0; k4 < 4; ++k4) {
+            store_row_chunk<DT>(p.dqkv, mrow * ld + colv + col + k4 * 8, dv + k4 * 8);
+            store_row_chunk<DT>(p.dqkv, mrow * ld + colk + col + k4 * 8, dk + k4 * 8);
           }
         }
       }
@@ -638,7 +687,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dq_kernel(const __gri
     }
     mbar_init(bar(QB_SF), 1);
     mbar_init(bar(QB_SF + 1), 1);
-    mbar_init(bar(QB_P), 128);
+    mbar_init(bar(QB_P), COMPUTE_THREADS);
     mbar_init(bar(QB_MM), 1);
     mbar_init(bar(QB_DRAIN), 1);
     tail->abort_flag = 0;
@@ -725,6 +774,9 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dq_kernel(const __gri
     }
     __syncwarp();
   } else if (warp >= 4) {
+    // Two groups of four warps; group g takes key columns [32g, 32g+32) of every
+    // 64-key tile and columns [64g, 64g+64) of dQ.
+    const int g = (warp - 4) >> 2;
     const int qw = warp & 3;
     const int r = qw * 32 + lane;
     const int q = q0 + r;
@@ -732,31 +784,33 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dq_kernel(const __gri
     const int64_t sidx = (static_cast<int64_t>(bi) * p.heads + head) * p.s_pad + q;
     const float lse_q = q < p.s ? p.lse[sidx] : 0.0f;
     const float del_q = q < p.s ? p.delta[sidx] : 0.0f;
+    const float c = p.scale_log2;
     bool ok = true;
     for (int n = 0; n < N; ++n) {
       const int buf = n & 1;
       ok = mbar_wait_bounded(bar(QB_SF + buf), (n >> 1) & 1u, abort_flag, p.status, p.timeout_ns);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
-      float sv[DQ_BK], dp[DQ_BK];
-      tmem_ld32(tl + buf * 64, sv);
-      tmem_ld32(tl + buf * 64 + 32, sv + 32);
-      tmem_ld32(tl + 128 + buf * 64, dp);
-      tmem_ld32(tl + 128 + buf * 64 + 32, dp + 32);
-      const int kk = n * DQ_BK;
+      float sv[32], dp[32];
+      tmem_ld32(tl + buf * 64 + g * 32, sv);
+      tmem_ld32(tl + 128 + buf * 64 + g * 32, dp);
+      const int kk = n * DQ_BK + g * 32;
+      const bool masked = q0 + DQ_BQ > p.s || kk + 32 > p.s || (p.causal && kk + 31 > q0);
+      if (masked) {  // tiles at the diagonal or past s: zero the invisible pairs first
 #pragma unroll
-      for (int j = 0; j < DQ_BK; ++j) {
-        const int key = kk + j;
-        const bool vis = q < p.s && key < p.s && (!p.causal || key <= q);
-        const float pr = vis ? ex2(sv[j] * p.scale_log2 - lse_q) : 0.0f;
-        dp[j] = pr * (dp[j] - del_q);
+        for (int j = 0; j < 32; ++j) {
+          const int key = kk + j;
+          if (!(q < p.s && key < p.s && (!p.causal || key <= q))) sv[j] = -INFINITY;
+        }
       }
+#pragma unroll
+      for (int j = 0; j < 32; ++j) dp[j] = ex2(fmaf(sv[j], c, -lse_q)) * (dp[j] - del_q);
       if (n > 0) {
         ok = mbar_wait_bounded(bar(QB_MM), (n - 1) & 1, abort_flag, p.status, p.timeout_ns);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       }
 #pragma unroll
-      for (int c = 0; c < DQ_BK / 8; ++c) st_swizzled(smem + DQ_DS, r, c, pack8<DT>(dp + c * 8));
+      for (int cc = 0; cc < 4; ++cc) st_swizzled(smem + DQ_DS, r, g * 4 + cc, pack8<DT>(dp + cc * 8));
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar(QB_P));
@@ -770,14 +824,15 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dq_kernel(const __gri
       const int64_t mrow = static_cast<int64_t>(q) * p.b + bi;
       const int64_t ld = 3 * static_cast<int64_t>(p.h);
 #pragma unroll 1
-      for (int c = 0; c < HD / 32; ++c) {
+      for (int cc = 0; cc < 2; ++cc) {
+        const int col = g * 64 + cc * 32;
         float dq[32];
-        tmem_ld32(tl + 256 + c * 32, dq);
+        tmem_ld32(tl + 256 + col, dq);
         if (q < p.s) {
 #pragma unroll
           for (int j = 0; j < 32; ++j) dq[j] *= p.scale;
 #pragma unroll
-          for (int g = 0; g < 4; ++g) store_row_chunk<DT>(p.dqkv, mrow * ld + colq + c * 32 + g * 8, dq + g * 8);
+          for (int k4 = 0; k4 < 4; ++k4) store_row_chunk<DT>(p.dqkv, mrow * ld + colq + col + k4 * 8, dq + k4 * 8);
         }
       }
     }

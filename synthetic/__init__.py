@@ -184,6 +184,9 @@ class AttnConfig:
 ATTN_CONFIGS = {
     "attn_tiny_tp2_bf16": AttnConfig("attn_tiny_tp2_bf16", 192, 2, 512, 4, 2, True, "bf16", False),
     "llama70b_attn_tpsp8_bf16": AttnConfig("llama70b_attn_tpsp8_bf16", 4096, 1, 8192, 64, 8, True, "bf16", True),
+    "llama70b_attn_unmasked_tpsp8_bf16": AttnConfig(
+        "llama70b_attn_unmasked_tpsp8_bf16", 4096, 1, 8192, 64, 8, True, "bf16", False
+    ),
 }
 
 
