@@ -170,11 +170,12 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_fwd_kernel(const __grid_c
   volatile int* abort_flag = &tail->abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // grid (heads, b, query tiles): the tile index varies slowest, so under the
-  // causal mask the longest tiles (the last ones) are dispatched first
+  // grid (query tiles, heads, b): the tiles of one head run side by side and
+  // share its K and V through L2; under the causal mask a head's longest tiles
+  // (the last ones) are dispatched first
   const int ntq = (p.s + F_BQ - 1) / F_BQ;
-  const int qt = p.causal ? ntq - 1 - static_cast<int>(blockIdx.z) : static_cast<int>(blockIdx.z);
-  const int head = blockIdx.x, bi = blockIdx.y;
+  const int qt = p.causal ? ntq - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x);
+  const int head = blockIdx.y, bi = blockIdx.z;
   const int q0 = qt * F_BQ;
   const int nkt = (p.s + F_BK - 1) / F_BK;
   const int N = p.causal ? min(nkt, (q0 + F_BQ - 1) / F_BK + 1) : nkt;
@@ -448,10 +449,11 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dkdv_kernel(const __g
   volatile int* abort_flag = &tail->abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // grid (heads, b, key tiles), the tile index slowest; under the causal mask the
-  // first key tiles see the most query tiles and are dispatched first
-  const int kt = static_cast<int>(blockIdx.z);
-  const int head = blockIdx.x, bi = blockIdx.y;
+  // grid (key tiles, heads, b): the tiles of one head share its Q and dO through
+  // L2; under the causal mask the first key tiles see the most query tiles and
+  // are dispatched first
+  const int kt = static_cast<int>(blockIdx.x);
+  const int head = blockIdx.y, bi = blockIdx.z;
   const int k0 = kt * KV_BK;
   const int nqt = (p.s + KV_BQ - 1) / KV_BQ;
   const int qt_first = p.causal ? k0 / KV_BQ : 0;
@@ -672,8 +674,8 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dq_kernel(const __gri
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   const int ntq = (p.s + DQ_BQ - 1) / DQ_BQ;
-  const int qt = p.causal ? ntq - 1 - static_cast<int>(blockIdx.z) : static_cast<int>(blockIdx.z);
-  const int head = blockIdx.x, bi = blockIdx.y;
+  const int qt = p.causal ? ntq - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x);
+  const int head = blockIdx.y, bi = blockIdx.z;
   const int q0 = qt * DQ_BQ;
   const int nkt = (p.s + DQ_BK - 1) / DQ_BK;
   const int N = p.causal ? min(nkt, (q0 + DQ_BQ - 1) / DQ_BK + 1) : nkt;
@@ -910,7 +912,7 @@ int check_shape(int64_t s, int64_t b, int64_t h, int heads, int tp, int sp, int 
   if (heads % tp != 0) return set_error(TPMLP_ERR_NOT_DIVISIBLE, "the number of heads must be divisible by tensor parallel size");
   if (sp && s % tp != 0)
     return set_error(TPMLP_ERR_NOT_DIVISIBLE, "First dimension of the tensor should be divisible by tensor parallel size");
-  if (s > 65535ll * 128 || s * b >= (1ll << 31) || 3 * h >= (1ll << 31) || b >= 65536)
+  if (s > 65535ll * 128 || s * b >= (1ll << 31) || 3 * h >= (1ll << 31) || b >= 65536 || heads > 65535)
     return set_error(TPMLP_ERR_UNSUPPORTED, "extent too large");
   Shape k;
   k.s = s;
@@ -1002,7 +1004,7 @@ int launch_core_forward(const Shape& k, const void* qkv, void* o, float* lse, cu
   if ((rc = make_map3(&p.qkv128, k.dtype, qkv, 3 * k.h, k.b, k.s, 128))) return rc;
   p.o = o;
   p.lse = lse;
-  const dim3 grid(static_cast<unsigned>(k.heads), static_cast<unsigned>(k.b), static_cast<unsigned>(k.s_pad / 128));
+  const dim3 grid(static_cast<unsigned>(k.s_pad / 128), static_cast<unsigned>(k.heads), static_cast<unsigned>(k.b));
   const void* fn = k.dtype == DT_BF16 ? reinterpret_cast<const void*>(attn_fwd_kernel<DT_BF16>)
                                       : reinterpret_cast<const void*>(attn_fwd_kernel<DT_F16>);
   if ((rc = set_smem(fn, F_SMEM))) return rc;
@@ -1041,7 +1043,7 @@ int launch_core_backward(const Shape& k, const void* qkv, const void* o, const f
   const unsigned gd = static_cast<unsigned>((warps * 32 + 255) / 256);
   if (bf) attn_bwd_delta_kernel<DT_BF16><<<gd, 256, 0, st>>>(dout, o, delta, p.s, p.b, p.h, p.heads, p.s_pad);
   else attn_bwd_delta_kernel<DT_F16><<<gd, 256, 0, st>>>(dout, o, delta, p.s, p.b, p.h, p.heads, p.s_pad);
-  const dim3 gkv(static_cast<unsigned>(k.heads), static_cast<unsigned>(k.b), static_cast<unsigned>(k.s_pad / 128));
+  const dim3 gkv(static_cast<unsigned>(k.s_pad / 128), static_cast<unsigned>(k.heads), static_cast<unsigned>(k.b));
   if (bf) attn_bwd_dkdv_kernel<DT_BF16><<<gkv, ATT_THREADS, KV_SMEM, st>>>(p);
   else attn_bwd_dkdv_kernel<DT_F16><<<gkv, ATT_THREADS, KV_SMEM, st>>>(p);
   if (bf) attn_bwd_dq_kernel<DT_BF16><<<gkv, ATT_THREADS, DQ_SMEM, st>>>(p);
