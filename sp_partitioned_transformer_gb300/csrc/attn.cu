@@ -160,6 +160,7 @@ constexpr uint32_t F_END = F_RED + 2 * 2 * 128 * 4;
 constexpr size_t F_SMEM = 1024 + F_END + sizeof(Tail);
 // barriers
 enum { FB_Q = 0, FB_KF = 1, FB_KE = 3, FB_VF = 5, FB_VE = 7, FB_SF = 9, FB_P = 11, FB_O = 12, FB_DRAIN = 13, FB_RED = 14 };
+static_assert(FB_RED + 2 <= 24, "barrier slots");
 
 template <int DT>
 __global__ void __launch_bounds__(ATT_THREADS, 1) attn_fwd_kernel(const __grid_constant__ AttnParams p) {
@@ -438,7 +439,9 @@ constexpr uint32_t KV_DST = KV_PT + 128 * HALF_ROW_BYTES;
 constexpr uint32_t KV_END = KV_DST + 128 * HALF_ROW_BYTES;
 constexpr uint32_t KV_STRIDE = (KV_STAGE + 1023) & ~1023u;
 constexpr size_t KV_SMEM = 1024 + KV_END + sizeof(Tail);
-enum { KB_KV = 0, KB_F = 1, KB_E = 4, KB_SF = 7, KB_P = 9, KB_MM = 10, KB_DRAIN = 11 };
+enum { KB_KV = 0, KB_F = 1, KB_E = KB_F + KV_ST, KB_SF = KB_E + KV_ST, KB_P = KB_SF + 2, KB_MM = KB_P + 1,
+       KB_DRAIN = KB_MM + 1, KB_COUNT = KB_DRAIN + 1 };
+static_assert(KB_COUNT <= 24, "barrier slots");
 
 template <int DT>
 __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dkdv_kernel(const __grid_constant__ AttnParams p) {
@@ -662,7 +665,9 @@ constexpr uint32_t DQ_Q = 0, DQ_DO = DQ_TILE, DQ_S0 = 2 * DQ_TILE;
 constexpr uint32_t DQ_DS = DQ_S0 + DQ_ST * DQ_STAGE;
 constexpr uint32_t DQ_END = DQ_DS + 128 * HALF_ROW_BYTES;
 constexpr size_t DQ_SMEM = 1024 + DQ_END + sizeof(Tail);
-enum { QB_QD = 0, QB_F = 1, QB_E = 4, QB_SF = 7, QB_P = 9, QB_MM = 10, QB_DRAIN = 11 };
+enum { QB_QD = 0, QB_F = 1, QB_E = QB_F + DQ_ST, QB_SF = QB_E + DQ_ST, QB_P = QB_SF + 2, QB_MM = QB_P + 1,
+       QB_DRAIN = QB_MM + 1, QB_COUNT = QB_DRAIN + 1 };
+static_assert(QB_COUNT <= 24, "barrier slots");
 
 template <int DT>
 __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dq_kernel(const __grid_constant__ AttnParams p) {
