@@ -338,6 +338,40 @@ def run_reference(args) -> int:
     return 0
 
 
+# ---------------------------------------------------------------- ranks
+# With --gpus N > 1 every rank runs an independent replica of the block on its
+# own GPU (the tensor shards are partitions inside one GPU): the ranks only meet
+# at the barriers around the timed region and in the max over their times.
+
+
+def rank_barrier(world: int, sync=None) -> None:
+    """Device synchronisation, then (N > 1) a process-group barrier, then again."""
+    import torch.distributed as dist
+
+    if sync is not None:
+        sync()
+    if world > 1:
+        dist.barrier()
+    if sync is not None:
+        sync()
+
+
+def max_over_ranks(x: float, world: int, device="cpu") -> float:
+    """The largest of the ranks' values (the job's time is its slowest replica's)."""
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(flops_per_replica: float, world: int, ms_max: float) -> float:
+    """Whole-job TFLOP/s: every replica's FLOPs over the slowest replica's time."""
+    return world * flops_per_replica / (ms_max / 1e3) / 1e12
+
+
 # ---------------------------------------------------------------- our arm
 
 
@@ -428,10 +462,7 @@ def run_ours(args) -> int:
             block_step(x, dz)
 
     def barrier():
-        torch.cuda.synchronize(dev)
-        if world > 1:
-            dist.barrier()
-        torch.cuda.synchronize(dev)
+        rank_barrier(world, lambda: torch.cuda.synchronize(dev))
 
     clocks = ClockSampler(gpu_uuid(local_rank)) if rank == 0 else None
     for _ in range(max(3, args.warmup)):
@@ -450,12 +481,9 @@ def run_ours(args) -> int:
     status = tpmlp.device_status()
     if status != 0:
         raise RuntimeError(f"device status {status}: {tpmlp.last_error()}")
-    ms_t = torch.tensor([ms], device=dev)
-    if world > 1:
-        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
-    ms_max = float(ms_t.item())
+    ms_max = max_over_ranks(ms, world, dev)
     flops = float(cfg.flops_fwd_bwd())
-    value = world * flops / (ms_max / 1e3) / 1e12
+    value = job_throughput(flops, world, ms_max)
 
     # ------------------------------------------------ end to end through the public API
     # Every step copies its input chunks (X, dZ) from pinned host memory and reads
@@ -527,12 +555,9 @@ def run_ours(args) -> int:
         run_e2e(n_e2e)
         e1.record(stream)
         barrier()
-        ms_e2e = e0.elapsed_time(e1) / n_e2e
-        t = torch.tensor([ms_e2e], device=dev)
-        if world > 1:
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e = {"value": world * flops / (float(t.item()) / 1e3) / 1e12, "unit": UNIT,
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": float(t.item()),
+        ms_e2e = max_over_ranks(e0.elapsed_time(e1) / n_e2e, world, dev)
+        e2e = {"value": job_throughput(flops, world, ms_e2e), "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e,
                "note": "pinned-host chunks in, results out every step; copies double-buffered on two "
                        "copy streams against the compute stream"}
 
