@@ -403,29 +403,30 @@ template <int DT>
 __global__ void __launch_bounds__(256) attn_bwd_delta_kernel(const void* __restrict__ dout,
                                                              const void* __restrict__ o, float* __restrict__ delta,
                                                              int s, int b, int h, int heads, int s_pad) {
-  // one warp per (token row, head); each lane takes 4 of the 128 columns
-  const int64_t wid = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
+  // one half-warp per (token row, head); each lane takes 8 of the 128 columns
+  // with 16-byte loads
+  const int64_t pid = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 4;
+  const int sub = threadIdx.x & 15;
   const int64_t total = static_cast<int64_t>(s_pad) * b * heads;
-  if (wid >= total) return;
-  const int head = static_cast<int>(wid % heads);
-  const int64_t rest = wid / heads;
+  if (pid >= total) return;  // whole half-warps leave together (total pairs fill them)
+  const int head = static_cast<int>(pid % heads);
+  const int64_t rest = pid / heads;
   const int bi = static_cast<int>(rest % b);
   const int q = static_cast<int>(rest / b);
   float acc = 0.0f;
   if (q < s) {
     using T = typename Storage<DT>::T;
-    const int64_t off = (static_cast<int64_t>(q) * b + bi) * h + head * HD + lane * 4;
-    const uint2 a = *reinterpret_cast<const uint2*>(static_cast<const T*>(dout) + off);
-    const uint2 c = *reinterpret_cast<const uint2*>(static_cast<const T*>(o) + off);
-    const T* ta = reinterpret_cast<const T*>(&a);
-    const T* tc = reinterpret_cast<const T*>(&c);
+    const int64_t off = (static_cast<int64_t>(q) * b + bi) * h + head * HD + sub * 8;
+    float a[8], c[8];
+    unpack8<DT>(ldg_nc_v4(static_cast<const T*>(dout) + off), a);
+    unpack8<DT>(ldg_nc_v4(static_cast<const T*>(o) + off), c);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) acc += Storage<DT>::to_f32(ta[i]) * Storage<DT>::to_f32(tc[i]);
+    for (int i = 0; i < 8; ++i) acc += a[i] * c[i];
   }
+  const unsigned mask = (threadIdx.x & 16) ? 0xffff0000u : 0x0000ffffu;
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (lane == 0) delta[(static_cast<int64_t>(bi) * heads + head) * s_pad + q] = acc;
+  for (int off = 8; off > 0; off >>= 1) acc += __shfl_xor_sync(mask, acc, off);
+  if (sub == 0) delta[(static_cast<int64_t>(bi) * heads + head) * s_pad + q] = acc;
 }
 
 // ================================================================== backward: dK, dV
@@ -603,11 +604,18 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dkdv_kernel(const __g
           if (!(q < p.s && key < p.s && (!p.causal || key <= q))) sv[j] = -INFINITY;
         }
       }
+      // P = 2^(S·c − lse2) and dS = P ⊙ (dP − Δ), the latter two elements per
+      // instruction (paired float32 arithmetic)
+      const float2 neg1 = make_float2(-1.0f, -1.0f);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const float pr = ex2(fmaf(sv[j], c, -lj[j]));
-        dp[j] = pr * (dp[j] - dj[j]);
-        sv[j] = pr;
+      for (int j = 0; j < 32; j += 2) {
+        const float2 pr = make_float2(ex2(fmaf(sv[j], c, -lj[j])), ex2(fmaf(sv[j + 1], c, -lj[j + 1])));
+        const float2 d = __ffma2_rn(make_float2(dj[j], dj[j + 1]), neg1, make_float2(dp[j], dp[j + 1]));
+        const float2 ds = __fmul2_rn(pr, d);
+        dp[j] = ds.x;
+        dp[j + 1] = ds.y;
+        sv[j] = pr.x;
+        sv[j + 1] = pr.y;
       }
       if (n > 0) {
         ok = mbar_wait_bounded(bar(KB_MM), (n - 1) & 1, abort_flag, p.status, p.timeout_ns);
@@ -810,8 +818,16 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dq_kernel(const __gri
           if (!(q < p.s && key < p.s && (!p.causal || key <= q))) sv[j] = -INFINITY;
         }
       }
+      // dS = 2^(S·c − lse2) ⊙ (dP − Δ), the product and difference two elements per
+      // instruction (paired float32 arithmetic)
+      const float2 ndel = make_float2(-del_q, -del_q);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) dp[j] = ex2(fmaf(sv[j], c, -lse_q)) * (dp[j] - del_q);
+      for (int j = 0; j < 32; j += 2) {
+        const float2 pr = make_float2(ex2(fmaf(sv[j], c, -lse_q)), ex2(fmaf(sv[j + 1], c, -lse_q)));
+        const float2 ds = __fmul2_rn(pr, __fadd2_rn(make_float2(dp[j], dp[j + 1]), ndel));
+        dp[j] = ds.x;
+        dp[j + 1] = ds.y;
+      }
       if (n > 0) {
         ok = mbar_wait_bounded(bar(QB_MM), (n - 1) & 1, abort_flag, p.status, p.timeout_ns);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
@@ -1044,8 +1060,8 @@ int launch_core_backward(const Shape& k, const void* qkv, const void* o, const f
                       : reinterpret_cast<const void*>(attn_bwd_dq_kernel<DT_F16>);
   if ((rc = set_smem(fkv, KV_SMEM)) || (rc = set_smem(fq, DQ_SMEM))) return rc;
   const int ph = prof_begin(PROF_ATTN, st);
-  const int64_t warps = k.s_pad * k.b * k.heads;
-  const unsigned gd = static_cast<unsigned>((warps * 32 + 255) / 256);
+  const int64_t row_heads = k.s_pad * k.b * k.heads;  // (row, head) pairs, a half-warp each
+  const unsigned gd = static_cast<unsigned>((row_heads * 16 + 255) / 256);
   if (bf) attn_bwd_delta_kernel<DT_BF16><<<gd, 256, 0, st>>>(dout, o, delta, p.s, p.b, p.h, p.heads, p.s_pad);
   else attn_bwd_delta_kernel<DT_F16><<<gd, 256, 0, st>>>(dout, o, delta, p.s, p.b, p.h, p.heads, p.s_pad);
   const dim3 gkv(static_cast<unsigned>(k.s_pad / 128), static_cast<unsigned>(k.heads), static_cast<unsigned>(k.b));
