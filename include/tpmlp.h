@@ -340,8 +340,9 @@ int tpmlp_wait_timeout_selftest(uint64_t timeout_ns, void* stream);
  *   dqkv   [s·b, 3h], dout [s·b, h]: backward scratch and outputs (dQKV, dO)
  * causal = 1 applies the decoder mask (key u visible to query t iff u ≤ t);
  * causal = 0 is the unmasked formula.  ws: tpmlp_attn_workspace_size() bytes,
- * 256-byte aligned (the forward needs it only under SP when the chunks of
- * s/tp·b rows are not whole multiples of 128 rows; the backward always).
+ * 256-byte aligned: the gathered X and dZ when SP chunks of s/tp·b rows are
+ * not whole multiples of 128 rows (the forward needs only these), then Δ and
+ * −lse2, each [b][heads][s_pad] float32 (backward).
  * Every on-chip wait is bounded (tpmlp_set_wait_timeout_ns): an expired wait
  * is reported through tpmlp_device_status() as TPMLP_ERR_TIMEOUT.  Results
  * are deterministic (no atomics).

@@ -138,6 +138,7 @@ struct AttnParams {
   void* o;             // forward: O [M, h] output
   float* lse;          // [b][heads][s_pad]: forward output, backward input
   const float* delta;  // [b][heads][s_pad] (backward)
+  const float* nlse;   // −lse2, same layout (backward; written beside Δ)
   void* dqkv;          // backward: dQKV [M, 3h]
   int s, b, h, heads, s_pad, causal;
   float scale_log2;    // log2(e)/√d
@@ -322,13 +323,19 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_fwd_kernel(const __grid_c
       const float m_use = m_new == -INFINITY ? 0.0f : m_new;
       const float mc = m_use * c;
       const float alpha = ex2((m - m_use) * c);
-      float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      // p = 2^(x·c − m·c) and the row sum, the FMA and the adds two elements per
+      // instruction (paired float32 arithmetic), four partial sums
+      const float2 c2 = make_float2(c, c), nmc2 = make_float2(-mc, -mc);
+      float2 s2[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
 #pragma unroll
-      for (int j = 0; j < 64; ++j) {
-        x[j] = ex2(fmaf(x[j], c, -mc));
-        s4[j & 3] += x[j];
+      for (int j = 0; j < 64; j += 2) {
+        const float2 a = __ffma2_rn(make_float2(x[j], x[j + 1]), c2, nmc2);
+        const float2 e = make_float2(ex2(a.x), ex2(a.y));
+        x[j] = e.x;
+        x[j + 1] = e.y;
+        s2[(j >> 1) & 1] = __fadd2_rn(s2[(j >> 1) & 1], e);
       }
-      l = l * alpha + ((s4[0] + s4[1]) + (s4[2] + s4[3]));
+      l = l * alpha + ((s2[0].x + s2[1].x) + (s2[0].y + s2[1].y));
       m = m_new;
       if (n > 0) {
         // P·V of the previous tile has finished: P's buffer is free and O holds
@@ -342,8 +349,13 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_fwd_kernel(const __grid_c
             float o[32];
             const uint32_t ta = tl + 256 + g * 64 + cc * 32;
             tmem_ld32(ta, o);
+            const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) o[j] *= alpha;
+            for (int j = 0; j < 32; j += 2) {
+              const float2 v = __fmul2_rn(make_float2(o[j], o[j + 1]), a2);
+              o[j] = v.x;
+              o[j + 1] = v.y;
+            }
             tmem_st32(ta, o);
           }
           tmem_st_wait();
@@ -401,7 +413,8 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_fwd_kernel(const __grid_c
 // ================================================================== backward: Δ
 template <int DT>
 __global__ void __launch_bounds__(256) attn_bwd_delta_kernel(const void* __restrict__ dout,
-                                                             const void* __restrict__ o, float* __restrict__ delta,
+                                                             const void* __restrict__ o, const float* __restrict__ lse,
+                                                             float* __restrict__ delta, float* __restrict__ nlse,
                                                              int s, int b, int h, int heads, int s_pad) {
   // one half-warp per (token row, head); each lane takes 8 of the 128 columns
   // with 16-byte loads
@@ -426,7 +439,11 @@ __global__ void __launch_bounds__(256) attn_bwd_delta_kernel(const void* __restr
   const unsigned mask = (threadIdx.x & 16) ? 0xffff0000u : 0x0000ffffu;
 #pragma unroll
   for (int off = 8; off > 0; off >>= 1) acc += __shfl_xor_sync(mask, acc, off);
-  if (sub == 0) delta[(static_cast<int64_t>(bi) * heads + head) * s_pad + q] = acc;
+  if (sub == 0) {
+    const int64_t i = (static_cast<int64_t>(bi) * heads + head) * s_pad + q;
+    delta[i] = acc;
+    nlse[i] = -lse[i];  // the dK/dV kernel's exponent argument is S·c + (−lse2)
+  }
 }
 
 // ================================================================== backward: dK, dV
@@ -463,7 +480,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dkdv_kernel(const __g
   const int qt_first = p.causal ? k0 / KV_BQ : 0;
   const int N = nqt - qt_first;
   const int colq = 3 * HD * head, colk = colq + HD, colv = colq + 2 * HD;
-  const float* lse_row = p.lse + (static_cast<int64_t>(bi) * p.heads + head) * p.s_pad;
+  const float* lse_row = p.nlse + (static_cast<int64_t>(bi) * p.heads + head) * p.s_pad;  // −lse2
   const float* delta_row = p.delta + (static_cast<int64_t>(bi) * p.heads + head) * p.s_pad;
 
   if (threadIdx.x == 0) {
@@ -606,10 +623,12 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dkdv_kernel(const __g
       }
       // P = 2^(S·c − lse2) and dS = P ⊙ (dP − Δ), the latter two elements per
       // instruction (paired float32 arithmetic)
-      const float2 neg1 = make_float2(-1.0f, -1.0f);
+      const float2 neg1 = make_float2(-1.0f, -1.0f), c2 = make_float2(c, c);
 #pragma unroll
       for (int j = 0; j < 32; j += 2) {
-        const float2 pr = make_float2(ex2(fmaf(sv[j], c, -lj[j])), ex2(fmaf(sv[j + 1], c, -lj[j + 1])));
+        // lj holds −lse2 (staged that way by the Δ kernel)
+        const float2 arg = __ffma2_rn(make_float2(sv[j], sv[j + 1]), c2, make_float2(lj[j], lj[j + 1]));
+        const float2 pr = make_float2(ex2(arg.x), ex2(arg.y));
         const float2 d = __ffma2_rn(make_float2(dj[j], dj[j + 1]), neg1, make_float2(dp[j], dp[j + 1]));
         const float2 ds = __fmul2_rn(pr, d);
         dp[j] = ds.x;
@@ -820,10 +839,11 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dq_kernel(const __gri
       }
       // dS = 2^(S·c − lse2) ⊙ (dP − Δ), the product and difference two elements per
       // instruction (paired float32 arithmetic)
-      const float2 ndel = make_float2(-del_q, -del_q);
+      const float2 ndel = make_float2(-del_q, -del_q), c2 = make_float2(c, c), nlse = make_float2(-lse_q, -lse_q);
 #pragma unroll
       for (int j = 0; j < 32; j += 2) {
-        const float2 pr = make_float2(ex2(fmaf(sv[j], c, -lse_q)), ex2(fmaf(sv[j + 1], c, -lse_q)));
+        const float2 arg = __ffma2_rn(make_float2(sv[j], sv[j + 1]), c2, nlse);
+        const float2 pr = make_float2(ex2(arg.x), ex2(arg.y));
         const float2 ds = __fmul2_rn(pr, __fadd2_rn(make_float2(dp[j], dp[j + 1]), ndel));
         dp[j] = ds.x;
         dp[j + 1] = ds.y;
@@ -966,8 +986,8 @@ Ws ws_layout(const Shape& k) {
   if (gathered) off += align256(act);
   w.dz_off = off;
   if (gathered) off += align256(act);
-  w.delta_off = off;
-  off += align256(static_cast<size_t>(k.b) * k.heads * k.s_pad * sizeof(float));
+  w.delta_off = off;  // Δ, then −lse2, each [b][heads][s_pad] float32
+  off += align256(2 * static_cast<size_t>(k.b) * k.heads * k.s_pad * sizeof(float));
   w.total = off;
   return w;
 }
@@ -1062,8 +1082,12 @@ int launch_core_backward(const Shape& k, const void* qkv, const void* o, const f
   const int ph = prof_begin(PROF_ATTN, st);
   const int64_t row_heads = k.s_pad * k.b * k.heads;  // (row, head) pairs, a half-warp each
   const unsigned gd = static_cast<unsigned>((row_heads * 16 + 255) / 256);
-  if (bf) attn_bwd_delta_kernel<DT_BF16><<<gd, 256, 0, st>>>(dout, o, delta, p.s, p.b, p.h, p.heads, p.s_pad);
-  else attn_bwd_delta_kernel<DT_F16><<<gd, 256, 0, st>>>(dout, o, delta, p.s, p.b, p.h, p.heads, p.s_pad);
+  float* nlse = delta + static_cast<int64_t>(k.b) * k.heads * k.s_pad;
+  p.nlse = nlse;
+  if (bf)
+    attn_bwd_delta_kernel<DT_BF16><<<gd, 256, 0, st>>>(dout, o, lse, delta, nlse, p.s, p.b, p.h, p.heads, p.s_pad);
+  else
+    attn_bwd_delta_kernel<DT_F16><<<gd, 256, 0, st>>>(dout, o, lse, delta, nlse, p.s, p.b, p.h, p.heads, p.s_pad);
   const dim3 gkv(static_cast<unsigned>(k.s_pad / 128), static_cast<unsigned>(k.heads), static_cast<unsigned>(k.b));
   if (bf) attn_bwd_dkdv_kernel<DT_BF16><<<gkv, ATT_THREADS, KV_SMEM, st>>>(p);
   else attn_bwd_dkdv_kernel<DT_F16><<<gkv, ATT_THREADS, KV_SMEM, st>>>(p);

@@ -180,8 +180,8 @@ def test_attention_workspace_formula(lib):
     def a256(x):
         return (x + 255) // 256 * 256
 
-    # 128-row chunks read in place: only Δ [b][heads][s_pad] float32
-    assert f(256, 1, 256, 2, 2, 1, 2) == a256(1 * 2 * 256 * 4)
-    # 96-row chunks: gathered X and dZ, then Δ (s_pad = 256)
-    assert f(192, 1, 256, 2, 2, 1, 2) == 2 * a256(192 * 256 * 2) + a256(2 * 256 * 4)
+    # 128-row chunks read in place: only Δ and −lse2, each [b][heads][s_pad] float32
+    assert f(256, 1, 256, 2, 2, 1, 2) == a256(2 * 1 * 2 * 256 * 4)
+    # 96-row chunks: gathered X and dZ, then Δ and −lse2 (s_pad = 256)
+    assert f(192, 1, 256, 2, 2, 1, 2) == 2 * a256(192 * 256 * 2) + a256(2 * 2 * 256 * 4)
     assert f(192, 1, 320, 2, 2, 1, 2) == 0  # invalid (h != 128·heads) -> 0
