@@ -64,7 +64,7 @@
 extern "C" {
 #endif
 
-#define TPMLP_ABI_VERSION 2
+#define TPMLP_ABI_VERSION 3
 #define TPMLP_MAX_TP 64
 
 typedef enum tpmlp_status {
@@ -339,15 +339,19 @@ int tpmlp_wait_timeout_selftest(uint64_t timeout_ns, void* stream);
  *   dwqkv, dwo  weight gradients (overwritten), storage type
  *   dqkv   [s·b, 3h], dout [s·b, h]: backward scratch and outputs (dQKV, dO)
  * causal = 1 applies the decoder mask (key u visible to query t iff u ≤ t);
- * causal = 0 is the unmasked formula.  ws: tpmlp_attn_workspace_size() bytes,
- * 256-byte aligned: the gathered X and dZ when SP chunks of s/tp·b rows are
- * not whole multiples of 128 rows (the forward needs only these), then Δ and
- * −lse2, each [b][heads][s_pad] float32 (backward).
+ * causal = 0 is the unmasked formula.  ws: tpmlp_attn_workspace_size() bytes
+ * (same causal flag as the calls), 256-byte aligned: the gathered X and dZ when
+ * SP chunks of s/tp·b rows are not whole multiples of 128 rows (the forward
+ * needs only the gathered X), then Δ and −lse2, each [b][heads][s_pad] float32,
+ * then the backward's 16-bit dSᵀ tiles: b·heads·T tiles of 16 KB (128 keys × 64
+ * queries), T = nk·nq − nk·(nk−1) under the causal mask, else nk·nq, with
+ * nk = ⌈s/128⌉ and nq = ⌈s/64⌉ (≈ b·heads·s²·2 bytes unmasked, half causal).
  * Every on-chip wait is bounded (tpmlp_set_wait_timeout_ns): an expired wait
  * is reported through tpmlp_device_status() as TPMLP_ERR_TIMEOUT.  Results
  * are deterministic (no atomics).
  * ------------------------------------------------------------------------- */
-size_t tpmlp_attn_workspace_size(int64_t s, int64_t b, int64_t h, int heads, int tp, int sp, int dtype);
+size_t tpmlp_attn_workspace_size(int64_t s, int64_t b, int64_t h, int heads, int tp, int sp, int dtype,
+                                 int causal);
 int tpmlp_attn_forward(int64_t s, int64_t b, int64_t h, int heads, int tp, int sp, int dtype, int causal,
                        const void* const* x, const void* wqkv, const void* wo, void* qkv, void* o,
                        float* lse, void* const* z, void* ws, size_t ws_bytes, void* stream);

@@ -152,7 +152,7 @@ def load(path: str | None = None):
     lib.tpmlp_sp_residual_dropout_backward.restype = i32
     lib.tpmlp_sp_residual_dropout_backward.argtypes = [vpp, vpp, f32, vpp, i64, i64, i64, i32, i32, vp]
     lib.tpmlp_attn_workspace_size.restype = sz
-    lib.tpmlp_attn_workspace_size.argtypes = [i64, i64, i64, i32, i32, i32, i32]
+    lib.tpmlp_attn_workspace_size.argtypes = [i64, i64, i64, i32, i32, i32, i32, i32]
     lib.tpmlp_attn_forward.restype = i32
     lib.tpmlp_attn_forward.argtypes = [i64, i64, i64, i32, i32, i32, i32, i32,
                                        vpp, vp, vp, vp, vp, vp, vpp, vp, sz, vp]
@@ -434,8 +434,9 @@ class MLPBlock:
 # ---------------------------------------------------------------- attention block
 
 
-def attn_workspace_size(s, b, h, heads, tp, sp, dtype) -> int:
-    return int(load().tpmlp_attn_workspace_size(s, b, h, heads, tp, int(bool(sp)), _dtype_code(dtype)))
+def attn_workspace_size(s, b, h, heads, tp, sp, dtype, causal) -> int:
+    return int(load().tpmlp_attn_workspace_size(s, b, h, heads, tp, int(bool(sp)), _dtype_code(dtype),
+                                                 int(bool(causal))))
 
 
 def attn_forward(x, wqkv, wo, qkv, o, lse, z, *, s, b, h, heads, tp, sp, causal, workspace=None, dtype=None,
@@ -467,7 +468,7 @@ class AttnBlock:
         self.dtype, self.causal, self.device = dtype, bool(causal), device
         self.M = s * b
         self.s_pad = (s + 127) // 128 * 128
-        n = attn_workspace_size(s, b, h, heads, tp, sp, dtype)
+        n = attn_workspace_size(s, b, h, heads, tp, sp, dtype, causal)
         self.ws = torch.empty(max(n, 256), dtype=torch.uint8, device=device)
 
     def _act(self):

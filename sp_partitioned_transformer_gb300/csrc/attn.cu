@@ -9,9 +9,10 @@
 //
 // The projections run on the tcgen05 GEMM (gemm_tc.cu).  The attention core is
 // three tcgen05 kernels (head width 128, 16-bit storage, float32 accumulation in
-// tensor memory), each one CTA of 8 warps: warp 0 issues TMA loads, warp 1
-// issues the MMAs, warp 2 owns the tensor-memory allocation and warps 4–7 do the
-// element-wise work with one thread per row of the 128-row tile.
+// tensor memory) and a small Δ kernel.  Each tcgen05 CTA has 12 warps: warp 0
+// issues TMA loads, warp 1 issues the MMAs, warp 2 owns the tensor-memory
+// allocation and warps 4–11 are two groups of four element-wise warps, one
+// thread per row of the 128-row tile, the groups splitting its columns.
 //
 //   attn_fwd_kernel   per (128-query tile, head, sequence): S = Q·Kᵀ into one of
 //                     two TMEM buffers (the next S is computed while the softmax
@@ -21,9 +22,11 @@
 //                     moved; O and the row log-sum-exp (lse2) written at the end.
 //   attn_bwd_dkdv_kernel  per (128-key tile, head, sequence), over 64-query tiles:
 //                     Sᵀ = K·Qᵀ and dPᵀ = V·dOᵀ, Pᵀ = 2^(Sᵀ·c − lse2),
-//                     dSᵀ = Pᵀ ⊙ (dPᵀ − Δ), dV += Pᵀ·dO, dK += dSᵀ·Q.
-//   attn_bwd_dq_kernel    per (128-query tile, head, sequence), over 64-key tiles:
-//                     S, dP recomputed, dS as above, dQ += dS·K.
+//                     dSᵀ = Pᵀ ⊙ (dPᵀ − Δ), dV += Pᵀ·dO, dK += dSᵀ·Q; each
+//                     16-bit dSᵀ tile is also bulk-stored to HBM.
+//   attn_bwd_dq_kernel    per (128-query tile, head, sequence), over 128-key
+//                     tiles: dQ += dS·K from the stored dSᵀ tiles (a streaming
+//                     contraction; S and dP are not recomputed).
 //   attn_bwd_delta_kernel Δ = rowsum(dO ⊙ O) per query row and head.
 // No atomics anywhere: every output element is written by one CTA, so results
 // are the same bits on every run.
@@ -133,19 +136,44 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* raw) {
 struct AttnParams {
   CUtensorMap qkv128;  // QKV [s][b][3h] as a 3-D tensor {3h, b, s}, box {64, 1, 128}
   CUtensorMap qkv64;   // same tensor, box {64, 1, 64}
-  CUtensorMap do128;   // dO [s][b][h] as {h, b, s}, box {64, 1, 128}
-  CUtensorMap do64;    // box {64, 1, 64}
+  CUtensorMap do64;    // dO [s][b][h] as {h, b, s}, box {64, 1, 64}
   void* o;             // forward: O [M, h] output
   float* lse;          // [b][heads][s_pad]: forward output, backward input
   const float* delta;  // [b][heads][s_pad] (backward)
   const float* nlse;   // −lse2, same layout (backward; written beside Δ)
   void* dqkv;          // backward: dQKV [M, 3h]
+  uint8_t* ds;         // backward: dSᵀ tiles, written by the dK/dV kernel, read by the dQ kernel
+  int64_t ds_head_tiles;  // dSᵀ tiles per (sequence, head)
+  int nqt64;           // 64-query tiles per sequence, ⌈s/64⌉
   int s, b, h, heads, s_pad, causal;
   float scale_log2;    // log2(e)/√d
   float scale;         // 1/√d
   unsigned* status;
   uint64_t timeout_ns;
 };
+
+// dSᵀ is kept in HBM as [128 keys × 64 queries] tiles, each the 16 KB image of
+// the 128-byte-swizzled shared-memory operand (one 64-column half).  Per
+// (sequence, head) the tiles of key tile kt are the query tiles qt_first(kt) …
+// ⌈s/64⌉−1 in order (qt_first = 2·kt under the causal mask, else 0); this is the
+// index of key tile kt's first tile.
+constexpr uint32_t DS_TILE = 128 * HALF_ROW_BYTES;
+__host__ __device__ __forceinline__ int64_t ds_tile_index(int kt, int nqt64, int causal) {
+  return causal ? static_cast<int64_t>(kt) * nqt64 - static_cast<int64_t>(kt) * (kt - 1)
+                : static_cast<int64_t>(kt) * nqt64;
+}
+
+__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
+               : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// All but the newest `n` bulk-store groups have finished reading shared memory.
+template <int n>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(n) : "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 template <int DT>
 __device__ __forceinline__ void store_row_chunk(void* base, int64_t off, const float* v) {
@@ -453,8 +481,8 @@ constexpr uint32_t KV_QTILE = 64 * 128 * 2;    // Q or dO tile of 64 rows, 16 KB
 constexpr uint32_t KV_STAGE = 2 * KV_QTILE + 512;  // Q, dO, lse2[64], Δ[64]
 constexpr uint32_t KV_K = 0, KV_V = KV_TILE, KV_S0 = 2 * KV_TILE;
 constexpr uint32_t KV_PT = KV_S0 + KV_ST * ((KV_STAGE + 1023) & ~1023u);
-constexpr uint32_t KV_DST = KV_PT + 128 * HALF_ROW_BYTES;
-constexpr uint32_t KV_END = KV_DST + 128 * HALF_ROW_BYTES;
+constexpr uint32_t KV_DST = KV_PT + 128 * HALF_ROW_BYTES;  // two dSᵀ buffers: MMA operand and HBM store
+constexpr uint32_t KV_END = KV_DST + 2 * DS_TILE;
 constexpr uint32_t KV_STRIDE = (KV_STAGE + 1023) & ~1023u;
 constexpr size_t KV_SMEM = 1024 + KV_END + sizeof(Tail);
 enum { KB_KV = 0, KB_F = 1, KB_E = KB_F + KV_ST, KB_SF = KB_E + KV_ST, KB_P = KB_SF + 2, KB_MM = KB_P + 1,
@@ -482,6 +510,9 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dkdv_kernel(const __g
   const int colq = 3 * HD * head, colk = colq + HD, colv = colq + 2 * HD;
   const float* lse_row = p.nlse + (static_cast<int64_t>(bi) * p.heads + head) * p.s_pad;  // −lse2
   const float* delta_row = p.delta + (static_cast<int64_t>(bi) * p.heads + head) * p.s_pad;
+  // this key tile's dSᵀ tiles in HBM, one per 64-query tile it visits
+  uint8_t* ds_out = p.ds + ((static_cast<int64_t>(bi) * p.heads + head) * p.ds_head_tiles +
+                            ds_tile_index(kt, p.nqt64, p.causal)) * DS_TILE;
 
   if (threadIdx.x == 0) {
     mbar_init(bar(KB_KV), 1);
@@ -568,13 +599,18 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dkdv_kernel(const __g
         if (!(ok = mbar_wait_bounded(bar(KB_P), n & 1, abort_flag, p.status, p.timeout_ns))) break;
         tc_fence_after();
         const uint32_t sQ = smem_u32(stage_base(st)), sDO = sQ + KV_QTILE;
+        const uint32_t sDSn = sDST + (n & 1) * DS_TILE;
+        bulk_store(ds_out + static_cast<int64_t>(n) * DS_TILE, sDSn, DS_TILE);  // dSᵀ for the dQ kernel
 #pragma unroll
         for (int ks = 0; ks < KV_BQ / 16; ++ks) {
           tc_mma_f16(tmem + 256, kmajor64(sPT, ks), mnmajor128(sDO, KV_BQ, ks), idesc_acc,
                      (n > 0 || ks > 0) ? 1u : 0u);
-          tc_mma_f16(tmem + 384, kmajor64(sDST, ks), mnmajor128(sQ, KV_BQ, ks), idesc_acc,
+          tc_mma_f16(tmem + 384, kmajor64(sDSn, ks), mnmajor128(sQ, KV_BQ, ks), idesc_acc,
                      (n > 0 || ks > 0) ? 1u : 0u);
         }
+        // the compute warps rewrite dSᵀ buffer (n+1)&1 once KB_MM of this step
+        // completes, so the store of step n−1 (that buffer) must have read it
+        bulk_wait_read<1>();
         tc_commit(bar(KB_MM));
         tc_commit(bar(KB_E + st));
         if (n + 2 < N) ok = issue_sdp(n + 2);
@@ -583,6 +619,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dkdv_kernel(const __g
         tc_commit(bar(KB_DRAIN));
         (void)mbar_wait_bounded(bar(KB_DRAIN), 0u, nullptr, nullptr, p.timeout_ns);
       }
+      bulk_wait_all();  // the dSᵀ stores are complete before the CTA exits
     }
     __syncwarp();
   } else if (warp >= 4) {
@@ -643,7 +680,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dkdv_kernel(const __g
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
         st_swizzled(smem + KV_PT, r, g * 4 + cc, pack8<DT>(sv + cc * 8));
-        st_swizzled(smem + KV_DST, r, g * 4 + cc, pack8<DT>(dp + cc * 8));
+        st_swizzled(smem + KV_DST + (n & 1) * DS_TILE, r, g * 4 + cc, pack8<DT>(dp + cc * 8));
       }
       fence_proxy_async_smem();
       tc_fence_before();
@@ -684,17 +721,18 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dkdv_kernel(const __g
 }
 
 // ================================================================== backward: dQ
-constexpr int DQ_BQ = 128, DQ_BK = 64, DQ_ST = 3;
-constexpr uint32_t DQ_TILE = 128 * 128 * 2;   // Q or dO, 32 KB
-constexpr uint32_t DQ_KTILE = 64 * 128 * 2;   // K or V tile of 64 rows, 16 KB
-constexpr uint32_t DQ_STAGE = 2 * DQ_KTILE;   // K, V
-constexpr uint32_t DQ_Q = 0, DQ_DO = DQ_TILE, DQ_S0 = 2 * DQ_TILE;
-constexpr uint32_t DQ_DS = DQ_S0 + DQ_ST * DQ_STAGE;
-constexpr uint32_t DQ_END = DQ_DS + 128 * HALF_ROW_BYTES;
+// dQ = (dS·K)/√d per 128-query tile, over the key tiles it sees, reading the dSᵀ
+// tiles the dK/dV kernel stored: two [128 keys × 64 queries] tiles side by side
+// are the [K = 128 keys] × [M = 128 queries] MN-major A operand, and the K tile
+// [128 keys × 128 d] as TMA lands it is the MN-major B operand.  Nothing is
+// recomputed; the kernel streams dSᵀ from HBM once.
+constexpr int DQ_ST = 3;
+constexpr uint32_t DQ_STAGE = 2 * DS_TILE + KV_TILE;  // dSᵀ for query rows 0–63 and 64–127, K
+constexpr uint32_t DQ_END = DQ_ST * DQ_STAGE;
 constexpr size_t DQ_SMEM = 1024 + DQ_END + sizeof(Tail);
-enum { QB_QD = 0, QB_F = 1, QB_E = QB_F + DQ_ST, QB_SF = QB_E + DQ_ST, QB_P = QB_SF + 2, QB_MM = QB_P + 1,
-       QB_DRAIN = QB_MM + 1, QB_COUNT = QB_DRAIN + 1 };
+enum { QB_F = 0, QB_E = QB_F + DQ_ST, QB_MM = QB_E + DQ_ST, QB_DRAIN = QB_MM + 1, QB_COUNT = QB_DRAIN + 1 };
 static_assert(QB_COUNT <= 24, "barrier slots");
+static_assert(DQ_SMEM <= 232448 && KV_SMEM <= 232448 && F_SMEM <= 232448, "shared memory per CTA");
 
 template <int DT>
 __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dq_kernel(const __grid_constant__ AttnParams p) {
@@ -705,164 +743,88 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dq_kernel(const __gri
   volatile int* abort_flag = &tail->abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  const int ntq = (p.s + DQ_BQ - 1) / DQ_BQ;
+  // grid (query tiles, heads, b); under the causal mask the last query tiles see
+  // the most key tiles and are dispatched first
+  const int ntq = (p.s + 127) / 128;
   const int qt = p.causal ? ntq - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x);
   const int head = blockIdx.y, bi = blockIdx.z;
-  const int q0 = qt * DQ_BQ;
-  const int nkt = (p.s + DQ_BK - 1) / DQ_BK;
-  const int N = p.causal ? min(nkt, (q0 + DQ_BQ - 1) / DQ_BK + 1) : nkt;
-  const int colq = 3 * HD * head, colk = colq + HD, colv = colq + 2 * HD;
+  const int q0 = qt * 128;
+  const int N = p.causal ? qt + 1 : ntq;  // key tiles of 128
+  // query rows 64–127 of this tile exist (else that half of A is never loaded:
+  // it only feeds output rows past s, which are not stored)
+  const bool upper = 2 * qt + 1 < p.nqt64;
+  const int colq = 3 * HD * head, colk = colq + HD;
+  const uint8_t* ds_head = p.ds + (static_cast<int64_t>(bi) * p.heads + head) * p.ds_head_tiles * DS_TILE;
 
   if (threadIdx.x == 0) {
-    mbar_init(bar(QB_QD), 1);
     for (int i = 0; i < DQ_ST; ++i) {
       mbar_init(bar(QB_F + i), 1);
       mbar_init(bar(QB_E + i), 1);
     }
-    mbar_init(bar(QB_SF), 1);
-    mbar_init(bar(QB_SF + 1), 1);
-    mbar_init(bar(QB_P), COMPUTE_THREADS);
     mbar_init(bar(QB_MM), 1);
     mbar_init(bar(QB_DRAIN), 1);
     tail->abort_flag = 0;
     fence_barrier_init();
   }
   if (warp == 2) {
-    tmem_alloc(smem_u32(&tail->tmem_slot), 512);
+    tmem_alloc(smem_u32(&tail->tmem_slot), 128);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = tail->tmem_slot;
-  // TMEM columns: S[2] at 0 / 64, dP[2] at 128 / 192, dQ at 256.
-  const uint32_t sQ = smem_u32(smem + DQ_Q), sDO = smem_u32(smem + DQ_DO), sDS = smem_u32(smem + DQ_DS);
-  auto stage_addr = [&](int st) { return smem_u32(smem + DQ_S0 + st * DQ_STAGE); };
+  const uint32_t tmem = tail->tmem_slot;  // dQ accumulator, columns 0–127
+  auto stage_addr = [&](int st) { return smem_u32(smem + st * DQ_STAGE); };
 
   if (warp == 0) {
     if (lane == 0) {
       tma_prefetch_map(&p.qkv128);
-      tma_prefetch_map(&p.qkv64);
-      tma_prefetch_map(&p.do128);
-      mbar_arrive_expect_tx(bar(QB_QD), 2 * DQ_TILE);
-      load_tile(sQ, &p.qkv128, bar(QB_QD), colq, bi, q0, 128);
-      load_tile(sDO, &p.do128, bar(QB_QD), head * HD, bi, q0, 128);
       bool ok = true;
       int issued = 0;
       for (int n = 0; ok && n < N; ++n) {
         const int st = n % DQ_ST;
         const uint32_t par = ((n / DQ_ST) & 1) ^ 1u;
         if (!(ok = mbar_wait_bounded(bar(QB_E + st), par, abort_flag, p.status, p.timeout_ns))) break;
-        const uint32_t f = bar(QB_F + st);
-        mbar_arrive_expect_tx(f, DQ_STAGE);
-        load_tile(stage_addr(st), &p.qkv64, f, colk, bi, n * DQ_BK, 64);
-        load_tile(stage_addr(st) + DQ_KTILE, &p.qkv64, f, colv, bi, n * DQ_BK, 64);
+        const uint32_t f = bar(QB_F + st), sa = stage_addr(st);
+        mbar_arrive_expect_tx(f, (upper ? 2 : 1) * DS_TILE + KV_TILE);
+        const uint8_t* src = ds_head + (ds_tile_index(n, p.nqt64, p.causal) + 2 * qt - (p.causal ? 2 * n : 0)) * DS_TILE;
+        bulk_load(sa, src, DS_TILE, f);
+        if (upper) bulk_load(sa + DS_TILE, src + DS_TILE, DS_TILE, f);
+        load_tile(sa + 2 * DS_TILE, &p.qkv128, f, colk, bi, n * 128, 128);
         issued = n + 1;
       }
-      if (!ok) {
-        (void)mbar_wait_bounded(bar(QB_QD), 0u, nullptr, nullptr, p.timeout_ns);
+      if (!ok)
         for (int n = issued > DQ_ST ? issued - DQ_ST : 0; n < issued; ++n)
           (void)mbar_wait_bounded(bar(QB_F + n % DQ_ST), (n / DQ_ST) & 1u, nullptr, nullptr, p.timeout_ns);
-      }
     }
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idesc_s = make_idesc_f16(DT == DT_BF16, false, false, 128, DQ_BK);
-      constexpr uint32_t idesc_acc = make_idesc_f16(DT == DT_BF16, false, true, 128, HD);
-      bool ok = mbar_wait_bounded(bar(QB_QD), 0u, abort_flag, p.status, p.timeout_ns);
-      auto issue_sdp = [&](int n) -> bool {
-        const int st = n % DQ_ST, buf = n & 1;
-        if (!mbar_wait_bounded(bar(QB_F + st), (n / DQ_ST) & 1u, abort_flag, p.status, p.timeout_ns)) return false;
-        tc_fence_after();
-        const uint32_t sKn = stage_addr(st), sVn = sKn + DQ_KTILE;
-#pragma unroll
-        for (int ks = 0; ks < HD / 16; ++ks) {
-          tc_mma_f16(tmem + buf * 64, kmajor128(sQ, 128, ks), kmajor128(sKn, 64, ks), idesc_s, ks > 0 ? 1u : 0u);
-          tc_mma_f16(tmem + 128 + buf * 64, kmajor128(sDO, 128, ks), kmajor128(sVn, 64, ks), idesc_s,
-                     ks > 0 ? 1u : 0u);
-        }
-        tc_commit(bar(QB_SF + buf));
-        return true;
-      };
-      if (ok) tc_fence_after();
-      if (ok) ok = issue_sdp(0);
-      if (ok && N > 1) ok = issue_sdp(1);
+      constexpr uint32_t idesc = make_idesc_f16(DT == DT_BF16, true, true, 128, HD);
+      bool ok = true;
       for (int n = 0; ok && n < N; ++n) {
         const int st = n % DQ_ST;
-        if (!(ok = mbar_wait_bounded(bar(QB_P), n & 1, abort_flag, p.status, p.timeout_ns))) break;
+        if (!(ok = mbar_wait_bounded(bar(QB_F + st), (n / DQ_ST) & 1u, abort_flag, p.status, p.timeout_ns))) break;
         tc_fence_after();
-        const uint32_t sKn = stage_addr(st);
+        const uint32_t sa = stage_addr(st), sk = sa + 2 * DS_TILE;
 #pragma unroll
-        for (int ks = 0; ks < DQ_BK / 16; ++ks)
-          tc_mma_f16(tmem + 256, kmajor64(sDS, ks), mnmajor128(sKn, DQ_BK, ks), idesc_acc,
-                     (n > 0 || ks > 0) ? 1u : 0u);
-        tc_commit(bar(QB_MM));
+        for (int ks = 0; ks < 128 / 16; ++ks)
+          tc_mma_f16(tmem, mnmajor128(sa, 128, ks), mnmajor128(sk, 128, ks), idesc, (n > 0 || ks > 0) ? 1u : 0u);
         tc_commit(bar(QB_E + st));
-        if (n + 2 < N) ok = issue_sdp(n + 2);
       }
-      if (!ok) {
-        tc_commit(bar(QB_DRAIN));
-        (void)mbar_wait_bounded(bar(QB_DRAIN), 0u, nullptr, nullptr, p.timeout_ns);
-      }
+      tc_commit(bar(ok ? QB_MM : QB_DRAIN));
+      if (!ok) (void)mbar_wait_bounded(bar(QB_DRAIN), 0u, nullptr, nullptr, p.timeout_ns);
     }
     __syncwarp();
   } else if (warp >= 4) {
-    // Two groups of four warps; group g takes key columns [32g, 32g+32) of every
-    // 64-key tile and columns [64g, 64g+64) of dQ.
+    // Two groups of four warps; group g stores columns [64g, 64g+64) of dQ.
     const int g = (warp - 4) >> 2;
     const int qw = warp & 3;
     const int r = qw * 32 + lane;
     const int q = q0 + r;
     const uint32_t tl = tmem + (static_cast<uint32_t>(qw * 32) << 16);
-    const int64_t sidx = (static_cast<int64_t>(bi) * p.heads + head) * p.s_pad + q;
-    const float lse_q = q < p.s ? p.lse[sidx] : 0.0f;
-    const float del_q = q < p.s ? p.delta[sidx] : 0.0f;
-    const float c = p.scale_log2;
-    bool ok = true;
-    for (int n = 0; n < N; ++n) {
-      const int buf = n & 1;
-      ok = mbar_wait_bounded(bar(QB_SF + buf), (n >> 1) & 1u, abort_flag, p.status, p.timeout_ns);
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-      tc_fence_after();
-      float sv[32], dp[32];
-      tmem_ld32(tl + buf * 64 + g * 32, sv);
-      tmem_ld32(tl + 128 + buf * 64 + g * 32, dp);
-      const int kk = n * DQ_BK + g * 32;
-      const bool masked = q0 + DQ_BQ > p.s || kk + 32 > p.s || (p.causal && kk + 31 > q0);
-      if (masked) {  // tiles at the diagonal or past s: zero the invisible pairs first
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int key = kk + j;
-          if (!(q < p.s && key < p.s && (!p.causal || key <= q))) sv[j] = -INFINITY;
-        }
-      }
-      // dS = 2^(S·c − lse2) ⊙ (dP − Δ), the product and difference two elements per
-      // instruction (paired float32 arithmetic)
-      const float2 ndel = make_float2(-del_q, -del_q), c2 = make_float2(c, c), nlse = make_float2(-lse_q, -lse_q);
-#pragma unroll
-      for (int j = 0; j < 32; j += 2) {
-        const float2 arg = __ffma2_rn(make_float2(sv[j], sv[j + 1]), c2, nlse);
-        const float2 pr = make_float2(ex2(arg.x), ex2(arg.y));
-        const float2 ds = __fmul2_rn(pr, __fadd2_rn(make_float2(dp[j], dp[j + 1]), ndel));
-        dp[j] = ds.x;
-        dp[j + 1] = ds.y;
-      }
-      if (n > 0) {
-        ok = mbar_wait_bounded(bar(QB_MM), (n - 1) & 1, abort_flag, p.status, p.timeout_ns);
-        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-      }
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc) st_swizzled(smem + DQ_DS, r, g * 4 + cc, pack8<DT>(dp + cc * 8));
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(bar(QB_P));
-    }
-    if (ok) {
-      ok = mbar_wait_bounded(bar(QB_MM), (N - 1) & 1, abort_flag, p.status, p.timeout_ns);
-      ok = __all_sync(0xffffffffu, ok);
-    }
-    if (ok) {
+    bool ok = mbar_wait_bounded(bar(QB_MM), 0u, abort_flag, p.status, p.timeout_ns);
+    if (__all_sync(0xffffffffu, ok)) {
       tc_fence_after();
       const int64_t mrow = static_cast<int64_t>(q) * p.b + bi;
       const int64_t ld = 3 * static_cast<int64_t>(p.h);
@@ -870,7 +832,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dq_kernel(const __gri
       for (int cc = 0; cc < 2; ++cc) {
         const int col = g * 64 + cc * 32;
         float dq[32];
-        tmem_ld32(tl + 256 + col, dq);
+        tmem_ld32(tl + col, dq);
         if (q < p.s) {
 #pragma unroll
           for (int j = 0; j < 32; ++j) dq[j] *= p.scale;
@@ -884,7 +846,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dq_kernel(const __gri
   __syncthreads();
   if (warp == 2) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc(tmem, 128);
   }
 }
 
@@ -973,9 +935,16 @@ int check_shape(int64_t s, int64_t b, int64_t h, int heads, int tp, int sp, int 
   return TPMLP_OK;
 }
 
-// workspace: [X gathered | dZ gathered] when SP chunks are not read in place, then Δ.
+// dSᵀ tiles per (sequence, head): key tiles of 128 × the 64-query tiles each visits.
+int64_t ds_head_tiles(const Shape& k) {
+  const int nkt = static_cast<int>((k.s + 127) / 128), nqt64 = static_cast<int>((k.s + 63) / 64);
+  return ds_tile_index(nkt, nqt64, k.causal);
+}
+
+// workspace: [X gathered | dZ gathered] when SP chunks are not read in place
+// (all the forward needs), then Δ and −lse2, then the dSᵀ tiles (backward).
 struct Ws {
-  size_t x_off, dz_off, delta_off, total;
+  size_t x_off, dz_off, delta_off, ds_off, fwd_total, total;
 };
 Ws ws_layout(const Shape& k) {
   Ws w{};
@@ -984,10 +953,13 @@ Ws ws_layout(const Shape& k) {
   const bool gathered = k.sp && !k.fused_ag;
   w.x_off = off;
   if (gathered) off += align256(act);
+  w.fwd_total = off;
   w.dz_off = off;
   if (gathered) off += align256(act);
   w.delta_off = off;  // Δ, then −lse2, each [b][heads][s_pad] float32
   off += align256(2 * static_cast<size_t>(k.b) * k.heads * k.s_pad * sizeof(float));
+  w.ds_off = off;
+  off += static_cast<size_t>(k.b) * k.heads * ds_head_tiles(k) * DS_TILE;
   w.total = off;
   return w;
 }
@@ -1061,18 +1033,20 @@ int launch_core_forward(const Shape& k, const void* qkv, void* o, float* lse, cu
 }
 
 int launch_core_backward(const Shape& k, const void* qkv, const void* o, const float* lse, const void* dout,
-                         float* delta, void* dqkv, cudaStream_t st) {
+                         float* delta, uint8_t* ds, void* dqkv, cudaStream_t st) {
   AttnParams p;
   int rc = base_params(k, &p);
   if (rc) return rc;
   if ((rc = make_map3(&p.qkv128, k.dtype, qkv, 3 * k.h, k.b, k.s, 128)) ||
       (rc = make_map3(&p.qkv64, k.dtype, qkv, 3 * k.h, k.b, k.s, 64)) ||
-      (rc = make_map3(&p.do128, k.dtype, dout, k.h, k.b, k.s, 128)) ||
       (rc = make_map3(&p.do64, k.dtype, dout, k.h, k.b, k.s, 64)))
     return rc;
   p.lse = const_cast<float*>(lse);
   p.delta = delta;
   p.dqkv = dqkv;
+  p.ds = ds;
+  p.ds_head_tiles = ds_head_tiles(k);
+  p.nqt64 = static_cast<int>((k.s + 63) / 64);
   const bool bf = k.dtype == DT_BF16;
   const void* fkv = bf ? reinterpret_cast<const void*>(attn_bwd_dkdv_kernel<DT_BF16>)
                        : reinterpret_cast<const void*>(attn_bwd_dkdv_kernel<DT_F16>);
@@ -1130,9 +1104,10 @@ using namespace tpmlp::attn;
 
 extern "C" {
 
-size_t tpmlp_attn_workspace_size(int64_t s, int64_t b, int64_t h, int heads, int tp, int sp, int dtype) {
+size_t tpmlp_attn_workspace_size(int64_t s, int64_t b, int64_t h, int heads, int tp, int sp, int dtype,
+                                 int causal) {
   Shape k;
-  if (check_shape(s, b, h, heads, tp, sp, dtype, 0, &k) != TPMLP_OK) return 0;
+  if (check_shape(s, b, h, heads, tp, sp, dtype, causal, &k) != TPMLP_OK) return 0;
   return ws_layout(k).total;
 }
 
@@ -1150,8 +1125,8 @@ int tpmlp_attn_forward(int64_t s, int64_t b, int64_t h, int heads, int tp, int s
   const Ws W = ws_layout(k);
   const bool gathered = k.sp && !k.fused_ag;
   if (gathered) {
-    if (ws == nullptr || ws_bytes < W.total)
-      return set_error(TPMLP_ERR_WORKSPACE, "workspace needs " + std::to_string(W.total) + " bytes");
+    if (ws == nullptr || ws_bytes < W.fwd_total)
+      return set_error(TPMLP_ERR_WORKSPACE, "workspace needs " + std::to_string(W.fwd_total) + " bytes");
     if ((rc = check_ptr(ws, 256, "ws"))) return rc;
   }
   if (k.M == 0) return TPMLP_OK;
@@ -1266,7 +1241,8 @@ int tpmlp_attn_backward(int64_t s, int64_t b, int64_t h, int heads, int tp, int 
     g.epi.ldo = h;
     if ((rc = launch_gemm_tc(g, st))) return rc;
   }
-  if ((rc = launch_core_backward(k, qkv, o, lse, dout, reinterpret_cast<float*>(wb(ws) + W.delta_off), dqkv, st)))
+  if ((rc = launch_core_backward(k, qkv, o, lse, dout, reinterpret_cast<float*>(wb(ws) + W.delta_off),
+                                 wb(ws) + W.ds_off, dqkv, st)))
     return rc;
   // dWqkv = dQKVᵀ·X.
   {

@@ -39,7 +39,7 @@ def test_header_declares_the_boundary():
 def test_library_exports_every_declared_symbol(lib):
     missing = [n for n in declared_functions() if not hasattr(lib, n)]
     assert not missing, missing
-    assert lib.tpmlp_abi_version() == 2
+    assert lib.tpmlp_abi_version() == 3
 
 
 def _ws(lib, *a):
@@ -175,13 +175,25 @@ def test_attention_rejects_bad_arguments_on_the_host(lib):
 def test_attention_workspace_formula(lib):
     f = lib.tpmlp_attn_workspace_size
     f.restype = ctypes.c_size_t
-    f.argtypes = [ctypes.c_int64] * 3 + [ctypes.c_int] * 4
+    f.argtypes = [ctypes.c_int64] * 3 + [ctypes.c_int] * 5
 
     def a256(x):
         return (x + 255) // 256 * 256
 
-    # 128-row chunks read in place: only Δ and −lse2, each [b][heads][s_pad] float32
-    assert f(256, 1, 256, 2, 2, 1, 2) == a256(2 * 1 * 2 * 256 * 4)
-    # 96-row chunks: gathered X and dZ, then Δ and −lse2 (s_pad = 256)
-    assert f(192, 1, 256, 2, 2, 1, 2) == 2 * a256(192 * 256 * 2) + a256(2 * 2 * 256 * 4)
-    assert f(192, 1, 320, 2, 2, 1, 2) == 0  # invalid (h != 128·heads) -> 0
+    def ds_tiles(s, causal):
+        """16 KB dSᵀ tiles per (sequence, head): key tile kt visits the 64-query
+        tiles from 2·kt (causal) or 0 to the last, counted here one by one."""
+        nk, nq = -(-s // 128), -(-s // 64)
+        return sum(nq - (2 * kt if causal else 0) for kt in range(nk))
+
+    # 128-row chunks read in place: Δ and −lse2, each [b][heads][s_pad] float32, then dSᵀ
+    for causal in (0, 1):
+        assert f(256, 1, 256, 2, 2, 1, 2, causal) == a256(2 * 1 * 2 * 256 * 4) + 2 * ds_tiles(256, causal) * 16384
+    # 96-row chunks: gathered X and dZ, then Δ and −lse2 (s_pad = 256), then dSᵀ
+    assert f(192, 1, 256, 2, 2, 1, 2, 1) == (2 * a256(192 * 256 * 2) + a256(2 * 2 * 256 * 4)
+                                             + 2 * ds_tiles(192, True) * 16384)
+    # ragged s = 100 (one key tile, two query tiles), b = 3, 2 heads, no SP
+    assert f(100, 3, 256, 2, 1, 0, 2, 1) == a256(2 * 3 * 2 * 128 * 4) + 3 * 2 * 2 * 16384
+    assert ds_tiles(4096, True) == 1056 and ds_tiles(4096, False) == 2048
+    assert f(192, 1, 320, 2, 2, 1, 2, 0) == 0  # invalid (h != 128·heads) -> 0
+    assert f(192, 1, 256, 2, 2, 1, 2, 2) == 0  # invalid causal flag -> 0

@@ -170,7 +170,7 @@ def test_empty_sequence(cuda_lib):
     Wo = torch.randn(h, h, device="cuda").to(d)
     dwqkv = torch.full((3 * h, h), 7.0, dtype=d, device="cuda")
     dwo = torch.full((h, h), 7.0, dtype=d, device="cuda")
-    ws = torch.empty(max(256, tpmlp.attn_workspace_size(0, 1, h, heads, tp, True, d)), dtype=torch.uint8,
+    ws = torch.empty(max(256, tpmlp.attn_workspace_size(0, 1, h, heads, tp, True, d, True)), dtype=torch.uint8,
                      device="cuda")
     kw = dict(s=0, b=1, h=h, heads=heads, tp=tp, sp=True, causal=True, workspace=ws)
     chunks2 = [dummy, dummy]
