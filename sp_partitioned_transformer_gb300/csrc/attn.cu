@@ -70,20 +70,91 @@ __device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* map, 
   tma_load_3d(dst + static_cast<uint32_t>(rows) * HALF_ROW_BYTES, map, bar, col + 64, bi, row0);
 }
 
-// K-major operand descriptors (rows = M or N, the 16-element K step ks along the
-// columns): a [rows × 128] tile, and a [rows × 64] half.
-__device__ __forceinline__ uint64_t kmajor128(uint32_t base, int rows, int ks) {
-  return make_sdesc_sw128(base + static_cast<uint32_t>(ks >> 2) * rows * HALF_ROW_BYTES + (ks & 3) * 32u, 16u,
-                          1024u);
+// Batched MMA issue.  The lane that issues the MMAs shares its sub-partition
+// with element-wise warps, so every instruction it spends per MMA delays the
+// tensor pipe: descriptors are built once per buffer (sdesc_*) and one asm
+// block issues a tile's K steps, each descriptor the base plus a constant (the
+// 14-bit address field never carries: shared-memory offsets stay below 2^18).
+__device__ __forceinline__ uint64_t sdesc_k(uint32_t base) { return make_sdesc_sw128(base, 16u, 1024u); }
+__device__ __forceinline__ uint64_t sdesc_mn(uint32_t base, int krows) {
+  return make_sdesc_sw128(base, static_cast<uint32_t>(krows) * HALF_ROW_BYTES, 1024u);
 }
-__device__ __forceinline__ uint64_t kmajor64(uint32_t base, int ks) {
-  return make_sdesc_sw128(base + ks * 32u, 16u, 1024u);
+// Descriptor offsets (16-byte units) of K step ks (16 elements).  K-major
+// [rows × 128] tile (rows = M or N, K along the columns, two 64-column halves of
+// rows × 128 bytes): step ks is 32 bytes into half ks/4.  MN-major [krows × 128]
+// tile (rows along K, 128 columns of M or N, the second 64-column half
+// krows·128 bytes on, the descriptor's leading offset): step ks is 16 rows,
+// 2048 bytes, further.
+__host__ __device__ constexpr uint32_t koff(int rows, int ks) {
+  return (static_cast<uint32_t>(ks >> 2) * rows * HALF_ROW_BYTES + (ks & 3) * 32u) >> 4;
 }
-// MN-major operand descriptor of a [krows × 128] tile whose rows run along K and
-// whose 128 columns are M or N: K step ks = rows 16·ks … 16·ks+15; the second
-// 64-column half is krows·128 bytes further on.
-__device__ __forceinline__ uint64_t mnmajor128(uint32_t base, int krows, int ks) {
-  return make_sdesc_sw128(base + ks * 2048u, static_cast<uint32_t>(krows) * HALF_ROW_BYTES, 1024u);
+__host__ __device__ constexpr uint32_t mnoff(int ks) { return (ks * 2048u) >> 4; }
+
+// D (+)= Σ_ks A_ks·B_ks over 8 K steps, A and B shared-memory descriptors;
+// the first step accumulates iff acc0, the others always.
+__device__ __forceinline__ void mma8_ss(uint32_t d, const uint64_t* a, const uint64_t* b, uint32_t idesc,
+                                        uint32_t acc0) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.b32 p, %18, 0;\n\t"
+      "setp.eq.b32 q, %18, %18;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %9, %17, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %2, %10, %17, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %11, %17, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %12, %17, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %13, %17, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %6, %14, %17, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %7, %15, %17, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %8, %16, %17, q;\n\t}" ::"r"(d),
+      "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(a[4]), "l"(a[5]), "l"(a[6]), "l"(a[7]), "l"(b[0]), "l"(b[1]),
+      "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7]), "r"(idesc), "r"(acc0)
+      : "memory");
+}
+// Same with A in tensor memory (M = 128 lanes × K 16-bit elements, two per
+// 32-bit column, element 2j in the low half of column j): NK K steps (4 or 8),
+// A columns a, a+8, a+16, ….
+template <int NK>
+__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, const uint64_t* b, uint32_t idesc, uint32_t acc0) {
+  static_assert(NK == 4 || NK == 8, "K steps");
+  if constexpr (NK == 4) {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.b32 p, %10, 0;\n\t"
+        "setp.eq.b32 q, %10, %10;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %5, %9, p;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], %6, %9, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %7, %9, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%4], %8, %9, q;\n\t}" ::"r"(d),
+        "r"(a), "r"(a + 8), "r"(a + 16), "r"(a + 24), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "r"(idesc),
+        "r"(acc0)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.b32 p, %18, 0;\n\t"
+        "setp.eq.b32 q, %18, %18;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %9, %17, p;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], %10, %17, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %11, %17, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%4], %12, %17, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], %13, %17, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%6], %14, %17, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%7], %15, %17, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%8], %16, %17, q;\n\t}" ::"r"(d),
+        "r"(a), "r"(a + 8), "r"(a + 16), "r"(a + 24), "r"(a + 32), "r"(a + 40), "r"(a + 48), "r"(a + 56),
+        "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7]), "r"(idesc), "r"(acc0)
+        : "memory");
+  }
+}
+// The 8 K-step descriptors of a K-major [rows × 128] tile / an MN-major tile.
+__device__ __forceinline__ void kdescs(uint64_t base, int rows, uint64_t* o) {
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) o[ks] = base + koff(rows, ks);
+}
+__device__ __forceinline__ void mndescs(uint64_t base, int nk, uint64_t* o) {
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks)
+    if (ks < nk) o[ks] = base + mnoff(ks);
 }
 
 // 16-byte chunk c (8 elements) of row r of a 128-byte-swizzled [rows × 64] half.
@@ -181,15 +252,66 @@ __device__ __forceinline__ void store_row_chunk(void* base, int64_t off, const f
 }
 
 // ================================================================== forward
+// Two 128-row query tiles (A, B) per CTA, each with its own group of four
+// element-wise warps.  The tensor pipe alternates between the tiles —
+// S_A = Q_A·Kᵀ, P_B·V, S_B = Q_B·Kᵀ, P_A·V, … — so while one group turns its
+// score tile into probabilities the MMAs of the other tile run.  P is written
+// back into tensor memory over its own S columns (16-bit, two per column) and
+// is the A operand of O += P·V straight from there, which leaves shared memory
+// for Q_A, Q_B and two stages each of K and V.  The exponentials use a running
+// reference maximum per row that is raised (and O, l rescaled) only when a
+// tile's probabilities would grow past 2^15 — the result is the same, softmax
+// does not depend on the reference — so the steady state needs no pass for the
+// row maximum and almost never touches O.
 constexpr int F_BQ = 128, F_BK = 128;
 constexpr uint32_t F_TILE = 128 * 128 * 2;  // 32 KB
-constexpr uint32_t F_Q = 0, F_K0 = F_TILE, F_V0 = 3 * F_TILE, F_P = 5 * F_TILE;
-constexpr uint32_t F_RED = 6 * F_TILE;                 // [2 parities][2 groups][128 rows] float
-constexpr uint32_t F_END = F_RED + 2 * 2 * 128 * 4;
+constexpr uint32_t F_QA = 0, F_QB = F_TILE, F_K0 = 2 * F_TILE, F_V0 = 4 * F_TILE;
+constexpr uint32_t F_END = 6 * F_TILE;
 constexpr size_t F_SMEM = 1024 + F_END + sizeof(Tail);
-// barriers
-enum { FB_Q = 0, FB_KF = 1, FB_KE = 3, FB_VF = 5, FB_VE = 7, FB_SF = 9, FB_P = 11, FB_O = 12, FB_DRAIN = 13, FB_RED = 14 };
-static_assert(FB_RED + 2 <= 24, "barrier slots");
+// barriers: Q; K full/empty [2]; V full/empty [2]; S full, P ready, O done per tile
+enum { FB_Q = 0, FB_KF = 1, FB_KE = 3, FB_VF = 5, FB_VE = 7, FB_SF = 9, FB_P = 11, FB_O = 13, FB_DRAIN = 15,
+       FB_COUNT = 16 };
+static_assert(FB_COUNT <= 24, "barrier slots");
+
+// 32 columns of this warp's lane quarter into registers, without waiting.
+__device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+// Wait for this thread's outstanding tensor-memory loads; the registers are
+// tied to the wait so that no use of them is scheduled before it.
+__device__ __forceinline__ void tmem_wait_ld_tied(uint32_t* r) {
+  asm volatile(
+      "tcgen05.wait::ld.sync.aligned;"
+      : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+        "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+        "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]),
+        "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]),
+        "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+      :
+      : "memory");
+}
+// The 128 float32 columns at taddr (one row per thread) into x.
+__device__ __forceinline__ void tmem_ld128(uint32_t taddr, float* x) {
+  uint32_t* r = reinterpret_cast<uint32_t*>(x);
+  tmem_ld32_async(taddr, r);
+  tmem_ld32_async(taddr + 32, r + 32);
+  tmem_ld32_async(taddr + 64, r + 64);
+  tmem_ld32_async(taddr + 96, r + 96);
+  tmem_wait_ld_tied(r);
+  tmem_wait_ld_tied(r + 32);
+  tmem_wait_ld_tied(r + 64);
+  tmem_wait_ld_tied(r + 96);
+}
 
 template <int DT>
 __global__ void __launch_bounds__(ATT_THREADS, 1) attn_fwd_kernel(const __grid_constant__ AttnParams p) {
@@ -200,15 +322,17 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_fwd_kernel(const __grid_c
   volatile int* abort_flag = &tail->abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // grid (query tiles, heads, b): the tiles of one head run side by side and
-  // share its K and V through L2; under the causal mask a head's longest tiles
-  // (the last ones) are dispatched first
-  const int ntq = (p.s + F_BQ - 1) / F_BQ;
-  const int qt = p.causal ? ntq - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x);
+  // grid (256-row query pairs, heads, b): a head's pairs run side by side and
+  // share its K and V through L2; under the causal mask the longest pairs (the
+  // last ones) are dispatched first
+  const int npt = (p.s + 2 * F_BQ - 1) / (2 * F_BQ);
+  const int pt = p.causal ? npt - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x);
   const int head = blockIdx.y, bi = blockIdx.z;
-  const int q0 = qt * F_BQ;
+  const int q0 = pt * 2 * F_BQ;
   const int nkt = (p.s + F_BK - 1) / F_BK;
-  const int N = p.causal ? min(nkt, (q0 + F_BQ - 1) / F_BK + 1) : nkt;
+  // key tiles each query tile sees (up to its diagonal under the mask); NA ≤ NB ≤ NA + 1
+  const int NA = p.causal ? min(nkt, 2 * pt + 1) : nkt;
+  const int NB = p.causal ? min(nkt, 2 * pt + 2) : nkt;
   const int colq = 3 * HD * head, colk = colq + HD, colv = colq + 2 * HD;
 
   if (threadIdx.x == 0) {
@@ -219,12 +343,10 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_fwd_kernel(const __grid_c
       mbar_init(bar(FB_VF + i), 1);
       mbar_init(bar(FB_VE + i), 1);
       mbar_init(bar(FB_SF + i), 1);
+      mbar_init(bar(FB_P + i), 128);
+      mbar_init(bar(FB_O + i), 1);
     }
-    mbar_init(bar(FB_P), COMPUTE_THREADS);
-    mbar_init(bar(FB_O), 1);
     mbar_init(bar(FB_DRAIN), 1);
-    mbar_init(bar(FB_RED), COMPUTE_THREADS);
-    mbar_init(bar(FB_RED + 1), COMPUTE_THREADS);
     tail->abort_flag = 0;
     fence_barrier_init();
   }
@@ -236,24 +358,27 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_fwd_kernel(const __grid_c
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tail->tmem_slot;
-  const uint32_t sQ = smem_u32(smem + F_Q), sP = smem_u32(smem + F_P);
+  // TMEM columns: S_A (later P_A) at 0, S_B (P_B) at 128, O_A at 256, O_B at 384.
+  const uint32_t sQA = smem_u32(smem + F_QA), sQB = smem_u32(smem + F_QB);
+  const uint32_t sK0 = smem_u32(smem + F_K0), sV0 = smem_u32(smem + F_V0);
 
   if (warp == 0) {
     if (lane == 0) {
       tma_prefetch_map(&p.qkv128);
-      uint32_t issued = 0;  // stages with copies that may still be in flight
-      mbar_arrive_expect_tx(bar(FB_Q), F_TILE);
-      load_tile(sQ, &p.qkv128, bar(FB_Q), colq, bi, q0, 128);
+      uint32_t issued = 0;  // K/V tiles with copies that may still be in flight
+      mbar_arrive_expect_tx(bar(FB_Q), 2 * F_TILE);
+      load_tile(sQA, &p.qkv128, bar(FB_Q), colq, bi, q0, 128);
+      load_tile(sQB, &p.qkv128, bar(FB_Q), colq, bi, q0 + F_BQ, 128);
       bool ok = true;
-      for (int n = 0; ok && n < N; ++n) {
+      for (int n = 0; ok && n < NB; ++n) {
         const int st = n & 1;
         const uint32_t par = ((n >> 1) & 1) ^ 1u;
         if (!(ok = mbar_wait_bounded(bar(FB_KE + st), par, abort_flag, p.status, p.timeout_ns))) break;
         mbar_arrive_expect_tx(bar(FB_KF + st), F_TILE);
-        load_tile(smem_u32(smem + F_K0 + st * F_TILE), &p.qkv128, bar(FB_KF + st), colk, bi, n * F_BK, 128);
+        load_tile(sK0 + st * F_TILE, &p.qkv128, bar(FB_KF + st), colk, bi, n * F_BK, 128);
         if (!(ok = mbar_wait_bounded(bar(FB_VE + st), par, abort_flag, p.status, p.timeout_ns))) break;
         mbar_arrive_expect_tx(bar(FB_VF + st), F_TILE);
-        load_tile(smem_u32(smem + F_V0 + st * F_TILE), &p.qkv128, bar(FB_VF + st), colv, bi, n * F_BK, 128);
+        load_tile(sV0 + st * F_TILE, &p.qkv128, bar(FB_VF + st), colv, bi, n * F_BK, 128);
         issued = static_cast<uint32_t>(n + 1);
       }
       if (!ok) {
@@ -267,38 +392,70 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_fwd_kernel(const __grid_c
     }
     __syncwarp();
   } else if (warp == 1) {
+    // One issuing lane for both tiles, alternating between them: its order is
+    // what staggers the two tiles' softmax by half a period (two issuers let the
+    // tiles fall into step and their softmaxes contend; measured slower).
     if (lane == 0) {
       constexpr uint32_t idesc_s = make_idesc_f16(DT == DT_BF16, false, false, 128, F_BK);
       constexpr uint32_t idesc_o = make_idesc_f16(DT == DT_BF16, false, true, 128, HD);
-      bool ok = mbar_wait_bounded(bar(FB_Q), 0u, abort_flag, p.status, p.timeout_ns);
-      auto issue_s = [&](int n) -> bool {
-        const int st = n & 1;
-        if (!mbar_wait_bounded(bar(FB_KF + st), (n >> 1) & 1u, abort_flag, p.status, p.timeout_ns)) return false;
-        tc_fence_after();
-        const uint32_t sK = smem_u32(smem + F_K0 + st * F_TILE);
-#pragma unroll
-        for (int ks = 0; ks < HD / 16; ++ks)
-          tc_mma_f16(tmem + st * F_BK, kmajor128(sQ, 128, ks), kmajor128(sK, 128, ks), idesc_s, ks > 0 ? 1u : 0u);
-        tc_commit(bar(FB_SF + st));
-        tc_commit(bar(FB_KE + st));
-        return true;
+      const uint64_t dQA = sdesc_k(sQA), dQB = sdesc_k(sQB);
+      const uint64_t dK0 = sdesc_k(sK0), dK1 = sdesc_k(sK0 + F_TILE);
+      const uint64_t dV0 = sdesc_mn(sV0, 128), dV1 = sdesc_mn(sV0 + F_TILE, 128);
+      auto wait_k = [&](int n) {
+        return mbar_wait_bounded(bar(FB_KF + (n & 1)), (n >> 1) & 1u, abort_flag, p.status, p.timeout_ns);
       };
-      if (ok) tc_fence_after();
-      if (ok) ok = issue_s(0);
-      if (ok && N > 1) ok = issue_s(1);
-      for (int n = 0; ok && n < N; ++n) {
-        const int st = n & 1;
-        if (!(ok = mbar_wait_bounded(bar(FB_P), n & 1, abort_flag, p.status, p.timeout_ns))) break;
-        if (!(ok = mbar_wait_bounded(bar(FB_VF + st), (n >> 1) & 1u, abort_flag, p.status, p.timeout_ns))) break;
+      auto issue_s = [&](int t, int n) {  // S_t = Q_t·K(n)ᵀ
+        uint64_t a[8], b[8];
+        kdescs(t ? dQB : dQA, 128, a);
+        kdescs((n & 1) ? dK1 : dK0, 128, b);
+        mma8_ss(tmem + t * 128, a, b, idesc_s, 0u);
+        tc_commit(bar(FB_SF + t));
+      };
+      auto issue_pv = [&](int t, int n) {  // O_t += P_t·V(n), P_t from tensor memory
+        uint64_t b[8];
+        mndescs((n & 1) ? dV1 : dV0, 8, b);
+        mma_ts<8>(tmem + 256 + t * 128, tmem + t * 128, b, idesc_o, n > 0 ? 1u : 0u);
+      };
+      bool ok = mbar_wait_bounded(bar(FB_Q), 0u, abort_flag, p.status, p.timeout_ns) && wait_k(0);
+      if (ok) {
         tc_fence_after();
-        const uint32_t sV = smem_u32(smem + F_V0 + st * F_TILE);
-#pragma unroll
-        for (int ks = 0; ks < F_BK / 16; ++ks)
-          tc_mma_f16(tmem + 256, kmajor128(sP, 128, ks), mnmajor128(sV, 128, ks), idesc_o,
-                     (n > 0 || ks > 0) ? 1u : 0u);
-        tc_commit(bar(FB_O));
-        tc_commit(bar(FB_VE + st));
-        if (n + 2 < N) ok = issue_s(n + 2);
+        issue_s(0, 0);
+        issue_s(1, 0);
+        tc_commit(bar(FB_KE + 0));
+      }
+      for (int n = 0; ok && n < NB; ++n) {
+        const int st = n & 1;
+        bool v_ready = false, k_ready = false;
+        if (n < NA) {
+          if (!(ok = mbar_wait_bounded(bar(FB_P + 0), n & 1, abort_flag, p.status, p.timeout_ns))) break;
+          if (!(ok = mbar_wait_bounded(bar(FB_VF + st), (n >> 1) & 1u, abort_flag, p.status, p.timeout_ns))) break;
+          v_ready = true;
+          tc_fence_after();
+          issue_pv(0, n);
+          if (n + 1 < NA) {
+            if (!(ok = wait_k(n + 1))) break;
+            k_ready = true;
+            tc_fence_after();
+            issue_s(0, n + 1);
+          } else {
+            tc_commit(bar(FB_O + 0));
+          }
+        }
+        if (!(ok = mbar_wait_bounded(bar(FB_P + 1), n & 1, abort_flag, p.status, p.timeout_ns))) break;
+        if (!v_ready &&
+            !(ok = mbar_wait_bounded(bar(FB_VF + st), (n >> 1) & 1u, abort_flag, p.status, p.timeout_ns)))
+          break;
+        tc_fence_after();
+        issue_pv(1, n);
+        tc_commit(bar(FB_VE + st));  // V(n) is free once both tiles' P·V have run
+        if (n + 1 < NB) {
+          if (!k_ready && !(ok = wait_k(n + 1))) break;
+          tc_fence_after();
+          issue_s(1, n + 1);
+          tc_commit(bar(FB_KE + ((n + 1) & 1)));  // K(n+1) is free once both tiles' S have run
+        } else {
+          tc_commit(bar(FB_O + 1));
+        }
       }
       if (!ok) {
         tc_commit(bar(FB_DRAIN));
@@ -307,127 +464,150 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_fwd_kernel(const __grid_c
     }
     __syncwarp();
   } else if (warp >= 4) {
-    // Two groups of four warps; group g takes columns [64g, 64g+64) of every S
-    // tile and of O, for the 128 rows (one per thread, = TMEM lane).  The row
-    // maximum is combined across the groups through shared memory and an
-    // mbarrier; each group keeps its own partial row sum until the end.
-    const int g = (warp - 4) >> 2;
+    // Group t (warps 4–7: tile A, 8–11: tile B); one thread per row, all 128
+    // columns of every S tile and of O.
+    const int t = (warp - 4) >> 2;
     const int qw = warp & 3;
     const int r = qw * 32 + lane;
-    const int q = q0 + r;
+    const int q0t = q0 + t * F_BQ;
+    const int q = q0t + r;
+    const int N = t ? NB : NA;
     const uint32_t tl = tmem + (static_cast<uint32_t>(qw * 32) << 16);
-    float* red = reinterpret_cast<float*>(smem + F_RED);
+    const uint32_t tS = tl + t * 128, tO = tl + 256 + t * 128;
     const float c = p.scale_log2;
-    float m = -INFINITY, l = 0.0f;  // running maximum of the raw scores; this group's partial sum
+    float m_ref = -INFINITY;  // reference (scaled) maximum of the exponentials
+    float l = 0.0f;           // row sum of 2^(x·c − m_ref)
     bool ok = true;
     for (int n = 0; n < N; ++n) {
-      const int st = n & 1;
-      ok = mbar_wait_bounded(bar(FB_SF + st), (n >> 1) & 1u, abort_flag, p.status, p.timeout_ns);
+      ok = mbar_wait_bounded(bar(FB_SF + t), n & 1, abort_flag, p.status, p.timeout_ns);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
-      float x[64];
-      tmem_ld32(tl + st * F_BK + g * 64, x);
-      tmem_ld32(tl + st * F_BK + g * 64 + 32, x + 32);
-      const int kb = n * F_BK + g * 64;
-      // only tiles reaching past s or across the diagonal need the mask
-      if (n * F_BK + F_BK > p.s || (p.causal && n * F_BK + F_BK - 1 > q0)) {
+      // Steady state: the exponentials are taken against the current reference
+      // m_ref directly and the tile is kept when its row sum is at most 2^15 —
+      // then every p ≤ 2^15 (representable in bf16 and fp16).  Otherwise (the
+      // row maximum moved up by more than about 2^8, and on the first tile) the
+      // tile is redone with a pass for its maximum first.  P stays in registers
+      // until the check has passed, so S is still intact for the second try.
+      // The mask applies to tiles reaching past s or across the diagonal only.
+      const bool need_mask = n * F_BK + F_BK > p.s || (p.causal && n * F_BK + F_BK - 1 > q0t);
+      auto load32 = [&](int h, float* x) {  // S columns [32h, 32h+32)
+        uint32_t* r = reinterpret_cast<uint32_t*>(x);
+        tmem_ld32_async(tS + h * 32, r);
+        tmem_wait_ld_tied(r);
+        if (need_mask) {
 #pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          const int key = kb + j;
-          if (!(key < p.s && (!p.causal || key <= q))) x[j] = -INFINITY;
-        }
-      }
-      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-      for (int j = 0; j < 64; ++j) m4[j & 3] = fmaxf(m4[j & 3], x[j]);
-      float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-      const int rb = n & 1;
-      red[(rb * 2 + g) * 128 + r] = mx;
-      mbar_arrive(bar(FB_RED + rb));
-      ok = mbar_wait_bounded(bar(FB_RED + rb), (n >> 1) & 1u, abort_flag, p.status, p.timeout_ns);
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-      mx = fmaxf(mx, red[(rb * 2 + (g ^ 1)) * 128 + r]);
-      const float m_new = fmaxf(m, mx);
-      const float m_use = m_new == -INFINITY ? 0.0f : m_new;
-      const float mc = m_use * c;
-      const float alpha = ex2((m - m_use) * c);
-      // p = 2^(x·c − m·c) and the row sum, the FMA and the adds two elements per
-      // instruction (paired float32 arithmetic), four partial sums
-      const float2 c2 = make_float2(c, c), nmc2 = make_float2(-mc, -mc);
-      float2 s2[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
-#pragma unroll
-      for (int j = 0; j < 64; j += 2) {
-        const float2 a = __ffma2_rn(make_float2(x[j], x[j + 1]), c2, nmc2);
-        const float2 e = make_float2(ex2(a.x), ex2(a.y));
-        x[j] = e.x;
-        x[j + 1] = e.y;
-        s2[(j >> 1) & 1] = __fadd2_rn(s2[(j >> 1) & 1], e);
-      }
-      l = l * alpha + ((s2[0].x + s2[1].x) + (s2[0].y + s2[1].y));
-      m = m_new;
-      if (n > 0) {
-        // P·V of the previous tile has finished: P's buffer is free and O holds
-        // the sum so far, to be rescaled to the new maximum.
-        ok = mbar_wait_bounded(bar(FB_O), (n - 1) & 1, abort_flag, p.status, p.timeout_ns);
-        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.0f)) {
-#pragma unroll 1
-          for (int cc = 0; cc < 2; ++cc) {
-            float o[32];
-            const uint32_t ta = tl + 256 + g * 64 + cc * 32;
-            tmem_ld32(ta, o);
-            const float2 a2 = make_float2(alpha, alpha);
-#pragma unroll
-            for (int j = 0; j < 32; j += 2) {
-              const float2 v = __fmul2_rn(make_float2(o[j], o[j + 1]), a2);
-              o[j] = v.x;
-              o[j + 1] = v.y;
-            }
-            tmem_st32(ta, o);
+          for (int j = 0; j < 32; ++j) {
+            const int key = n * F_BK + h * 32 + j;
+            if (!(key < p.s && (!p.causal || key <= q))) x[j] = -INFINITY;
           }
-          tmem_st_wait();
+        }
+      };
+      // p = 2^(x·c − mu) for the 128 columns, packed to 16 bits into pk (two per
+      // word), the row sum returned; two elements per instruction
+      uint32_t pk[64];
+      auto exp_tile = [&](float mu) -> float {
+        const float2 c2 = make_float2(c, c), nmu2 = make_float2(-mu, -mu);
+        float2 s2[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          float x[32];
+          load32(h, x);
+#pragma unroll
+          for (int j8 = 0; j8 < 4; ++j8) {
+            float e8[8];
+#pragma unroll
+            for (int i = 0; i < 8; i += 2) {
+              const float2 a = __ffma2_rn(make_float2(x[8 * j8 + i], x[8 * j8 + i + 1]), c2, nmu2);
+              const float2 e = make_float2(ex2(a.x), ex2(a.y));
+              e8[i] = e.x;
+              e8[i + 1] = e.y;
+              s2[(i >> 1) & 1] = __fadd2_rn(s2[(i >> 1) & 1], e);
+            }
+            const uint4 v = pack8<DT>(e8);
+            pk[16 * h + 4 * j8] = v.x;
+            pk[16 * h + 4 * j8 + 1] = v.y;
+            pk[16 * h + 4 * j8 + 2] = v.z;
+            pk[16 * h + 4 * j8 + 3] = v.w;
+          }
+        }
+        return (s2[0].x + s2[1].x) + (s2[0].y + s2[1].y);
+      };
+      float tsum = 0.0f;
+      bool redo = m_ref == -INFINITY;
+      if (!__any_sync(0xffffffffu, redo)) {
+        tsum = exp_tile(m_ref);
+        redo = !(tsum <= 32768.0f);  // also true for inf
+      }
+      bool rescale = false;
+      float alpha = 1.0f;
+      if (__any_sync(0xffffffffu, redo)) {
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll 1
+        for (int h = 0; h < 4; ++h) {
+          float x[32];
+          load32(h, x);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) m4[j & 3] = fmaxf(m4[j & 3], x[j]);
+        }
+        const float mxc = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * c;
+        const bool grow = mxc > m_ref;
+        rescale = __any_sync(0xffffffffu, grow);
+        if (grow) {
+          alpha = m_ref == -INFINITY ? 0.0f : ex2(m_ref - mxc);
+          l *= alpha;
+          m_ref = mxc;
+        }
+        tsum = exp_tile(m_ref == -INFINITY ? 0.0f : m_ref);
+      }
+      l += tsum;
+      // P over the first 64 columns of its S tile, two 16-bit elements per column
+      tmem_st32(tS, reinterpret_cast<const float*>(pk));
+      tmem_st32(tS + 32, reinterpret_cast<const float*>(pk + 32));
+      if (rescale && n > 0) {
+        // O holds the sum so far (its P·V finished before this S did); it is
+        // brought to the new reference before this tile's P·V is issued
+        const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll 1
+        for (int cc = 0; cc < 4; ++cc) {
+          float o[32];
+          tmem_ld32(tO + cc * 32, o);
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            const float2 v = __fmul2_rn(make_float2(o[j], o[j + 1]), a2);
+            o[j] = v.x;
+            o[j + 1] = v.y;
+          }
+          tmem_st32(tO + cc * 32, o);
         }
       }
-      // P as the A operand of O += P·V: row r, keys [64g, 64g+64) = half g.
-#pragma unroll
-      for (int cc = 0; cc < 8; ++cc) st_swizzled(smem + F_P + g * (128 * HALF_ROW_BYTES), r, cc, pack8<DT>(x + cc * 8));
-      fence_proxy_async_smem();
+      tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar(FB_P));
+      mbar_arrive(bar(FB_P + t));
     }
     if (ok) {
-      ok = mbar_wait_bounded(bar(FB_O), (N - 1) & 1, abort_flag, p.status, p.timeout_ns);
+      ok = mbar_wait_bounded(bar(FB_O + t), 0u, abort_flag, p.status, p.timeout_ns);
       ok = __all_sync(0xffffffffu, ok);
-    }
-    if (ok) {
-      // the two groups' partial sums (exchange slot of iteration N)
-      const int rb = N & 1;
-      red[(rb * 2 + g) * 128 + r] = l;
-      mbar_arrive(bar(FB_RED + rb));
-      ok = mbar_wait_bounded(bar(FB_RED + rb), (N >> 1) & 1u, abort_flag, p.status, p.timeout_ns);
-      ok = __all_sync(0xffffffffu, ok);
-      if (ok) l += red[(rb * 2 + (g ^ 1)) * 128 + r];
     }
     if (ok) {
       tc_fence_after();
       const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
       const int64_t mrow = static_cast<int64_t>(q) * p.b + bi;
 #pragma unroll 1
-      for (int cc = 0; cc < 2; ++cc) {
+      for (int cc = 0; cc < 4; ++cc) {
         float o[32];
-        tmem_ld32(tl + 256 + g * 64 + cc * 32, o);
+        tmem_ld32(tO + cc * 32, o);
         if (q < p.s) {
 #pragma unroll
           for (int j = 0; j < 32; ++j) o[j] *= inv_l;
 #pragma unroll
           for (int k4 = 0; k4 < 4; ++k4)
-            store_row_chunk<DT>(p.o, mrow * p.h + head * HD + g * 64 + cc * 32 + k4 * 8, o + k4 * 8);
+            store_row_chunk<DT>(p.o, mrow * p.h + head * HD + cc * 32 + k4 * 8, o + k4 * 8);
         }
       }
-      // rows past s (the padded tail of the last tile) get 0: the backward reads whole tiles
-      if (g == 0)
-        p.lse[(static_cast<int64_t>(bi) * p.heads + head) * p.s_pad + q] = q < p.s ? m * c + __log2f(l) : 0.0f;
+      // rows past s (the padded tail of the last 128-row tile) get 0: the
+      // backward reads whole tiles; rows past s_pad do not exist
+      if (q < p.s_pad)
+        p.lse[(static_cast<int64_t>(bi) * p.heads + head) * p.s_pad + q] = q < p.s ? m_ref + __log2f(l) : 0.0f;
     }
   }
   tc_fence_before();
@@ -475,19 +655,39 @@ __global__ void __launch_bounds__(256) attn_bwd_delta_kernel(const void* __restr
 }
 
 // ================================================================== backward: dK, dV
-constexpr int KV_BK = 128, KV_BQ = 64, KV_ST = 3;
+// Per (128-key tile, head, sequence) over 64-query tiles.  Tensor memory holds
+// Sᵀ and dPᵀ (one buffer: the element-wise warps release it as soon as they have
+// loaded it, so Sᵀ/dPᵀ of the next query tile are computed while they work),
+// the 16-bit Pᵀ and dSᵀ (two buffers), which are the A operands of dV += Pᵀ·dO
+// and dK += dSᵀ·Q straight from tensor memory, and the dV and dK accumulators.
+// Shared memory holds K, V, a 3-deep ring of (Q, dO, −lse2, Δ) and three dSᵀ
+// buffers for the bulk stores to HBM.  Keeping P and dS out of shared memory
+// matters: the kernel is bound by shared-memory bandwidth (operand reads of the
+// MMAs, TMA writes, the dSᵀ stores), not by the tensor pipe.
+constexpr int KV_BK = 128, KV_BQ = 64, KV_ST = 3, KV_DSB = 3;
 constexpr uint32_t KV_TILE = 128 * 128 * 2;    // K or V tile, 32 KB
 constexpr uint32_t KV_QTILE = 64 * 128 * 2;    // Q or dO tile of 64 rows, 16 KB
-constexpr uint32_t KV_STAGE = 2 * KV_QTILE + 512;  // Q, dO, lse2[64], Δ[64]
-constexpr uint32_t KV_K = 0, KV_V = KV_TILE, KV_S0 = 2 * KV_TILE;
-constexpr uint32_t KV_PT = KV_S0 + KV_ST * ((KV_STAGE + 1023) & ~1023u);
-constexpr uint32_t KV_DST = KV_PT + 128 * HALF_ROW_BYTES;  // two dSᵀ buffers: MMA operand and HBM store
-constexpr uint32_t KV_END = KV_DST + 2 * DS_TILE;
+constexpr uint32_t KV_STAGE = 2 * KV_QTILE + 512;  // Q, dO, −lse2[64], Δ[64]
 constexpr uint32_t KV_STRIDE = (KV_STAGE + 1023) & ~1023u;
+constexpr uint32_t KV_K = 0, KV_V = KV_TILE, KV_S0 = 2 * KV_TILE;
+constexpr uint32_t KV_DST = KV_S0 + KV_ST * KV_STRIDE;  // KV_DSB dSᵀ buffers for the HBM stores
+constexpr uint32_t KV_END = KV_DST + KV_DSB * DS_TILE;
 constexpr size_t KV_SMEM = 1024 + KV_END + sizeof(Tail);
-enum { KB_KV = 0, KB_F = 1, KB_E = KB_F + KV_ST, KB_SF = KB_E + KV_ST, KB_P = KB_SF + 2, KB_MM = KB_P + 1,
-       KB_DRAIN = KB_MM + 1, KB_COUNT = KB_DRAIN + 1 };
+// TMEM columns
+constexpr uint32_t KT_S = 0, KT_DP = 64, KT_P = 128, KT_DV = 256, KT_DK = 384;  // P/dS buffer b at KT_P + 64b
+enum { KB_KV = 0, KB_F = 1, KB_E = KB_F + KV_ST, KB_SF = KB_E + KV_ST, KB_SC = KB_SF + 1, KB_P = KB_SC + 1,
+       KB_MM = KB_P + 2, KB_DRAIN = KB_MM + 2, KB_COUNT = KB_DRAIN + 1 };
 static_assert(KB_COUNT <= 24, "barrier slots");
+
+// 16 32-bit columns of this warp's lane quarter from registers.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+      "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
 
 template <int DT>
 __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dkdv_kernel(const __grid_constant__ AttnParams p) {
@@ -521,9 +721,11 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dkdv_kernel(const __g
       mbar_init(bar(KB_E + i), 1);
     }
     mbar_init(bar(KB_SF), 1);
-    mbar_init(bar(KB_SF + 1), 1);
-    mbar_init(bar(KB_P), COMPUTE_THREADS);
-    mbar_init(bar(KB_MM), 1);
+    mbar_init(bar(KB_SC), COMPUTE_THREADS);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(KB_P + i), COMPUTE_THREADS);
+      mbar_init(bar(KB_MM + i), 1);
+    }
     mbar_init(bar(KB_DRAIN), 1);
     tail->abort_flag = 0;
     fence_barrier_init();
@@ -536,9 +738,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dkdv_kernel(const __g
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tail->tmem_slot;
-  // TMEM columns: Sᵀ[2] at 0 / 64, dPᵀ[2] at 128 / 192, dV at 256, dK at 384.
-  const uint32_t sK = smem_u32(smem + KV_K), sV = smem_u32(smem + KV_V);
-  const uint32_t sPT = smem_u32(smem + KV_PT), sDST = smem_u32(smem + KV_DST);
+  const uint32_t sK = smem_u32(smem + KV_K), sV = smem_u32(smem + KV_V), sDST = smem_u32(smem + KV_DST);
   auto stage_base = [&](int st) { return smem + KV_S0 + st * KV_STRIDE; };
 
   if (warp == 0) {
@@ -577,43 +777,48 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dkdv_kernel(const __g
       constexpr uint32_t idesc_s = make_idesc_f16(DT == DT_BF16, false, false, 128, KV_BQ);
       constexpr uint32_t idesc_acc = make_idesc_f16(DT == DT_BF16, false, true, 128, HD);
       bool ok = mbar_wait_bounded(bar(KB_KV), 0u, abort_flag, p.status, p.timeout_ns);
+      const uint64_t dKs = sdesc_k(sK), dVs = sdesc_k(sV);
+      // Sᵀ = K·Qᵀ and dPᵀ = V·dOᵀ of query tile n
       auto issue_sdp = [&](int n) -> bool {
-        const int st = n % KV_ST, buf = n & 1;
+        const int st = n % KV_ST;
         if (!mbar_wait_bounded(bar(KB_F + st), (n / KV_ST) & 1u, abort_flag, p.status, p.timeout_ns)) return false;
         tc_fence_after();
         const uint32_t sQ = smem_u32(stage_base(st)), sDO = sQ + KV_QTILE;
-#pragma unroll
-        for (int ks = 0; ks < HD / 16; ++ks) {
-          tc_mma_f16(tmem + buf * 64, kmajor128(sK, 128, ks), kmajor128(sQ, 64, ks), idesc_s, ks > 0 ? 1u : 0u);
-          tc_mma_f16(tmem + 128 + buf * 64, kmajor128(sV, 128, ks), kmajor128(sDO, 64, ks), idesc_s,
-                     ks > 0 ? 1u : 0u);
-        }
-        tc_commit(bar(KB_SF + buf));
+        uint64_t a[8], b[8];
+        kdescs(dKs, 128, a);
+        kdescs(sdesc_k(sQ), 64, b);
+        mma8_ss(tmem + KT_S, a, b, idesc_s, 0u);
+        kdescs(dVs, 128, a);
+        kdescs(sdesc_k(sDO), 64, b);
+        mma8_ss(tmem + KT_DP, a, b, idesc_s, 0u);
+        tc_commit(bar(KB_SF));
         return true;
       };
       if (ok) tc_fence_after();
       if (ok) ok = issue_sdp(0);
-      if (ok && N > 1) ok = issue_sdp(1);
       for (int n = 0; ok && n < N; ++n) {
-        const int st = n % KV_ST;
-        if (!(ok = mbar_wait_bounded(bar(KB_P), n & 1, abort_flag, p.status, p.timeout_ns))) break;
+        const int st = n % KV_ST, b = n & 1;
+        if (n + 1 < N) {
+          // the element-wise warps have loaded Sᵀ/dPᵀ of tile n: compute tile n+1's
+          if (!(ok = mbar_wait_bounded(bar(KB_SC), n & 1, abort_flag, p.status, p.timeout_ns))) break;
+          tc_fence_after();
+          if (!(ok = issue_sdp(n + 1))) break;
+        }
+        if (!(ok = mbar_wait_bounded(bar(KB_P + b), (n >> 1) & 1u, abort_flag, p.status, p.timeout_ns))) break;
         tc_fence_after();
         const uint32_t sQ = smem_u32(stage_base(st)), sDO = sQ + KV_QTILE;
-        const uint32_t sDSn = sDST + (n & 1) * DS_TILE;
-        bulk_store(ds_out + static_cast<int64_t>(n) * DS_TILE, sDSn, DS_TILE);  // dSᵀ for the dQ kernel
-#pragma unroll
-        for (int ks = 0; ks < KV_BQ / 16; ++ks) {
-          tc_mma_f16(tmem + 256, kmajor64(sPT, ks), mnmajor128(sDO, KV_BQ, ks), idesc_acc,
-                     (n > 0 || ks > 0) ? 1u : 0u);
-          tc_mma_f16(tmem + 384, kmajor64(sDSn, ks), mnmajor128(sQ, KV_BQ, ks), idesc_acc,
-                     (n > 0 || ks > 0) ? 1u : 0u);
-        }
-        // the compute warps rewrite dSᵀ buffer (n+1)&1 once KB_MM of this step
-        // completes, so the store of step n−1 (that buffer) must have read it
+        bulk_store(ds_out + static_cast<int64_t>(n) * DS_TILE, sDST + (n % KV_DSB) * DS_TILE, DS_TILE);
+        const uint32_t tP = tmem + KT_P + b * 64;  // Pᵀ at +0, dSᵀ at +32 (16-bit, two per column)
+        uint64_t bd[8];
+        mndescs(sdesc_mn(sDO, KV_BQ), 4, bd);
+        mma_ts<4>(tmem + KT_DV, tP, bd, idesc_acc, n > 0 ? 1u : 0u);
+        mndescs(sdesc_mn(sQ, KV_BQ), 4, bd);
+        mma_ts<4>(tmem + KT_DK, tP + 32, bd, idesc_acc, n > 0 ? 1u : 0u);
+        // the element-wise warps rewrite dSᵀ buffer (n+2)%3 once MM of this step
+        // completes; the store of step n−1 (that buffer) must have read it
         bulk_wait_read<1>();
-        tc_commit(bar(KB_MM));
+        tc_commit(bar(KB_MM + b));
         tc_commit(bar(KB_E + st));
-        if (n + 2 < N) ok = issue_sdp(n + 2);
       }
       if (!ok) {
         tc_commit(bar(KB_DRAIN));
@@ -633,13 +838,17 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dkdv_kernel(const __g
     const float c = p.scale_log2;
     bool ok = true;
     for (int n = 0; n < N; ++n) {
-      const int st = n % KV_ST, buf = n & 1;
-      ok = mbar_wait_bounded(bar(KB_SF + buf), (n >> 1) & 1u, abort_flag, p.status, p.timeout_ns);
+      const int st = n % KV_ST, b = n & 1;
+      ok = mbar_wait_bounded(bar(KB_SF), n & 1, abort_flag, p.status, p.timeout_ns);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
       float sv[32], dp[32];
-      tmem_ld32(tl + buf * 64 + g * 32, sv);
-      tmem_ld32(tl + 128 + buf * 64 + g * 32, dp);
+      tmem_ld32_async(tl + KT_S + g * 32, reinterpret_cast<uint32_t*>(sv));
+      tmem_ld32_async(tl + KT_DP + g * 32, reinterpret_cast<uint32_t*>(dp));
+      tmem_wait_ld_tied(reinterpret_cast<uint32_t*>(sv));
+      tmem_wait_ld_tied(reinterpret_cast<uint32_t*>(dp));
+      tc_fence_before();
+      mbar_arrive(bar(KB_SC));  // Sᵀ/dPᵀ may be overwritten by the next tile's
       const float4* lse4 = reinterpret_cast<const float4*>(stage_base(st) + 2 * KV_QTILE) + g * 8;
       const float4* del4 = lse4 + 16;
       const int qq = (qt_first + n) * KV_BQ + g * 32;
@@ -659,11 +868,10 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dkdv_kernel(const __g
         }
       }
       // P = 2^(S·c − lse2) and dS = P ⊙ (dP − Δ), the latter two elements per
-      // instruction (paired float32 arithmetic)
+      // instruction (paired float32 arithmetic); lj holds −lse2
       const float2 neg1 = make_float2(-1.0f, -1.0f), c2 = make_float2(c, c);
 #pragma unroll
       for (int j = 0; j < 32; j += 2) {
-        // lj holds −lse2 (staged that way by the Δ kernel)
         const float2 arg = __ffma2_rn(make_float2(sv[j], sv[j + 1]), c2, make_float2(lj[j], lj[j + 1]));
         const float2 pr = make_float2(ex2(arg.x), ex2(arg.y));
         const float2 d = __ffma2_rn(make_float2(dj[j], dj[j + 1]), neg1, make_float2(dp[j], dp[j + 1]));
@@ -673,21 +881,35 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dkdv_kernel(const __g
         sv[j] = pr.x;
         sv[j + 1] = pr.y;
       }
-      if (n > 0) {
-        ok = mbar_wait_bounded(bar(KB_MM), (n - 1) & 1, abort_flag, p.status, p.timeout_ns);
-        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-      }
+      uint32_t pk[16], dk16[16];
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
-        st_swizzled(smem + KV_PT, r, g * 4 + cc, pack8<DT>(sv + cc * 8));
-        st_swizzled(smem + KV_DST + (n & 1) * DS_TILE, r, g * 4 + cc, pack8<DT>(dp + cc * 8));
+        const uint4 a = pack8<DT>(sv + cc * 8), d = pack8<DT>(dp + cc * 8);
+        pk[4 * cc] = a.x; pk[4 * cc + 1] = a.y; pk[4 * cc + 2] = a.z; pk[4 * cc + 3] = a.w;
+        dk16[4 * cc] = d.x; dk16[4 * cc + 1] = d.y; dk16[4 * cc + 2] = d.z; dk16[4 * cc + 3] = d.w;
       }
+      if (n >= 2) {
+        // dV/dK of tile n−2 (the last reader of this P/dS buffer) have run, and
+        // the bulk store of tile n−3 (the last reader of this dSᵀ buffer) has
+        // read it (MM is committed after that store's read)
+        ok = mbar_wait_bounded(bar(KB_MM + b), ((n - 2) >> 1) & 1u, abort_flag, p.status, p.timeout_ns);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        tc_fence_after();
+      }
+      const uint32_t tP = tl + KT_P + b * 64;
+      tmem_st16(tP + g * 16, pk);
+      tmem_st16(tP + 32 + g * 16, dk16);
+      uint8_t* dsb = smem + KV_DST + (n % KV_DSB) * DS_TILE;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc)
+        st_swizzled(dsb, r, g * 4 + cc, make_uint4(dk16[4 * cc], dk16[4 * cc + 1], dk16[4 * cc + 2], dk16[4 * cc + 3]));
+      tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(bar(KB_P));
+      mbar_arrive(bar(KB_P + b));
     }
     if (ok) {
-      ok = mbar_wait_bounded(bar(KB_MM), (N - 1) & 1, abort_flag, p.status, p.timeout_ns);
+      ok = mbar_wait_bounded(bar(KB_MM + ((N - 1) & 1)), ((N - 1) >> 1) & 1u, abort_flag, p.status, p.timeout_ns);
       ok = __all_sync(0xffffffffu, ok);
     }
     if (ok) {
@@ -698,8 +920,8 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dkdv_kernel(const __g
       for (int cc = 0; cc < 2; ++cc) {
         const int col = g * 64 + cc * 32;
         float dv[32], dk[32];
-        tmem_ld32(tl + 256 + col, dv);
-        tmem_ld32(tl + 384 + col, dk);
+        tmem_ld32(tl + KT_DV + col, dv);
+        tmem_ld32(tl + KT_DK + col, dk);
         if (key < p.s) {
 #pragma unroll
           for (int j = 0; j < 32; ++j) dk[j] *= p.scale;
@@ -807,9 +1029,10 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dq_kernel(const __gri
         if (!(ok = mbar_wait_bounded(bar(QB_F + st), (n / DQ_ST) & 1u, abort_flag, p.status, p.timeout_ns))) break;
         tc_fence_after();
         const uint32_t sa = stage_addr(st), sk = sa + 2 * DS_TILE;
-#pragma unroll
-        for (int ks = 0; ks < 128 / 16; ++ks)
-          tc_mma_f16(tmem, mnmajor128(sa, 128, ks), mnmajor128(sk, 128, ks), idesc, (n > 0 || ks > 0) ? 1u : 0u);
+        uint64_t a[8], b[8];
+        mndescs(sdesc_mn(sa, 128), 8, a);
+        mndescs(sdesc_mn(sk, 128), 8, b);
+        mma8_ss(tmem, a, b, idesc, n > 0 ? 1u : 0u);
         tc_commit(bar(QB_E + st));
       }
       tc_commit(bar(ok ? QB_MM : QB_DRAIN));
@@ -1017,7 +1240,8 @@ int launch_core_forward(const Shape& k, const void* qkv, void* o, float* lse, cu
   if ((rc = make_map3(&p.qkv128, k.dtype, qkv, 3 * k.h, k.b, k.s, 128))) return rc;
   p.o = o;
   p.lse = lse;
-  const dim3 grid(static_cast<unsigned>(k.s_pad / 128), static_cast<unsigned>(k.heads), static_cast<unsigned>(k.b));
+  const dim3 grid(static_cast<unsigned>((k.s + 2 * F_BQ - 1) / (2 * F_BQ)), static_cast<unsigned>(k.heads),
+                  static_cast<unsigned>(k.b));
   const void* fn = k.dtype == DT_BF16 ? reinterpret_cast<const void*>(attn_fwd_kernel<DT_BF16>)
                                       : reinterpret_cast<const void*>(attn_fwd_kernel<DT_F16>);
   if ((rc = set_smem(fn, F_SMEM))) return rc;
