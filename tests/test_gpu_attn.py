@@ -158,6 +158,42 @@ def test_llama70b_width_attention_sampled(cuda_lib):
     assert rel_err(dwqkv[qrows], dqkv[:, qrows].T @ X) <= TOL
 
 
+@pytest.mark.parametrize("causal", [True, False], ids=["causal", "unmasked"])
+def test_growing_scores_raise_the_softmax_reference(cuda_lib, causal):
+    """Token rows of X scaled up linearly along the sequence (×1 … ×10) make the
+    scores grow along the keys, so a row's maximum rises by far more than 2^15
+    between key tiles many times over: the forward's exponentials must raise
+    their reference maximum mid-sequence and rescale O and the row sum (the
+    path that plain N(0, 1) inputs only take on each row's first tile).  Scores
+    this sharp make the block output sensitive to the rounding of QKV itself, so
+    the core is checked against the oracle's core on the GPU's own QKV and dO."""
+    tpmlp = cuda_lib
+    cfg = AttnConfig("growing", 512, 1, 256, 2, 1, False, "bf16", causal)
+    t = attn_inputs(cfg)
+    ramp = torch.linspace(1.0, 10.0, cfg.s).view(cfg.s, 1, 1)
+    t["X"] = (t["X"].float() * ramp).to(cfg.torch_dtype)
+    _, blk, fw, bw, cat = _run(tpmlp, cfg, t)
+    s, d = cfg.s, cfg.d
+    Q, K, V = O.split_qkv(to_np(fw["qkv"]), cfg.heads)
+    # the workload does exercise the path: per row, key tiles whose maximum
+    # exceeds everything before it by more than 15 (log2 units)
+    x = np.einsum("thd,uhd->htu", Q.reshape(s, cfg.heads, d), K.reshape(s, cfg.heads, d)) * (O.LOG2E / np.sqrt(d))
+    if causal:
+        x = np.where(np.triu(np.ones((s, s), dtype=bool), k=1), -np.inf, x)
+    tile_max = x.reshape(cfg.heads, s, s // 128, 128).max(axis=-1)
+    running = np.maximum.accumulate(tile_max, axis=-1)
+    jumps = int((tile_max[..., 1:] > running[..., :-1] + 15).sum())
+    assert jumps > 20, jumps  # 27 causal, 51 unmasked
+    core = O.attention_core_forward(Q, K, V, s, cfg.b, cfg.heads, causal)
+    assert rel_err(to_np(fw["o"]), core["O"]) <= 1e-2
+    lse = to_np(fw["lse"])[:, :, :s]
+    assert np.abs(lse - core["lse2"]).max() <= 1e-3 * np.abs(core["lse2"]).max()
+    gc = O.attention_core_backward(Q, K, V, to_np(bw["dout"]), s, cfg.b, cfg.heads, causal)
+    dq, dk, dv = O.split_qkv(to_np(bw["dqkv"]), cfg.heads)
+    for name, got, want in (("dQ", dq, gc["dQ"]), ("dK", dk, gc["dK"]), ("dV", dv, gc["dV"])):
+        assert rel_err(got, want) <= TOL, name
+
+
 def test_empty_sequence(cuda_lib):
     """s = 0: nothing to compute; the weight gradients are empty sums (zero).
     (Buffers are non-empty dummies: the ABI rejects NULL pointers.)"""
