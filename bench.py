@@ -722,6 +722,82 @@ def run_attention(args) -> int:
                              "share_of_step": v["ms"] / args.steps / ms}
     a = prof["attn_core"]
     achieved = a["work"] / (a["ms"] / 1e3) / 1e12
+
+    # ------------------------------------------------ end to end through the C ABI
+    # Every step uploads the X and dZ chunks from pinned host memory and
+    # downloads Z and dX, double-buffered on two copy streams against the compute
+    # stream (weights and weight gradients stay on the device), as for the MLP.
+    e2e = None
+    if not args.no_e2e:
+        as_list = lambda v: list(v) if isinstance(v, (list, tuple)) else [v]  # noqa: E731
+        pin = lambda v: v.cpu().pin_memory()  # noqa: E731
+        nset = 2
+        xin = [[c.clone() for c in as_list(x)] for _ in range(nset)]
+        dzin = [[c.clone() for c in as_list(dz)] for _ in range(nset)]
+        fws = [blk.forward(x, Wqkv, Wo, stream=stream) for _ in range(nset)]
+        bws = [blk.backward(x, Wqkv, Wo, fws[k], dz, stream=stream) for k in range(nset)]
+        xh = [pin(c) for c in as_list(x)]
+        dzh = [pin(c) for c in as_list(dz)]
+        zh = [[torch.empty_like(v, device="cpu").pin_memory() for v in as_list(fws[0]["z"])] for _ in range(nset)]
+        dxh = [[torch.empty_like(v, device="cpu").pin_memory() for v in as_list(bws[0]["dx"])] for _ in range(nset)]
+        h2d = sum(v.numel() * v.element_size() for v in xh + dzh)
+        d2h = sum(v.numel() * v.element_size() for v in zh[0] + dxh[0])
+        s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        in_ready = [torch.cuda.Event() for _ in range(nset)]
+        done = [torch.cuda.Event() for _ in range(nset)]
+        out_done = [torch.cuda.Event() for _ in range(nset)]
+
+        def upload(k):
+            with torch.cuda.stream(s_in):
+                s_in.wait_event(done[k])  # the set's previous step has consumed its inputs
+                for d_, h_ in zip(xin[k] + dzin[k], xh + dzh):
+                    d_.copy_(h_, non_blocking=True)
+                in_ready[k].record(s_in)
+
+        def run_e2e(n):
+            for k in range(nset):
+                done[k].record(stream)
+                out_done[k].record(stream)
+            upload(0)
+            for i in range(n):
+                k = i % nset
+                if i + 1 < n:
+                    upload((i + 1) % nset)
+                stream.wait_event(in_ready[k])
+                stream.wait_event(out_done[k])  # the set's previous results have been downloaded
+                xk = xin[k] if cfg.sp else xin[k][0]
+                dzk = dzin[k] if cfg.sp else dzin[k][0]
+                f_, b_ = fws[k], bws[k]
+                tpmlp.attn_forward(xk, Wqkv, Wo, f_["qkv"], f_["o"], f_["lse"], f_["z"], **kw)
+                tpmlp.attn_backward(xk, Wqkv, Wo, f_["qkv"], f_["o"], f_["lse"], dzk, b_["dx"], b_["dwqkv"],
+                                    b_["dwo"], b_["dqkv"], b_["dout"], **kw)
+                done[k].record(stream)
+                with torch.cuda.stream(s_out):
+                    s_out.wait_event(done[k])
+                    for h_, d_ in zip(zh[k] + dxh[k], as_list(f_["z"]) + as_list(b_["dx"])):
+                        h_.copy_(d_, non_blocking=True)
+                    out_done[k].record(s_out)
+            stream.wait_stream(s_out)
+
+        run_e2e(max(3, args.warmup))
+        n_e2e = max(4, args.steps // 2)
+        e0.record(stream)
+        run_e2e(n_e2e)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        if tpmlp.device_status() != 0:
+            raise RuntimeError(f"device status {tpmlp.device_status()}: {tpmlp.last_error()}")
+        ms_e2e = e0.elapsed_time(e1) / n_e2e
+        e2e = {"value": flops / (ms_e2e / 1e3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e,
+               "note": "pinned-host chunks in, results out every step; copies double-buffered on two "
+                       "copy streams against the compute stream"}
+
+    # ------------------------------------------------ CPU oracle baseline
+    cpu = None
+    if not args.no_cpu_baseline:
+        cpu = attn_oracle_baseline(cfg, t, args.cpu_seconds)
+
     line = {
         "metric": "TP/SP attention block fwd+bwd TFLOP/s on 1 GB300 and % of dense BF16 peak",
         "value": flops / (ms / 1e3) / 1e12,
@@ -748,11 +824,48 @@ def run_attention(args) -> int:
                      "peak_source": f"{peak_src} bf16_tflops_sustained", "traffic": None, "per_kernel": per_kernel},
         "gpu_launches": sum(v["launches"] for v in prof.values()),
         "clocks": clock_info,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
         "device": {"name": torch.cuda.get_device_name(dev),
                    "sms": torch.cuda.get_device_properties(dev).multi_processor_count},
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+def attn_oracle_baseline(cfg, inputs, target_s: float):
+    """The fp64 oracle's attention block fwd+bwd (its backward runs the forward
+    too) on the first s' tokens of every sequence with full weights, s' sized so
+    one run takes about target_s and at most 1024 (the oracle holds several
+    [b, heads, s', s'] fp64 matrices); FLOPs counted as on the GPU (24·M'·h² for
+    the projections, 12·b·h per visible query-key pair)."""
+    import oracle as O
+
+    X = inputs["X"].double().numpy()
+    dZ = inputs["dZ"].double().numpy()
+    Wqkv = inputs["Wqkv"].double().numpy()
+    Wo = inputs["Wo"].double().numpy()
+
+    def flops(sp_):
+        pairs = sp_ * (sp_ + 1) / 2 if cfg.causal else float(sp_) * sp_
+        return 24.0 * sp_ * cfg.b * cfg.h * cfg.h + 12.0 * cfg.b * cfg.h * pairs
+
+    def run(sp_):
+        t0 = time.perf_counter()
+        O.attn_backward(X[:sp_].reshape(sp_ * cfg.b, cfg.h), Wqkv, Wo, dZ[:sp_].reshape(sp_ * cfg.b, cfg.h), sp_,
+                        cfg.b, cfg.heads, cfg.causal)
+        return time.perf_counter() - t0
+
+    probe = min(32, cfg.s)
+    t_probe = run(probe)
+    sp_ = probe
+    if t_probe < target_s:
+        sp_ = int(min(cfg.s, 1024, max(probe, probe * target_s / max(t_probe, 1e-3))))
+        sp_ = max(probe, sp_ // 32 * 32)
+    t_run = run(sp_)
+    return {"value": flops(sp_) / t_run / 1e12, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"first {sp_} of {cfg.s} tokens of each of {cfg.b} sequence(s), full weights, fp64 NumPy "
+                      f"attention block fwd+bwd, one run of {t_run:.1f} s"}
 
 
 def main(argv=None) -> int:
