@@ -300,18 +300,6 @@ __device__ __forceinline__ void tmem_wait_ld_tied(uint32_t* r) {
       :
       : "memory");
 }
-// The 128 float32 columns at taddr (one row per thread) into x.
-__device__ __forceinline__ void tmem_ld128(uint32_t taddr, float* x) {
-  uint32_t* r = reinterpret_cast<uint32_t*>(x);
-  tmem_ld32_async(taddr, r);
-  tmem_ld32_async(taddr + 32, r + 32);
-  tmem_ld32_async(taddr + 64, r + 64);
-  tmem_ld32_async(taddr + 96, r + 96);
-  tmem_wait_ld_tied(r);
-  tmem_wait_ld_tied(r + 32);
-  tmem_wait_ld_tied(r + 64);
-  tmem_wait_ld_tied(r + 96);
-}
 
 template <int DT>
 __global__ void __launch_bounds__(ATT_THREADS, 1) attn_fwd_kernel(const __grid_constant__ AttnParams p) {
