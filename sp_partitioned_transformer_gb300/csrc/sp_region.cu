@@ -178,12 +178,13 @@ __device__ __forceinline__ void stage8(uint8_t* row, const void* src, int vi) {
   if constexpr (DT == DT_F32) d[1] = s[1];
 }
 
-// Sum of (a, b) over the CTA; the fixed shuffle/warp order makes it deterministic.
-__device__ __forceinline__ float2 block_sum2(float a, float b, float2* red) {
+// Sum of (a, b) over the CTA; the fixed shuffle/warp order makes it
+// deterministic.  red[] must be free (a __syncthreads since its last read):
+// one barrier.
+__device__ __forceinline__ float2 block_sum2_free(float a, float b, float2* red) {
   a = warp_sum(a);
   b = warp_sum(b);
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  __syncthreads();  // previous use of red[] finished
   if (lane == 0) red[w] = make_float2(a, b);
   __syncthreads();
   const float2 t = lane < STREAM_THREADS / 32 ? red[lane] : make_float2(0.0f, 0.0f);
@@ -278,7 +279,14 @@ __global__ void __launch_bounds__(STREAM_THREADS) ln_fwd_stream_kernel(ChunkSet 
       ring_issue(ring, full, cs, k - 1 + S, h, rpc, sizeof(T));
     }
     const uint8_t* row = ring.base + static_cast<size_t>(s) * ring.rb_al;
-    float sum = 0.0f;
+    // Mean and variance from one block reduction of the shifted sums
+    // Σ(x − c) and Σ(x − c)², c = the row's first element (the shifted-data
+    // method: with c inside the data's range the subtraction
+    // E[(x−c)²] − E[x−c]² does not cancel away the variance the way raw
+    // Σx² − (Σx)²/h does when the mean is large against the spread).  red[] is
+    // free: every thread passed this row's first barrier after reading it.
+    const float c = Storage<DT>::to_f32(reinterpret_cast<const T*>(row)[0]);
+    float s1 = 0.0f, s2 = 0.0f;
 #pragma unroll
     for (int kk = 0; kk < V; ++kk) {
       const int vi = tid + kk * STREAM_THREADS;
@@ -286,22 +294,17 @@ __global__ void __launch_bounds__(STREAM_THREADS) ln_fwd_stream_kernel(ChunkSet 
         float v[8];
         lds8<DT>(row, vi, v);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) sum += v[i];
+        for (int i = 0; i < 8; ++i) {
+          const float d = v[i] - c;
+          s1 += d;
+          s2 = fmaf(d, d, s2);
+        }
       }
     }
-    const float mu = block_sum2(sum, 0.0f, red).x * inv_h;
-    float q = 0.0f;
-#pragma unroll
-    for (int kk = 0; kk < V; ++kk) {
-      const int vi = tid + kk * STREAM_THREADS;
-      if (vi < nv) {
-        float v[8];
-        lds8<DT>(row, vi, v);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) q += (v[i] - mu) * (v[i] - mu);
-      }
-    }
-    const float r = 1.0f / sqrtf(block_sum2(q, 0.0f, red).x * inv_h + eps);
+    const float2 st = block_sum2_free(s1, s2, red);
+    const float dm = st.x * inv_h;
+    const float mu = c + dm;
+    const float r = 1.0f / sqrtf(fmaxf(st.y * inv_h - dm * dm, 0.0f) + eps);
     const int64_t m = blockIdx.x + k * G;
     const int64_t j = m / rpc;
     T* y = static_cast<T*>(cs.out[j]) + (m - j * rpc) * h;
@@ -410,7 +413,7 @@ __global__ void __launch_bounds__(STREAM_THREADS) ln_bwd_stream_kernel(ChunkSet 
         }
       }
     }
-    const float2 tot = block_sum2(sg1, sgx, red);
+    const float2 tot = block_sum2_free(sg1, sgx, red);  // red[] free: the row's first barrier follows its last read
     const float mg = tot.x * inv_h, mgx = tot.y * inv_h;
     const int64_t j = m / rpc;
     T* dx = static_cast<T*>(cs.out[j]) + (m - j * rpc) * h;

@@ -69,6 +69,30 @@ def test_layernorm_forward_and_backward(cuda_lib, dt, s, b, h, tp):
     assert tpmlp.device_status() == 0
 
 
+@pytest.mark.parametrize("s,b,h,tp", [(16, 2, 136, 2), (40, 2, 2056, 4), (48, 1, 6144, 2)])
+def test_layernorm_statistics_with_a_large_mean(cuda_lib, s, b, h, tp):
+    """Rows at 1000 + 0.5·N(0, 1) in float32: the variance is 4·10⁻⁶ of the mean
+    square, so E[x²] − E[x]² in float32 would cancel it away; mean and rstd must
+    still match the fp64 oracle to 1e-5 (warp-per-row and streamed kernels)."""
+    tpmlp = cuda_lib
+    inp = sp_region_inputs(s, b, h, 0.1, seed=7 + h, dtype="f32")
+    R = (inp["R"] * 0.5 + 1000.0).cuda()
+    gamma, beta = inp["gamma"].cuda(), inp["beta"].cuda()
+    x = chunks(R, tp)
+    y = [torch.full_like(c, float("nan")) for c in x]
+    mean = torch.empty(s * b, device="cuda")
+    rstd = torch.empty(s * b, device="cuda")
+    tpmlp.sp_layernorm_forward(x, gamma, beta, EPS, y, mean, rstd, s=s, b=b, h=h, tp=tp)
+    torch.cuda.synchronize()
+    ref = O.layernorm_forward(_flat(R.cpu()), to_np(inp["gamma"]), to_np(inp["beta"]), EPS)
+    assert rel_err(to_np(mean), ref["mean"]) <= 1e-5
+    assert rel_err(to_np(rstd), ref["rstd"]) <= 1e-5
+    # Y carries the float32 rounding of a mean near 1000 (half an ulp, 3·10⁻⁵)
+    # in every x − mean, about 10⁻⁴ of the normalised values
+    assert rel_err(_flat(torch.cat(y)), ref["Y"]) <= 1e-4
+    assert tpmlp.device_status() == 0
+
+
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
 @pytest.mark.parametrize("p", [0.0, 0.1])
 @pytest.mark.parametrize("s,b,h,tp", [(64, 2, 136, 2), (9, 1, 5, 3)])
