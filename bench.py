@@ -119,6 +119,29 @@ def ncu_traffic(config_name: str, mode: str):
     return ent
 
 
+def attn_kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "sp_partitioned_transformer_gb300", "csrc")
+    for f in ("attn.cu", "common.cuh"):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def attn_ncu_traffic(config_name: str):
+    """DRAM bytes of one fwd+bwd pass of the attention core (its four kernels) from
+    the committed ncu summary, if it was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "attn_dram_traffic.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+    except (OSError, ValueError):
+        return None
+    if d.get("kernel_source_sha256_16") != attn_kernel_source_hash():
+        return None
+    return d.get("per_step", {}).get(config_name)
+
+
 class ClockSampler:
     """nvidia-smi samples of SM clock and throttle reasons while the GPU is loaded."""
 
@@ -722,6 +745,7 @@ def run_attention(args) -> int:
                              "share_of_step": v["ms"] / args.steps / ms}
     a = prof["attn_core"]
     achieved = a["work"] / (a["ms"] / 1e3) / 1e12
+    traffic = attn_ncu_traffic(cfg.name)
 
     # ------------------------------------------------ end to end through the C ABI
     # Every step uploads the X and dZ chunks from pinned host memory and
@@ -821,7 +845,11 @@ def run_attention(args) -> int:
         "roofline": {"bound": "tensor", "kernel": "tpmlp::attn core (attn_fwd_kernel, attn_bwd_dkdv_kernel, "
                                                   "attn_bwd_dq_kernel, attn_bwd_delta_kernel)",
                      "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                     "peak_source": f"{peak_src} bf16_tflops_sustained", "traffic": None, "per_kernel": per_kernel},
+                     "peak_source": f"{peak_src} bf16_tflops_sustained",
+                     "traffic": traffic.get("dram_bytes_per_pass") if traffic else None,
+                     "traffic_note": "DRAM bytes of one fwd+bwd pass of the four core kernels (ncu, "
+                                     "profiles/attn_dram_traffic.json, matched to the built source)",
+                     "per_kernel": per_kernel},
         "gpu_launches": sum(v["launches"] for v in prof.values()),
         "clocks": clock_info,
         "e2e": e2e,
