@@ -9,7 +9,7 @@ import pytest
 import torch
 
 import oracle as O
-from gpu_common import TOL, assert_block_close, oracle_block, rel_err, run_block, to_np
+from gpu_common import TOL, assert_block_close, oracle_block, rel_err, run_block
 from synthetic import CONFIGS, block_inputs
 
 pytestmark = pytest.mark.gpu

@@ -5,11 +5,9 @@ Checks: (1) on a zeroed main_grad, one call leaves exactly the accumulator, so
 rounding it to the storage type reproduces tpmlp_backward's dW bit for bit, and
 dX, dU are unchanged; (2) two micro-batches accumulate to the oracle's gradient
 of the concatenated batch; (3) s = 0 leaves main_grad untouched."""
-import numpy as np
 import pytest
 import torch
 
-import oracle as O
 from gpu_common import TOL, chunks, oracle_block, rel_err, to_np
 from synthetic import CONFIGS, BlockConfig, block_inputs
 

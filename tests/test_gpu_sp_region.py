@@ -3,7 +3,6 @@ oracle: LayerNorm forward/backward on the [s/tp, b, h] chunks, dropout +
 residual, and the whole MLP sublayer R → LayerNorm → block → dropout + residual
 (forward and backward) with the LayerNorm's output chunks fed to the block as
 its SP input chunks (fc1 reads them in place)."""
-import numpy as np
 import pytest
 import torch
 
