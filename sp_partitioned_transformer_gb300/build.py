@@ -11,6 +11,7 @@ from __future__ import annotations
 
 import argparse
 import concurrent.futures as cf
+import fcntl
 import os
 import shutil
 import subprocess
@@ -61,12 +62,26 @@ def _up_to_date() -> bool:
 
 
 def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    """Compile (if stale) and return the path of libtpmlp.so."""
+    """Compile (if stale) and return the path of libtpmlp.so.  Concurrent callers
+    (one process per GPU under torchrun, parallel test workers) take an exclusive
+    file lock, so one of them compiles and the others find the library up to
+    date."""
     if not force and not ptxas_info and _up_to_date():
         return LIB_PATH
+    os.makedirs(LIB_DIR, exist_ok=True)
+    with open(os.path.join(LIB_DIR, ".build.lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        try:
+            if not force and not ptxas_info and _up_to_date():
+                return LIB_PATH
+            return _compile(verbose, ptxas_info)
+        finally:
+            fcntl.flock(lock, fcntl.LOCK_UN)
+
+
+def _compile(verbose: bool, ptxas_info: bool) -> str:
     nvcc = _nvcc()
     os.makedirs(BUILD_DIR, exist_ok=True)
-    os.makedirs(LIB_DIR, exist_ok=True)
     extra = ["-Xptxas", "-v"] if ptxas_info else []
 
     def compile_one(src: str) -> tuple[str, str]:
