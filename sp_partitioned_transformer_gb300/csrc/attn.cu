@@ -643,37 +643,46 @@ __global__ void __launch_bounds__(256) attn_bwd_delta_kernel(const void* __restr
 }
 
 // ================================================================== backward: dK, dV
-// Per (128-key tile, head, sequence) over 64-query tiles.  Tensor memory holds
-// Sᵀ and dPᵀ (one buffer: the element-wise warps release it as soon as they have
-// loaded it, so Sᵀ/dPᵀ of the next query tile are computed while they work),
-// the 16-bit Pᵀ and dSᵀ (two buffers), which are the A operands of dV += Pᵀ·dO
-// and dK += dSᵀ·Q straight from tensor memory, and the dV and dK accumulators.
-// Shared memory holds K, V, a 3-deep ring of (Q, dO, −lse2, Δ) and three dSᵀ
-// buffers for the bulk stores to HBM.  Keeping P and dS out of shared memory
-// matters: the kernel is bound by shared-memory bandwidth (operand reads of the
-// MMAs, TMA writes, the dSᵀ stores), not by the tensor pipe.
-constexpr int KV_BK = 128, KV_BQ = 64, KV_ST = 3, KV_DSB = 3;
+// Per (128-key tile, head, sequence) over 64-query tiles.  K and V never change
+// within a CTA, so after TMA lands them the element-wise warps copy them into
+// tensor memory (16-bit, two per column), where they are the A operands of
+// Sᵀ = K·Qᵀ and dPᵀ = V·dOᵀ: those MMAs (N = 64) then read only Q or dO from
+// shared memory — with both operands there they are capped by shared-memory
+// reads.  Tensor memory: Sᵀ and dPᵀ (one buffer, released by the element-wise
+// warps as soon as they have loaded it, so the next tile's are computed while
+// they work), K and V, the dV and dK accumulators.  Pᵀ and dSᵀ go to shared
+// memory, in the 64 KB K and V arrived in (one Pᵀ buffer, three dSᵀ buffers):
+// they are the A operands of dV += Pᵀ·dO and dK += dSᵀ·Q, and each dSᵀ tile is
+// also bulk-stored to HBM for the dQ kernel.
+constexpr int KV_BK = 128, KV_BQ = 64, KV_ST = 4, KV_DSB = 3;
 constexpr uint32_t KV_TILE = 128 * 128 * 2;    // K or V tile, 32 KB
 constexpr uint32_t KV_QTILE = 64 * 128 * 2;    // Q or dO tile of 64 rows, 16 KB
 constexpr uint32_t KV_STAGE = 2 * KV_QTILE + 512;  // Q, dO, −lse2[64], Δ[64]
 constexpr uint32_t KV_STRIDE = (KV_STAGE + 1023) & ~1023u;
-constexpr uint32_t KV_K = 0, KV_V = KV_TILE, KV_S0 = 2 * KV_TILE;
-constexpr uint32_t KV_DST = KV_S0 + KV_ST * KV_STRIDE;  // KV_DSB dSᵀ buffers for the HBM stores
-constexpr uint32_t KV_END = KV_DST + KV_DSB * DS_TILE;
+// K and V land at KV_K, KV_V; once they are in tensor memory the same 64 KB holds
+// Pᵀ (KV_PT) and the dSᵀ buffers (KV_DST + b·DS_TILE)
+constexpr uint32_t KV_K = 0, KV_V = KV_TILE, KV_PT = 0, KV_DST = DS_TILE, KV_S0 = 2 * KV_TILE;
+static_assert(KV_DST + KV_DSB * DS_TILE <= 2 * KV_TILE, "Pᵀ and dSᵀ buffers fit where K and V landed");
+constexpr uint32_t KV_END = KV_S0 + KV_ST * KV_STRIDE;
 constexpr size_t KV_SMEM = 1024 + KV_END + sizeof(Tail);
 // TMEM columns
-constexpr uint32_t KT_S = 0, KT_DP = 64, KT_P = 128, KT_DV = 256, KT_DK = 384;  // P/dS buffer b at KT_P + 64b
-enum { KB_KV = 0, KB_F = 1, KB_E = KB_F + KV_ST, KB_SF = KB_E + KV_ST, KB_SC = KB_SF + 1, KB_P = KB_SC + 1,
-       KB_MM = KB_P + 2, KB_DRAIN = KB_MM + 2, KB_COUNT = KB_DRAIN + 1 };
-static_assert(KB_COUNT <= 24, "barrier slots");
+constexpr uint32_t KT_S = 0, KT_DP = 64, KT_K = 128, KT_V = 192, KT_DV = 256, KT_DK = 384;
+enum { KB_KV = 0, KB_KVT = 1, KB_F = 2, KB_E = KB_F + KV_ST, KB_SF = KB_E + KV_ST, KB_SC = KB_SF + 1, KB_P = KB_SC + 1,
+       KB_MM = KB_P + 1, KB_DRAIN = KB_MM + 1, KB_COUNT = KB_DRAIN + 1 };
+static_assert(KB_COUNT <= 32, "barrier slots");
 
-// 16 32-bit columns of this warp's lane quarter from registers.
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* v) {
+// D (+)= Σ_ks A_ks·B_ks over 4 K steps, A and B shared-memory descriptors.
+__device__ __forceinline__ void mma4_ss(uint32_t d, const uint64_t* a, const uint64_t* b, uint32_t idesc,
+                                        uint32_t acc0) {
   asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
-      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
-      "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.b32 p, %10, 0;\n\t"
+      "setp.eq.b32 q, %10, %10;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %5, %9, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %2, %6, %9, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %7, %9, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %8, %9, q;\n\t}" ::"r"(d),
+      "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "r"(idesc), "r"(acc0)
       : "memory");
 }
 
@@ -704,16 +713,15 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dkdv_kernel(const __g
 
   if (threadIdx.x == 0) {
     mbar_init(bar(KB_KV), 1);
+    mbar_init(bar(KB_KVT), COMPUTE_THREADS);
     for (int i = 0; i < KV_ST; ++i) {
       mbar_init(bar(KB_F + i), 1);
       mbar_init(bar(KB_E + i), 1);
     }
     mbar_init(bar(KB_SF), 1);
     mbar_init(bar(KB_SC), COMPUTE_THREADS);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(KB_P + i), COMPUTE_THREADS);
-      mbar_init(bar(KB_MM + i), 1);
-    }
+    mbar_init(bar(KB_P), COMPUTE_THREADS);
+    mbar_init(bar(KB_MM), 1);
     mbar_init(bar(KB_DRAIN), 1);
     tail->abort_flag = 0;
     fence_barrier_init();
@@ -726,7 +734,8 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dkdv_kernel(const __g
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tail->tmem_slot;
-  const uint32_t sK = smem_u32(smem + KV_K), sV = smem_u32(smem + KV_V), sDST = smem_u32(smem + KV_DST);
+  const uint32_t sK = smem_u32(smem + KV_K), sV = smem_u32(smem + KV_V);
+  const uint32_t sPT = smem_u32(smem + KV_PT), sDST = smem_u32(smem + KV_DST);
   auto stage_base = [&](int st) { return smem + KV_S0 + st * KV_STRIDE; };
 
   if (warp == 0) {
@@ -764,48 +773,54 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dkdv_kernel(const __g
     if (lane == 0) {
       constexpr uint32_t idesc_s = make_idesc_f16(DT == DT_BF16, false, false, 128, KV_BQ);
       constexpr uint32_t idesc_acc = make_idesc_f16(DT == DT_BF16, false, true, 128, HD);
-      bool ok = mbar_wait_bounded(bar(KB_KV), 0u, abort_flag, p.status, p.timeout_ns);
-      const uint64_t dKs = sdesc_k(sK), dVs = sdesc_k(sV);
-      // Sᵀ = K·Qᵀ and dPᵀ = V·dOᵀ of query tile n
+      // K and V are in tensor memory
+      bool ok = mbar_wait_bounded(bar(KB_KVT), 0u, abort_flag, p.status, p.timeout_ns);
+      // Sᵀ = K·Qᵀ and dPᵀ = V·dOᵀ of query tile n, K and V from tensor memory
       auto issue_sdp = [&](int n) -> bool {
         const int st = n % KV_ST;
         if (!mbar_wait_bounded(bar(KB_F + st), (n / KV_ST) & 1u, abort_flag, p.status, p.timeout_ns)) return false;
         tc_fence_after();
         const uint32_t sQ = smem_u32(stage_base(st)), sDO = sQ + KV_QTILE;
-        uint64_t a[8], b[8];
-        kdescs(dKs, 128, a);
+        uint64_t b[8];
         kdescs(sdesc_k(sQ), 64, b);
-        mma8_ss(tmem + KT_S, a, b, idesc_s, 0u);
-        kdescs(dVs, 128, a);
+        mma_ts<8>(tmem + KT_S, tmem + KT_K, b, idesc_s, 0u);
         kdescs(sdesc_k(sDO), 64, b);
-        mma8_ss(tmem + KT_DP, a, b, idesc_s, 0u);
+        mma_ts<8>(tmem + KT_DP, tmem + KT_V, b, idesc_s, 0u);
         tc_commit(bar(KB_SF));
         return true;
       };
       if (ok) tc_fence_after();
       if (ok) ok = issue_sdp(0);
+      const uint64_t dPT = sdesc_k(sPT);
       for (int n = 0; ok && n < N; ++n) {
-        const int st = n % KV_ST, b = n & 1;
+        const int st = n % KV_ST;
         if (n + 1 < N) {
           // the element-wise warps have loaded Sᵀ/dPᵀ of tile n: compute tile n+1's
           if (!(ok = mbar_wait_bounded(bar(KB_SC), n & 1, abort_flag, p.status, p.timeout_ns))) break;
           tc_fence_after();
           if (!(ok = issue_sdp(n + 1))) break;
         }
-        if (!(ok = mbar_wait_bounded(bar(KB_P + b), (n >> 1) & 1u, abort_flag, p.status, p.timeout_ns))) break;
+        if (!(ok = mbar_wait_bounded(bar(KB_P), n & 1, abort_flag, p.status, p.timeout_ns))) break;
         tc_fence_after();
         const uint32_t sQ = smem_u32(stage_base(st)), sDO = sQ + KV_QTILE;
-        bulk_store(ds_out + static_cast<int64_t>(n) * DS_TILE, sDST + (n % KV_DSB) * DS_TILE, DS_TILE);
-        const uint32_t tP = tmem + KT_P + b * 64;  // Pᵀ at +0, dSᵀ at +32 (16-bit, two per column)
-        uint64_t bd[8];
+        const uint32_t sDSn = sDST + (n % KV_DSB) * DS_TILE;
+        bulk_store(ds_out + static_cast<int64_t>(n) * DS_TILE, sDSn, DS_TILE);  // dSᵀ for the dQ kernel
+        // dV += Pᵀ·dO and dK += dSᵀ·Q: A a [128 keys × 64 queries] K-major half,
+        // K step ks 32 bytes along it; B MN-major from the stage
+        uint64_t a[4], bd[8];
+        const uint64_t dDS = sdesc_k(sDSn);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) a[ks] = dPT + 2u * ks;
         mndescs(sdesc_mn(sDO, KV_BQ), 4, bd);
-        mma_ts<4>(tmem + KT_DV, tP, bd, idesc_acc, n > 0 ? 1u : 0u);
+        mma4_ss(tmem + KT_DV, a, bd, idesc_acc, n > 0 ? 1u : 0u);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) a[ks] = dDS + 2u * ks;
         mndescs(sdesc_mn(sQ, KV_BQ), 4, bd);
-        mma_ts<4>(tmem + KT_DK, tP + 32, bd, idesc_acc, n > 0 ? 1u : 0u);
-        // the element-wise warps rewrite dSᵀ buffer (n+2)%3 once MM of this step
-        // completes; the store of step n−1 (that buffer) must have read it
+        mma4_ss(tmem + KT_DK, a, bd, idesc_acc, n > 0 ? 1u : 0u);
+        // the element-wise warps rewrite Pᵀ and dSᵀ buffer (n+1)%3 once MM of
+        // this step completes; the store of step n−2 (that buffer) must have read it
         bulk_wait_read<1>();
-        tc_commit(bar(KB_MM + b));
+        tc_commit(bar(KB_MM));
         tc_commit(bar(KB_E + st));
       }
       if (!ok) {
@@ -824,9 +839,36 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dkdv_kernel(const __g
     const int key = k0 + r;
     const uint32_t tl = tmem + (static_cast<uint32_t>(qw * 32) << 16);
     const float c = p.scale_log2;
-    bool ok = true;
-    for (int n = 0; n < N; ++n) {
-      const int st = n % KV_ST, b = n & 1;
+    // K (group 0) or V (group 1) row r from the swizzled tile into tensor memory,
+    // two 16-bit elements per column
+    bool ok = mbar_wait_bounded(bar(KB_KV), 0u, abort_flag, p.status, p.timeout_ns);
+    if (__all_sync(0xffffffffu, ok)) {
+      const uint8_t* tile = smem + (g ? KV_V : KV_K);
+      uint32_t w[64];
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) {
+          const uint4 v = *reinterpret_cast<const uint4*>(tile + hf * (128 * HALF_ROW_BYTES) + r * HALF_ROW_BYTES +
+                                                          ((cc ^ (r & 7)) << 4));
+          w[32 * hf + 4 * cc] = v.x;
+          w[32 * hf + 4 * cc + 1] = v.y;
+          w[32 * hf + 4 * cc + 2] = v.z;
+          w[32 * hf + 4 * cc + 3] = v.w;
+        }
+      const uint32_t tkv = tl + (g ? KT_V : KT_K);
+      tmem_st32(tkv, reinterpret_cast<const float*>(w));
+      tmem_st32(tkv + 32, reinterpret_cast<const float*>(w + 32));
+      tmem_st_wait();
+    } else {
+      ok = false;
+    }
+    // every compute thread has read K and V before their bytes are reused for Pᵀ/dSᵀ
+    asm volatile("bar.sync 1, %0;" ::"n"(COMPUTE_THREADS) : "memory");
+    tc_fence_before();
+    mbar_arrive(bar(KB_KVT));
+    for (int n = 0; ok && n < N; ++n) {
+      const int st = n % KV_ST;
       ok = mbar_wait_bounded(bar(KB_SF), n & 1, abort_flag, p.status, p.timeout_ns);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
@@ -869,35 +911,23 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dkdv_kernel(const __g
         sv[j] = pr.x;
         sv[j + 1] = pr.y;
       }
-      uint32_t pk[16], dk16[16];
+      if (n > 0) {
+        // dV/dK of tile n−1 (the last reader of Pᵀ) have run, and with them the
+        // wait for the store of tile n−3 (the last reader of this dSᵀ buffer)
+        ok = mbar_wait_bounded(bar(KB_MM), (n - 1) & 1, abort_flag, p.status, p.timeout_ns);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      }
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
-        const uint4 a = pack8<DT>(sv + cc * 8), d = pack8<DT>(dp + cc * 8);
-        pk[4 * cc] = a.x; pk[4 * cc + 1] = a.y; pk[4 * cc + 2] = a.z; pk[4 * cc + 3] = a.w;
-        dk16[4 * cc] = d.x; dk16[4 * cc + 1] = d.y; dk16[4 * cc + 2] = d.z; dk16[4 * cc + 3] = d.w;
+        st_swizzled(smem + KV_PT, r, g * 4 + cc, pack8<DT>(sv + cc * 8));
+        st_swizzled(smem + KV_DST + (n % KV_DSB) * DS_TILE, r, g * 4 + cc, pack8<DT>(dp + cc * 8));
       }
-      if (n >= 2) {
-        // dV/dK of tile n−2 (the last reader of this P/dS buffer) have run, and
-        // the bulk store of tile n−3 (the last reader of this dSᵀ buffer) has
-        // read it (MM is committed after that store's read)
-        ok = mbar_wait_bounded(bar(KB_MM + b), ((n - 2) >> 1) & 1u, abort_flag, p.status, p.timeout_ns);
-        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-        tc_fence_after();
-      }
-      const uint32_t tP = tl + KT_P + b * 64;
-      tmem_st16(tP + g * 16, pk);
-      tmem_st16(tP + 32 + g * 16, dk16);
-      uint8_t* dsb = smem + KV_DST + (n % KV_DSB) * DS_TILE;
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc)
-        st_swizzled(dsb, r, g * 4 + cc, make_uint4(dk16[4 * cc], dk16[4 * cc + 1], dk16[4 * cc + 2], dk16[4 * cc + 3]));
-      tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(bar(KB_P + b));
+      mbar_arrive(bar(KB_P));
     }
     if (ok) {
-      ok = mbar_wait_bounded(bar(KB_MM + ((N - 1) & 1)), ((N - 1) >> 1) & 1u, abort_flag, p.status, p.timeout_ns);
+      ok = mbar_wait_bounded(bar(KB_MM), (N - 1) & 1, abort_flag, p.status, p.timeout_ns);
       ok = __all_sync(0xffffffffu, ok);
     }
     if (ok) {
