@@ -27,6 +27,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cstdlib>
 #include <mutex>
 
 #include "internal.h"
@@ -78,17 +79,20 @@ struct Params {
   EpiParams epi;
 };
 
-__device__ __forceinline__ void decode_tile(int t, const Params& p, int& part, int& mb, int& nb) {
-  const int per_part = p.mt * p.nt;
+__device__ __forceinline__ void decode_tile_nt(int t, const Params& p, int nt, int& part, int& mb, int& nb) {
+  const int per_part = p.mt * nt;
   part = t / per_part;
   const int r = t - part * per_part;
-  const int span = GROUP_M * p.nt;
+  const int span = GROUP_M * nt;
   const int g = r / span;
   const int first_m = g * GROUP_M;
   const int gsz = min(p.mt - first_m, GROUP_M);
   const int rr = r - g * span;
   mb = first_m + rr % gsz;
   nb = rr / gsz;
+}
+__device__ __forceinline__ void decode_tile(int t, const Params& p, int& part, int& mb, int& nb) {
+  decode_tile_nt(t, p, p.nt, part, mb, nb);
 }
 
 // ---------------------------------------------------------------- epilogues
@@ -522,6 +526,18 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
 // and "accumulator full" barriers.  Each CTA's tensor memory holds its 128 rows
 // of both 256-column accumulators; both epilogues release an accumulator by
 // arriving on the even CTA's "accumulator empty" barrier.
+// TMA load whose box lands at the same offset in every CTA of `mask` (a
+// multicast within the cluster), each destination CTA's bytes completing on its
+// pair's even-CTA barrier at bar_cluster's offset.
+__device__ __forceinline__ void tma_load_2d_pair_mc(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster,
+                                                    int32_t c0, int32_t c1, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1), "h"(mask)
+      : "memory");
+}
+
 constexpr int PAIR_STAGES = 6;
 constexpr int HALF_M = BM;      // rows of A per CTA
 constexpr int PA_BYTES = HALF_M * BK * 2;  // 16 KB
@@ -531,7 +547,11 @@ constexpr int PAIR_NUM_BARS = 2 * PAIR_STAGES + 5;
 constexpr size_t PAIR_SMEM_BYTES = 1024 + static_cast<size_t>(PAIR_STAGES) * PSTAGE_BYTES + 256;
 
 // TN: N extent of the pair's tile; each CTA holds TN/2 rows of B.
-template <int DT, bool A_MN, bool B_MN, int TN>
+// MC: a cluster of two pairs on the tiles (mb, 2j) and (mb, 2j+1), which share
+// their A panel: each CTA loads 64 of its 128 A rows per stage and multicasts
+// them to its counterpart in the other pair, halving the A reads from L2; a
+// stage is refilled once both pairs' MMAs have released it.
+template <int DT, bool A_MN, bool B_MN, int TN, bool MC>
 __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_constant__ Params p) {
   constexpr int HALF_N = TN / 2;
   // bytes of one stage (both CTAs): A halves + B halves; an MN-major B half is
@@ -553,13 +573,25 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t rank = cluster_ctarank();  // 0: issues the pair's MMAs
+  const uint32_t crank = cluster_ctarank();
+  const uint32_t rank = crank & 1u;              // within the pair; 0 issues the pair's MMAs
+  const uint32_t pr = MC ? (crank >> 1) : 0u;    // the pair within the cluster
+  const uint32_t lead = 2u * pr;                 // cluster rank of this pair's even CTA
   const bool leader = rank == 0;
+  const uint16_t pair_mask = static_cast<uint16_t>(0x3u << lead);
+  auto decode = [&](int t, int& part, int& mb, int& nb) {
+    if constexpr (MC) {
+      decode_tile_nt(t, p, p.nt >> 1, part, mb, nb);
+      nb = 2 * nb + static_cast<int>(pr);
+    } else {
+      decode_tile(t, p, part, mb, nb);
+    }
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < PAIR_STAGES; ++s) {
       mbar_init(full0 + 8u * s, 1);
-      mbar_init(empty0 + 8u * s, 1);
+      mbar_init(empty0 + 8u * s, MC ? 2 : 1);  // with MC both pairs' MMAs release a stage
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull0 + 8u * a, 1);
@@ -578,9 +610,9 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  const int cluster_id = static_cast<int>(blockIdx.x >> 1);
-  const int nclusters = static_cast<int>(gridDim.x >> 1);
-  const int num_tiles = p.mt * p.nt * p.nparts;
+  const int cluster_id = static_cast<int>(blockIdx.x >> (MC ? 2 : 1));
+  const int nclusters = static_cast<int>(gridDim.x >> (MC ? 2 : 1));
+  const int num_tiles = p.mt * (MC ? (p.nt >> 1) : p.nt) * p.nparts;  // MC: tile pairs
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer (both CTAs)
@@ -595,7 +627,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
       bool ok = true;
       for (int t = cluster_id; ok && t < num_tiles; t += nclusters) {
         int part, mb, nb;
-        decode_tile(t, p, part, mb, nb);
+        decode(t, part, mb, nb);
         const int m_off = mb * (2 * HALF_M) + static_cast<int>(rank) * HALF_M;
         int n_row;  // first B row (K-major) / column (MN-major) this CTA loads
         if (p.swiglu_up_row > 0)
@@ -613,12 +645,29 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
               break;
             }
             const uint32_t fb_local = full0 + 8u * stage;
-            const uint32_t fb = mapa_shared(fb_local, 0);  // the even CTA's barrier
+            const uint32_t fb = mapa_shared(fb_local, lead);  // the pair's even-CTA barrier
             if (leader) mbar_arrive_expect_tx(fb_local, 2 * CTA_STAGE_TX);
             const uint32_t sa = smem_u32(smem_a + stage * PA_BYTES);
             const uint32_t sb = smem_u32(smem_b + stage * PB_BYTES);
             const int k0 = kb * BK;
-            if constexpr (!A_MN) {
+            if constexpr (MC) {
+              // this CTA's share of its A rows: 64-row slice pr, sent to itself and
+              // to the same-rank CTA of the other pair (same offset in both)
+              const uint16_t mc_mask = static_cast<uint16_t>((1u << rank) | (1u << (2u + rank)));
+              const int m_sl = m_off + 64 * static_cast<int>(pr);
+              if constexpr (!A_MN) {
+                const uint32_t dst = sa + pr * (64u * 128u);
+                if (p.a_chunk_rows > 0) {
+                  // the slice lies in the 128-row block's chunk; past M: zero fill
+                  const int j = min(m_off / p.a_chunk_rows, p.a_nchunks - 1);
+                  tma_load_2d_pair_mc(dst, ma + j, fb, k0, m_sl - j * p.a_chunk_rows, mc_mask);
+                } else {
+                  tma_load_2d_pair_mc(dst, ma, fb, k0, m_sl, mc_mask);
+                }
+              } else {
+                tma_load_2d_pair_mc(sa + pr * MN_BOX_BYTES, ma, fb, m_sl, k0, mc_mask);
+              }
+            } else if constexpr (!A_MN) {
               if (p.a_chunk_rows > 0) {
                 // rows past M (last tile) read the last chunk out of range: zero fill
                 const int j = min(m_off / p.a_chunk_rows, p.a_nchunks - 1);
@@ -669,7 +718,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
       bool ok = true;
       for (int t = cluster_id; ok && t < num_tiles; t += nclusters, ++it) {
         int part, mb, nb;
-        decode_tile(t, p, part, mb, nb);
+        decode(t, part, mb, nb);
         const int acc = it & 1;
         const uint32_t acc_phase = static_cast<uint32_t>(it >> 1) & 1u;
         if (!mbar_wait_bounded(tempty0 + 8u * acc, acc_phase ^ 1u, abort_flag, p.status, p.timeout_ns)) {
@@ -698,7 +747,9 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
               tc_mma_f16_pair(d_tmem, ad, bd, idesc, accumulate);
               accumulate = 1u;
             }
-            tc_commit_pair_mc(empty0 + 8u * stage, 0x3);  // frees the stage in both CTAs
+            // frees the stage in both CTAs (with MC: in all four, each stage
+            // counting both pairs' releases)
+            tc_commit_pair_mc(empty0 + 8u * stage, MC ? static_cast<uint16_t>(0xF) : pair_mask);
             if (++stage == PAIR_STAGES) {
               stage = 0;
               phase ^= 1u;
@@ -706,10 +757,10 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
           }
         }
         if (!ok) break;
-        tc_commit_pair_mc(tfull0 + 8u * acc, 0x3);  // both CTAs' accumulator halves ready
+        tc_commit_pair_mc(tfull0 + 8u * acc, pair_mask);  // both CTAs' accumulator halves ready
       }
       if (!ok) {
-        tc_commit_pair_mc(drain_bar, 0x1);
+        tc_commit_pair_mc(drain_bar, static_cast<uint16_t>(1u << lead));
         (void)mbar_wait_bounded(drain_bar, 0u, nullptr, nullptr, p.timeout_ns);
       }
     }
@@ -717,11 +768,11 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
   } else if (warp >= 4) {
     // ------------------------------------------------------------ epilogue (both CTAs)
     const int q = warp & 3;
-    const uint32_t tempty_leader = mapa_shared(tempty0, 0);
+    const uint32_t tempty_leader = mapa_shared(tempty0, lead);
     int it = 0;
     for (int t = cluster_id; t < num_tiles; t += nclusters, ++it) {
       int part, mb, nb;
-      decode_tile(t, p, part, mb, nb);
+      decode(t, part, mb, nb);
       const int acc = it & 1;
       const uint32_t acc_phase = static_cast<uint32_t>(it >> 1) & 1u;
       const int64_t m = static_cast<int64_t>(mb) * (2 * HALF_M) + static_cast<int64_t>(rank) * HALF_M + q * 32 + lane;
@@ -781,62 +832,68 @@ static int make_map(CUtensorMap* m, int dtype, const void* base, int64_t inner, 
   return TPMLP_OK;
 }
 
+// mode 0: one CTA per tile; 1: CTA pairs (clusters of 2); 2: two pairs per
+// cluster sharing A by multicast (clusters of 4; tiles counted in pairs).
 template <int DT, bool A_MN, bool B_MN, int TN>
-static int launch_one(const Params& p, int64_t tiles, bool pair, cudaStream_t st, const DeviceInfo& dev) {
+static int launch_one(const Params& p, int64_t tiles, int mode, cudaStream_t st, const DeviceInfo& dev) {
   static std::mutex mu;
-  static bool attr_set[64][2] = {};
-  static int max_clusters[64] = {};
+  static bool attr_set[64][3] = {};
+  static int max_clusters[64][3] = {};
   auto* k1 = gemm_kernel<DT, A_MN, B_MN>;
-  auto* k2 = gemm_pair_kernel<DT, A_MN, B_MN, TN>;
+  auto* k2 = gemm_pair_kernel<DT, A_MN, B_MN, TN, false>;
+  auto* k4 = gemm_pair_kernel<DT, A_MN, B_MN, TN, true>;
+  auto* kp = mode == 2 ? k4 : k2;
+  const unsigned csize = mode == 2 ? 4u : 2u;
   int clusters = 0;
   {
     std::lock_guard<std::mutex> lk(mu);
     const int d = (dev.device >= 0 && dev.device < 64) ? dev.device : 0;
-    if (!attr_set[d][pair]) {
+    if (!attr_set[d][mode]) {
       const cudaError_t e =
-          pair ? cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(PAIR_SMEM_BYTES))
+          mode ? cudaFuncSetAttribute(kp, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(PAIR_SMEM_BYTES))
                : cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(SMEM_BYTES));
       if (e != cudaSuccess) return set_error(TPMLP_ERR_CUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
-      if (pair) {
+      if (mode) {
         cudaLaunchConfig_t cfg = {};
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.x = csize;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
-        cfg.gridDim = dim3(2 * static_cast<unsigned>(std::max(1, dev.num_sms / 2)));
+        cfg.gridDim = dim3(csize * static_cast<unsigned>(std::max(1, dev.num_sms / static_cast<int>(csize))));
         cfg.blockDim = dim3(THREADS);
         cfg.dynamicSmemBytes = PAIR_SMEM_BYTES;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int n = 0;
-        const cudaError_t e2 = cudaOccupancyMaxActiveClusters(&n, k2, &cfg);
+        const cudaError_t e2 = cudaOccupancyMaxActiveClusters(&n, kp, &cfg);
         if (e2 != cudaSuccess || n <= 0)
           return set_error(TPMLP_ERR_CUDA, std::string("cudaOccupancyMaxActiveClusters: ") + cudaGetErrorString(e2));
-        max_clusters[d] = n;
+        max_clusters[d][mode] = n;
       }
-      attr_set[d][pair] = true;
+      attr_set[d][mode] = true;
     }
-    clusters = max_clusters[d];
+    clusters = max_clusters[d][mode];
   }
-  if (!pair) {
+  if (mode == 0) {
     const int grid = static_cast<int>(std::min<int64_t>(tiles, dev.num_sms));
     k1<<<grid, THREADS, SMEM_BYTES, st>>>(p);
   } else {
-    const int nclusters = static_cast<int>(std::min<int64_t>(tiles, clusters));
+    const int64_t units = mode == 2 ? tiles / 2 : tiles;  // work items of one cluster
+    const int nclusters = static_cast<int>(std::min<int64_t>(units, clusters));
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.x = csize;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    cfg.gridDim = dim3(2 * static_cast<unsigned>(nclusters));
+    cfg.gridDim = dim3(csize * static_cast<unsigned>(nclusters));
     cfg.blockDim = dim3(THREADS);
     cfg.dynamicSmemBytes = PAIR_SMEM_BYTES;
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, k2, p);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kp, p);
     if (e != cudaSuccess) return set_error(TPMLP_ERR_CUDA, std::string("2-SM GEMM launch: ") + cudaGetErrorString(e));
   }
   const cudaError_t e = cudaGetLastError();
@@ -845,19 +902,29 @@ static int launch_one(const Params& p, int64_t tiles, bool pair, cudaStream_t st
 }
 
 template <int DT, int TN>
-static int dispatch_tn(const Params& p, int64_t tiles, bool pair, cudaStream_t st, const DeviceInfo& dev, bool a_mn,
+static int dispatch_tn(const Params& p, int64_t tiles, int mode, cudaStream_t st, const DeviceInfo& dev, bool a_mn,
                        bool b_mn) {
-  if (!a_mn && !b_mn) return launch_one<DT, false, false, TN>(p, tiles, pair, st, dev);
-  if (!a_mn && b_mn) return launch_one<DT, false, true, TN>(p, tiles, pair, st, dev);
-  if (a_mn && b_mn) return launch_one<DT, true, true, TN>(p, tiles, pair, st, dev);
+  if (!a_mn && !b_mn) return launch_one<DT, false, false, TN>(p, tiles, mode, st, dev);
+  if (!a_mn && b_mn) return launch_one<DT, false, true, TN>(p, tiles, mode, st, dev);
+  if (a_mn && b_mn) return launch_one<DT, true, true, TN>(p, tiles, mode, st, dev);
   return set_error(TPMLP_ERR_UNSUPPORTED, "MN-major A with K-major B is not instantiated");
 }
 
 template <int DT>
-static int dispatch(const Params& p, int64_t tiles, bool pair, int tn, cudaStream_t st, const DeviceInfo& dev,
+static int dispatch(const Params& p, int64_t tiles, int mode, int tn, cudaStream_t st, const DeviceInfo& dev,
                     bool a_mn, bool b_mn) {
   (void)tn;
-  return dispatch_tn<DT, BN>(p, tiles, pair, st, dev, a_mn, b_mn);
+  return dispatch_tn<DT, BN>(p, tiles, mode, st, dev, a_mn, b_mn);
+}
+
+// Two CTA pairs per cluster sharing A by multicast: on unless
+// TPMLP_GEMM_MULTICAST=0.
+static bool multicast_enabled() {
+  static const bool on = [] {
+    const char* v = std::getenv("TPMLP_GEMM_MULTICAST");
+    return !(v != nullptr && v[0] == '0');
+  }();
+  return on;
 }
 
 }  // namespace tc
@@ -888,6 +955,10 @@ int launch_gemm_tc(const GemmDesc& g, cudaStream_t st) {
   p.mt = static_cast<int32_t>((g.M + (pair ? 2 * BM : BM) - 1) / (pair ? 2 * BM : BM));
   const int tile_n = swiglu ? tn / 2 : tn;
   p.nt = static_cast<int32_t>((g.N + tile_n - 1) / tile_n);
+  // two pairs per cluster on neighbouring N tiles of one M block (A shared)
+  const bool mc = pair && !swiglu && p.nt % 2 == 0 && multicast_enabled();
+  const int mode = pair ? (mc ? 2 : 1) : 0;
+  const uint32_t a_box_rows = mc ? 64u : static_cast<uint32_t>(BM);  // K-major A: each CTA loads half its rows
   p.swiglu_up_row = static_cast<int32_t>(g.swiglu_up_row);
   p.a_chunk_rows = chunked ? static_cast<int32_t>(g.a_chunk_rows) : 0;
   p.a_nchunks = chunked ? static_cast<int32_t>(g.a_chunks.size()) : 0;
@@ -925,11 +996,11 @@ int launch_gemm_tc(const GemmDesc& g, cudaStream_t st) {
         d.map_a = nmaps;
         if (chunked) {
           for (int j = 0; j < chunks; ++j) {
-            rc = make_map(&p.maps[nmaps++], g.dtype, g.a_chunks[j], s.k, g.a_chunk_rows, g.lda, BK, BM);
+            rc = make_map(&p.maps[nmaps++], g.dtype, g.a_chunks[j], s.k, g.a_chunk_rows, g.lda, BK, a_box_rows);
             if (rc != TPMLP_OK) return rc;
           }
         } else if (!g.a_mn) {
-          rc = make_map(&p.maps[nmaps++], g.dtype, s.a, s.k, g.M, g.lda, BK, BM);
+          rc = make_map(&p.maps[nmaps++], g.dtype, s.a, s.k, g.M, g.lda, BK, a_box_rows);
         } else {
           rc = make_map(&p.maps[nmaps++], g.dtype, s.a, g.M, s.k, g.lda, 64, BK);
         }
@@ -955,9 +1026,9 @@ int launch_gemm_tc(const GemmDesc& g, cudaStream_t st) {
     const double work = 2.0 * static_cast<double>(g.M) * static_cast<double>(swiglu ? 2 * g.N : g.N) * ksum;
     const int ph = prof_begin(PROF_GEMM_TC, st);
     if (g.dtype == DT_BF16)
-      rc = dispatch<DT_BF16>(p, tiles, pair, tn, st, *dev, g.a_mn, g.b_mn);
+      rc = dispatch<DT_BF16>(p, tiles, mode, tn, st, *dev, g.a_mn, g.b_mn);
     else
-      rc = dispatch<DT_F16>(p, tiles, pair, tn, st, *dev, g.a_mn, g.b_mn);
+      rc = dispatch<DT_F16>(p, tiles, mode, tn, st, *dev, g.a_mn, g.b_mn);
     prof_end(ph, work, st);
     if (rc != TPMLP_OK) return rc;
     seg_i += nsegs;
