@@ -560,7 +560,10 @@ def run_ours(args) -> int:
                 xk = xin[k] if cfg.sp else xin[k][0]
                 dzk = dzin[k] if cfg.sp else dzin[k][0]
                 blk.forward(xk, W1, W2, out=fws[k], stream=stream)
-                blk.backward(xk, W1, W2, fws[k], dzk, out=bws[k], stream=stream)
+                if args.main_grad:
+                    blk.backward_main_grad(xk, W1, W2, fws[k], dzk, mg1, mg2, out=bws[k], stream=stream)
+                else:
+                    blk.backward(xk, W1, W2, fws[k], dzk, out=bws[k], stream=stream)
                 done[k].record(stream)
                 with torch.cuda.stream(s_out):
                     s_out.wait_event(done[k])

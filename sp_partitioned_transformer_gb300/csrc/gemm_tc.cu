@@ -79,20 +79,21 @@ struct Params {
   EpiParams epi;
 };
 
-__device__ __forceinline__ void decode_tile_nt(int t, const Params& p, int nt, int& part, int& mb, int& nb) {
-  const int per_part = p.mt * nt;
+// Tile t of an mt × nt grid per partial, in groups of GROUP_M rows.
+__device__ __forceinline__ void decode_tile_grid(int t, int mt, int nt, int& part, int& mb, int& nb) {
+  const int per_part = mt * nt;
   part = t / per_part;
   const int r = t - part * per_part;
   const int span = GROUP_M * nt;
   const int g = r / span;
   const int first_m = g * GROUP_M;
-  const int gsz = min(p.mt - first_m, GROUP_M);
+  const int gsz = min(mt - first_m, GROUP_M);
   const int rr = r - g * span;
   mb = first_m + rr % gsz;
   nb = rr / gsz;
 }
 __device__ __forceinline__ void decode_tile(int t, const Params& p, int& part, int& mb, int& nb) {
-  decode_tile_nt(t, p, p.nt, part, mb, nb);
+  decode_tile_grid(t, p.mt, p.nt, part, mb, nb);
 }
 
 // ---------------------------------------------------------------- epilogues
@@ -547,11 +548,16 @@ constexpr int PAIR_NUM_BARS = 2 * PAIR_STAGES + 5;
 constexpr size_t PAIR_SMEM_BYTES = 1024 + static_cast<size_t>(PAIR_STAGES) * PSTAGE_BYTES + 256;
 
 // TN: N extent of the pair's tile; each CTA holds TN/2 rows of B.
-// MC: a cluster of two pairs on the tiles (mb, 2j) and (mb, 2j+1), which share
+// Pair slot q (the q-th cluster of 2) computes the tiles t = q, q + S, q + 2S, …
+// (S slots).  MCX: the launch asks for clusters of 4 where the GPCs have room
+// (and pairs elsewhere) and tiles are numbered so that tiles 2u and 2u + 1 are
+// the neighbours (mb, 2j) and (mb, 2j + 1).  A cluster of 4 holds the slots 2k
+// and 2k + 1, so with S even its two pairs always work on tiles that share
 // their A panel: each CTA loads 64 of its 128 A rows per stage and multicasts
-// them to its counterpart in the other pair, halving the A reads from L2; a
-// stage is refilled once both pairs' MMAs have released it.
-template <int DT, bool A_MN, bool B_MN, int TN, bool MC>
+// them to its counterpart in the other pair, halving the A reads from L2, and
+// a stage is refilled once both pairs' MMAs have released it.  A cluster of 2
+// loads all of its A rows itself (as two 64-row boxes).
+template <int DT, bool A_MN, bool B_MN, int TN, bool MCX>
 __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_constant__ Params p) {
   constexpr int HALF_N = TN / 2;
   // bytes of one stage (both CTAs): A halves + B halves; an MN-major B half is
@@ -575,14 +581,17 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
   const int lane = threadIdx.x & 31;
   const uint32_t crank = cluster_ctarank();
   const uint32_t rank = crank & 1u;              // within the pair; 0 issues the pair's MMAs
-  const uint32_t pr = MC ? (crank >> 1) : 0u;    // the pair within the cluster
+  const bool mc = MCX && cluster_nctarank() == 4u;  // two pairs sharing A
+  const uint32_t pr = crank >> 1;                // the pair within the cluster (= its slot's parity)
   const uint32_t lead = 2u * pr;                 // cluster rank of this pair's even CTA
   const bool leader = rank == 0;
   const uint16_t pair_mask = static_cast<uint16_t>(0x3u << lead);
+  // CTAs whose stages this pair's MMAs read: its own, and with mc the other pair's
+  const uint16_t empty_mask = mc ? static_cast<uint16_t>(0xFu) : pair_mask;
   auto decode = [&](int t, int& part, int& mb, int& nb) {
-    if constexpr (MC) {
-      decode_tile_nt(t, p, p.nt >> 1, part, mb, nb);
-      nb = 2 * nb + static_cast<int>(pr);
+    if constexpr (MCX) {
+      decode_tile_grid(t >> 1, p.mt, p.nt >> 1, part, mb, nb);
+      nb = 2 * nb + (t & 1);
     } else {
       decode_tile(t, p, part, mb, nb);
     }
@@ -591,7 +600,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
   if (threadIdx.x == 0) {
     for (int s = 0; s < PAIR_STAGES; ++s) {
       mbar_init(full0 + 8u * s, 1);
-      mbar_init(empty0 + 8u * s, MC ? 2 : 1);  // with MC both pairs' MMAs release a stage
+      mbar_init(empty0 + 8u * s, mc ? 2 : 1);  // the pairs whose MMAs read this CTA's stage
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull0 + 8u * a, 1);
@@ -610,9 +619,11 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  const int cluster_id = static_cast<int>(blockIdx.x >> (MC ? 2 : 1));
-  const int nclusters = static_cast<int>(gridDim.x >> (MC ? 2 : 1));
-  const int num_tiles = p.mt * (MC ? (p.nt >> 1) : p.nt) * p.nparts;  // MC: tile pairs
+  // A cluster of 4 is enumerated as if the grid held only clusters of 4 and
+  // groups the blocks of the clusters of 2 numbered 2k and 2k + 1.
+  const int slot = static_cast<int>(mc ? 2u * cluster_id_x() + pr : cluster_id_x());
+  const int nslots = static_cast<int>(gridDim.x >> 1);
+  const int num_tiles = p.mt * p.nt * p.nparts;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer (both CTAs)
@@ -625,7 +636,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
       uint32_t phase = 0;
       uint32_t issued_mask = 0, issued_phase = 0;
       bool ok = true;
-      for (int t = cluster_id; ok && t < num_tiles; t += nclusters) {
+      for (int t = slot; ok && t < num_tiles; t += nslots) {
         int part, mb, nb;
         decode(t, part, mb, nb);
         const int m_off = mb * (2 * HALF_M) + static_cast<int>(rank) * HALF_M;
@@ -650,10 +661,11 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
             const uint32_t sa = smem_u32(smem_a + stage * PA_BYTES);
             const uint32_t sb = smem_u32(smem_b + stage * PB_BYTES);
             const int k0 = kb * BK;
-            if constexpr (MC) {
+            if (mc) {
               // this CTA's share of its A rows: 64-row slice pr, sent to itself and
-              // to the same-rank CTA of the other pair (same offset in both)
-              const uint16_t mc_mask = static_cast<uint16_t>((1u << rank) | (1u << (2u + rank)));
+              // to the same-rank CTA of the pair on the neighbouring N tile (same
+              // offset in both)
+              const uint16_t mc_mask = static_cast<uint16_t>((1u << crank) | (1u << (crank ^ 2u)));
               const int m_sl = m_off + 64 * static_cast<int>(pr);
               if constexpr (!A_MN) {
                 const uint32_t dst = sa + pr * (64u * 128u);
@@ -667,6 +679,12 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
               } else {
                 tma_load_2d_pair_mc(sa + pr * MN_BOX_BYTES, ma, fb, m_sl, k0, mc_mask);
               }
+            } else if constexpr (MCX && !A_MN) {
+              // a cluster of 2 in a launch whose K-major A map has 64-row boxes
+              const int j = p.a_chunk_rows > 0 ? min(m_off / p.a_chunk_rows, p.a_nchunks - 1) : 0;
+              const int r0 = m_off - j * p.a_chunk_rows;
+              tma_load_2d_pair(sa, ma + j, fb, k0, r0);
+              tma_load_2d_pair(sa + 64u * 128u, ma + j, fb, k0, r0 + 64);
             } else if constexpr (!A_MN) {
               if (p.a_chunk_rows > 0) {
                 // rows past M (last tile) read the last chunk out of range: zero fill
@@ -716,7 +734,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
       uint32_t phase = 0;
       int it = 0;
       bool ok = true;
-      for (int t = cluster_id; ok && t < num_tiles; t += nclusters, ++it) {
+      for (int t = slot; ok && t < num_tiles; t += nslots, ++it) {
         int part, mb, nb;
         decode(t, part, mb, nb);
         const int acc = it & 1;
@@ -747,9 +765,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
               tc_mma_f16_pair(d_tmem, ad, bd, idesc, accumulate);
               accumulate = 1u;
             }
-            // frees the stage in both CTAs (with MC: in all four, each stage
-            // counting both pairs' releases)
-            tc_commit_pair_mc(empty0 + 8u * stage, MC ? static_cast<uint16_t>(0xF) : pair_mask);
+            // frees the stage in both CTAs (with mc: in all four)
+            tc_commit_pair_mc(empty0 + 8u * stage, empty_mask);
             if (++stage == PAIR_STAGES) {
               stage = 0;
               phase ^= 1u;
@@ -770,7 +787,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
     const int q = warp & 3;
     const uint32_t tempty_leader = mapa_shared(tempty0, lead);
     int it = 0;
-    for (int t = cluster_id; t < num_tiles; t += nclusters, ++it) {
+    for (int t = slot; t < num_tiles; t += nslots, ++it) {
       int part, mb, nb;
       decode(t, part, mb, nb);
       const int acc = it & 1;
@@ -832,18 +849,18 @@ static int make_map(CUtensorMap* m, int dtype, const void* base, int64_t inner, 
   return TPMLP_OK;
 }
 
-// mode 0: one CTA per tile; 1: CTA pairs (clusters of 2); 2: two pairs per
-// cluster sharing A by multicast (clusters of 4; tiles counted in pairs).
+// mode 0: one CTA per tile; 1: CTA pairs (clusters of 2); 2: CTA pairs, grouped
+// into clusters of 4 that share A by multicast wherever a GPC has room for one
+// (the preferred cluster dimension; clusters of 4 fit 144 of a GB300's 152 SMs,
+// the rest run as plain pairs).
 template <int DT, bool A_MN, bool B_MN, int TN>
 static int launch_one(const Params& p, int64_t tiles, int mode, cudaStream_t st, const DeviceInfo& dev) {
   static std::mutex mu;
   static bool attr_set[64][3] = {};
   static int max_clusters[64][3] = {};
   auto* k1 = gemm_kernel<DT, A_MN, B_MN>;
-  auto* k2 = gemm_pair_kernel<DT, A_MN, B_MN, TN, false>;
-  auto* k4 = gemm_pair_kernel<DT, A_MN, B_MN, TN, true>;
-  auto* kp = mode == 2 ? k4 : k2;
-  const unsigned csize = mode == 2 ? 4u : 2u;
+  auto* kp = mode == 2 ? gemm_pair_kernel<DT, A_MN, B_MN, TN, true> : gemm_pair_kernel<DT, A_MN, B_MN, TN, false>;
+  const unsigned csize = 2u;
   int clusters = 0;
   {
     std::lock_guard<std::mutex> lk(mu);
@@ -879,20 +896,26 @@ static int launch_one(const Params& p, int64_t tiles, int mode, cudaStream_t st,
     const int grid = static_cast<int>(std::min<int64_t>(tiles, dev.num_sms));
     k1<<<grid, THREADS, SMEM_BYTES, st>>>(p);
   } else {
-    const int64_t units = mode == 2 ? tiles / 2 : tiles;  // work items of one cluster
-    const int nclusters = static_cast<int>(std::min<int64_t>(units, clusters));
+    // pair slots; with mode 2 an even number (tiles is even there), so that the
+    // grid divides into clusters of 4
+    int slots = static_cast<int>(std::min<int64_t>(tiles, clusters));
+    if (mode == 2) slots = std::max(2, slots & ~1);
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = csize;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    cfg.gridDim = dim3(csize * static_cast<unsigned>(nclusters));
+    attr[1].id = cudaLaunchAttributePreferredClusterDimension;
+    attr[1].val.preferredClusterDim.x = 4;
+    attr[1].val.preferredClusterDim.y = 1;
+    attr[1].val.preferredClusterDim.z = 1;
+    cfg.gridDim = dim3(csize * static_cast<unsigned>(slots));
     cfg.blockDim = dim3(THREADS);
     cfg.dynamicSmemBytes = PAIR_SMEM_BYTES;
     cfg.stream = st;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = mode == 2 ? 2 : 1;
     const cudaError_t e = cudaLaunchKernelEx(&cfg, kp, p);
     if (e != cudaSuccess) return set_error(TPMLP_ERR_CUDA, std::string("2-SM GEMM launch: ") + cudaGetErrorString(e));
   }
@@ -917,8 +940,7 @@ static int dispatch(const Params& p, int64_t tiles, int mode, int tn, cudaStream
   return dispatch_tn<DT, BN>(p, tiles, mode, st, dev, a_mn, b_mn);
 }
 
-// Two CTA pairs per cluster sharing A by multicast: on unless
-// TPMLP_GEMM_MULTICAST=0.
+// A multicast between two CTA pairs (mode 2): on unless TPMLP_GEMM_MULTICAST=0.
 static bool multicast_enabled() {
   static const bool on = [] {
     const char* v = std::getenv("TPMLP_GEMM_MULTICAST");
@@ -955,10 +977,11 @@ int launch_gemm_tc(const GemmDesc& g, cudaStream_t st) {
   p.mt = static_cast<int32_t>((g.M + (pair ? 2 * BM : BM) - 1) / (pair ? 2 * BM : BM));
   const int tile_n = swiglu ? tn / 2 : tn;
   p.nt = static_cast<int32_t>((g.N + tile_n - 1) / tile_n);
-  // two pairs per cluster on neighbouring N tiles of one M block (A shared)
+  // pairs of pairs on neighbouring N tiles of one M block (A shared)
   const bool mc = pair && !swiglu && p.nt % 2 == 0 && multicast_enabled();
   const int mode = pair ? (mc ? 2 : 1) : 0;
-  const uint32_t a_box_rows = mc ? 64u : static_cast<uint32_t>(BM);  // K-major A: each CTA loads half its rows
+  const uint32_t a_box_rows = mc ? 64u : static_cast<uint32_t>(BM);  // K-major A: 64-row boxes
+  const uint32_t b_box_rows = static_cast<uint32_t>(pair ? tn / 2 : (swiglu ? BN / 2 : BN));
   p.swiglu_up_row = static_cast<int32_t>(g.swiglu_up_row);
   p.a_chunk_rows = chunked ? static_cast<int32_t>(g.a_chunk_rows) : 0;
   p.a_nchunks = chunked ? static_cast<int32_t>(g.a_chunks.size()) : 0;
@@ -1007,8 +1030,7 @@ int launch_gemm_tc(const GemmDesc& g, cudaStream_t st) {
         if (rc != TPMLP_OK) return rc;
         d.map_b = nmaps;
         if (!g.b_mn)
-          rc = make_map(&p.maps[nmaps++], g.dtype, s.b, s.k, g.b_rows, g.ldb, BK,
-                        static_cast<uint32_t>(pair ? tn / 2 : (swiglu ? BN / 2 : BN)));
+          rc = make_map(&p.maps[nmaps++], g.dtype, s.b, s.k, g.b_rows, g.ldb, BK, b_box_rows);
         else
           rc = make_map(&p.maps[nmaps++], g.dtype, s.b, g.N, s.k, g.ldb, 64, BK);
         if (rc != TPMLP_OK) return rc;
