@@ -17,8 +17,9 @@
 //               shared-memory descriptors into one of two TMEM accumulators;
 //   warp 2      TMEM allocator (512 columns = two 128×256 fp32 accumulators);
 //   warps 4-7   epilogue: tcgen05.ld of the finished accumulator (each warp its
-//               32-lane quarter), activation math, 16-byte global stores, so the
-//               epilogue of tile t overlaps the MMAs of tile t+1.
+//               32-lane quarter), activation math, outputs staged through a
+//               per-warp shared-memory buffer and stored as whole 128-byte
+//               lines, so the epilogue of tile t overlaps the MMAs of tile t+1.
 // K-major and MN-major operands are both read straight from their row-major
 // storage: for MN-major operands TMA loads 64(MN)×64(K) boxes and the UMMA
 // descriptor walks them with LBO = 8 KB (next 64-wide MN block) and SBO = 1 KB
@@ -50,7 +51,12 @@ constexpr int MAX_SEGS = 16;
 constexpr int MAX_PARTS = 16;
 constexpr int GROUP_M = 16;
 constexpr int NUM_BARS = 2 * STAGES + 5;
-constexpr size_t SMEM_BYTES = 1024 + static_cast<size_t>(STAGES) * STAGE_BYTES + 256;
+// Epilogue staging: two 32-row × 128-byte buffers for each of the 4 epilogue
+// warps, after the 256-byte barrier block.
+constexpr int EPI_STAGE_BYTES = 32 * 128;
+constexpr int EPI_WARP_BYTES = 2 * EPI_STAGE_BYTES;
+constexpr int EPI_SMEM_BYTES = 4 * EPI_WARP_BYTES;
+constexpr size_t SMEM_BYTES = 1024 + static_cast<size_t>(STAGES) * STAGE_BYTES + 256 + EPI_SMEM_BYTES;
 
 // MN-major box: 64 elements along M/N (128 bytes) × 64 K-rows = 8 KB.
 constexpr uint32_t MN_BOX_BYTES = 64 * BK * 2;
@@ -97,6 +103,50 @@ __device__ __forceinline__ void decode_tile(int t, const Params& p, int& part, i
 }
 
 // ---------------------------------------------------------------- epilogues
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
+               : "memory");
+  return v;
+}
+
+// Output staging.  After tcgen05.ld a lane holds one row, so storing straight
+// from registers makes every warp store touch 32 rows × 16 bytes (32 lines).
+// Instead lane r puts its row's 16-byte units u of a 128-byte line segment into
+// slot u ^ (r & 7) of row r of a 32 × 128-byte buffer (conflict-free: the 8
+// lanes of a quarter-warp hit 8 different slots), and the flush reads it back
+// with 8 consecutive lanes on one row, so each warp store writes 4 whole lines.
+__device__ __forceinline__ void stage_put(uint32_t buf, int lane, int unit, uint4 v) {
+  sts128(buf + static_cast<uint32_t>(lane) * 128u + (static_cast<uint32_t>(unit ^ (lane & 7)) << 4), v);
+}
+// Writes the staged line segments of rows m0 .. m0 + 31: row m's segment starts
+// at byte address line(m); rows at or past M and units at or past `units` are
+// skipped.
+template <typename LineFn>
+__device__ __forceinline__ void stage_flush(uint32_t buf, int lane, int64_t m0, int64_t M, int units, LineFn line) {
+  __syncwarp();
+  const int u = lane & 7;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int r = i * 4 + (lane >> 3);
+    const uint4 v = lds128(buf + static_cast<uint32_t>(r) * 128u + (static_cast<uint32_t>(u ^ (r & 7)) << 4));
+    const int64_t m = m0 + r;
+    if (m < M && u < units) *reinterpret_cast<uint4*>(line(m) + u * 16) = v;
+  }
+  __syncwarp();
+}
+// 16-byte units of a line segment starting at column n that lie (start) before N
+__device__ __forceinline__ int units_before(int64_t N, int64_t n, int cols_per_unit) {
+  const int64_t left = N - n;
+  if (left <= 0) return 0;
+  const int64_t u = (left + cols_per_unit - 1) / cols_per_unit;
+  return u >= 8 ? 8 : static_cast<int>(u);
+}
+
 template <int DT>
 __device__ __forceinline__ void epi_chunk(const Params& p, int64_t m, int64_t n0, const float* v,
                                           int part) {
@@ -168,13 +218,12 @@ __device__ __forceinline__ void epi_swiglu_fwd(const Params& p, int64_t m, int64
 
 // fc2 input gradient epilogue for 8 columns: dU = act'(U) ⊙ dY.  SwiGLU:
 // dG = dY·Up·silu'(G) and dUp = dY·silu(G), written to dU's gate and up halves.
+// (packed into *gate, and for SwiGLU the up half into *up)
 template <int DT>
-__device__ __forceinline__ void epi_dact8(const EpiParams& e, int64_t m, int64_t n, const float* dy, uint4 u_raw,
-                                          uint4 up_raw) {
-  using T = typename Storage<DT>::T;
+__device__ __forceinline__ void epi_dact8(const EpiParams& e, const float* dy, uint4 u_raw, uint4 up_raw,
+                                          uint4* gate, uint4* upo) {
   float u[8], r[8];
   unpack8<DT>(u_raw, u);
-  T* out = static_cast<T*>(e.out) + m * e.ldo + n;
   if (e.act == ACT_SWIGLU) {
     float up[8], r2[8];
     unpack8<DT>(up_raw, up);
@@ -184,13 +233,13 @@ __device__ __forceinline__ void epi_dact8(const EpiParams& e, int64_t m, int64_t
       r[i] = dy[i] * up[i] * (sg * (1.0f + u[i] * (1.0f - sg)));
       r2[i] = dy[i] * (u[i] * sg);
     }
-    *reinterpret_cast<uint4*>(out) = pack8<DT>(r);
-    *reinterpret_cast<uint4*>(out + e.swiglu_F) = pack8<DT>(r2);
+    *gate = pack8<DT>(r);
+    *upo = pack8<DT>(r2);
     return;
   }
 #pragma unroll
   for (int i = 0; i < 8; ++i) r[i] = dy[i] * act_grad<false>(e.act, u[i]);
-  *reinterpret_cast<uint4*>(out) = pack8<DT>(r);
+  *gate = pack8<DT>(r);
 }
 
 // L2 prefetch of the saved U row segment a fc2-input-gradient tile will read,
@@ -221,11 +270,16 @@ __device__ __forceinline__ void epi_prefetch_aux(const Params& p, int64_t m, int
 
 // Drains one 128-row × BN-column accumulator (this warp's 32 lanes = rows)
 // from tensor memory and runs the epilogue.  All 32 lanes execute the
-// tcgen05.ld instructions; rows past M only skip their stores.
+// tcgen05.ld instructions; rows past M only skip their stores.  `stage` is this
+// warp's pair of staging buffers.
 template <int DT, int TN>
 __device__ __forceinline__ void epilogue_tile(const Params& p, uint32_t trow, int64_t m, bool row_ok, int nb,
-                                              int part) {
+                                              int part, uint32_t stage) {
+  static_assert(TN % 64 == 0, "16-bit outputs are staged in 64-column line segments");
   const EpiParams& e = p.epi;
+  const int lane = static_cast<int>(m & 31);  // rows of a warp start at a multiple of 32
+  const int64_t m0 = m - lane;
+  const uint32_t buf0 = stage, buf1 = stage + EPI_STAGE_BYTES;
   if (p.swiglu_up_row > 0) {
 #pragma unroll 1
     for (int c = 0; c < TN / 64; ++c) {
@@ -242,6 +296,8 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, uint32_t trow, in
     const T* urow = static_cast<const T*>(e.aux) + m * e.ldaux;
     const int64_t nbase = static_cast<int64_t>(nb) * TN;
     uint4 cur[4], curup[4], nxt[4], nxtup[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) cur[j] = curup[j] = nxt[j] = nxtup[j] = make_uint4(0, 0, 0, 0);
     auto load = [&](int c, uint4* dst, uint4* dstup) {
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -258,12 +314,24 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, uint32_t trow, in
       if (c + 1 < TN / 32) load(c + 1, nxt, nxtup);  // one chunk ahead
       float v[32];
       tmem_ld32(trow + c * 32, v);
-      if (row_ok) {
+      const int half = c & 1;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int64_t n = nbase + c * 32 + 8 * j;
-          if (n < p.N) epi_dact8<DT>(e, m, n, v + 8 * j, cur[j], curup[j]);
-        }
+      for (int j = 0; j < 4; ++j) {
+        uint4 g, u2;
+        epi_dact8<DT>(e, v + 8 * j, cur[j], curup[j], &g, &u2);
+        stage_put(buf0, lane, half * 4 + j, g);
+        if (swi) stage_put(buf1, lane, half * 4 + j, u2);
+      }
+      if (half) {
+        const int64_t nl = nbase + (c - 1) * 32;
+        const int units = units_before(p.N, nl, 8);
+        char* base = static_cast<char*>(e.out);
+        stage_flush(buf0, lane, m0, p.M, units,
+                    [&](int64_t mm) { return base + (mm * e.ldo + nl) * static_cast<int64_t>(sizeof(T)); });
+        if (swi)
+          stage_flush(buf1, lane, m0, p.M, units, [&](int64_t mm) {
+            return base + (mm * e.ldo + e.swiglu_F + nl) * static_cast<int64_t>(sizeof(T));
+          });
       }
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -307,11 +375,70 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, uint32_t trow, in
     }
     return;
   }
+  const int64_t nbase = static_cast<int64_t>(nb) * TN;
+  if (e.kind == EPI_F32) {
+    // float32 partials: a 32-column chunk is one 128-byte line segment
+    char* base = static_cast<char*>(e.out) + static_cast<int64_t>(p.part_base + part) * e.part_stride * 4;
+#pragma unroll 1
+    for (int c = 0; c < TN / 32; ++c) {
+      float v[32];
+      tmem_ld32(trow + c * 32, v);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        stage_put(buf0, lane, j,
+                  make_uint4(__float_as_uint(v[4 * j]), __float_as_uint(v[4 * j + 1]), __float_as_uint(v[4 * j + 2]),
+                             __float_as_uint(v[4 * j + 3])));
+      const int64_t nl = nbase + c * 32;
+      stage_flush(buf0, lane, m0, p.M, units_before(p.N, nl, 4),
+                  [&](int64_t mm) { return base + (mm * e.ldo + nl) * 4; });
+    }
+    return;
+  }
+  if (e.kind == EPI_STORE || e.kind == EPI_ACT) {
+    using T = typename Storage<DT>::T;
+    const bool act = e.kind == EPI_ACT;
+#pragma unroll 1
+    for (int c = 0; c < TN / 32; ++c) {
+      float v[32];
+      tmem_ld32(trow + c * 32, v);
+      const int half = c & 1;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        stage_put(buf0, lane, half * 4 + j, pack8<DT>(v + 8 * j));
+        if (act) {
+          float a[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) a[i] = act_fwd<false>(e.act, v[8 * j + i]);
+          stage_put(buf1, lane, half * 4 + j, pack8<DT>(a));
+        }
+      }
+      if (half) {
+        const int64_t nl = nbase + (c - 1) * 32;
+        const int units = units_before(p.N, nl, 8);
+        if (e.kind == EPI_STORE && e.scatter) {
+          stage_flush(buf0, lane, m0, p.M, units, [&](int64_t mm) {
+            const int64_t sh = mm / e.rows_per_shard;
+            return static_cast<char*>(e.shard[sh]) + ((mm - sh * e.rows_per_shard) * e.ldo + nl) * static_cast<int64_t>(sizeof(T));
+          });
+        } else {
+          char* base = static_cast<char*>(e.out);
+          stage_flush(buf0, lane, m0, p.M, units,
+                      [&](int64_t mm) { return base + (mm * e.ldo + nl) * static_cast<int64_t>(sizeof(T)); });
+        }
+        if (act) {
+          char* base2 = static_cast<char*>(e.out2);
+          stage_flush(buf1, lane, m0, p.M, units,
+                      [&](int64_t mm) { return base2 + (mm * e.ldo2 + nl) * static_cast<int64_t>(sizeof(T)); });
+        }
+      }
+    }
+    return;
+  }
 #pragma unroll 1
   for (int c = 0; c < TN / 32; ++c) {
     float v[32];
     tmem_ld32(trow + c * 32, v);
-    if (row_ok) epi_chunk<DT>(p, m, static_cast<int64_t>(nb) * TN + c * 32, v, p.part_base + part);
+    if (row_ok) epi_chunk<DT>(p, m, nbase + c * 32, v, p.part_base + part);
   }
 }
 
@@ -503,7 +630,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
       const uint32_t trow = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
-      epilogue_tile<DT, BN>(p, trow, m, row_ok, nb, part);
+      epilogue_tile<DT, BN>(p, trow, m, row_ok, nb, part,
+                            smem_u32(smem + STAGES * STAGE_BYTES + 256) + static_cast<uint32_t>(q * EPI_WARP_BYTES));
       tc_fence_before();
       mbar_arrive(tempty0 + 8u * acc);
     }
@@ -545,7 +673,7 @@ constexpr int PA_BYTES = HALF_M * BK * 2;  // 16 KB
 constexpr int PB_BYTES = 128 * BK * 2;     // 16 KB: room for up to 128 B rows per CTA
 constexpr int PSTAGE_BYTES = PA_BYTES + PB_BYTES;
 constexpr int PAIR_NUM_BARS = 2 * PAIR_STAGES + 5;
-constexpr size_t PAIR_SMEM_BYTES = 1024 + static_cast<size_t>(PAIR_STAGES) * PSTAGE_BYTES + 256;
+constexpr size_t PAIR_SMEM_BYTES = 1024 + static_cast<size_t>(PAIR_STAGES) * PSTAGE_BYTES + 256 + EPI_SMEM_BYTES;
 
 // TN: N extent of the pair's tile; each CTA holds TN/2 rows of B.
 // Pair slot q (the q-th cluster of 2) computes the tiles t = q, q + S, q + 2S, …
@@ -799,7 +927,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
       const uint32_t trow = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
-      epilogue_tile<DT, TN>(p, trow, m, row_ok, nb, part);
+      epilogue_tile<DT, TN>(p, trow, m, row_ok, nb, part,
+                            smem_u32(smem + PAIR_STAGES * PSTAGE_BYTES + 256) + static_cast<uint32_t>(q * EPI_WARP_BYTES));
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(tempty_leader + 8u * acc);
