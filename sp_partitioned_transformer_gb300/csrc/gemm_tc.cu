@@ -139,6 +139,29 @@ __device__ __forceinline__ void stage_flush(uint32_t buf, int lane, int64_t m0, 
   }
   __syncwarp();
 }
+// The read counterpart: loads the 128-byte line segments of rows m0 .. m0 + 31
+// (row m's at byte address line(m), 8 lanes per row, rows at or past M and
+// units at or past `units` read as zero) into the buffer in the same layout,
+// for stage_get to hand each lane its own row's units.
+template <typename LineFn>
+__device__ __forceinline__ void stage_fill(uint32_t buf, int lane, int64_t m0, int64_t M, int units, LineFn line) {
+  const int u = lane & 7;
+  uint4 t[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int64_t m = m0 + i * 4 + (lane >> 3);
+    t[i] = (m < M && u < units) ? ldg_nc_v4(line(m) + u * 16) : make_uint4(0, 0, 0, 0);
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int r = i * 4 + (lane >> 3);
+    sts128(buf + static_cast<uint32_t>(r) * 128u + (static_cast<uint32_t>(u ^ (r & 7)) << 4), t[i]);
+  }
+  __syncwarp();
+}
+__device__ __forceinline__ uint4 stage_get(uint32_t buf, int lane, int unit) {
+  return lds128(buf + static_cast<uint32_t>(lane) * 128u + (static_cast<uint32_t>(unit ^ (lane & 7)) << 4));
+}
 // 16-byte units of a line segment starting at column n that lie (start) before N
 __device__ __forceinline__ int units_before(int64_t N, int64_t n, int cols_per_unit) {
   const int64_t left = N - n;
@@ -291,53 +314,46 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, uint32_t trow, in
     return;
   }
   if (e.kind == EPI_DACT) {
+    // Per 64-column segment: the saved U (and for SwiGLU the up half) is read as
+    // whole lines through the staging buffers, each lane takes its row's units,
+    // and the buffers are then reused to stage dU.
     using T = typename Storage<DT>::T;
     const bool swi = e.act == ACT_SWIGLU;
-    const T* urow = static_cast<const T*>(e.aux) + m * e.ldaux;
     const int64_t nbase = static_cast<int64_t>(nb) * TN;
-    uint4 cur[4], curup[4], nxt[4], nxtup[4];
+    const char* ubase = static_cast<const char*>(e.aux);
+    char* obase = static_cast<char*>(e.out);
+    constexpr int64_t ES = static_cast<int64_t>(sizeof(T));
+#pragma unroll 1
+    for (int sg = 0; sg < TN / 64; ++sg) {
+      const int64_t nl = nbase + sg * 64;
+      const int units = units_before(p.N, nl, 8);
+      stage_fill(buf0, lane, m0, p.M, units, [&](int64_t mm) { return ubase + (mm * e.ldaux + nl) * ES; });
+      if (swi)
+        stage_fill(buf1, lane, m0, p.M, units,
+                   [&](int64_t mm) { return ubase + (mm * e.ldaux + e.swiglu_F + nl) * ES; });
+      uint4 ug[8], uu[8];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) cur[j] = curup[j] = nxt[j] = nxtup[j] = make_uint4(0, 0, 0, 0);
-    auto load = [&](int c, uint4* dst, uint4* dstup) {
+      for (int j = 0; j < 8; ++j) {
+        ug[j] = stage_get(buf0, lane, j);
+        uu[j] = swi ? stage_get(buf1, lane, j) : make_uint4(0, 0, 0, 0);
+      }
+      __syncwarp();  // every lane has its units before the buffers take dU
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int64_t n = nbase + c * 32 + 8 * j;
-        if (row_ok && n < p.N) {
-          dst[j] = ldg_nc_v4(urow + n);
-          if (swi) dstup[j] = ldg_nc_v4(urow + e.swiglu_F + n);
+      for (int half = 0; half < 2; ++half) {
+        float v[32];
+        tmem_ld32(trow + (2 * sg + half) * 32, v);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint4 g, u2;
+          epi_dact8<DT>(e, v + 8 * j, ug[half * 4 + j], uu[half * 4 + j], &g, &u2);
+          stage_put(buf0, lane, half * 4 + j, g);
+          if (swi) stage_put(buf1, lane, half * 4 + j, u2);
         }
       }
-    };
-    load(0, cur, curup);
-#pragma unroll 1
-    for (int c = 0; c < TN / 32; ++c) {
-      if (c + 1 < TN / 32) load(c + 1, nxt, nxtup);  // one chunk ahead
-      float v[32];
-      tmem_ld32(trow + c * 32, v);
-      const int half = c & 1;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        uint4 g, u2;
-        epi_dact8<DT>(e, v + 8 * j, cur[j], curup[j], &g, &u2);
-        stage_put(buf0, lane, half * 4 + j, g);
-        if (swi) stage_put(buf1, lane, half * 4 + j, u2);
-      }
-      if (half) {
-        const int64_t nl = nbase + (c - 1) * 32;
-        const int units = units_before(p.N, nl, 8);
-        char* base = static_cast<char*>(e.out);
-        stage_flush(buf0, lane, m0, p.M, units,
-                    [&](int64_t mm) { return base + (mm * e.ldo + nl) * static_cast<int64_t>(sizeof(T)); });
-        if (swi)
-          stage_flush(buf1, lane, m0, p.M, units, [&](int64_t mm) {
-            return base + (mm * e.ldo + e.swiglu_F + nl) * static_cast<int64_t>(sizeof(T));
-          });
-      }
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        cur[j] = nxt[j];
-        curup[j] = nxtup[j];
-      }
+      stage_flush(buf0, lane, m0, p.M, units, [&](int64_t mm) { return obase + (mm * e.ldo + nl) * ES; });
+      if (swi)
+        stage_flush(buf1, lane, m0, p.M, units,
+                    [&](int64_t mm) { return obase + (mm * e.ldo + e.swiglu_F + nl) * ES; });
     }
     return;
   }
