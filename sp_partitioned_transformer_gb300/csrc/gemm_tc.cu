@@ -143,14 +143,21 @@ __device__ __forceinline__ void stage_flush(uint32_t buf, int lane, int64_t m0, 
 // (row m's at byte address line(m), 8 lanes per row, rows at or past M and
 // units at or past `units` read as zero) into the buffer in the same layout,
 // for stage_get to hand each lane its own row's units.
-template <typename LineFn>
+// COHERENT: L2-coherent loads, for data this kernel writes back (main_grad);
+// otherwise the read-only path.
+template <bool COHERENT = false, typename LineFn>
 __device__ __forceinline__ void stage_fill(uint32_t buf, int lane, int64_t m0, int64_t M, int units, LineFn line) {
   const int u = lane & 7;
   uint4 t[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int64_t m = m0 + i * 4 + (lane >> 3);
-    t[i] = (m < M && u < units) ? ldg_nc_v4(line(m) + u * 16) : make_uint4(0, 0, 0, 0);
+    if (m < M && u < units) {
+      const char* a = line(m) + u * 16;
+      t[i] = COHERENT ? __ldcg(reinterpret_cast<const uint4*>(a)) : ldg_nc_v4(a);
+    } else {
+      t[i] = make_uint4(0, 0, 0, 0);
+    }
   }
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
@@ -168,75 +175,6 @@ __device__ __forceinline__ int units_before(int64_t N, int64_t n, int cols_per_u
   if (left <= 0) return 0;
   const int64_t u = (left + cols_per_unit - 1) / cols_per_unit;
   return u >= 8 ? 8 : static_cast<int>(u);
-}
-
-template <int DT>
-__device__ __forceinline__ void epi_chunk(const Params& p, int64_t m, int64_t n0, const float* v,
-                                          int part) {
-  using T = typename Storage<DT>::T;
-  const EpiParams& e = p.epi;
-  const int64_t N = p.N;
-  if (e.kind == EPI_F32) {
-    float* o = static_cast<float*>(e.out) + static_cast<int64_t>(part) * e.part_stride + m * e.ldo + n0;
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-      if (n0 + 4 * j < N)
-        reinterpret_cast<float4*>(o)[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-    return;
-  }
-  if (e.kind == EPI_STORE) {
-    T* row;
-    if (e.scatter) {
-      const int64_t sh = m / e.rows_per_shard;
-      row = static_cast<T*>(e.shard[sh]) + (m - sh * e.rows_per_shard) * e.ldo;
-    } else {
-      row = static_cast<T*>(e.out) + m * e.ldo;
-    }
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      if (n0 + 8 * j < N) *reinterpret_cast<uint4*>(row + n0 + 8 * j) = pack8<DT>(v + 8 * j);
-    return;
-  }
-  if (e.kind == EPI_ACT) {
-    T* u = static_cast<T*>(e.out) + m * e.ldo + n0;
-    T* y = static_cast<T*>(e.out2) + m * e.ldo2 + n0;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      if (n0 + 8 * j < N) {
-        float a[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) a[i] = act_fwd<false>(e.act, v[8 * j + i]);
-        *reinterpret_cast<uint4*>(u + 8 * j) = pack8<DT>(v + 8 * j);
-        *reinterpret_cast<uint4*>(y + 8 * j) = pack8<DT>(a);
-      }
-    }
-    return;
-  }
-}
-
-// SwiGLU fc1: 32 gate and the matching 32 up columns of one row.
-template <int DT>
-__device__ __forceinline__ void epi_swiglu_fwd(const Params& p, int64_t m, int64_t n0,
-                                               const float* g, const float* up) {
-  using T = typename Storage<DT>::T;
-  const EpiParams& e = p.epi;
-  T* ug = static_cast<T*>(e.out) + m * e.ldo + n0;
-  T* uu = ug + e.swiglu_F;
-  T* y = static_cast<T*>(e.out2) + m * e.ldo2 + n0;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    if (n0 + 8 * j < p.N) {
-      float a[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float x = g[8 * j + i];
-        a[i] = x * sigmoid_f<false>(x) * up[8 * j + i];
-      }
-      *reinterpret_cast<uint4*>(ug + 8 * j) = pack8<DT>(g + 8 * j);
-      *reinterpret_cast<uint4*>(uu + 8 * j) = pack8<DT>(up + 8 * j);
-      *reinterpret_cast<uint4*>(y + 8 * j) = pack8<DT>(a);
-    }
-  }
 }
 
 // fc2 input gradient epilogue for 8 columns: dU = act'(U) ⊙ dY.  SwiGLU:
@@ -296,20 +234,51 @@ __device__ __forceinline__ void epi_prefetch_aux(const Params& p, int64_t m, int
 // tcgen05.ld instructions; rows past M only skip their stores.  `stage` is this
 // warp's pair of staging buffers.
 template <int DT, int TN>
-__device__ __forceinline__ void epilogue_tile(const Params& p, uint32_t trow, int64_t m, bool row_ok, int nb,
-                                              int part, uint32_t stage) {
+__device__ __forceinline__ void epilogue_tile(const Params& p, uint32_t trow, int64_t m, int nb, int part,
+                                              uint32_t stage) {
   static_assert(TN % 64 == 0, "16-bit outputs are staged in 64-column line segments");
   const EpiParams& e = p.epi;
   const int lane = static_cast<int>(m & 31);  // rows of a warp start at a multiple of 32
   const int64_t m0 = m - lane;
   const uint32_t buf0 = stage, buf1 = stage + EPI_STAGE_BYTES;
   if (p.swiglu_up_row > 0) {
+    // SwiGLU fc1, per 64-column segment of the gate half (two 32-column chunks):
+    // the gate and up halves of U go out through the two staging buffers, then
+    // Y = silu(gate) · up through the first.
+    static_assert(TN % 128 == 0, "SwiGLU tiles hold whole 64-column gate and up segments");
+    using T = typename Storage<DT>::T;
+    constexpr int64_t ES = static_cast<int64_t>(sizeof(T));
+    char* ubase = static_cast<char*>(e.out);
+    char* ybase = static_cast<char*>(e.out2);
 #pragma unroll 1
-    for (int c = 0; c < TN / 64; ++c) {
-      float g[32], up[32];
-      tmem_ld32(trow + c * 32, g);
-      tmem_ld32(trow + TN / 2 + c * 32, up);
-      if (row_ok) epi_swiglu_fwd<DT>(p, m, static_cast<int64_t>(nb) * (TN / 2) + c * 32, g, up);
+    for (int sg = 0; sg < TN / 128; ++sg) {
+      const int64_t nl = static_cast<int64_t>(nb) * (TN / 2) + sg * 64;
+      const int units = units_before(p.N, nl, 8);
+      uint4 yk[8];
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        float g[32], up[32];
+        tmem_ld32(trow + (2 * sg + half) * 32, g);
+        tmem_ld32(trow + TN / 2 + (2 * sg + half) * 32, up);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          stage_put(buf0, lane, half * 4 + j, pack8<DT>(g + 8 * j));
+          stage_put(buf1, lane, half * 4 + j, pack8<DT>(up + 8 * j));
+          float a[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float x = g[8 * j + i];
+            a[i] = x * sigmoid_f<false>(x) * up[8 * j + i];
+          }
+          yk[half * 4 + j] = pack8<DT>(a);
+        }
+      }
+      stage_flush(buf0, lane, m0, p.M, units, [&](int64_t mm) { return ubase + (mm * e.ldo + nl) * ES; });
+      stage_flush(buf1, lane, m0, p.M, units,
+                  [&](int64_t mm) { return ubase + (mm * e.ldo + e.swiglu_F + nl) * ES; });
+#pragma unroll
+      for (int j = 0; j < 8; ++j) stage_put(buf0, lane, j, yk[j]);
+      stage_flush(buf0, lane, m0, p.M, units, [&](int64_t mm) { return ybase + (mm * e.ldo2 + nl) * ES; });
     }
     return;
   }
@@ -358,36 +327,30 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, uint32_t trow, in
     return;
   }
   if (e.kind == EPI_ACC_F32) {
-    // main_grad += C: the float32 row segment of chunk c+1 is loaded while chunk
-    // c is added and stored (read-modify-write of the same elements by the same
-    // thread, so L2-coherent loads rather than the read-only path).
-    float* orow = static_cast<float*>(e.out) + m * e.ldo;
+    // main_grad += C, one 32-column (128-byte) line segment at a time: the
+    // segment is read as whole lines with L2-coherent loads (this kernel writes
+    // it back), each lane adds its row's accumulator values in place, and the
+    // segment is written back as whole lines.
+    char* base = static_cast<char*>(e.out);
     const int64_t nbase = static_cast<int64_t>(nb) * TN;
-    float4 cur[8], nxt[8];
-    auto load = [&](int c, float4* dst) {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int64_t n = nbase + c * 32 + 4 * j;
-        if (row_ok && n < p.N) dst[j] = __ldcg(reinterpret_cast<const float4*>(orow + n));
-      }
-    };
-    load(0, cur);
 #pragma unroll 1
     for (int c = 0; c < TN / 32; ++c) {
-      if (c + 1 < TN / 32) load(c + 1, nxt);
+      const int64_t nl = nbase + c * 32;
+      const int units = units_before(p.N, nl, 4);
+      auto line = [&](int64_t mm) { return base + (mm * e.ldo + nl) * 4; };
+      stage_fill<true>(buf0, lane, m0, p.M, units, line);
       float v[32];
       tmem_ld32(trow + c * 32, v);
-      if (row_ok) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int64_t n = nbase + c * 32 + 4 * j;
-          if (n < p.N)
-            *reinterpret_cast<float4*>(orow + n) =
-                make_float4(cur[j].x + v[4 * j], cur[j].y + v[4 * j + 1], cur[j].z + v[4 * j + 2], cur[j].w + v[4 * j + 3]);
-        }
+      for (int j = 0; j < 8; ++j) {
+        uint4 o = stage_get(buf0, lane, j);
+        o.x = __float_as_uint(__uint_as_float(o.x) + v[4 * j]);
+        o.y = __float_as_uint(__uint_as_float(o.y) + v[4 * j + 1]);
+        o.z = __float_as_uint(__uint_as_float(o.z) + v[4 * j + 2]);
+        o.w = __float_as_uint(__uint_as_float(o.w) + v[4 * j + 3]);
+        stage_put(buf0, lane, j, o);
       }
-#pragma unroll
-      for (int j = 0; j < 8; ++j) cur[j] = nxt[j];
+      stage_flush(buf0, lane, m0, p.M, units, line);
     }
     return;
   }
@@ -449,12 +412,6 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, uint32_t trow, in
       }
     }
     return;
-  }
-#pragma unroll 1
-  for (int c = 0; c < TN / 32; ++c) {
-    float v[32];
-    tmem_ld32(trow + c * 32, v);
-    if (row_ok) epi_chunk<DT>(p, m, nbase + c * 32, v, p.part_base + part);
   }
 }
 
@@ -640,13 +597,12 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
       const int acc = it & 1;
       const uint32_t acc_phase = static_cast<uint32_t>(it >> 1) & 1u;
       const int64_t m = static_cast<int64_t>(mb) * BM + q * 32 + lane;
-      const bool row_ok = m < p.M;
       epi_prefetch_aux<BN>(p, m, nb, DT == DT_F32 ? 4 : 2);
       const bool ok = mbar_wait_bounded(tfull0 + 8u * acc, acc_phase, abort_flag, p.status, p.timeout_ns);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
       const uint32_t trow = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
-      epilogue_tile<DT, BN>(p, trow, m, row_ok, nb, part,
+      epilogue_tile<DT, BN>(p, trow, m, nb, part,
                             smem_u32(smem + STAGES * STAGE_BYTES + 256) + static_cast<uint32_t>(q * EPI_WARP_BYTES));
       tc_fence_before();
       mbar_arrive(tempty0 + 8u * acc);
@@ -937,13 +893,12 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
       const int acc = it & 1;
       const uint32_t acc_phase = static_cast<uint32_t>(it >> 1) & 1u;
       const int64_t m = static_cast<int64_t>(mb) * (2 * HALF_M) + static_cast<int64_t>(rank) * HALF_M + q * 32 + lane;
-      const bool row_ok = m < p.M;
       epi_prefetch_aux<TN>(p, m, nb, DT == DT_F32 ? 4 : 2);
       const bool ok = mbar_wait_bounded(tfull0 + 8u * acc, acc_phase, abort_flag, p.status, p.timeout_ns);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
       const uint32_t trow = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
-      epilogue_tile<DT, TN>(p, trow, m, row_ok, nb, part,
+      epilogue_tile<DT, TN>(p, trow, m, nb, part,
                             smem_u32(smem + PAIR_STAGES * PSTAGE_BYTES + 256) + static_cast<uint32_t>(q * EPI_WARP_BYTES));
       tc_fence_before();
       __syncwarp();
