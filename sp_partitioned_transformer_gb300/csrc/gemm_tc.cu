@@ -10,6 +10,12 @@
 // ("Tensor Parallelism（TP）与 Sequence Parallelism（SP）", §2–§5;
 // "tensor-parallelism-matrix-split", §Backward：为什么有些梯度需要求和).
 //
+// Two kernels: gemm_pair_kernel (every GEMM with M > 128) computes 256×256
+// tiles on CTA pairs with tcgen05.mma cta_group::2 and a 6-stage ring, and is
+// launched with a preferred cluster of 4 so that two pairs on neighbouring N
+// tiles share their A rows by TMA multicast (described at its definition);
+// gemm_kernel (M ≤ 128) is the single-CTA form below.
+//
 // Design (one CTA per SM, persistent over output tiles):
 //   warp 0      TMA producer: 128-byte-swizzled 128×64 A and 256×64 B tiles
 //               into a 4-stage shared-memory ring (mbarrier full/empty pairs);
