@@ -40,6 +40,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "TP/SP MLP fwd+bwd TFLOP/s on 1 GB300 and % of dense BF16 peak"
+ATTN_METRIC = "TP/SP attention block fwd+bwd TFLOP/s on 1 GB300 and % of dense BF16 peak"
 UNIT = "TFLOP/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -66,6 +67,29 @@ def parse_args(argv=None):
 
 
 # ---------------------------------------------------------------- helpers
+
+
+L2_BYTES = 129e6  # GB300 L2
+
+
+def l2_note(tensors: dict) -> str:
+    """How the timed steps stand to the L2 cache (no flush between steps): the
+    main tensors one step reads and writes, with their sizes, together are or
+    are not larger than L2."""
+    sizes = ", ".join(f"{k} {v / 1e6:.0f} MB" for k, v in tensors.items())
+    if sum(tensors.values()) > L2_BYTES:
+        return f"inputs larger than L2 ({sizes} per step), no flush"
+    return f"L2-resident ({sizes} per step), no flush: a small-case figure"
+
+
+def attn_workload_desc(cfg) -> dict:
+    """The attention block's config entry (the same in both arms)."""
+    return {"workload": f"TP self-attention [s,b,h]=[{cfg.s},{cfg.b},{cfg.h}] {cfg.heads} heads of {cfg.d} "
+                        f"tp={cfg.tp} SP {'on' if cfg.sp else 'off'} {'causal' if cfg.causal else 'unmasked'} "
+                        f"{cfg.dtype}, fwd+bwd",
+            "name": cfg.name, "flops_per_step": float(cfg.flops_fwd_bwd()),
+            "flops_note": "24·M·h² projections + 12·b·h·(visible query-key pairs) core, no recomputation",
+            "l2": l2_note({"Wqkv": 3 * cfg.h * cfg.h * 2, "QKV": 3 * cfg.s * cfg.b * cfg.h * 2})}
 
 
 def workload_desc(cfg) -> dict:
@@ -319,11 +343,42 @@ def measure_dim0(tpmlp, cfg, dev, stream, iters: int = 50) -> dict:
 # ---------------------------------------------------------------- reference arm
 
 
+def run_reference_attention(args, world: int) -> int:
+    """The reference arm of --block attention: the fp64 attention oracle, timed
+    on a bounded sample of the attention workload, under the attention arm's
+    metric and config."""
+    from synthetic import ATTN_CONFIGS, attn_inputs
+
+    name = args.config if args.config in ATTN_CONFIGS else "llama70b_attn_tpsp8_bf16"
+    cfg = ATTN_CONFIGS[name]
+    per_step_s = max(0.2, min(3.0, 150.0 / max(1, args.steps + args.warmup)))
+    run, sp_, fl = attn_oracle_sample(cfg, attn_inputs(cfg), per_step_s)
+    for _ in range(args.warmup):
+        run(sp_)
+    times = [run(sp_) for _ in range(args.steps)]
+    t = sum(times) / len(times)
+    value = fl / t / 1e12
+    sample = (f"first {sp_} of {cfg.s} tokens of each of {cfg.b} sequence(s), full weights; fp64 NumPy attention "
+              f"block fwd+bwd")
+    line = {
+        "impl": "reference", "metric": ATTN_METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": attn_workload_desc(cfg),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_reference(args) -> int:
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     if rank != 0:
         return 0
+    if args.block == "attention":
+        return run_reference_attention(args, world)
     from synthetic import CONFIGS, block_inputs
 
     cfg = CONFIGS[args.config]
@@ -660,8 +715,8 @@ def run_ours(args) -> int:
         "data": "synthetic",
         "config": {**workload_desc(cfg), "reduce": args.mode,
                    "variant": ("sp-sublayer " if args.sp_region else "") + ("main_grad" if args.main_grad else "block"),
-                   "l2": f"inputs larger than L2: W1 and W2 are {cfg.fc1_rows * cfg.h * ebytes / 1e6:.0f} and "
-                         f"{cfg.h * cfg.f * ebytes / 1e6:.0f} MB, no flush",
+                   "l2": l2_note({"W1": cfg.fc1_rows * cfg.h * ebytes, "W2": cfg.h * cfg.f * ebytes,
+                                  "U": cfg.M * cfg.fc1_rows * ebytes, "Y": cfg.M * cfg.f * ebytes}),
                    "flops_per_step": flops,
                    "replicas": world},
         "frac_of_dense_bf16_peak": {"sustained": value / world / peak,
@@ -826,7 +881,7 @@ def run_attention(args) -> int:
         cpu = attn_oracle_baseline(cfg, t, args.cpu_seconds)
 
     line = {
-        "metric": "TP/SP attention block fwd+bwd TFLOP/s on 1 GB300 and % of dense BF16 peak",
+        "metric": ATTN_METRIC,
         "value": flops / (ms / 1e3) / 1e12,
         "unit": UNIT,
         "n_gpus": 1,
@@ -838,12 +893,7 @@ def run_attention(args) -> int:
         "vs_baseline": None,
         "dtype": cfg.dtype,
         "data": "synthetic",
-        "config": {"workload": f"TP self-attention [s,b,h]=[{cfg.s},{cfg.b},{cfg.h}] {cfg.heads} heads of {cfg.d} "
-                               f"tp={cfg.tp} SP {'on' if cfg.sp else 'off'} {'causal' if cfg.causal else 'unmasked'} "
-                               f"{cfg.dtype}, fwd+bwd",
-                   "name": cfg.name, "flops_per_step": flops,
-                   "flops_note": "24·M·h² projections + 12·b·h·(visible query-key pairs) core, no recomputation",
-                   "l2": f"inputs larger than L2: Wqkv is {3 * cfg.h * cfg.h * 2 / 1e6:.0f} MB, no flush"},
+        "config": attn_workload_desc(cfg),
         "frac_of_dense_bf16_peak": {"sustained": flops / (ms / 1e3) / 1e12 / peak, "peak_source": peak_src},
         "roofline": {"bound": "tensor", "kernel": "tpmlp::attn core (attn_fwd_kernel, attn_bwd_dkdv_kernel, "
                                                   "attn_bwd_dq_kernel, attn_bwd_delta_kernel)",
@@ -864,12 +914,13 @@ def run_attention(args) -> int:
     return 0
 
 
-def attn_oracle_baseline(cfg, inputs, target_s: float):
+def attn_oracle_sample(cfg, inputs, target_s: float):
     """The fp64 oracle's attention block fwd+bwd (its backward runs the forward
     too) on the first s' tokens of every sequence with full weights, s' sized so
     one run takes about target_s and at most 1024 (the oracle holds several
     [b, heads, s', s'] fp64 matrices); FLOPs counted as on the GPU (24·M'·h² for
-    the projections, 12·b·h per visible query-key pair)."""
+    the projections, 12·b·h per visible query-key pair).  Returns (run, s',
+    flops): run(s') times one pass in seconds."""
     import oracle as O
 
     X = inputs["X"].double().numpy()
@@ -893,8 +944,14 @@ def attn_oracle_baseline(cfg, inputs, target_s: float):
     if t_probe < target_s:
         sp_ = int(min(cfg.s, 1024, max(probe, probe * target_s / max(t_probe, 1e-3))))
         sp_ = max(probe, sp_ // 32 * 32)
+    return run, sp_, flops(sp_)
+
+
+def attn_oracle_baseline(cfg, inputs, target_s: float):
+    """One timed oracle run of attn_oracle_sample's size, as a cpu_baseline entry."""
+    run, sp_, fl = attn_oracle_sample(cfg, inputs, target_s)
     t_run = run(sp_)
-    return {"value": flops(sp_) / t_run / 1e12, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+    return {"value": fl / t_run / 1e12, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
             "sample": f"first {sp_} of {cfg.s} tokens of each of {cfg.b} sequence(s), full weights, fp64 NumPy "
                       f"attention block fwd+bwd, one run of {t_run:.1f} s"}
 

@@ -34,3 +34,22 @@ def test_reference_arm_prints_one_complete_line(capsys, monkeypatch):
     e2e = d["e2e"]
     assert e2e["value"] == pytest.approx(d["value"]) and e2e["unit"] == d["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+
+
+def test_attention_reference_arm_uses_the_attention_metric(capsys, monkeypatch):
+    sys.path.insert(0, ROOT)
+    import bench
+
+    monkeypatch.setenv("RANK", "0")
+    monkeypatch.setenv("WORLD_SIZE", "1")
+    argv = ["--impl", "reference", "--block", "attention", "--config", "attn_tiny_tp2_bf16", "--steps", "1",
+            "--warmup", "0"]
+    assert bench.main(argv) == 0
+    lines = [ln for ln in capsys.readouterr().out.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["metric"] == bench.ATTN_METRIC and d["unit"] == bench.UNIT
+    assert d["value"] > 0 and d["config"]["name"] == "attn_tiny_tp2_bf16"
+    assert d["config"]["flops_per_step"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and "sequence" in d["cpu_baseline"]["sample"]
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
