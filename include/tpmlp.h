@@ -53,6 +53,12 @@
  *   h and f/tp multiples of 8, every pointer 16-byte aligned.  Otherwise the
  *   call returns TPMLP_ERR_UNSUPPORTED.  The TPMLP_F32 path (CUDA-core float32)
  *   has no shape or alignment requirement beyond 4-byte alignment.
+ *
+ * Environment (read once per process):
+ *   TPMLP_GEMM_MULTICAST=0  run the tensor-core GEMMs as plain 2-SM pairs
+ *                           instead of clusters of 4 that share their A rows by
+ *                           TMA multicast (the default); results are
+ *                           bit-identical either way.
  */
 #ifndef TPMLP_H_
 #define TPMLP_H_
