@@ -53,12 +53,6 @@
  *   h and f/tp multiples of 8, every pointer 16-byte aligned.  Otherwise the
  *   call returns TPMLP_ERR_UNSUPPORTED.  The TPMLP_F32 path (CUDA-core float32)
  *   has no shape or alignment requirement beyond 4-byte alignment.
- *
- * Environment (read once per process):
- *   TPMLP_GEMM_MULTICAST=0  run the tensor-core GEMMs as plain 2-SM pairs
- *                           instead of clusters of 4 that share their A rows by
- *                           TMA multicast (the default); results are
- *                           bit-identical either way.
  */
 #ifndef TPMLP_H_
 #define TPMLP_H_
@@ -106,13 +100,19 @@ typedef enum tpmlp_reduce {
 /* ---------------------------------------------------------------------------
  * tpmlp_workspace_size — bytes of device workspace that tpmlp_forward and
  * tpmlp_backward need for these arguments (the maximum of the two).
- *   SP on:   the gathered input [M,h] and, in backward, the gathered dZ [M,h];
+ *   SP on:   the gathered input [M,h] and, in backward, the gathered dZ [M,h]
+ *            (neither when every SP chunk is a whole number of 128-row
+ *            blocks: the tensor-core GEMMs then read the chunks in place);
  *   PARTIALS: tp float32 partial sums [tp, M, h].
- * Returns 0 for invalid arguments (tpmlp_last_error() says why) or when no
+ * tpmlp_forward_workspace_size gives the forward's own need (no dZ slot);
+ * tpmlp_forward accepts a workspace of that size.
+ * Both return 0 for invalid arguments (tpmlp_last_error() says why) or when no
  * workspace is needed.  The workspace must be 256-byte aligned.
  * ------------------------------------------------------------------------- */
 size_t tpmlp_workspace_size(int64_t s, int64_t b, int64_t h, int64_t f, int tp, int sp,
                             int dtype, int act, int mode);
+size_t tpmlp_forward_workspace_size(int64_t s, int64_t b, int64_t h, int64_t f, int tp, int sp,
+                                    int dtype, int act, int mode);
 
 /* ---------------------------------------------------------------------------
  * tpmlp_forward — forward pass of the block.
@@ -224,12 +224,14 @@ int tpmlp_reduce_scatter_dim0(const float* partials, void* const* out, int64_t s
  * the library as device memory.  Every GPU that loads the library holds it
  * until the process exits.  The call allocates nothing (no cudaMalloc,
  * cudaFree or allocating library routine).
- *   - Sizes whose workspace (tpmlp_workspace_size) exceeds the scratch are
- *     rejected with TPMLP_ERR_WORKSPACE and a message giving both sizes; use
- *     tpmlp_forward with a caller workspace for those.
- *   - The first call on each device looks up the scratch array's device
- *     address (cudaGetSymbolAddress) with that device current; make that first
- *     call before any stream capture on the device.
+ *   - Sizes whose forward workspace (tpmlp_forward_workspace_size) exceeds
+ *     the scratch are rejected with TPMLP_ERR_WORKSPACE and a message giving
+ *     both sizes; use tpmlp_forward with a caller workspace for those.
+ *   - The first call in each CUDA context of a device — the first call on the
+ *     device, and the first after the caller replaced the context (e.g. by
+ *     cudaDeviceReset) — looks up the scratch array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture on the device.
  *   - All calls share the one array and it keeps the last call's contents.
  *     Nothing in it needs to start at zero (each call writes every scratch
  *     byte it reads).  Calls that can overlap on the GPU — on different

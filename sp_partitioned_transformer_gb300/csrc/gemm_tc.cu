@@ -11,10 +11,10 @@
 // "tensor-parallelism-matrix-split", §Backward：为什么有些梯度需要求和).
 //
 // Two kernels: gemm_pair_kernel (every GEMM with M > 128) computes 256×256
-// tiles on CTA pairs with tcgen05.mma cta_group::2 and a 6-stage ring, and is
-// launched with a preferred cluster of 4 so that two pairs on neighbouring N
-// tiles share their A rows by TMA multicast (described at its definition);
-// gemm_kernel (M ≤ 128) is the single-CTA form below.
+// tiles on CTA pairs (clusters of 2) with tcgen05.mma cta_group::2 and a
+// 6-stage ring, each CTA loading its own operand halves with plain TMA
+// (described at its definition); gemm_kernel (M ≤ 128) is the single-CTA form
+// below.
 //
 // Design (one CTA per SM, persistent over output tiles):
 //   warp 0      TMA producer: 128-byte-swizzled 128×64 A and 256×64 B tiles
@@ -34,7 +34,6 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
-#include <cstdlib>
 #include <mutex>
 
 #include "internal.h"
@@ -633,18 +632,6 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
 // and "accumulator full" barriers.  Each CTA's tensor memory holds its 128 rows
 // of both 256-column accumulators; both epilogues release an accumulator by
 // arriving on the even CTA's "accumulator empty" barrier.
-// TMA load whose box lands at the same offset in every CTA of `mask` (a
-// multicast within the cluster), each destination CTA's bytes completing on its
-// pair's even-CTA barrier at bar_cluster's offset.
-__device__ __forceinline__ void tma_load_2d_pair_mc(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster,
-                                                    int32_t c0, int32_t c1, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1), "h"(mask)
-      : "memory");
-}
-
 constexpr int PAIR_STAGES = 6;
 constexpr int HALF_M = BM;      // rows of A per CTA
 constexpr int PA_BYTES = HALF_M * BK * 2;  // 16 KB
@@ -655,15 +642,9 @@ constexpr size_t PAIR_SMEM_BYTES = 1024 + static_cast<size_t>(PAIR_STAGES) * PST
 
 // TN: N extent of the pair's tile; each CTA holds TN/2 rows of B.
 // Pair slot q (the q-th cluster of 2) computes the tiles t = q, q + S, q + 2S, …
-// (S slots).  MCX: the launch asks for clusters of 4 where the GPCs have room
-// (and pairs elsewhere) and tiles are numbered so that tiles 2u and 2u + 1 are
-// the neighbours (mb, 2j) and (mb, 2j + 1).  A cluster of 4 holds the slots 2k
-// and 2k + 1, so with S even its two pairs always work on tiles that share
-// their A panel: each CTA loads 64 of its 128 A rows per stage and multicasts
-// them to its counterpart in the other pair, halving the A reads from L2, and
-// a stage is refilled once both pairs' MMAs have released it.  A cluster of 2
-// loads all of its A rows itself (as two 64-row boxes).
-template <int DT, bool A_MN, bool B_MN, int TN, bool MCX>
+// (S slots).  Every CTA loads its own 128 A rows and TN/2 B rows: no operand
+// is shared between clusters, so every copy stays inside its own pair.
+template <int DT, bool A_MN, bool B_MN, int TN>
 __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_constant__ Params p) {
   constexpr int HALF_N = TN / 2;
   // bytes of one stage (both CTAs): A halves + B halves; an MN-major B half is
@@ -685,28 +666,16 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t crank = cluster_ctarank();
-  const uint32_t rank = crank & 1u;              // within the pair; 0 issues the pair's MMAs
-  const bool mc = MCX && cluster_nctarank() == 4u;  // two pairs sharing A
-  const uint32_t pr = crank >> 1;                // the pair within the cluster (= its slot's parity)
-  const uint32_t lead = 2u * pr;                 // cluster rank of this pair's even CTA
+  const uint32_t rank = cluster_ctarank();  // within the pair; 0 issues the pair's MMAs
+  constexpr uint32_t lead = 0u;              // cluster rank of the pair's even CTA
   const bool leader = rank == 0;
-  const uint16_t pair_mask = static_cast<uint16_t>(0x3u << lead);
-  // CTAs whose stages this pair's MMAs read: its own, and with mc the other pair's
-  const uint16_t empty_mask = mc ? static_cast<uint16_t>(0xFu) : pair_mask;
-  auto decode = [&](int t, int& part, int& mb, int& nb) {
-    if constexpr (MCX) {
-      decode_tile_grid(t >> 1, p.mt, p.nt >> 1, part, mb, nb);
-      nb = 2 * nb + (t & 1);
-    } else {
-      decode_tile(t, p, part, mb, nb);
-    }
-  };
+  constexpr uint16_t pair_mask = 0x3u;       // both CTAs of the pair
+  auto decode = [&](int t, int& part, int& mb, int& nb) { decode_tile(t, p, part, mb, nb); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < PAIR_STAGES; ++s) {
       mbar_init(full0 + 8u * s, 1);
-      mbar_init(empty0 + 8u * s, mc ? 2 : 1);  // the pairs whose MMAs read this CTA's stage
+      mbar_init(empty0 + 8u * s, 1);  // the pair's MMA commit
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull0 + 8u * a, 1);
@@ -725,9 +694,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  // A cluster of 4 is enumerated as if the grid held only clusters of 4 and
-  // groups the blocks of the clusters of 2 numbered 2k and 2k + 1.
-  const int slot = static_cast<int>(mc ? 2u * cluster_id_x() + pr : cluster_id_x());
+  const int slot = static_cast<int>(cluster_id_x());
   const int nslots = static_cast<int>(gridDim.x >> 1);
   const int num_tiles = p.mt * p.nt * p.nparts;
 
@@ -767,31 +734,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
             const uint32_t sa = smem_u32(smem_a + stage * PA_BYTES);
             const uint32_t sb = smem_u32(smem_b + stage * PB_BYTES);
             const int k0 = kb * BK;
-            if (mc) {
-              // this CTA's share of its A rows: 64-row slice pr, sent to itself and
-              // to the same-rank CTA of the pair on the neighbouring N tile (same
-              // offset in both)
-              const uint16_t mc_mask = static_cast<uint16_t>((1u << crank) | (1u << (crank ^ 2u)));
-              const int m_sl = m_off + 64 * static_cast<int>(pr);
-              if constexpr (!A_MN) {
-                const uint32_t dst = sa + pr * (64u * 128u);
-                if (p.a_chunk_rows > 0) {
-                  // the slice lies in the 128-row block's chunk; past M: zero fill
-                  const int j = min(m_off / p.a_chunk_rows, p.a_nchunks - 1);
-                  tma_load_2d_pair_mc(dst, ma + j, fb, k0, m_sl - j * p.a_chunk_rows, mc_mask);
-                } else {
-                  tma_load_2d_pair_mc(dst, ma, fb, k0, m_sl, mc_mask);
-                }
-              } else {
-                tma_load_2d_pair_mc(sa + pr * MN_BOX_BYTES, ma, fb, m_sl, k0, mc_mask);
-              }
-            } else if constexpr (MCX && !A_MN) {
-              // a cluster of 2 in a launch whose K-major A map has 64-row boxes
-              const int j = p.a_chunk_rows > 0 ? min(m_off / p.a_chunk_rows, p.a_nchunks - 1) : 0;
-              const int r0 = m_off - j * p.a_chunk_rows;
-              tma_load_2d_pair(sa, ma + j, fb, k0, r0);
-              tma_load_2d_pair(sa + 64u * 128u, ma + j, fb, k0, r0 + 64);
-            } else if constexpr (!A_MN) {
+            if constexpr (!A_MN) {
               if (p.a_chunk_rows > 0) {
                 // rows past M (last tile) read the last chunk out of range: zero fill
                 const int j = min(m_off / p.a_chunk_rows, p.a_nchunks - 1);
@@ -871,8 +814,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
               tc_mma_f16_pair(d_tmem, ad, bd, idesc, accumulate);
               accumulate = 1u;
             }
-            // frees the stage in both CTAs (with mc: in all four)
-            tc_commit_pair_mc(empty0 + 8u * stage, empty_mask);
+            tc_commit_pair_mc(empty0 + 8u * stage, pair_mask);  // frees the stage in both CTAs
             if (++stage == PAIR_STAGES) {
               stage = 0;
               phase ^= 1u;
@@ -955,23 +897,20 @@ static int make_map(CUtensorMap* m, int dtype, const void* base, int64_t inner, 
   return TPMLP_OK;
 }
 
-// mode 0: one CTA per tile; 1: CTA pairs (clusters of 2); 2: CTA pairs, grouped
-// into clusters of 4 that share A by multicast wherever a GPC has room for one
-// (the preferred cluster dimension; clusters of 4 fit 144 of a GB300's 152 SMs,
-// the rest run as plain pairs).
+// mode 0: one CTA per tile; 1: CTA pairs (clusters of 2).
 template <int DT, bool A_MN, bool B_MN, int TN>
 static int launch_one(const Params& p, int64_t tiles, int mode, cudaStream_t st, const DeviceInfo& dev) {
   static std::mutex mu;
-  static bool attr_set[64][3] = {};
-  static int max_clusters[64][3] = {};
+  static uint64_t attr_gen[64][2] = {};  // the device context the attributes were set in
+  static int max_clusters[64][2] = {};
   auto* k1 = gemm_kernel<DT, A_MN, B_MN>;
-  auto* kp = mode == 2 ? gemm_pair_kernel<DT, A_MN, B_MN, TN, true> : gemm_pair_kernel<DT, A_MN, B_MN, TN, false>;
+  auto* kp = gemm_pair_kernel<DT, A_MN, B_MN, TN>;
   const unsigned csize = 2u;
   int clusters = 0;
   {
     std::lock_guard<std::mutex> lk(mu);
     const int d = (dev.device >= 0 && dev.device < 64) ? dev.device : 0;
-    if (!attr_set[d][mode]) {
+    if (attr_gen[d][mode] != dev.generation) {
       const cudaError_t e =
           mode ? cudaFuncSetAttribute(kp, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(PAIR_SMEM_BYTES))
                : cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(SMEM_BYTES));
@@ -994,7 +933,7 @@ static int launch_one(const Params& p, int64_t tiles, int mode, cudaStream_t st,
           return set_error(TPMLP_ERR_CUDA, std::string("cudaOccupancyMaxActiveClusters: ") + cudaGetErrorString(e2));
         max_clusters[d][mode] = n;
       }
-      attr_set[d][mode] = true;
+      attr_gen[d][mode] = dev.generation;
     }
     clusters = max_clusters[d][mode];
   }
@@ -1002,26 +941,20 @@ static int launch_one(const Params& p, int64_t tiles, int mode, cudaStream_t st,
     const int grid = static_cast<int>(std::min<int64_t>(tiles, dev.num_sms));
     k1<<<grid, THREADS, SMEM_BYTES, st>>>(p);
   } else {
-    // pair slots; with mode 2 an even number (tiles is even there), so that the
-    // grid divides into clusters of 4
-    int slots = static_cast<int>(std::min<int64_t>(tiles, clusters));
-    if (mode == 2) slots = std::max(2, slots & ~1);
+    // pair slots: at most the resident clusters of 2
+    const int slots = static_cast<int>(std::min<int64_t>(tiles, clusters));
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[2];
+    cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = csize;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    attr[1].id = cudaLaunchAttributePreferredClusterDimension;
-    attr[1].val.preferredClusterDim.x = 4;
-    attr[1].val.preferredClusterDim.y = 1;
-    attr[1].val.preferredClusterDim.z = 1;
     cfg.gridDim = dim3(csize * static_cast<unsigned>(slots));
     cfg.blockDim = dim3(THREADS);
     cfg.dynamicSmemBytes = PAIR_SMEM_BYTES;
     cfg.stream = st;
     cfg.attrs = attr;
-    cfg.numAttrs = mode == 2 ? 2 : 1;
+    cfg.numAttrs = 1;
     const cudaError_t e = cudaLaunchKernelEx(&cfg, kp, p);
     if (e != cudaSuccess) return set_error(TPMLP_ERR_CUDA, std::string("2-SM GEMM launch: ") + cudaGetErrorString(e));
   }
@@ -1044,15 +977,6 @@ static int dispatch(const Params& p, int64_t tiles, int mode, int tn, cudaStream
                     bool a_mn, bool b_mn) {
   (void)tn;
   return dispatch_tn<DT, BN>(p, tiles, mode, st, dev, a_mn, b_mn);
-}
-
-// A multicast between two CTA pairs (mode 2): on unless TPMLP_GEMM_MULTICAST=0.
-static bool multicast_enabled() {
-  static const bool on = [] {
-    const char* v = std::getenv("TPMLP_GEMM_MULTICAST");
-    return !(v != nullptr && v[0] == '0');
-  }();
-  return on;
 }
 
 }  // namespace tc
@@ -1083,10 +1007,8 @@ int launch_gemm_tc(const GemmDesc& g, cudaStream_t st) {
   p.mt = static_cast<int32_t>((g.M + (pair ? 2 * BM : BM) - 1) / (pair ? 2 * BM : BM));
   const int tile_n = swiglu ? tn / 2 : tn;
   p.nt = static_cast<int32_t>((g.N + tile_n - 1) / tile_n);
-  // pairs of pairs on neighbouring N tiles of one M block (A shared)
-  const bool mc = pair && !swiglu && p.nt % 2 == 0 && multicast_enabled();
-  const int mode = pair ? (mc ? 2 : 1) : 0;
-  const uint32_t a_box_rows = mc ? 64u : static_cast<uint32_t>(BM);  // K-major A: 64-row boxes
+  const int mode = pair ? 1 : 0;
+  const uint32_t a_box_rows = static_cast<uint32_t>(BM);  // K-major A: one 128-row box per CTA
   const uint32_t b_box_rows = static_cast<uint32_t>(pair ? tn / 2 : (swiglu ? BN / 2 : BN));
   p.swiglu_up_row = static_cast<int32_t>(g.swiglu_up_row);
   p.a_chunk_rows = chunked ? static_cast<int32_t>(g.a_chunk_rows) : 0;
