@@ -18,6 +18,8 @@
 //   fc1 weight gradient dW1 = dUᵀ·X           GEMM (MN-major A and B)
 //   fc1 input gradient + f's backward sum     as fc2 forward: partials + shard
 //                                             sum, or the fused K-concatenation.
+#include <cudaTypedefs.h>
+
 #include <atomic>
 #include <cstring>
 #include <mutex>
@@ -42,6 +44,31 @@ uint64_t wait_timeout_ns() { return g_timeout_ns.load(); }
 
 static std::mutex g_dev_mu;
 static DeviceInfo g_devs[64];
+static uint64_t g_generation = 0;
+
+// Unique id of the calling thread's current CUDA context, 0 if it has none or
+// the driver cannot say.  Ids are never reused within a process.
+static unsigned long long current_context_id() {
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &ptr, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(ptr);
+    ptr = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &ptr, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(ptr);
+  });
+  if (get_current == nullptr || get_id == nullptr) return 0;
+  CUcontext c = nullptr;
+  if (get_current(&c) != CUDA_SUCCESS || c == nullptr) return 0;
+  unsigned long long id = 0;
+  return get_id(c, &id) == CUDA_SUCCESS ? id : 0;
+}
 
 int current_device(DeviceInfo** out) {
   int d = 0;
@@ -50,7 +77,14 @@ int current_device(DeviceInfo** out) {
   if (d < 0 || d >= 64) return set_error(TPMLP_ERR_CUDA, "device ordinal out of range");
   std::lock_guard<std::mutex> lk(g_dev_mu);
   DeviceInfo& info = g_devs[d];
-  if (info.device < 0) {
+  // The status word's address is looked up on every call: the lookup also makes
+  // the runtime's context current on this thread, whose id then tells whether
+  // the cached state still belongs to the live context.
+  void* status_addr = nullptr;
+  e = cudaGetSymbolAddress(&status_addr, g_status_word);
+  if (e != cudaSuccess) return set_error(TPMLP_ERR_CUDA, std::string("cudaGetSymbolAddress: ") + cudaGetErrorString(e));
+  const unsigned long long ctx = current_context_id();
+  if (info.device < 0 || ctx == 0 || ctx != info.ctx_id) {
     int sms = 0, smem = 0;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, d);
     if (e != cudaSuccess) return set_error(TPMLP_ERR_CUDA, std::string("cudaDeviceGetAttribute: ") + cudaGetErrorString(e));
@@ -59,15 +93,14 @@ int current_device(DeviceInfo** out) {
     int smem_sm = 0;
     e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, d);
     if (e != cudaSuccess) return set_error(TPMLP_ERR_CUDA, std::string("cudaDeviceGetAttribute: ") + cudaGetErrorString(e));
-    void* addr = nullptr;
-    e = cudaGetSymbolAddress(&addr, g_status_word);
-    if (e != cudaSuccess) return set_error(TPMLP_ERR_CUDA, std::string("cudaGetSymbolAddress: ") + cudaGetErrorString(e));
-    info.status = static_cast<unsigned*>(addr);
     info.num_sms = sms;
     info.max_smem_optin = static_cast<size_t>(smem);
     info.smem_per_sm = static_cast<size_t>(smem_sm);
     info.device = d;
+    info.ctx_id = ctx;
+    info.generation = ++g_generation;
   }
+  info.status = static_cast<unsigned*>(status_addr);
   *out = &info;
   return TPMLP_OK;
 }
@@ -83,6 +116,7 @@ struct ProfRec {
 thread_local bool g_prof_on = false;
 thread_local std::vector<ProfRec> g_prof_recs;
 thread_local std::vector<cudaEvent_t> g_prof_events;
+thread_local uint64_t g_prof_generation = 0;  // the device context the events were made in
 }  // namespace
 
 int prof_begin(int kind, cudaStream_t st) {
@@ -133,7 +167,8 @@ bool fused_gather(const Block& k) {
   return k.sp && k.dtype != DT_F32 && k.tp <= 16 && ((k.s / k.tp) * k.b) % 128 == 0;
 }
 
-WsLayout ws_layout(const Block& k) {
+// forward: the forward's own layout, without the backward's gathered-dZ slot.
+WsLayout ws_layout(const Block& k, bool forward = false) {
   WsLayout L{};
   size_t off = 0;
   const size_t act_bytes = static_cast<size_t>(k.M) * k.h * k.e;
@@ -141,7 +176,7 @@ WsLayout ws_layout(const Block& k) {
   L.x_off = off;
   if (gathered) off += align256(act_bytes);
   L.dz_off = off;
-  if (gathered) off += align256(act_bytes);
+  if (gathered && !forward) off += align256(act_bytes);
   L.p_off = off;
   if (k.mode == TPMLP_REDUCE_PARTIALS) off += align256(static_cast<size_t>(k.tp) * k.M * k.h * 4);
   L.total = off;
@@ -244,17 +279,20 @@ int shard_sum_partials(const Block& k, void* const* out, void* ws, const WsLayou
 struct SideStream {
   cudaStream_t stream = nullptr;
   cudaEvent_t fork = nullptr, join = nullptr;
+  uint64_t generation = 0;  // the device context they were created in
 };
 std::mutex g_side_mu;
 SideStream g_side[64];
 
-int side_stream_locked(SideStream** out) {
-  int d = 0;
-  cudaError_t e = cudaGetDevice(&d);
-  if (e != cudaSuccess || d < 0 || d >= 64) return set_error(TPMLP_ERR_CUDA, "cudaGetDevice failed");
+int side_stream_locked(const DeviceInfo& dev, SideStream** out) {
+  const int d = dev.device;
+  if (d < 0 || d >= 64) return set_error(TPMLP_ERR_CUDA, "device ordinal out of range");
   SideStream& ss = g_side[d];
-  if (ss.stream == nullptr) {
-    e = cudaStreamCreateWithFlags(&ss.stream, cudaStreamNonBlocking);
+  if (ss.stream == nullptr || ss.generation != dev.generation) {
+    // (handles of a context that was torn down are gone with it: not destroyed here)
+    ss = SideStream{};
+    ss.generation = dev.generation;
+    cudaError_t e = cudaStreamCreateWithFlags(&ss.stream, cudaStreamNonBlocking);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming);
     if (e != cudaSuccess) return set_error(TPMLP_ERR_CUDA, std::string("side stream: ") + cudaGetErrorString(e));
@@ -335,7 +373,7 @@ int forward_workspace_bytes(int64_t s, int64_t b, int64_t h, int64_t f, int tp, 
   Block k;
   const int rc = check_block(s, b, h, f, tp, sp, dtype, act, mode, &k);
   if (rc != TPMLP_OK) return rc;
-  *bytes = ws_layout(k).total;
+  *bytes = ws_layout(k, /*forward=*/true).total;
   return TPMLP_OK;
 }
 
@@ -471,7 +509,7 @@ static int backward_impl(int64_t s, int64_t b, int64_t h, int64_t f, int tp, int
     if ((rc = row_parallel_and_reduce(k, true, du, w1, dx, ws, L, st, /*defer_shard_sum=*/true))) return rc;
     std::lock_guard<std::mutex> lk(g_side_mu);
     SideStream* ss = nullptr;
-    if ((rc = side_stream_locked(&ss))) return rc;
+    if ((rc = side_stream_locked(*dev, &ss))) return rc;
     cudaError_t e = cudaEventRecord(ss->fork, st);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(ss->stream, ss->fork, 0);
     if (e != cudaSuccess) return set_error(TPMLP_ERR_CUDA, std::string("fork: ") + cudaGetErrorString(e));
@@ -498,6 +536,13 @@ const char* tpmlp_last_error(void) { return g_last_error.c_str(); }
 
 int tpmlp_profile_start(void) {
   g_prof_recs.clear();
+  DeviceInfo* dev = nullptr;
+  const int rc = current_device(&dev);
+  if (rc != TPMLP_OK) return rc;
+  if (dev->generation != g_prof_generation) {
+    g_prof_events.clear();  // events of another context: not reused, not destroyed
+    g_prof_generation = dev->generation;
+  }
   g_prof_on = true;
   return TPMLP_OK;
 }
@@ -533,6 +578,12 @@ size_t tpmlp_workspace_size(int64_t s, int64_t b, int64_t h, int64_t f, int tp, 
   return ws_layout(k).total;
 }
 
+size_t tpmlp_forward_workspace_size(int64_t s, int64_t b, int64_t h, int64_t f, int tp, int sp, int dtype, int act,
+                                    int mode) {
+  size_t bytes = 0;
+  return forward_workspace_bytes(s, b, h, f, tp, sp, dtype, act, mode, &bytes) == TPMLP_OK ? bytes : 0;
+}
+
 int tpmlp_forward(int64_t s, int64_t b, int64_t h, int64_t f, int tp, int sp, int dtype, int act, int mode,
                   const void* const* x, const void* w1, const void* w2, void* u, void* y, void* const* z,
                   void* ws, size_t ws_bytes, void* stream) {
@@ -544,7 +595,7 @@ int tpmlp_forward(int64_t s, int64_t b, int64_t h, int64_t f, int tp, int sp, in
   if ((rc = check_ptrs(x, nio, al, "x")) || (rc = check_ptr(w1, al, "w1")) || (rc = check_ptr(w2, al, "w2")) ||
       (rc = check_ptr(u, al, "u")) || (rc = check_ptr(y, al, "y")) || (rc = check_ptrs(z, nio, al, "z")))
     return rc;
-  const WsLayout L = ws_layout(k);
+  const WsLayout L = ws_layout(k, /*forward=*/true);
   if (L.total > 0) {
     if (ws == nullptr || ws_bytes < L.total)
       return set_error(TPMLP_ERR_WORKSPACE, "workspace needs " + std::to_string(L.total) + " bytes");

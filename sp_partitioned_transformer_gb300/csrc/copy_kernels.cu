@@ -121,12 +121,12 @@ int launch_copy_chunks(const void* const* src, void* const* dst, int n, int64_t 
   const int ph = prof_begin(PROF_COPY, st);
   if ((align_or & 15u) == 0) {
     // 16-byte aligned chunks: TMA bulk copies, 3 single-thread CTAs per SM
-    static bool attr_set[64] = {};
-    if (dev->device >= 0 && dev->device < 64 && !attr_set[dev->device]) {
+    static uint64_t attr_gen[64] = {};  // the device context the attribute was set in
+    if (dev->device >= 0 && dev->device < 64 && attr_gen[dev->device] != dev->generation) {
       const cudaError_t e = cudaFuncSetAttribute(copy_chunks_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  2 * BULK_SLAB);
       if (e != cudaSuccess) return set_error(TPMLP_ERR_CUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
-      attr_set[dev->device] = true;
+      attr_gen[dev->device] = dev->generation;
     }
     const int64_t spc = (bytes + BULK_SLAB - 1) / BULK_SLAB;
     const int64_t total = spc * n;

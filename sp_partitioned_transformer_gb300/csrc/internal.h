@@ -16,14 +16,21 @@ namespace tpmlp {
 int set_error(int code, const std::string& msg);
 
 // Per-device state (SM count, address of the device status word, timeout).
+// It belongs to one CUDA context of the device: when the caller tears the
+// context down (cudaDeviceReset) and a new one takes its place, the next
+// current_device() call refreshes it and gives it a new `generation`, and
+// every cache keyed on a device (kernel attributes, streams, symbol addresses)
+// compares that number before it reuses what it holds.
 struct DeviceInfo {
   int device = -1;
   int num_sms = 0;
   unsigned* status = nullptr;  // device address of the status word
   size_t max_smem_optin = 0;
   size_t smem_per_sm = 0;  // shared memory of one SM (all resident CTAs)
+  unsigned long long ctx_id = 0;  // unique id of the context (cuCtxGetId)
+  uint64_t generation = 0;        // > 0; process-wide, changes with the context
 };
-// Returns TPMLP_OK and fills `info` for the current device.
+// Returns TPMLP_OK and fills `info` for the current device and its context.
 int current_device(DeviceInfo** info);
 uint64_t wait_timeout_ns();
 

@@ -26,23 +26,29 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
 std::mutex g_mu;
 void* g_scratch_addr[64] = {};
+uint64_t g_scratch_gen[64] = {};  // the device context each address belongs to
 
-// Device address of the scratch array on the current device, looked up once per
-// device (the first call on each device does this lookup).
+// Device address of the scratch array in the current device's context.  The
+// lookup runs on the first call in each context of a device — the first call
+// on a device, and the first after the caller replaced its context (for
+// example by cudaDeviceReset), since an address from a torn-down context must
+// never reach a kernel.  Make that first call before any stream capture.
 int scratch_address(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return set_error(TPMLP_ERR_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(e));
-  if (dev < 0 || dev >= 64) return set_error(TPMLP_ERR_CUDA, "device ordinal out of range");
+  DeviceInfo* dev = nullptr;
+  int rc = current_device(&dev);
+  if (rc != TPMLP_OK) return rc;
+  const int d = dev->device;
+  if (d < 0 || d >= 64) return set_error(TPMLP_ERR_CUDA, "device ordinal out of range");
   std::lock_guard<std::mutex> lk(g_mu);
-  if (g_scratch_addr[dev] == nullptr) {
+  if (g_scratch_addr[d] == nullptr || g_scratch_gen[d] != dev->generation) {
     void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess || p == nullptr)
       return set_error(TPMLP_ERR_CUDA, std::string("cudaGetSymbolAddress(scratch): ") + cudaGetErrorString(e));
-    g_scratch_addr[dev] = p;
+    g_scratch_addr[d] = p;
+    g_scratch_gen[d] = dev->generation;
   }
-  *out = g_scratch_addr[dev];
+  *out = g_scratch_addr[d];
   return TPMLP_OK;
 }
 
