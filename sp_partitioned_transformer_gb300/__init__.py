@@ -6,7 +6,7 @@ library has not been built, ``load()`` raises; there is no fallback path.
 
 Entry points mirror the C ABI in ``include/tpmlp.h``:
 
-* ``workspace_size``, ``forward``, ``backward``
+* ``workspace_size``, ``forward_workspace_size``, ``forward``, ``backward``
 * ``split_dim0``, ``gather_dim0``, ``reduce_scatter_dim0``
 * ``last_error``, ``device_status``, ``set_wait_timeout_ns``, ``wait_timeout_selftest``
 
@@ -30,6 +30,7 @@ __all__ = [
     "ACT",
     "MODE",
     "workspace_size",
+    "forward_workspace_size",
     "forward",
     "forward_noalloc",
     "NOALLOC_SCRATCH_BYTES",
@@ -115,6 +116,8 @@ def load(path: str | None = None):
     lib.tpmlp_last_error.argtypes = []
     lib.tpmlp_workspace_size.restype = sz
     lib.tpmlp_workspace_size.argtypes = [i64, i64, i64, i64, i32, i32, i32, i32, i32]
+    lib.tpmlp_forward_workspace_size.restype = sz
+    lib.tpmlp_forward_workspace_size.argtypes = [i64, i64, i64, i64, i32, i32, i32, i32, i32]
     lib.tpmlp_forward.restype = i32
     lib.tpmlp_forward.argtypes = [i64, i64, i64, i64, i32, i32, i32, i32, i32,
                                   vpp, vp, vp, vp, vp, vpp, vp, sz, vp]
@@ -220,6 +223,11 @@ def last_error() -> str:
 
 def workspace_size(s, b, h, f, tp, sp, dtype, act="gelu", mode="fused") -> int:
     return int(load().tpmlp_workspace_size(s, b, h, f, tp, int(sp), _dtype_code(dtype), ACT[act], MODE[mode]))
+
+
+def forward_workspace_size(s, b, h, f, tp, sp, dtype, act="gelu", mode="fused") -> int:
+    return int(load().tpmlp_forward_workspace_size(s, b, h, f, tp, int(sp), _dtype_code(dtype), ACT[act],
+                                                   MODE[mode]))
 
 
 def forward(x, w1, w2, u, y, z, *, s, b, h, f, tp, sp, act="gelu", mode="fused", workspace=None,

@@ -117,6 +117,29 @@ def test_forward_rejects_bad_arguments_on_the_host(lib):
     assert _fwd(lib, mode=0, ws=FAKE + 16, ws_bytes=1 << 30) == UNSUP  # ws must be 256-byte aligned
 
 
+def test_forward_workspace_leaves_out_the_backward_dz_slot(lib):
+    """The forward gathers only X: its workspace is the gathered X (when SP
+    chunks are not whole 128-row blocks) plus, in PARTIALS mode, the tp float32
+    partials; the backward also gathers dZ.  (That tpmlp_forward runs on
+    exactly the forward's size is checked on the GPU, by the allocation-free
+    forward whose built-in scratch sits between the two sizes.)"""
+    fws = lib.tpmlp_forward_workspace_size
+    fws.restype = ctypes.c_size_t
+    fws.argtypes = [ctypes.c_int64] * 4 + [ctypes.c_int] * 5
+    M, h = 96 * 2, 136
+    g = ((M * h * 2 + 255) // 256) * 256
+    p = 2 * M * h * 4
+    assert fws(96, 2, 136, 272, 2, 1, 2, 0, 1) == g
+    assert _ws(lib, 96, 2, 136, 272, 2, 1, 2, 0, 1) == 2 * g
+    assert fws(96, 2, 136, 272, 2, 1, 2, 0, 0) == g + p
+    assert _ws(lib, 96, 2, 136, 272, 2, 1, 2, 0, 0) == 2 * g + p
+    assert fws(512, 4, 1024, 4096, 4, 1, 2, 0, 1) == 0  # chunks read in place
+    assert fws(16, 2, 64, 250, 4, 0, 0, 0, 1) == 0  # invalid -> 0
+    # one byte less than the forward's size is refused before anything runs
+    assert _fwd(lib, s=96, b=2, h=136, f=272, sp=1, ws=FAKE * 256, ws_bytes=g - 1) == WORKSPACE
+    assert str(g).encode() in lib.tpmlp_last_error()
+
+
 def test_backward_and_dim0_ops_reject_bad_arguments(lib):
     vp1 = _vp(FAKE)
     rc = lib.tpmlp_backward(16, 2, 64, 256, 2, 0, 2, 0, 1, vp1, FAKE, FAKE, FAKE, FAKE, vp1, _vp(None), FAKE,

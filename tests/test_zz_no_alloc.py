@@ -23,6 +23,10 @@ CASES = [
     (CONFIGS["tpsp4_bf16"], "fused"),
     # SwiGLU with SP, ragged shapes, fp16
     (BlockConfig("nz", 96, 2, 136, 288, 4, True, "f16", "swiglu"), "partials"),
+    # 765-token SP chunks (not whole 128-row blocks): the forward gathers X into
+    # ≈47.8 MiB of scratch, which fits, while forward and backward together
+    # (X and dZ gathered) would need ≈95.6 MiB, which does not
+    (BlockConfig("between", 6120, 1, 4096, 2048, 8, True, "bf16", "gelu"), "fused"),
 ]
 
 
@@ -41,6 +45,11 @@ def _cat(z, sp):
 @pytest.mark.parametrize("cfg,mode", CASES, ids=[f"{c.name}-{m}" for c, m in CASES])
 def test_noalloc_forward_matches_workspace_forward_twice(cuda_lib, cfg, mode):
     tpmlp = cuda_lib
+    need = tpmlp.forward_workspace_size(cfg.s, cfg.b, cfg.h, cfg.f, cfg.tp, cfg.sp, cfg.torch_dtype, cfg.act, mode)
+    assert need <= tpmlp.NOALLOC_SCRATCH_BYTES
+    if cfg.name == "between":
+        assert tpmlp.workspace_size(cfg.s, cfg.b, cfg.h, cfg.f, cfg.tp, cfg.sp, cfg.torch_dtype, cfg.act,
+                                    mode) > tpmlp.NOALLOC_SCRATCH_BYTES
     for call, seed in enumerate((101, 202)):
         t = block_inputs(cfg, seed=seed)
         blk, x, W1, W2, ref = _run_reference_forward(tpmlp, cfg, mode, t)
@@ -63,10 +72,14 @@ def test_noalloc_forward_matches_workspace_forward_twice(cuda_lib, cfg, mode):
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch(cuda_lib):
-    """The 22B-width TP+SP config in PARTIALS mode needs ≈0.9 GB of scratch."""
+    """The 22B-width TP+SP config in PARTIALS mode needs 8·4096·6144·4 bytes
+    (≈0.8 GB) of scratch for its float32 partials; its SP chunks are read in
+    place, so no gathered X adds to that."""
     tpmlp = cuda_lib
     cfg = CONFIGS["w22b_tpsp8_bf16"]
-    need = tpmlp.workspace_size(cfg.s, cfg.b, cfg.h, cfg.f, cfg.tp, cfg.sp, cfg.torch_dtype, cfg.act, "partials")
+    need = tpmlp.forward_workspace_size(cfg.s, cfg.b, cfg.h, cfg.f, cfg.tp, cfg.sp, cfg.torch_dtype, cfg.act,
+                                        "partials")
+    assert need == 8 * 4096 * 6144 * 4
     assert need > tpmlp.NOALLOC_SCRATCH_BYTES
     lib = tpmlp.load()
     fake = 1 << 20  # never dereferenced: the size check fails first
