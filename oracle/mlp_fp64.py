@@ -458,7 +458,8 @@ def _f64(a):
 
 
 def sampled_reference(X, W1, W2, dZ, act, rows, feats, chunk=4096):
-    """Z[rows], dX[rows], dW1[feature rows], dW2[:, feats] of ``mlp_backward``.
+    """Z[rows], dX[rows], U[rows], Y[rows], dU[rows], dW1[feature rows] and
+    dW2[:, feats] of ``mlp_backward``.
 
     X, dZ: [M, h]; W1: [fc1_rows, h]; W2: [h, f]; any float dtype (converted to
     fp64 slice by slice).  ``feats`` index the ffn width f (F for SwiGLU; the
@@ -498,8 +499,8 @@ def sampled_reference(X, W1, W2, dZ, act, rows, feats, chunk=4096):
     dUc = act_backward(Uc, dYc, act)
     dW1_rows = dUc.T @ Xf
     dW2_cols = dZf.T @ Yc
-    return {"Z_rows": Zr, "dX_rows": dXr, "dW1_rows": dW1_rows, "dW1_row_index": w1_rows,
-            "dW2_cols": dW2_cols}
+    return {"Z_rows": Zr, "dX_rows": dXr, "U_rows": Ur, "Y_rows": Yr, "dU_rows": dUr,
+            "dW1_rows": dW1_rows, "dW1_row_index": w1_rows, "dW2_cols": dW2_cols}
 
 
 # --------------------------------------------------------------------------

@@ -1,9 +1,11 @@
 """Parity at the five workload configurations, in the launch configuration the
 benchmark times.  The tiny and TP+SP configurations are compared element by
-element against the full fp64 oracle; at the 8.3B, 22B and Llama-70B widths the
-oracle computes sampled token rows (Z, dX) and sampled ffn features (rows of
-dW1, columns of dW2) one by one, plus the fused/partials cross-check on every
-element."""
+element against the full fp64 oracle.  At the 8.3B, 22B and Llama-70B widths the
+oracle computes sampled token rows (whole rows of Z, dX, U, Y and dU) and
+sampled ffn features (rows of dW1, columns of dW2) one by one.  The samples take
+at least one token in every 256-row block and one feature in every 256-column
+block, so every 256×256 output tile of all six GEMMs holds elements compared with
+the oracle; the fused/partials cross-check then covers every element."""
 import numpy as np
 import pytest
 import torch
@@ -29,14 +31,29 @@ def test_small_configs_full_parity(cuda_lib, name, mode):
     print(name, mode, errs)
 
 
-def _sample_indices(n, k, seed, chunk=None):
+TILE = 256  # the pair GEMM's output tile is 256 × 256
+
+
+def _sample_indices(n, seed, chunk=None, tile=TILE):
+    """One random index inside every `tile`-wide block of [0, n), the first and
+    last index, and both sides of every `chunk` boundary (SP chunks, TP shards)."""
     rng = np.random.default_rng(seed)
-    idx = set(rng.choice(n, size=min(k, n), replace=False).tolist())
+    idx = {int(lo + rng.integers(0, min(tile, n - lo))) for lo in range(0, n, tile)}
     idx |= {0, n - 1}
     if chunk:
         for j in range(1, n // chunk):
             idx |= {j * chunk - 1, j * chunk}
     return np.array(sorted(idx))
+
+
+def test_samples_hit_every_tile():
+    rows = _sample_indices(8192, 1, chunk=1024)
+    assert len({r // TILE for r in rows}) == 8192 // TILE
+    feats = _sample_indices(28672, 2, chunk=3584)
+    assert len({f // TILE for f in feats}) == 28672 // TILE
+    assert {3583, 3584, 0, 28671} <= set(feats.tolist())
+    ragged = _sample_indices(300, 3)
+    assert len({r // TILE for r in ragged}) == 2 and 299 in ragged
 
 
 @pytest.mark.parametrize("name", ["w8p3b_tp8_f16", "w22b_tpsp8_bf16", "llama70b_swiglu_tpsp8_bf16"])
@@ -46,8 +63,8 @@ def test_large_configs_sampled_parity(cuda_lib, name):
     dt = _dt(cfg)
     M = cfg.M
     fused = run_block(cuda_lib, inp, cfg.s, cfg.b, cfg.h, cfg.f, cfg.tp, cfg.sp, cfg.act, "fused", dt)
-    rows = _sample_indices(M, 12, 1, chunk=M // cfg.tp)  # includes the SP chunk boundaries
-    feats = _sample_indices(cfg.f, 12, 2, chunk=cfg.f // cfg.tp)  # includes the TP shard boundaries
+    rows = _sample_indices(M, 1, chunk=M // cfg.tp)  # every 256-row block, the SP chunk boundaries
+    feats = _sample_indices(cfg.f, 2, chunk=cfg.f // cfg.tp)  # every 256-column block, the TP shard boundaries
     X = inp["X"].float().numpy().reshape(M, cfg.h)
     dZ = inp["dZ"].float().numpy().reshape(M, cfg.h)
     ref = O.sampled_reference(X, inp["W1"].float().numpy(), inp["W2"].float().numpy(), dZ, cfg.act, rows, feats)
@@ -56,8 +73,11 @@ def test_large_configs_sampled_parity(cuda_lib, name):
         "dX": rel_err(fused["dX"][rows], ref["dX_rows"]),
         "dW1": rel_err(fused["dW1"][ref["dW1_row_index"]], ref["dW1_rows"]),
         "dW2": rel_err(fused["dW2"][:, feats], ref["dW2_cols"]),
+        "U": rel_err(fused["U"][rows], ref["U_rows"]),
+        "Y": rel_err(fused["Y"][rows], ref["Y_rows"]),
+        "dU": rel_err(fused["dU"][rows], ref["dU_rows"]),
     }
-    print(name, "fused sampled", errs)
+    print(name, "fused sampled", len(rows), "rows", len(feats), "features", errs)
     assert all(e <= TOL[dt] for e in errs.values()), errs
     for k in ("Z", "dX", "dW1", "dW2", "U", "Y", "dU"):
         assert np.isfinite(fused[k]).all(), k
