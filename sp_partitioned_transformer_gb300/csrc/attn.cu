@@ -12,14 +12,19 @@
 // tensor memory) and a small Δ kernel.  Each tcgen05 CTA has 12 warps: warp 0
 // issues TMA loads, warp 1 issues the MMAs, warp 2 owns the tensor-memory
 // allocation and warps 4–11 are two groups of four element-wise warps, one
-// thread per row of the 128-row tile, the groups splitting its columns.
+// thread per row of a 128-row tile (in the forward each group owns one of the
+// CTA's two query tiles; in dK/dV the groups split a tile's columns).
 //
-//   attn_fwd_kernel   per (128-query tile, head, sequence): S = Q·Kᵀ into one of
-//                     two TMEM buffers (the next S is computed while the softmax
-//                     works on this one), streaming softmax in base 2, P written
-//                     to shared memory as a 128-byte-swizzled operand, O += P·V in
-//                     TMEM, O rescaled in TMEM only when a warp's row maximum
-//                     moved; O and the row log-sum-exp (lse2) written at the end.
+//   attn_fwd_kernel   per (pair of 128-query tiles A and B, head, sequence):
+//                     K and V tiles stream through 2-deep TMA rings; the issuing
+//                     lane alternates S_A = Q_A·Kᵀ, P_B·V, S_B = Q_B·Kᵀ, P_A·V,
+//                     so one element-wise group's softmax (base 2, streaming)
+//                     overlaps the other tile's MMAs; P is written back into
+//                     TMEM over its own S columns and is the A operand of
+//                     O += P·V from there; O is rescaled in TMEM only when a
+//                     tile's probabilities would pass 2^15 against the running
+//                     reference maximum; O and the row log-sum-exp (lse2) are
+//                     written at the end.
 //   attn_bwd_dkdv_kernel  per (128-key tile, head, sequence), over 64-query tiles:
 //                     Sᵀ = K·Qᵀ and dPᵀ = V·dOᵀ, Pᵀ = 2^(Sᵀ·c − lse2),
 //                     dSᵀ = Pᵀ ⊙ (dPᵀ − Δ), dV += Pᵀ·dO, dK += dSᵀ·Q; each
