@@ -8,11 +8,13 @@
 // The LayerNorm's outputs are the chunks the block's fc1 reads in place (the
 // all-gather fused into its loads), so no gathered copy of the activation is
 // ever made.  Everything here is token-wise and HBM-bound:
-//   ln_fwd_stream_kernel  persistent CTAs stream token rows through a TMA-bulk
-//                         shared-memory ring (h >= 1024, 16-byte aligned rows):
-//                         mean, variance (two passes over the staged row),
-//                         normalise + affine, save mean/rstd;
-//   ln_bwd_stream_kernel  the same ring over (x, dy[, dx]) rows:
+//   ln_fwd_warp_kernel    16-bit rows up to h = 8192: one warp per row, each
+//                         warp's row brought in by TMA bulk copies into its own
+//                         slot and held in registers; one-pass shifted
+//                         statistics, normalise + affine, save mean/rstd;
+//   ln_fwd_stream_kernel  float32 rows (h >= 1024, 16-byte aligned): persistent
+//                         CTAs stream rows through a TMA-bulk shared-memory ring;
+//   ln_bwd_stream_kernel  the same ring over (x, dy) rows:
 //                         dx = rstd·(g − mean(g) − x̂·mean(g·x̂)), g = dy·γ, written
 //                         or added to the residual gradient, and each CTA's dγ, dβ
 //                         partial sums over its rows; ln_bwd_reduce_parts_kernel
@@ -136,6 +138,74 @@ __global__ void __launch_bounds__(256) ln_fwd_kernel(ChunkSet cs, const void* __
   }
 }
 
+// ------------------------------------------------------------------ rows held in registers
+// 16-bit rows up to h = 8192 as NV 8-element vectors a lane (lane l owns the
+// vectors l, l + 32, …), kept packed: at most 128 data registers a thread.
+constexpr int REG_MAX_NV = 32;
+
+// 8 packed 16-bit values -> 4 float pairs.
+template <int DT>
+__device__ __forceinline__ void unpack8_pairs(const uint4& r, float2* f) {
+  const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if constexpr (DT == DT_BF16)
+      f[i] = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+    else
+      f[i] = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+  }
+}
+
+// The same conversion as volatile asm: the compiler converts again at every
+// use and cannot hoist conversions ahead, which keeps the backward's registers
+// (row vectors, dγ/dβ accumulators) within two CTAs per SM.
+template <int DT>
+__device__ __forceinline__ void unpack8_pairs_v(const uint4& r, float2* f) {
+  const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if constexpr (DT == DT_BF16) {
+      // a bf16 is the upper half of the float with the same value
+      uint32_t lo, hi;
+      asm volatile("{\n\tshl.b32 %0, %2, 16;\n\tand.b32 %1, %2, 0xffff0000;\n\t}" : "=r"(lo), "=r"(hi) : "r"(w[i]));
+      f[i] = make_float2(__uint_as_float(lo), __uint_as_float(hi));
+    } else {
+      float a, b;
+      asm volatile("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+                   : "=f"(a), "=f"(b)
+                   : "r"(w[i]));
+      f[i] = make_float2(a, b);
+    }
+  }
+}
+
+// An optimisation barrier on a row held in registers: the compiler must assume
+// the packed values changed, so it converts them again at their next use
+// instead of keeping every converted float of the row live (which would double
+// the registers a row needs).  It emits no instruction.
+template <int NV>
+__device__ __forceinline__ void reg_fence(uint4 (&v)[NV]) {
+#pragma unroll
+  for (int k = 0; k < NV; ++k) asm volatile("" : "+r"(v[k].x), "+r"(v[k].y), "+r"(v[k].z), "+r"(v[k].w));
+}
+
+template <int DT>
+__device__ __forceinline__ uint4 pack8_pairs(const float2* f) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if constexpr (DT == DT_BF16) {
+      const __nv_bfloat162 b = __float22bfloat162_rn(f[i]);
+      w[i] = *reinterpret_cast<const uint32_t*>(&b);
+    } else {
+      const __half2 b = __float22half2_rn(f[i]);
+      w[i] = *reinterpret_cast<const uint32_t*>(&b);
+    }
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+
 // ------------------------------------------------------------------ streamed row kernels
 // Persistent CTAs of 256 threads; CTA g takes the token rows g, g + G, g + 2G, ...
 // (G = grid size).  Thread 0 keeps the CTA's next S rows in flight with TMA bulk
@@ -181,13 +251,14 @@ __device__ __forceinline__ void stage8(uint8_t* row, const void* src, int vi) {
 // Sum of (a, b) over the CTA; the fixed shuffle/warp order makes it
 // deterministic.  red[] must be free (a __syncthreads since its last read):
 // one barrier.
+template <int THREADS = STREAM_THREADS>
 __device__ __forceinline__ float2 block_sum2_free(float a, float b, float2* red) {
   a = warp_sum(a);
   b = warp_sum(b);
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (lane == 0) red[w] = make_float2(a, b);
   __syncthreads();
-  const float2 t = lane < STREAM_THREADS / 32 ? red[lane] : make_float2(0.0f, 0.0f);
+  const float2 t = lane < THREADS / 32 ? red[lane] : make_float2(0.0f, 0.0f);
   return make_float2(warp_sum(t.x), warp_sum(t.y));
 }
 
@@ -226,6 +297,171 @@ __device__ __forceinline__ void ring_drain(const RowRing& ring, uint64_t* full, 
 }
 
 __host__ __device__ __forceinline__ uint32_t pad128(uint32_t x) { return (x + 127u) & ~127u; }
+
+// ------------------------------------------------------------------ LN forward, one warp per row
+// Persistent CTAs of `wpc` warps, one per SM.  Warp w of CTA c takes the rows
+// g, g + W, g + 2W, … (g = c·wpc + w, W = all warps of the grid).  Each warp
+// owns one shared-memory slot: a TMA bulk copy (issued by lane 0) brings row k
+// into it, the lanes copy the row into registers (NV packed vectors a lane) and
+// at once lane 0 refills the slot with row k + 1, whose load then overlaps row
+// k's arithmetic.  γ and β are staged in shared memory once per CTA (the only
+// block barrier).  Statistics take one pass over the registers:
+// the shifted sums Σ(x − c), Σ(x − c)² with c the row's first element (which
+// keeps the variance when the mean is large against the spread), two warp
+// reductions, then y = (x − μ)·rstd·γ + β.  EXACT: h = 256·NV, so every lane
+// owns exactly NV vectors and no vector is predicated.
+template <int NV>
+struct LnFwdShape {
+  static constexpr int MAX_WARPS = NV <= 24 ? 16 : 8;  // registers: 128 (NV ≤ 24) or 255 a thread
+};
+
+template <int DT, int NV, bool EXACT>
+__global__ void __launch_bounds__(32 * LnFwdShape<NV>::MAX_WARPS, 1)
+    ln_fwd_warp_kernel(ChunkSet cs, const void* __restrict__ gamma, const void* __restrict__ beta, float eps,
+                       float* __restrict__ mean, float* __restrict__ rstd, int64_t M, int64_t h, int64_t rpc,
+                       unsigned* status, uint64_t timeout_ns) {
+  static_assert(DT != DT_F32 && NV >= 1 && NV <= REG_MAX_NV, "16-bit rows of at most 32 vectors a lane");
+  using T = typename Storage<DT>::T;
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t full[LnFwdShape<NV>::MAX_WARPS];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int wpc = blockDim.x >> 5;
+  const int nv = static_cast<int>(h / 8);
+  const uint32_t rb = static_cast<uint32_t>(h * sizeof(T));
+  uint4* gs = reinterpret_cast<uint4*>(smem);  // γ, β (16-bit, as stored)
+  uint4* bs = reinterpret_cast<uint4*>(smem + pad128(rb));
+  uint8_t* slot = smem + 2 * pad128(rb) + static_cast<size_t>(w) * pad128(rb);
+  const uint32_t bar = smem_u32(&full[w]);
+  const int64_t W = static_cast<int64_t>(gridDim.x) * wpc;
+  const int64_t g = static_cast<int64_t>(blockIdx.x) * wpc + w;
+  const int64_t cnt = g < M ? (M - g + W - 1) / W : 0;
+  auto issue = [&](int64_t k) {  // lane 0: row g + k·W into the slot
+    const int64_t m = g + k * W;
+    const int64_t jj = m / rpc;
+    mbar_arrive_expect_tx(bar, rb);
+    bulk_g2s(smem_u32(slot), static_cast<const uint8_t*>(cs.in[jj]) + (m - jj * rpc) * h * static_cast<int64_t>(sizeof(T)),
+             rb, bar);
+  };
+  if (lane == 0) {
+    mbar_init(bar, 1);
+    fence_barrier_init();
+    if (cnt > 0) issue(0);
+  }
+  for (int vi = threadIdx.x; vi < nv; vi += blockDim.x) {
+    gs[vi] = __ldg(static_cast<const uint4*>(gamma) + vi);
+    bs[vi] = __ldg(static_cast<const uint4*>(beta) + vi);
+  }
+  __syncthreads();
+  const float inv_h = 1.0f / static_cast<float>(h);
+  for (int64_t k = 0; k < cnt; ++k) {
+    // every lane waits (acquiring the bulk copy's bytes itself); all give up together
+    const bool ok = mbar_wait_bounded(bar, static_cast<uint32_t>(k & 1), nullptr, status, timeout_ns);
+    if (!__all_sync(0xffffffffu, ok)) {
+      if (lane == 0) (void)mbar_wait_bounded(bar, static_cast<uint32_t>(k & 1), nullptr, nullptr, timeout_ns);
+      return;
+    }
+    uint4 v[NV];
+    const uint4* row = reinterpret_cast<const uint4*>(slot);
+#pragma unroll
+    for (int kk = 0; kk < NV; ++kk) {
+      const int vi = lane + 32 * kk;
+      v[kk] = (EXACT || vi < nv) ? row[vi] : make_uint4(0u, 0u, 0u, 0u);
+    }
+    __syncwarp();  // every lane has copied the row out of the slot
+    if (lane == 0 && k + 1 < cnt) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      issue(k + 1);
+    }
+    // c = the row's first element (lane 0's first value)
+    float c;
+    {
+      float2 f0[4];
+      unpack8_pairs<DT>(v[0], f0);
+      c = __shfl_sync(0xffffffffu, f0[0].x, 0);
+    }
+    const float2 nc2 = make_float2(-c, -c);
+    float2 s1 = make_float2(0.0f, 0.0f), s2 = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int kk = 0; kk < NV; ++kk) {
+      if (EXACT || lane + 32 * kk < nv) {
+        float2 f[4];
+        unpack8_pairs<DT>(v[kk], f);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 d = __fadd2_rn(f[i], nc2);
+          s1 = __fadd2_rn(s1, d);
+          s2 = __ffma2_rn(d, d, s2);
+        }
+      }
+    }
+    const float dm = warp_sum(s1.x + s1.y) * inv_h;
+    const float var = fmaxf(warp_sum(s2.x + s2.y) * inv_h - dm * dm, 0.0f);
+    const float mu = c + dm;
+    const float r = 1.0f / sqrtf(var + eps);
+    reg_fence(v);
+    // y = (x·r − μ·r)·γ + β
+    const float2 r2 = make_float2(r, r);
+    const float2 nmr2 = make_float2(-mu * r, -mu * r);
+    const int64_t m = g + k * W;
+    const int64_t jj = m / rpc;
+    uint4* y = reinterpret_cast<uint4*>(static_cast<T*>(cs.out[jj]) + (m - jj * rpc) * h);
+#pragma unroll
+    for (int kk = 0; kk < NV; ++kk) {
+      const int vi = lane + 32 * kk;
+      if (EXACT || vi < nv) {
+        float2 f[4], gg[4], bbv[4], o[4];
+        unpack8_pairs<DT>(v[kk], f);
+        unpack8_pairs<DT>(gs[vi], gg);
+        unpack8_pairs<DT>(bs[vi], bbv);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[i] = __ffma2_rn(__ffma2_rn(f[i], r2, nmr2), gg[i], bbv[i]);
+        y[vi] = pack8_pairs<DT>(o);
+      }
+    }
+    if (lane == 0) {
+      mean[m] = mu;
+      rstd[m] = r;
+    }
+  }
+}
+
+template <int DT, int NV>
+bool ln_fwd_warp_nv(const ChunkSet& cs, const void* gamma, const void* beta, float eps, float* mean, float* rstd,
+                    int64_t M, int64_t h, int64_t rpc, cudaStream_t st) {
+  DeviceInfo* dev = nullptr;
+  if (current_device(&dev) != TPMLP_OK || dev == nullptr) return false;
+  const size_t slot = pad128(static_cast<uint32_t>(h * 2));
+  const size_t fixed = 2 * slot;  // γ and β
+  const size_t cap = dev->max_smem_optin > 1024 ? dev->max_smem_optin - 1024 : 0;  // static shared memory
+  if (cap <= fixed) return false;
+  const int wpc = static_cast<int>(std::min<size_t>(LnFwdShape<NV>::MAX_WARPS, (cap - fixed) / slot));
+  if (wpc < 1) return false;
+  const size_t smem = fixed + static_cast<size_t>(wpc) * slot;
+  const bool exact = h == 256 * NV;
+  auto* fn = exact ? ln_fwd_warp_kernel<DT, NV, true> : ln_fwd_warp_kernel<DT, NV, false>;
+  // (always set: the kernel's static shared memory counts against the default 48 KB too)
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  // one CTA per SM, and no more warps than rows
+  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(dev->num_sms, (M + wpc - 1) / wpc)));
+  fn<<<grid, 32 * wpc, smem, st>>>(cs, gamma, beta, eps, mean, rstd, M, h, rpc, dev->status, wait_timeout_ns());
+  return true;
+}
+
+template <int DT>
+bool ln_fwd_registers(const ChunkSet& cs, const void* gamma, const void* beta, float eps, float* mean, float* rstd,
+                      int64_t M, int64_t h, int64_t rpc, cudaStream_t st) {
+  const int64_t per_lane = (h / 8 + 31) / 32;
+  if (per_lane <= 4) return ln_fwd_warp_nv<DT, 4>(cs, gamma, beta, eps, mean, rstd, M, h, rpc, st);
+  if (per_lane <= 8) return ln_fwd_warp_nv<DT, 8>(cs, gamma, beta, eps, mean, rstd, M, h, rpc, st);
+  if (per_lane <= 12) return ln_fwd_warp_nv<DT, 12>(cs, gamma, beta, eps, mean, rstd, M, h, rpc, st);
+  if (per_lane <= 16) return ln_fwd_warp_nv<DT, 16>(cs, gamma, beta, eps, mean, rstd, M, h, rpc, st);
+  if (per_lane <= 24) return ln_fwd_warp_nv<DT, 24>(cs, gamma, beta, eps, mean, rstd, M, h, rpc, st);
+  if (per_lane <= REG_MAX_NV) return ln_fwd_warp_nv<DT, 32>(cs, gamma, beta, eps, mean, rstd, M, h, rpc, st);
+  return false;
+}
 
 // Shared memory: [γ | β | ring of S slots of one x row].
 template <int DT, int V>
@@ -331,30 +567,61 @@ __global__ void __launch_bounds__(STREAM_THREADS) ln_fwd_stream_kernel(ChunkSet 
 // dx = rstd·(g − mean(g) − x̂·mean(g·x̂)), g = dy·γ, written or added to dx; and
 // this CTA's partial sums of dγ = Σ dy·x̂ and dβ = Σ dy over its rows, in row
 // order, stored as part[blockIdx.x][:] and part[G + blockIdx.x][:].
-// Shared memory: [γ | ring of S slots of (x, dy[, dx]) rows].
-template <int DT, int V>
-__global__ void __launch_bounds__(STREAM_THREADS) ln_bwd_stream_kernel(ChunkSet cs, const void* __restrict__ gamma,
+// Shared memory: a ring of S slots of (x, dy) rows; thread 0 keeps S − 1 rows
+// in flight while one is computed.  Each thread keeps its vectors of γ in
+// registers for the whole kernel and, per row, its vectors of x and dy (copied
+// out of the slot once) and of the dx being accumulated into (read from global
+// memory at the start of the row, so the load overlaps the row's first barrier
+// and its reduction); the element-wise math runs on float pairs.
+template <int DT>
+__device__ __forceinline__ void raw_to_pairs(const uint4* raw, float2* f) {
+  if constexpr (DT == DT_F32) {
+    f[0] = make_float2(__uint_as_float(raw[0].x), __uint_as_float(raw[0].y));
+    f[1] = make_float2(__uint_as_float(raw[0].z), __uint_as_float(raw[0].w));
+    f[2] = make_float2(__uint_as_float(raw[1].x), __uint_as_float(raw[1].y));
+    f[3] = make_float2(__uint_as_float(raw[1].z), __uint_as_float(raw[1].w));
+  } else {
+    unpack8_pairs_v<DT>(raw[0], f);
+  }
+}
+template <int DT>
+__device__ __forceinline__ void pairs_to_raw(const float2* f, uint4* raw) {
+  if constexpr (DT == DT_F32) {
+    raw[0] = make_uint4(__float_as_uint(f[0].x), __float_as_uint(f[0].y), __float_as_uint(f[1].x),
+                        __float_as_uint(f[1].y));
+    raw[1] = make_uint4(__float_as_uint(f[2].x), __float_as_uint(f[2].y), __float_as_uint(f[3].x),
+                        __float_as_uint(f[3].y));
+  } else {
+    raw[0] = pack8_pairs<DT>(f);
+  }
+}
+
+template <int DT, int V, int THREADS>
+__global__ void __launch_bounds__(THREADS, (THREADS == 256 ? 2 : 1)) ln_bwd_stream_kernel(ChunkSet cs, const void* __restrict__ gamma,
                                                                        const float* __restrict__ mean,
                                                                        const float* __restrict__ rstd, int accumulate,
                                                                        float* __restrict__ part, int64_t M, int64_t h,
                                                                        int64_t rpc, int S, unsigned* status,
                                                                        uint64_t timeout_ns) {
   using T = typename Storage<DT>::T;
+  constexpr int RAW = DT == DT_F32 ? 2 : 1;  // 16-byte units of an 8-element vector
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t full[STREAM_MAX_SLOTS];
-  __shared__ float2 red[STREAM_THREADS / 32];
+  __shared__ float2 red[THREADS / 32];
   __shared__ int abort_flag;
   const int tid = threadIdx.x;
   const int nv = static_cast<int>(h / 8);
   const uint32_t rb = static_cast<uint32_t>(h * sizeof(T));
-  uint8_t* sg = smem;
-  const RowRing ring{smem + pad128(rb), rb, pad128(rb), accumulate ? 3 : 2, S};
+  const RowRing ring{smem, rb, pad128(rb), 2, S};
   const int64_t G = gridDim.x;
   const int64_t cnt = (M - blockIdx.x + G - 1) / G;
+  uint4 graw[V][RAW];  // this thread's vectors of γ
 #pragma unroll
-  for (int k = 0; k < V; ++k) {
-    const int vi = tid + k * STREAM_THREADS;
-    if (vi < nv) stage8<DT>(sg, gamma, vi);
+  for (int kk = 0; kk < V; ++kk) {
+    const int vi = tid + kk * THREADS;
+#pragma unroll
+    for (int u = 0; u < RAW; ++u)
+      graw[kk][u] = vi < nv ? __ldg(reinterpret_cast<const uint4*>(gamma) + vi * RAW + u) : make_uint4(0, 0, 0, 0);
   }
   if (tid == 0) {
     abort_flag = 0;
@@ -362,11 +629,11 @@ __global__ void __launch_bounds__(STREAM_THREADS) ln_bwd_stream_kernel(ChunkSet 
     fence_barrier_init();
     for (int64_t k = 0; k < S && k < cnt; ++k) ring_issue(ring, full, cs, k, h, rpc, sizeof(T));
   }
-  float ag[V][8], ab[V][8];
+  float2 ag[V][4], ab[V][4];
 #pragma unroll
   for (int kk = 0; kk < V; ++kk)
 #pragma unroll
-    for (int i = 0; i < 8; ++i) ag[kk][i] = ab[kk][i] = 0.0f;
+    for (int i = 0; i < 4; ++i) ag[kk][i] = ab[kk][i] = make_float2(0.0f, 0.0f);
   const float inv_h = 1.0f / static_cast<float>(h);
   float mu_next = cnt > 0 ? mean[blockIdx.x] : 0.0f;
   float r_next = cnt > 0 ? rstd[blockIdx.x] : 0.0f;
@@ -378,60 +645,85 @@ __global__ void __launch_bounds__(STREAM_THREADS) ln_bwd_stream_kernel(ChunkSet 
       mu_next = mean[m + G];
       r_next = rstd[m + G];
     }
+    const int64_t j = m / rpc;
+    uint4* dx = reinterpret_cast<uint4*>(static_cast<T*>(cs.out[j]) + (m - j * rpc) * h);
+    // the dx being accumulated into: loaded now, used after the row's reduction
+    uint4 oraw[V][RAW];
+    if (accumulate) {
+#pragma unroll
+      for (int kk = 0; kk < V; ++kk) {
+        const int vi = tid + kk * THREADS;
+#pragma unroll
+        for (int u = 0; u < RAW; ++u) oraw[kk][u] = vi < nv ? dx[vi * RAW + u] : make_uint4(0, 0, 0, 0);
+      }
+    }
     if (tid == 0 &&
         !mbar_wait_bounded(smem_u32(&full[s]), static_cast<uint32_t>((k / S) & 1), nullptr, status, timeout_ns))
       abort_flag = 1;
-    __syncthreads();  // row k is in slot s; every thread is done with row k - 1
+    __syncthreads();  // row k is in slot s; every thread is done with row k − 1
     if (abort_flag) {
       if (tid == 0) ring_drain(ring, full, k, cnt, status, timeout_ns);
       return;
     }
-    if (tid == 0 && k >= 1 && k - 1 + S < cnt) {
+    const uint8_t* xs = ring.base + static_cast<size_t>(s) * ring.nin * ring.rb_al;
+    const uint8_t* ds = xs + ring.rb_al;
+    uint4 xraw[V][RAW], draw[V][RAW];
+#pragma unroll
+    for (int kk = 0; kk < V; ++kk) {
+      const int vi = tid + kk * THREADS;
+#pragma unroll
+      for (int u = 0; u < RAW; ++u) {
+        xraw[kk][u] = vi < nv ? reinterpret_cast<const uint4*>(xs)[vi * RAW + u] : make_uint4(0, 0, 0, 0);
+        draw[kk][u] = vi < nv ? reinterpret_cast<const uint4*>(ds)[vi * RAW + u] : make_uint4(0, 0, 0, 0);
+      }
+    }
+    if (tid == 0 && k >= 1 && k - 1 + S < cnt) {  // row k − 1's slot is free
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       ring_issue(ring, full, cs, k - 1 + S, h, rpc, sizeof(T));
     }
-    const uint8_t* xs = ring.base + static_cast<size_t>(s) * ring.nin * ring.rb_al;
-    const uint8_t* ds = xs + ring.rb_al;
-    const uint8_t* os = xs + 2 * ring.rb_al;
-    float sg1 = 0.0f, sgx = 0.0f;
+    const float2 r2 = make_float2(r, r), nmr2 = make_float2(-mu * r, -mu * r);
+    float2 sg1 = make_float2(0.0f, 0.0f), sgx = make_float2(0.0f, 0.0f);
 #pragma unroll
     for (int kk = 0; kk < V; ++kk) {
-      const int vi = tid + kk * STREAM_THREADS;
-      if (vi < nv) {
-        float xv[8], d[8], g[8];
-        lds8<DT>(xs, vi, xv);
-        lds8<DT>(ds, vi, d);
-        lds8<DT>(sg, vi, g);
+      if (tid + kk * THREADS < nv) {
+        float2 xv[4], d[4], g[4];
+        raw_to_pairs<DT>(xraw[kk], xv);
+        raw_to_pairs<DT>(draw[kk], d);
+        raw_to_pairs<DT>(graw[kk], g);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float xh = (xv[i] - mu) * r;
-          const float gi = d[i] * g[i];
-          sg1 += gi;
-          sgx += gi * xh;
-          ag[kk][i] += d[i] * xh;
-          ab[kk][i] += d[i];
+        for (int i = 0; i < 4; ++i) {
+          const float2 xh = __ffma2_rn(xv[i], r2, nmr2);
+          const float2 gi = __fmul2_rn(d[i], g[i]);
+          sg1 = __fadd2_rn(sg1, gi);
+          sgx = __ffma2_rn(gi, xh, sgx);
+          ag[kk][i] = __ffma2_rn(d[i], xh, ag[kk][i]);
+          ab[kk][i] = __fadd2_rn(ab[kk][i], d[i]);
         }
       }
     }
-    const float2 tot = block_sum2_free(sg1, sgx, red);  // red[] free: the row's first barrier follows its last read
-    const float mg = tot.x * inv_h, mgx = tot.y * inv_h;
-    const int64_t j = m / rpc;
-    T* dx = static_cast<T*>(cs.out[j]) + (m - j * rpc) * h;
+    // red[] is free: every thread passed this row's first barrier after its last read
+    const float2 tot = block_sum2_free<THREADS>(sg1.x + sg1.y, sgx.x + sgx.y, red);
+    const float2 nmg2 = make_float2(-tot.x * inv_h, -tot.x * inv_h);
+    const float2 nmgx2 = make_float2(-tot.y * inv_h, -tot.y * inv_h);
 #pragma unroll
     for (int kk = 0; kk < V; ++kk) {
-      const int vi = tid + kk * STREAM_THREADS;
+      const int vi = tid + kk * THREADS;
       if (vi < nv) {
-        float xv[8], d[8], g[8], o[8];
-        lds8<DT>(xs, vi, xv);
-        lds8<DT>(ds, vi, d);
-        lds8<DT>(sg, vi, g);
-        if (accumulate) lds8<DT>(os, vi, o);
+        float2 xv[4], d[4], g[4], o[4];
+        raw_to_pairs<DT>(xraw[kk], xv);
+        raw_to_pairs<DT>(draw[kk], d);
+        raw_to_pairs<DT>(graw[kk], g);
+        if (accumulate) raw_to_pairs<DT>(oraw[kk], o);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float t = r * (d[i] * g[i] - mg - (xv[i] - mu) * r * mgx);
-          o[i] = accumulate ? o[i] + t : t;
+        for (int i = 0; i < 4; ++i) {
+          const float2 xh = __ffma2_rn(xv[i], r2, nmr2);
+          const float2 t = __ffma2_rn(xh, nmgx2, __ffma2_rn(d[i], g[i], nmg2));  // g − mean(g) − x̂·mean(g·x̂)
+          o[i] = accumulate ? __ffma2_rn(t, r2, o[i]) : __fmul2_rn(t, r2);
         }
-        st8<DT>(dx, static_cast<int64_t>(vi) * 8, o);
+        uint4 out[RAW];
+        pairs_to_raw<DT>(o, out);
+#pragma unroll
+        for (int u = 0; u < RAW; ++u) dx[vi * RAW + u] = out[u];
       }
     }
   }
@@ -439,42 +731,63 @@ __global__ void __launch_bounds__(STREAM_THREADS) ln_bwd_stream_kernel(ChunkSet 
   float* pb = part + (G + blockIdx.x) * h;
 #pragma unroll
   for (int kk = 0; kk < V; ++kk) {
-    const int vi = tid + kk * STREAM_THREADS;
+    const int vi = tid + kk * THREADS;
     if (vi < nv) {
       float4* qg = reinterpret_cast<float4*>(pg + static_cast<int64_t>(vi) * 8);
       float4* qb = reinterpret_cast<float4*>(pb + static_cast<int64_t>(vi) * 8);
-      qg[0] = make_float4(ag[kk][0], ag[kk][1], ag[kk][2], ag[kk][3]);
-      qg[1] = make_float4(ag[kk][4], ag[kk][5], ag[kk][6], ag[kk][7]);
-      qb[0] = make_float4(ab[kk][0], ab[kk][1], ab[kk][2], ab[kk][3]);
-      qb[1] = make_float4(ab[kk][4], ab[kk][5], ab[kk][6], ab[kk][7]);
+      qg[0] = make_float4(ag[kk][0].x, ag[kk][0].y, ag[kk][1].x, ag[kk][1].y);
+      qg[1] = make_float4(ag[kk][2].x, ag[kk][2].y, ag[kk][3].x, ag[kk][3].y);
+      qb[0] = make_float4(ab[kk][0].x, ab[kk][0].y, ab[kk][1].x, ab[kk][1].y);
+      qb[1] = make_float4(ab[kk][2].x, ab[kk][2].y, ab[kk][3].x, ab[kk][3].y);
     }
   }
 }
 
-// dγ[c], dβ[c] from the G per-CTA partials (part = [dγ rows G | dβ rows G] of h):
-// eight row-strided partial sums per column, then added in index order — the
-// same association on every run.
-__global__ void __launch_bounds__(256) ln_bwd_reduce_parts_kernel(const float* __restrict__ part,
-                                                                  float* __restrict__ dgamma,
-                                                                  float* __restrict__ dbeta, int64_t h, int64_t G) {
-  __shared__ float acc[8][33];
-  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-  const int64_t col = static_cast<int64_t>(blockIdx.x) * 32 + tx;  // over [dγ | dβ], 2h columns
-  float a = 0.0f;
+// dγ[c], dβ[c] from the G per-CTA partials (part = [dγ rows G | dβ rows G] of h,
+// h a multiple of 4): a CTA takes 64 consecutive columns of [dγ | dβ] as 16
+// float4 quads, its 32 row groups add the rows g ≡ group (mod 32) with every
+// load independent of the others, and the 32 group sums are added in group
+// order — the same association on every run.
+constexpr int RP_QUADS = 16, RP_GROUPS = 32;
+
+__global__ void __launch_bounds__(RP_QUADS * RP_GROUPS) ln_bwd_reduce_parts_kernel(const float* __restrict__ part,
+                                                                                   float* __restrict__ dgamma,
+                                                                                   float* __restrict__ dbeta,
+                                                                                   int64_t h, int64_t G) {
+  __shared__ float4 acc[RP_GROUPS][RP_QUADS];
+  const int tx = threadIdx.x % RP_QUADS, ty = threadIdx.x / RP_QUADS;
+  const int64_t col = (static_cast<int64_t>(blockIdx.x) * RP_QUADS + tx) * 4;  // over [dγ | dβ], 2h columns
+  float4 a = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
   if (col < 2 * h) {
     const int64_t which = col >= h ? 1 : 0;
-    const float* p = part + which * G * h + (col - which * h);
-#pragma unroll 4
-    for (int64_t g = ty; g < G; g += 8) a += p[g * h];
+    const float4* p = reinterpret_cast<const float4*>(part + which * G * h + (col - which * h));
+    const int64_t step = h / 4;  // float4s per partial row
+#pragma unroll 8
+    for (int64_t g = ty; g < G; g += RP_GROUPS) {
+      const float4 v = __ldcs(p + g * step);
+      a.x += v.x;
+      a.y += v.y;
+      a.z += v.z;
+      a.w += v.w;
+    }
   }
   acc[ty][tx] = a;
   __syncthreads();
   if (ty == 0 && col < 2 * h) {
-    float t = acc[0][tx];
+    float4 t = acc[0][tx];
 #pragma unroll
-    for (int y = 1; y < 8; ++y) t += acc[y][tx];
-    if (col < h) dgamma[col] = t;
-    else dbeta[col - h] = t;
+    for (int y = 1; y < RP_GROUPS; ++y) {
+      const float4 u = acc[y][tx];
+      t.x += u.x;
+      t.y += u.y;
+      t.z += u.z;
+      t.w += u.w;
+    }
+    float* out = col < h ? dgamma + col : dbeta + (col - h);  // 4-byte aligned: scalar stores
+    out[0] = t.x;
+    out[1] = t.y;
+    out[2] = t.z;
+    out[3] = t.w;
   }
 }
 
@@ -710,7 +1023,8 @@ struct StreamPlan {
   size_t smem = 0;
 };
 
-StreamPlan plan_stream(const void* fn, size_t fixed, size_t slot, int ctas_per_sm, int64_t max_grid) {
+StreamPlan plan_stream(const void* fn, size_t fixed, size_t slot, int ctas_per_sm, int64_t max_grid,
+                       int threads = STREAM_THREADS) {
   StreamPlan p;
   DeviceInfo* dev = nullptr;
   if (current_device(&dev) != TPMLP_OK || dev == nullptr || max_grid < 1) return p;
@@ -721,13 +1035,13 @@ StreamPlan plan_stream(const void* fn, size_t fixed, size_t slot, int ctas_per_s
   S = std::max(S, 2);
   const size_t smem = fixed + static_cast<size_t>(S) * slot;
   if (smem > cap) return p;
-  if (smem > 48 * 1024 &&
-      cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess) {
+  // (always set: the kernel's static shared memory counts against the default 48 KB too)
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess) {
     cudaGetLastError();
     return p;
   }
   int occ = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, STREAM_THREADS, smem) != cudaSuccess || occ < 1) {
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, threads, smem) != cudaSuccess || occ < 1) {
     cudaGetLastError();
     return p;
   }
@@ -780,37 +1094,39 @@ bool ln_fwd_streamed(const ChunkSet& cs, const void* gamma, const void* beta, fl
   }
 }
 
-template <int DT, int V>
+template <int DT, int V, int THREADS>
 bool ln_bwd_streamed_v(const ChunkSet& cs, const void* gamma, const float* mean, const float* rstd, int accumulate,
                        float* dgamma, float* dbeta, float* part, int64_t max_parts, int64_t M, int64_t h, int64_t rpc,
                        cudaStream_t st) {
-  const void* fn = reinterpret_cast<const void*>(ln_bwd_stream_kernel<DT, V>);
+  const void* fn = reinterpret_cast<const void*>(ln_bwd_stream_kernel<DT, V, THREADS>);
   const size_t rb = pad128(static_cast<uint32_t>(h * sizeof(typename Storage<DT>::T)));
-  const StreamPlan p = plan_stream(fn, rb, (accumulate ? 3 : 2) * rb, 2, std::min(M, max_parts));
+  const StreamPlan p = plan_stream(fn, 0, 2 * rb, THREADS == 256 ? 2 : 1, std::min(M, max_parts), THREADS);
   if (!p.ok) return false;
   DeviceInfo* dev = nullptr;
   current_device(&dev);
-  ln_bwd_stream_kernel<DT, V><<<p.grid, STREAM_THREADS, p.smem, st>>>(cs, gamma, mean, rstd, accumulate, part, M, h,
-                                                                     rpc, p.S, dev->status, wait_timeout_ns());
-  ln_bwd_reduce_parts_kernel<<<static_cast<unsigned>((2 * h + 31) / 32), 256, 0, st>>>(part, dgamma, dbeta, h,
-                                                                                       p.grid);
+  ln_bwd_stream_kernel<DT, V, THREADS><<<p.grid, THREADS, p.smem, st>>>(cs, gamma, mean, rstd, accumulate, part, M, h,
+                                                                       rpc, p.S, dev->status, wait_timeout_ns());
+  ln_bwd_reduce_parts_kernel<<<static_cast<unsigned>((2 * h / 4 + RP_QUADS - 1) / RP_QUADS), RP_QUADS * RP_GROUPS, 0,
+                               st>>>(part, dgamma, dbeta, h, p.grid);
   return true;
 }
 
+// Threads per CTA and vectors per thread for a row of nv 8-element vectors:
+// 256 threads and two CTAs per SM (so that one CTA's barrier waits are covered
+// by the other's work) up to three vectors a thread; wider rows, 512 threads.
 template <int DT>
 bool ln_bwd_streamed(const ChunkSet& cs, const void* gamma, const float* mean, const float* rstd, int accumulate,
                      float* dgamma, float* dbeta, float* part, int64_t max_parts, int64_t M, int64_t h, int64_t rpc,
                      cudaStream_t st) {
-  switch ((h / 8 + STREAM_THREADS - 1) / STREAM_THREADS) {
-#define LNBS(V) \
-  case V: return ln_bwd_streamed_v<DT, V>(cs, gamma, mean, rstd, accumulate, dgamma, dbeta, part, max_parts, M, h, rpc, st)
-    LNBS(1);
-    LNBS(2);
-    LNBS(3);
-    LNBS(4);
+  const int64_t nv = h / 8;
+#define LNBS(V, TH) \
+  return ln_bwd_streamed_v<DT, V, TH>(cs, gamma, mean, rstd, accumulate, dgamma, dbeta, part, max_parts, M, h, rpc, st)
+  if (nv <= 256) LNBS(1, 256);
+  if (nv <= 512) LNBS(2, 256);
+  if (nv <= 768) LNBS(3, 256);
+  if (nv <= 1024) LNBS(2, 512);
 #undef LNBS
-    default: return false;
-  }
+  return false;
 }
 
 }  // namespace
@@ -830,7 +1146,12 @@ int launch_ln_forward(const void* const* x, const void* gamma, const void* beta,
                                   (8 * e)) == 0;
   const int ph = prof_begin(PROF_SP_REGION, st);
   bool streamed = false;
-  if (vec && h >= STREAM_MIN_H && h <= 8 * STREAM_THREADS * STREAM_MAX_V) {
+  if (vec && dtype != DT_F32) {
+    // 16-bit rows up to h = 8192: a warp per row, the row in registers
+    streamed = dtype == DT_F16 ? ln_fwd_registers<DT_F16>(cs, gamma, beta, eps, mean, rstd, M, h, rpc, st)
+                               : ln_fwd_registers<DT_BF16>(cs, gamma, beta, eps, mean, rstd, M, h, rpc, st);
+  }
+  if (!streamed && vec && h >= STREAM_MIN_H && h <= 8 * STREAM_THREADS * STREAM_MAX_V) {
     if (dtype == DT_F32) streamed = ln_fwd_streamed<DT_F32>(cs, gamma, beta, eps, mean, rstd, M, h, rpc, st);
     else if (dtype == DT_F16) streamed = ln_fwd_streamed<DT_F16>(cs, gamma, beta, eps, mean, rstd, M, h, rpc, st);
     else streamed = ln_fwd_streamed<DT_BF16>(cs, gamma, beta, eps, mean, rstd, M, h, rpc, st);
