@@ -19,12 +19,18 @@ Parallelism（SP）", §0 notation).  Activations ``[s, b, h]`` are flattened to
 
 Readings taken where the pages are silent (each listed in the design notes):
 
-A1. Row layout of Wqkv.  The pages give the fused weight's interleaving per
-    query group, [q₁ q₂ k₁ v₁ | q₃ q₄ k₂ v₂ | …] for grouped-query attention; with
-    one query head per group (multi-head attention, as the pages' parameter count
-    3h² + h² assumes) that is, per head j, rows [3dj, 3dj+d) = Wq_j,
-    [3dj+d, 3dj+2d) = Wk_j, [3dj+2d, 3dj+3d) = Wv_j.  Tensor shard i owns heads
-    [i·a/tp, (i+1)·a/tp), i.e. the contiguous rows [i·3h/tp, (i+1)·3h/tp).
+A1. Row layout of Wqkv.  The pages give the fused weight as [h + 2·h_kv, h] and
+    its interleaving per query group, [q₁ q₂ k₁ v₁ | q₃ q₄ k₂ v₂ | …] for
+    grouped-query attention: with G key/value heads (groups) and r = a/G query
+    heads per group, group g holds rows [g·(r+2)·d, (g+1)·(r+2)·d): its r query
+    heads' q rows in head order, then its k rows, then its v rows.  Query head j
+    belongs to group j // r.  With one query head per group (multi-head
+    attention, G = a, as the pages' parameter count 3h² + h² assumes) that is,
+    per head j, rows [3dj, 3dj+d) = Wq_j, [3dj+d, 3dj+2d) = Wk_j,
+    [3dj+2d, 3dj+3d) = Wv_j.  Tensor shard i owns groups [i·G/tp, (i+1)·G/tp),
+    i.e. the contiguous rows [i·(h+2h_kv)/tp, (i+1)·(h+2h_kv)/tp); G must be a
+    multiple of tp (the pages' fallback when it is not, an all-gather of QKV
+    before slicing, is not taken).
 A2. O's column layout: head j occupies columns [jd, (j+1)d) (heads concatenated),
     so shard i's slice of O is columns [i·h/tp, (i+1)·h/tp) — exactly the rows of
     Wo's input dimension it owns.
@@ -37,6 +43,12 @@ A4. No bias, no dropout on the probabilities, no softmax scaling other than
 A5. ``lse2`` is the base-2 log-sum-exp of the scaled scores of each query row,
     log2 Σ_u 2^(x_tu) with x = (q·k/√d)·log2(e): the statistic a streaming
     softmax keeps for its backward pass.
+A6. Grouped-query attention: query head j attends with its group's key and
+    value head g(j) = j // r, O_j = softmax(Q_j·K_gᵀ/√d)·V_g; a key/value head
+    shared by r query heads receives the sum of their gradients.  The head
+    width d = h/a is free (the pages use 128 and 96).
+
+``kv_heads`` (G) defaults to ``heads`` (multi-head attention) everywhere.
 """
 from __future__ import annotations
 
@@ -46,7 +58,9 @@ import numpy as np
 
 __all__ = [
     "LOG2E",
+    "qkv_width",
     "qkv_head_rows",
+    "qkv_row_labels",
     "split_qkv",
     "merge_qkv",
     "attention_core_forward",
@@ -64,31 +78,62 @@ def _f64(a):
     return np.asarray(a, dtype=np.float64)
 
 
-def qkv_head_rows(heads, d, j):
-    """Rows of Wqkv (or columns of QKV) holding head j's q, k and v (reading A1)."""
-    base = 3 * d * j
-    return (range(base, base + d), range(base + d, base + 2 * d), range(base + 2 * d, base + 3 * d))
+def qkv_width(heads, d, kv_heads=None):
+    """Rows of the fused Wqkv: h + 2·h_kv = (a + 2G)·d."""
+    G = heads if kv_heads is None else kv_heads
+    return (heads + 2 * G) * d
 
 
-def split_qkv(QKV, heads):
-    """[M, 3h] head-interleaved → Q, K, V, each [M, h] with head j in columns [jd, (j+1)d)."""
+def qkv_head_rows(heads, d, j, kv_heads=None):
+    """Rows of Wqkv (or columns of QKV) holding query head j's q, and its
+    group's k and v (reading A1)."""
+    G = heads if kv_heads is None else kv_heads
+    r = heads // G
+    g = j // r
+    base = g * (r + 2) * d
+    q0 = base + (j - g * r) * d
+    k0 = base + r * d
+    return (range(q0, q0 + d), range(k0, k0 + d), range(k0 + d, k0 + 2 * d))
+
+
+def qkv_row_labels(heads, kv_heads):
+    """The fused weight's head blocks in row order, as the pages print them:
+    'q1', 'q2', 'k1', 'v1', 'q3', … (query heads numbered 1…a, groups 1…G)."""
+    r = heads // kv_heads
+    out = []
+    for g in range(kv_heads):
+        out += [f"q{g * r + i + 1}" for i in range(r)] + [f"k{g + 1}", f"v{g + 1}"]
+    return out
+
+
+def split_qkv(QKV, heads, kv_heads=None):
+    """[M, h + 2h_kv] group-interleaved → Q [M, h] (query head j in columns
+    [jd, (j+1)d)), K and V [M, h_kv] (group g in columns [gd, (g+1)d))."""
+    G = heads if kv_heads is None else kv_heads
     QKV = _f64(QKV)
-    M, three_h = QKV.shape
-    h = three_h // 3
-    d = h // heads
-    r = QKV.reshape(M, heads, 3, d)
-    return (r[:, :, 0, :].reshape(M, h), r[:, :, 1, :].reshape(M, h), r[:, :, 2, :].reshape(M, h))
+    M, width = QKV.shape
+    d = width // (heads + 2 * G)
+    r = heads // G
+    t = QKV.reshape(M, G, r + 2, d)
+    return (t[:, :, :r, :].reshape(M, heads * d), t[:, :, r, :].reshape(M, G * d), t[:, :, r + 1, :].reshape(M, G * d))
 
 
-def merge_qkv(Q, K, V, heads):
+def merge_qkv(Q, K, V, heads, kv_heads=None):
     """Inverse of split_qkv."""
+    G = heads if kv_heads is None else kv_heads
     M, h = Q.shape
     d = h // heads
-    out = np.empty((M, heads, 3, d))
-    out[:, :, 0, :] = _f64(Q).reshape(M, heads, d)
-    out[:, :, 1, :] = _f64(K).reshape(M, heads, d)
-    out[:, :, 2, :] = _f64(V).reshape(M, heads, d)
-    return out.reshape(M, 3 * h)
+    r = heads // G
+    out = np.empty((M, G, r + 2, d))
+    out[:, :, :r, :] = _f64(Q).reshape(M, G, r, d)
+    out[:, :, r, :] = _f64(K).reshape(M, G, d)
+    out[:, :, r + 1, :] = _f64(V).reshape(M, G, d)
+    return out.reshape(M, (heads + 2 * G) * d)
+
+
+def _group_of(heads, kv_heads):
+    """g(j) for every query head j (reading A6)."""
+    return np.arange(heads) // (heads // kv_heads)
 
 
 def _per_sequence(T, s, b, heads):
@@ -114,11 +159,16 @@ def _scores(q, k, causal):
     return x
 
 
-def attention_core_forward(Q, K, V, s, b, heads, causal=False):
-    """O = softmax(QKᵀ/√d)V per sequence and head.  Q, K, V: [M, h].
+def attention_core_forward(Q, K, V, s, b, heads, causal=False, kv_heads=None):
+    """O_j = softmax(Q_j·K_gᵀ/√d)·V_g per sequence and query head j, g = g(j).
+    Q: [M, h]; K, V: [M, h_kv].
 
     Returns {"O": [M, h], "lse2": [b, heads, s], "P": [b, heads, s, s]}."""
-    q, k, v = (_per_sequence(T, s, b, heads) for T in (Q, K, V))
+    G = heads if kv_heads is None else kv_heads
+    q = _per_sequence(Q, s, b, heads)
+    grp = _group_of(heads, G)
+    k = _per_sequence(K, s, b, G)[:, grp]  # query head j sees its group's keys and values
+    v = _per_sequence(V, s, b, G)[:, grp]
     x = _scores(q, k, causal)
     mx = x.max(axis=-1, keepdims=True)
     e = np.exp2(x - mx)
@@ -129,85 +179,101 @@ def attention_core_forward(Q, K, V, s, b, heads, causal=False):
     return {"O": _from_per_sequence(o), "lse2": lse2, "P": P}
 
 
-def attention_core_backward(Q, K, V, dO, s, b, heads, causal=False):
-    """Gradients of the attention core given dO = ∂L/∂O: dQ, dK, dV, each [M, h].
+def attention_core_backward(Q, K, V, dO, s, b, heads, causal=False, kv_heads=None):
+    """Gradients of the attention core given dO = ∂L/∂O: dQ [M, h], dK, dV [M, h_kv].
 
-    dV = Pᵀ·dO, dP = dO·Vᵀ, dS = P ⊙ (dP − rowsum(dP ⊙ P)) (softmax Jacobian),
-    dQ = dS·K/√d, dK = dSᵀ·Q/√d."""
-    q, k, v, do = (_per_sequence(T, s, b, heads) for T in (Q, K, V, dO))
+    Per query head j (group g): dV_j = P_jᵀ·dO_j, dP_j = dO_j·V_gᵀ,
+    dS_j = P_j ⊙ (dP_j − rowsum(dP_j ⊙ P_j)) (softmax Jacobian),
+    dQ_j = dS_j·K_g/√d, dK_j = dS_jᵀ·Q_j/√d; a group's dK and dV are the sums
+    over its query heads (reading A6)."""
+    G = heads if kv_heads is None else kv_heads
+    q, do = (_per_sequence(T, s, b, heads) for T in (Q, dO))
+    grp = _group_of(heads, G)
+    k = _per_sequence(K, s, b, G)[:, grp]
+    v = _per_sequence(V, s, b, G)[:, grp]
     d = q.shape[-1]
-    P = attention_core_forward(Q, K, V, s, b, heads, causal)["P"]
+    P = attention_core_forward(Q, K, V, s, b, heads, causal, G)["P"]
     dv = np.einsum("...tu,...td->...ud", P, do)
     dP = np.einsum("...td,...ud->...tu", do, v)
     dS = P * (dP - (dP * P).sum(axis=-1, keepdims=True))
     dq = np.einsum("...tu,...ud->...td", dS, k) / math.sqrt(d)
     dk = np.einsum("...tu,...td->...ud", dS, q) / math.sqrt(d)
-    return {"dQ": _from_per_sequence(dq), "dK": _from_per_sequence(dk), "dV": _from_per_sequence(dv)}
+    dk_g = np.zeros((dk.shape[0], G) + dk.shape[2:])
+    dv_g = np.zeros_like(dk_g)
+    for j in range(heads):  # a shared key/value head collects its query heads' gradients
+        dk_g[:, grp[j]] += dk[:, j]
+        dv_g[:, grp[j]] += dv[:, j]
+    return {"dQ": _from_per_sequence(dq), "dK": _from_per_sequence(dk_g), "dV": _from_per_sequence(dv_g)}
 
 
-def attn_forward(X, Wqkv, Wo, s, b, heads, causal=False):
-    """The unsharded block.  X: [M, h] (or [s, b, h]); Wqkv: [3h, h]; Wo: [h, h]."""
+def attn_forward(X, Wqkv, Wo, s, b, heads, causal=False, kv_heads=None):
+    """The unsharded block.  X: [M, h] (or [s, b, h]); Wqkv: [h + 2h_kv, h]; Wo: [h, h]."""
     X = _f64(X).reshape(s * b, -1)
     QKV = X @ _f64(Wqkv).T
-    Q, K, V = split_qkv(QKV, heads)
-    core = attention_core_forward(Q, K, V, s, b, heads, causal)
+    Q, K, V = split_qkv(QKV, heads, kv_heads)
+    core = attention_core_forward(Q, K, V, s, b, heads, causal, kv_heads)
     Z = core["O"] @ _f64(Wo).T
     return {"QKV": QKV, "O": core["O"], "lse2": core["lse2"], "Z": Z}
 
 
-def attn_backward(X, Wqkv, Wo, dZ, s, b, heads, causal=False):
+def attn_backward(X, Wqkv, Wo, dZ, s, b, heads, causal=False, kv_heads=None):
     """Gradients of the unsharded block given dZ: dX, dWqkv, dWo (and dO, dQKV)."""
     X = _f64(X).reshape(s * b, -1)
     dZ = _f64(dZ).reshape(s * b, -1)
-    fw = attn_forward(X, Wqkv, Wo, s, b, heads, causal)
+    fw = attn_forward(X, Wqkv, Wo, s, b, heads, causal, kv_heads)
     dWo = dZ.T @ fw["O"]
     dO = dZ @ _f64(Wo)
-    Q, K, V = split_qkv(fw["QKV"], heads)
-    g = attention_core_backward(Q, K, V, dO, s, b, heads, causal)
-    dQKV = merge_qkv(g["dQ"], g["dK"], g["dV"], heads)
+    Q, K, V = split_qkv(fw["QKV"], heads, kv_heads)
+    g = attention_core_backward(Q, K, V, dO, s, b, heads, causal, kv_heads)
+    dQKV = merge_qkv(g["dQ"], g["dK"], g["dV"], heads, kv_heads)
     dWqkv = dQKV.T @ X
     dX = dQKV @ _f64(Wqkv)
     return {"dX": dX, "dWqkv": dWqkv, "dWo": dWo, "dO": dO, "dQKV": dQKV}
 
 
-def attn_forward_sharded(X, Wqkv, Wo, s, b, heads, tp, causal=False):
-    """The tensor-parallel form: shard i takes Wqkv rows [i·3h/tp, (i+1)·3h/tp)
-    (its heads) and Wo columns [i·h/tp, (i+1)·h/tp); Z is the sum of the shards'
-    partial outputs (g)."""
+def attn_forward_sharded(X, Wqkv, Wo, s, b, heads, tp, causal=False, kv_heads=None):
+    """The tensor-parallel form: shard i takes Wqkv rows
+    [i·(h+2h_kv)/tp, (i+1)·(h+2h_kv)/tp) (its groups, with their query heads)
+    and Wo columns [i·h/tp, (i+1)·h/tp); Z is the sum of the shards' partial
+    outputs (g)."""
+    G = heads if kv_heads is None else kv_heads
     X = _f64(X).reshape(s * b, -1)
     h = X.shape[1]
-    hs, a_s = h // tp, heads // tp
+    hs, a_s, g_s = h // tp, heads // tp, G // tp
+    ws = (Wqkv.shape[0]) // tp
     Z = np.zeros((s * b, h))
     for i in range(tp):
-        QKV_i = X @ _f64(Wqkv)[3 * hs * i: 3 * hs * (i + 1)].T
-        Q, K, V = split_qkv(QKV_i, a_s)
-        O_i = attention_core_forward(Q, K, V, s, b, a_s, causal)["O"]
+        QKV_i = X @ _f64(Wqkv)[ws * i: ws * (i + 1)].T
+        Q, K, V = split_qkv(QKV_i, a_s, g_s)
+        O_i = attention_core_forward(Q, K, V, s, b, a_s, causal, g_s)["O"]
         Z += O_i @ _f64(Wo)[:, hs * i: hs * (i + 1)].T
     return Z
 
 
-def attn_backward_sharded(X, Wqkv, Wo, dZ, s, b, heads, tp, causal=False):
+def attn_backward_sharded(X, Wqkv, Wo, dZ, s, b, heads, tp, causal=False, kv_heads=None):
     """Shard-local gradients: dWqkv and dWo are concatenations of the shards'
     blocks; dX is the sum of the shards' partial input gradients (f backward)."""
+    G = heads if kv_heads is None else kv_heads
     X = _f64(X).reshape(s * b, -1)
     dZ = _f64(dZ).reshape(s * b, -1)
     h = X.shape[1]
-    hs, a_s = h // tp, heads // tp
+    hs, a_s, g_s = h // tp, heads // tp, G // tp
+    ws = (Wqkv.shape[0]) // tp
     dX = np.zeros_like(X)
-    dWqkv = np.zeros((3 * h, h))
+    dWqkv = np.zeros((Wqkv.shape[0], h))
     dWo = np.zeros((h, h))
     for i in range(tp):
-        rq = slice(3 * hs * i, 3 * hs * (i + 1))
+        rq = slice(ws * i, ws * (i + 1))
         ro = slice(hs * i, hs * (i + 1))
         Wqkv_i = _f64(Wqkv)[rq]
         Wo_i = _f64(Wo)[:, ro]
         QKV_i = X @ Wqkv_i.T
-        Q, K, V = split_qkv(QKV_i, a_s)
-        O_i = attention_core_forward(Q, K, V, s, b, a_s, causal)["O"]
+        Q, K, V = split_qkv(QKV_i, a_s, g_s)
+        O_i = attention_core_forward(Q, K, V, s, b, a_s, causal, g_s)["O"]
         dWo[:, ro] = dZ.T @ O_i
         dO_i = dZ @ Wo_i
-        g = attention_core_backward(Q, K, V, dO_i, s, b, a_s, causal)
-        dQKV_i = merge_qkv(g["dQ"], g["dK"], g["dV"], a_s)
+        g = attention_core_backward(Q, K, V, dO_i, s, b, a_s, causal, g_s)
+        dQKV_i = merge_qkv(g["dQ"], g["dK"], g["dV"], a_s, g_s)
         dWqkv[rq] = dQKV_i.T @ X
         dX += dQKV_i @ Wqkv_i
     return {"dX": dX, "dWqkv": dWqkv, "dWo": dWo}

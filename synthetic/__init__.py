@@ -137,9 +137,12 @@ def sp_region_inputs(s: int, b: int, h: int, p: float, seed: int, dtype: str = "
 
 @dataclass(frozen=True)
 class AttnConfig:
-    """One tensor-parallel self-attention workload: h = heads·128 (head width 128,
-    "Tensor Parallelism（TP）与 Sequence Parallelism（SP）", §6 numbers:
-    heads = 64, head_dim = 128 at H = 8192)."""
+    """One tensor-parallel self-attention workload: h = heads·d with head width
+    d = 128 ("Tensor Parallelism（TP）与 Sequence Parallelism（SP）", §6 numbers:
+    heads = 64, head_dim = 128 at H = 8192) or 96 (the 22B model of "Sequence
+    Parallel 与 Context Parallel", h = 6144, a = 64; the 8.3B model's 96 per
+    head), and ``kv_heads`` key/value heads (grouped-query attention, 8 × 128 at
+    the Llama-70B-like width; 0 means one per query head, i.e. multi-head)."""
 
     name: str
     s: int
@@ -151,6 +154,7 @@ class AttnConfig:
     dtype: str
     causal: bool
     seed: int = 0
+    kv_heads: int = 0
 
     @property
     def M(self) -> int:
@@ -161,21 +165,36 @@ class AttnConfig:
         return self.h // self.heads
 
     @property
+    def groups(self) -> int:
+        """Key/value heads (query groups)."""
+        return self.kv_heads or self.heads
+
+    @property
+    def h_kv(self) -> int:
+        return self.groups * self.d
+
+    @property
+    def qkv_rows(self) -> int:
+        """Rows of the fused Wqkv: h + 2·h_kv."""
+        return self.h + 2 * self.h_kv
+
+    @property
     def torch_dtype(self) -> torch.dtype:
         return TORCH_DTYPES[self.dtype]
 
     def flops_fwd_bwd(self) -> int:
         """Matmul FLOPs of one forward+backward, without recomputation.
 
-        Projections: QKV 2·M·h·3h and output 2·M·h·h forward, twice that backward
-        (input and weight gradients): 24·M·h².  Core per sequence and head: QKᵀ and
-        P·V forward (2·s²·d each), dV, dP, dQ, dK backward (2·s²·d each): 12·s²·d,
-        i.e. 12·b·s²·h over all heads — halved (to the visible pairs, ≈ s²/2) with
-        the causal mask."""
+        Projections: QKV 2·M·h·(h + 2h_kv) and output 2·M·h·h forward, twice that
+        backward (input and weight gradients): 12·M·h·(h + h_kv) (24·M·h² for
+        multi-head attention).  Core per sequence and query head: QKᵀ and P·V
+        forward (2·s²·d each), dV, dP, dQ, dK backward (2·s²·d each): 12·s²·d,
+        i.e. 12·b·s²·h over all query heads — halved (to the visible pairs,
+        ≈ s²/2) with the causal mask."""
         core = 12 * self.b * self.s * self.s * self.h
         if self.causal:
             core = 12 * self.b * (self.s * (self.s + 1) // 2) * self.h
-        return 24 * self.M * self.h * self.h + core
+        return 12 * self.M * self.h * (self.h + self.h_kv) + core
 
     def with_(self, **kw) -> "AttnConfig":
         return replace(self, **kw)
@@ -187,16 +206,22 @@ ATTN_CONFIGS = {
     "llama70b_attn_unmasked_tpsp8_bf16": AttnConfig(
         "llama70b_attn_unmasked_tpsp8_bf16", 4096, 1, 8192, 64, 8, True, "bf16", False
     ),
+    # grouped-query attention at the Llama-70B-like width: 64 query heads, 8 KV heads of 128
+    "llama70b_gqa_attn_tpsp8_bf16": AttnConfig(
+        "llama70b_gqa_attn_tpsp8_bf16", 4096, 1, 8192, 64, 8, True, "bf16", True, kv_heads=8
+    ),
+    # the 22B model: h = 6144, 64 heads of 96, s = 4096, t = 8, SP
+    "w22b_attn_tpsp8_bf16": AttnConfig("w22b_attn_tpsp8_bf16", 4096, 1, 6144, 64, 8, True, "bf16", True),
 }
 
 
 def attn_inputs(cfg: AttnConfig, seed: int | None = None) -> dict[str, torch.Tensor]:
-    """CPU tensors X [s,b,h], Wqkv [3h,h], Wo [h,h], dZ [s,b,h] in cfg.dtype:
+    """CPU tensors X [s,b,h], Wqkv [h+2h_kv,h], Wo [h,h], dZ [s,b,h] in cfg.dtype:
     X, dZ ~ N(0, 1), weights ~ N(0, 0.02), drawn in that order from one generator."""
     g = torch.Generator().manual_seed(cfg.seed if seed is None else seed)
     dt = cfg.torch_dtype
     X = torch.randn(cfg.s, cfg.b, cfg.h, generator=g)
-    Wqkv = torch.randn(3 * cfg.h, cfg.h, generator=g).mul_(0.02)
+    Wqkv = torch.randn(cfg.qkv_rows, cfg.h, generator=g).mul_(0.02)
     Wo = torch.randn(cfg.h, cfg.h, generator=g).mul_(0.02)
     dZ = torch.randn(cfg.s, cfg.b, cfg.h, generator=g)
     return {"X": X.to(dt), "Wqkv": Wqkv.to(dt), "Wo": Wo.to(dt), "dZ": dZ.to(dt)}

@@ -221,3 +221,152 @@ def test_attention_parameter_count_per_shard():
     for j in range(heads // tp * i, heads // tp * (i + 1)):
         for r in O.qkv_head_rows(heads, d, j):
             assert set(r) <= rows
+
+
+# ---------------------------------------------------------------- grouped-query attention (reading A6)
+
+
+def _gqa_case(s, b, heads, kv, d, seed=0, wscale=0.3):
+    h = heads * d
+    X = _rand((s * b, h), seed)
+    Wqkv = _rand((O.qkv_width(heads, d, kv), h), seed + 1, wscale)
+    Wo = _rand((h, h), seed + 2, wscale)
+    dZ = _rand((s * b, h), seed + 3)
+    return X, Wqkv, Wo, dZ
+
+
+def test_fused_weight_rows_follow_the_printed_interleave():
+    """The "tensor-parallel-megatron" reading (attention section) prints the GQA
+    fused weight as [q₁ q₂ k₁ v₁ | q₃ q₄ k₂ v₂ | …] and its shape as
+    [h + 2·h_kv, h]: four query heads in two groups, block by block."""
+    assert O.qkv_row_labels(4, 2) == ["q1", "q2", "k1", "v1", "q3", "q4", "k2", "v2"]
+    assert O.qkv_row_labels(2, 2) == ["q1", "k1", "v1", "q2", "k2", "v2"]  # MHA
+    d = 3
+    assert O.qkv_width(4, d, 2) == 4 * d + 2 * 2 * d
+    labels = O.qkv_row_labels(4, 2)
+    for j in range(4):
+        q, k, v = O.qkv_head_rows(4, d, j, 2)
+        assert labels[q.start // d] == f"q{j + 1}"
+        assert labels[k.start // d] == f"k{j // 2 + 1}" and labels[v.start // d] == f"v{j // 2 + 1}"
+        assert len(q) == len(k) == len(v) == d
+
+
+def _loops_forward_gqa(X, Wqkv, Wo, s, b, heads, kv, causal):
+    """Scalar loops from reading A6: query head j uses the k and v rows of its
+    group j // (heads/kv), located by the printed labels."""
+    M, h = X.shape
+    d = h // heads
+    labels = O.qkv_row_labels(heads, kv)
+    row0 = {lab: i * d for i, lab in enumerate(labels)}
+    QKV = [[sum(X[m][c] * Wqkv[r][c] for c in range(h)) for r in range(len(labels) * d)] for m in range(M)]
+    Ocat = [[0.0] * h for _ in range(M)]
+    r = heads // kv
+    for bi in range(b):
+        for j in range(heads):
+            qb, kb, vb = row0[f"q{j + 1}"], row0[f"k{j // r + 1}"], row0[f"v{j // r + 1}"]
+            for t in range(s):
+                mt = t * b + bi
+                sc = []
+                for u in range(s):
+                    if causal and u > t:
+                        continue
+                    dot = sum(QKV[mt][qb + e] * QKV[u * b + bi][kb + e] for e in range(d))
+                    sc.append((u, dot / math.sqrt(d)))
+                top = max(v for _, v in sc)
+                w = [(u, math.exp(v - top)) for u, v in sc]
+                tot = sum(x for _, x in w)
+                for e in range(d):
+                    Ocat[mt][j * d + e] = sum(x / tot * QKV[u * b + bi][vb + e] for u, x in w)
+    Z = [[sum(Ocat[m][c] * Wo[n][c] for c in range(h)) for n in range(h)] for m in range(M)]
+    return np.array(Ocat), np.array(Z)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_gqa_forward_matches_scalar_loops(causal):
+    s, b, heads, kv, d = 3, 2, 4, 2, 2
+    X, Wqkv, Wo, _ = _gqa_case(s, b, heads, kv, d, seed=51)
+    fw = O.attn_forward(X, Wqkv, Wo, s, b, heads, causal, kv)
+    Ol, Zl = _loops_forward_gqa(X, Wqkv, Wo, s, b, heads, kv, causal)
+    assert np.allclose(fw["O"], Ol, rtol=1e-12, atol=1e-12)
+    assert np.allclose(fw["Z"], Zl, rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_gqa_gradients_by_central_differences(causal):
+    """A key/value head shared by several query heads: its weights' gradient is
+    the sum over the heads that read it, which finite differences see directly."""
+    s, b, heads, kv, d = 4, 2, 4, 2, 2
+    X, Wqkv, Wo, dZ = _gqa_case(s, b, heads, kv, d, seed=61, wscale=0.5)
+    g = O.attn_backward(X, Wqkv, Wo, dZ, s, b, heads, causal, kv)
+
+    def loss():
+        return float((O.attn_forward(X, Wqkv, Wo, s, b, heads, causal, kv)["Z"] * dZ).sum())
+
+    eps = 1e-6
+    rng = np.random.default_rng(6)
+    k_rows = [r for j in range(heads) for r in O.qkv_head_rows(heads, d, j, kv)[1]]
+    for name, T, picks in (("dX", X, None), ("dWqkv", Wqkv, k_rows), ("dWqkv", Wqkv, None), ("dWo", Wo, None)):
+        for _ in range(10):
+            idx = tuple(int(rng.integers(0, n)) for n in T.shape)
+            if picks is not None:  # a row of a shared key head
+                idx = (int(picks[rng.integers(0, len(picks))]), idx[1])
+            old = T[idx]
+            T[idx] = old + eps
+            lp = loss()
+            T[idx] = old - eps
+            lm = loss()
+            T[idx] = old
+            fd = (lp - lm) / (2 * eps)
+            assert abs(g[name][idx] - fd) <= 1e-6 * max(1.0, abs(fd)), (name, idx, g[name][idx], fd)
+
+
+def test_gqa_with_one_group_per_head_is_multi_head_attention():
+    """kv_heads = heads is the MHA layout (reading A1): both calls agree bit for bit."""
+    s, b, heads, d = 4, 2, 2, 3
+    X, Wqkv, Wo, dZ = _case(s, b, heads, d, seed=71)
+    a = O.attn_backward(X, Wqkv, Wo, dZ, s, b, heads, True)
+    g = O.attn_backward(X, Wqkv, Wo, dZ, s, b, heads, True, heads)
+    for k in ("dX", "dWqkv", "dWo"):
+        assert np.array_equal(a[k], g[k]), k
+
+
+def test_gqa_is_not_attention_with_separate_key_heads():
+    """Sharing matters: giving every query head its own copy of the key/value
+    weights and then perturbing one copy changes only that head's output, while
+    perturbing a shared group's weights changes every head of the group."""
+    s, b, heads, kv, d = 4, 1, 4, 2, 2
+    X, Wqkv, Wo, _ = _gqa_case(s, b, heads, kv, d, seed=81)
+    base = O.attn_forward(X, Wqkv, Wo, s, b, heads, False, kv)["O"]
+    W2 = Wqkv.copy()
+    W2[list(O.qkv_head_rows(heads, d, 0, kv)[1])] += 0.5  # group 0's k rows (heads 0 and 1)
+    o2 = O.attn_forward(X, W2, Wo, s, b, heads, False, kv)["O"]
+    changed = [not np.allclose(o2[:, j * d:(j + 1) * d], base[:, j * d:(j + 1) * d]) for j in range(heads)]
+    assert changed == [True, True, False, False]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_gqa_sharded_by_groups_equals_unsharded(causal):
+    s, b, heads, kv, d, tp = 4, 2, 8, 4, 2, 2
+    X, Wqkv, Wo, dZ = _gqa_case(s, b, heads, kv, d, seed=91)
+    full = O.attn_forward(X, Wqkv, Wo, s, b, heads, causal, kv)
+    assert np.allclose(O.attn_forward_sharded(X, Wqkv, Wo, s, b, heads, tp, causal, kv), full["Z"], atol=1e-12)
+    gb = O.attn_backward(X, Wqkv, Wo, dZ, s, b, heads, causal, kv)
+    gs = O.attn_backward_sharded(X, Wqkv, Wo, dZ, s, b, heads, tp, causal, kv)
+    for k in ("dX", "dWqkv", "dWo"):
+        assert np.allclose(gs[k], gb[k], atol=1e-11), k
+    # shard i's Wqkv rows are exactly its groups' blocks, query heads included
+    ws = O.qkv_width(heads, d, kv) // tp
+    for i in range(tp):
+        rows = set(range(ws * i, ws * (i + 1)))
+        for j in range(heads // tp * i, heads // tp * (i + 1)):
+            for r in O.qkv_head_rows(heads, d, j, kv):
+                assert set(r) <= rows
+
+
+def test_gqa_workload_sizes():
+    """The pages' GQA numbers: 8 KV heads × 128 = h_kv 1024 against MHA's 8192 at
+    64 heads × 128 (an 8× smaller KV); the fused weight of the Llama-70B-like width
+    is [8192 + 2·1024, 8192]."""
+    assert 8 * 128 == 1024 and 64 * 128 == 8192 and 8192 // 1024 == 8
+    assert O.qkv_width(64, 128, 8) == 8192 + 2 * 1024
+    assert O.qkv_width(64, 128) == 3 * 8192
