@@ -84,12 +84,14 @@ def l2_note(tensors: dict) -> str:
 
 def attn_workload_desc(cfg) -> dict:
     """The attention block's config entry (the same in both arms)."""
-    return {"workload": f"TP self-attention [s,b,h]=[{cfg.s},{cfg.b},{cfg.h}] {cfg.heads} heads of {cfg.d} "
+    kv = f" ({cfg.groups} key/value heads)" if cfg.groups != cfg.heads else ""
+    return {"workload": f"TP self-attention [s,b,h]=[{cfg.s},{cfg.b},{cfg.h}] {cfg.heads} heads of {cfg.d}{kv} "
                         f"tp={cfg.tp} SP {'on' if cfg.sp else 'off'} {'causal' if cfg.causal else 'unmasked'} "
                         f"{cfg.dtype}, fwd+bwd",
-            "name": cfg.name, "flops_per_step": float(cfg.flops_fwd_bwd()),
-            "flops_note": "24·M·h² projections + 12·b·h·(visible query-key pairs) core, no recomputation",
-            "l2": l2_note({"Wqkv": 3 * cfg.h * cfg.h * 2, "QKV": 3 * cfg.s * cfg.b * cfg.h * 2})}
+            "name": cfg.name, "kv_heads": cfg.groups, "flops_per_step": float(cfg.flops_fwd_bwd()),
+            "flops_note": "12·M·h·(h + h_kv) projections + 12·b·h·(visible query-key pairs) core, "
+                          "no recomputation",
+            "l2": l2_note({"Wqkv": cfg.qkv_rows * cfg.h * 2, "QKV": cfg.qkv_rows * cfg.s * cfg.b * 2})}
 
 
 def workload_desc(cfg) -> dict:
@@ -864,12 +866,13 @@ def run_attention(args) -> int:
     X, Wqkv, Wo, dZ = (t[k].to(dev) for k in ("X", "Wqkv", "Wo", "dZ"))
     x = [c.contiguous() for c in X.chunk(cfg.tp)] if cfg.sp else X
     dz = [c.contiguous() for c in dZ.chunk(cfg.tp)] if cfg.sp else dZ
-    blk = tpmlp.AttnBlock(cfg.s, cfg.b, cfg.h, cfg.heads, cfg.tp, cfg.sp, cfg.torch_dtype, cfg.causal, device=dev)
+    blk = tpmlp.AttnBlock(cfg.s, cfg.b, cfg.h, cfg.heads, cfg.tp, cfg.sp, cfg.torch_dtype, cfg.causal, device=dev,
+                          kv_heads=cfg.groups)
     stream = torch.cuda.current_stream(dev)
     fw = blk.forward(x, Wqkv, Wo, stream=stream)
     bw = blk.backward(x, Wqkv, Wo, fw, dz, stream=stream)
     kw = dict(s=cfg.s, b=cfg.b, h=cfg.h, heads=cfg.heads, tp=cfg.tp, sp=cfg.sp, causal=cfg.causal,
-              workspace=blk.ws, stream=stream)
+              kv_heads=cfg.groups, workspace=blk.ws, stream=stream)
 
     def step():
         tpmlp.attn_forward(x, Wqkv, Wo, fw["qkv"], fw["o"], fw["lse"], fw["z"], **kw)
@@ -1036,7 +1039,7 @@ def attn_oracle_sample(cfg, inputs, target_s: float):
     """The fp64 oracle's attention block fwd+bwd (its backward runs the forward
     too) on the first s' tokens of every sequence with full weights, s' sized so
     one run takes about target_s and at most 1024 (the oracle holds several
-    [b, heads, s', s'] fp64 matrices); FLOPs counted as on the GPU (24·M'·h² for
+    [b, heads, s', s'] fp64 matrices); FLOPs counted as on the GPU (12·M'·h·(h + h_kv) for
     the projections, 12·b·h per visible query-key pair).  Returns (run, s',
     flops): run(s') times one pass in seconds."""
     import oracle as O
@@ -1048,12 +1051,12 @@ def attn_oracle_sample(cfg, inputs, target_s: float):
 
     def flops(sp_):
         pairs = sp_ * (sp_ + 1) / 2 if cfg.causal else float(sp_) * sp_
-        return 24.0 * sp_ * cfg.b * cfg.h * cfg.h + 12.0 * cfg.b * cfg.h * pairs
+        return 12.0 * sp_ * cfg.b * cfg.h * (cfg.h + cfg.h_kv) + 12.0 * cfg.b * cfg.h * pairs
 
     def run(sp_):
         t0 = time.perf_counter()
         O.attn_backward(X[:sp_].reshape(sp_ * cfg.b, cfg.h), Wqkv, Wo, dZ[:sp_].reshape(sp_ * cfg.b, cfg.h), sp_,
-                        cfg.b, cfg.heads, cfg.causal)
+                        cfg.b, cfg.heads, cfg.causal, cfg.groups)
         return time.perf_counter() - t0
 
     probe = min(32, cfg.s)

@@ -64,7 +64,7 @@
 extern "C" {
 #endif
 
-#define TPMLP_ABI_VERSION 3
+#define TPMLP_ABI_VERSION 4
 #define TPMLP_MAX_TP 64
 
 typedef enum tpmlp_status {
@@ -328,24 +328,35 @@ int tpmlp_wait_timeout_selftest(uint64_t timeout_ns, void* stream);
  * partitions of one device's buffers and the shard sums are folded into the
  * GEMM accumulators (the fused mode).
  *
- * Shapes: head width d = 128, so h = 128·heads; heads % tp == 0 (else
- * TPMLP_ERR_NOT_DIVISIBLE), s % tp == 0 under SP; float16 or bfloat16 storage
- * (float32 -> TPMLP_ERR_UNSUPPORTED); b < 65536, s ≤ 65535·128.  Activations
- * are sequence-first [s, b, ·] (row m = t·b + bi); every pointer 16-byte aligned.
+ * Grouped-query attention ("tensor-parallel-megatron" reading, attention
+ * section): kv_heads key/value heads (query groups) G, each shared by
+ * r = heads/G query heads; kv_heads = heads is multi-head attention.  The fused
+ * weight is [h + 2·h_kv, h] (h_kv = G·d), interleaved per group as the reading
+ * prints it, [q₁ q₂ k₁ v₁ | q₃ q₄ k₂ v₂ | …]: group g holds rows
+ * [g·(r+2)·d, (g+1)·(r+2)·d), its r query heads' q rows, then its k rows, then
+ * its v rows.  Query head j belongs to group j / r.  Tensor shard i owns groups
+ * [i·G/tp, (i+1)·G/tp) — contiguous rows of Wqkv, whole heads.
+ *
+ * Shapes: head width d = h/heads of 128 or 96 (else TPMLP_ERR_UNSUPPORTED);
+ * heads % kv_heads == 0 and kv_heads % tp == 0 (else TPMLP_ERR_NOT_DIVISIBLE:
+ * a shard must hold whole groups), s % tp == 0 under SP; float16 or bfloat16
+ * storage (float32 -> TPMLP_ERR_UNSUPPORTED); b < 65536, s ≤ 65535·128.
+ * Activations are sequence-first [s, b, ·] (row m = t·b + bi); every pointer
+ * 16-byte aligned.  W = h + 2·h_kv below.
  *   x      sp ? tp chunk pointers [s/tp, b, h] : one pointer [s, b, h]
- *   wqkv   [3h, h]: rows 3·128·j … 3·128·j+383 are head j's q, k and v rows
- *          (128 each); tensor shard i owns the contiguous rows of its heads
- *   wo     [h, h]: shard i owns the columns of its heads
- *   qkv    [s·b, 3h] output of the forward, input of the backward (head j's q,
- *          k, v in columns 384·j …)
- *   o      [s·b, h] attention output before the projection (head j in
- *          columns 128·j …); forward output, backward input
+ *   wqkv   [W, h], rows in the group layout above
+ *   wo     [h, h]: shard i owns the columns of its query heads
+ *   qkv    [s·b, W] output of the forward, input of the backward (columns in
+ *          the group layout)
+ *   o      [s·b, h] attention output before the projection (query head j in
+ *          columns d·j …); forward output, backward input
  *   lse    [b][heads][s_pad] float32, s_pad = s rounded up to a multiple of 128:
  *          log2 Σ_u 2^(x_tu) of each query row's scaled scores
  *          x = (q·k/√d)·log2(e); forward output, backward input
  *   z, dz, dx  like x
  *   dwqkv, dwo  weight gradients (overwritten), storage type
- *   dqkv   [s·b, 3h], dout [s·b, h]: backward scratch and outputs (dQKV, dO)
+ *   dqkv   [s·b, W], dout [s·b, h]: backward scratch and outputs (dQKV, dO); a
+ *          key/value head's gradient is the sum over its query heads
  * causal = 1 applies the decoder mask (key u visible to query t iff u ≤ t);
  * causal = 0 is the unmasked formula.  ws: tpmlp_attn_workspace_size() bytes
  * (same causal flag as the calls), 256-byte aligned: the gathered X and dZ when
@@ -358,13 +369,13 @@ int tpmlp_wait_timeout_selftest(uint64_t timeout_ns, void* stream);
  * is reported through tpmlp_device_status() as TPMLP_ERR_TIMEOUT.  Results
  * are deterministic (no atomics).
  * ------------------------------------------------------------------------- */
-size_t tpmlp_attn_workspace_size(int64_t s, int64_t b, int64_t h, int heads, int tp, int sp, int dtype,
-                                 int causal);
-int tpmlp_attn_forward(int64_t s, int64_t b, int64_t h, int heads, int tp, int sp, int dtype, int causal,
-                       const void* const* x, const void* wqkv, const void* wo, void* qkv, void* o,
+size_t tpmlp_attn_workspace_size(int64_t s, int64_t b, int64_t h, int heads, int kv_heads, int tp, int sp,
+                                 int dtype, int causal);
+int tpmlp_attn_forward(int64_t s, int64_t b, int64_t h, int heads, int kv_heads, int tp, int sp, int dtype,
+                       int causal, const void* const* x, const void* wqkv, const void* wo, void* qkv, void* o,
                        float* lse, void* const* z, void* ws, size_t ws_bytes, void* stream);
-int tpmlp_attn_backward(int64_t s, int64_t b, int64_t h, int heads, int tp, int sp, int dtype, int causal,
-                        const void* const* x, const void* wqkv, const void* wo, const void* qkv,
+int tpmlp_attn_backward(int64_t s, int64_t b, int64_t h, int heads, int kv_heads, int tp, int sp, int dtype,
+                        int causal, const void* const* x, const void* wqkv, const void* wo, const void* qkv,
                         const void* o, const float* lse, const void* const* dz, void* const* dx,
                         void* dwqkv, void* dwo, void* dqkv, void* dout, void* ws, size_t ws_bytes,
                         void* stream);

@@ -155,12 +155,12 @@ def load(path: str | None = None):
     lib.tpmlp_sp_residual_dropout_backward.restype = i32
     lib.tpmlp_sp_residual_dropout_backward.argtypes = [vpp, vpp, f32, vpp, i64, i64, i64, i32, i32, vp]
     lib.tpmlp_attn_workspace_size.restype = sz
-    lib.tpmlp_attn_workspace_size.argtypes = [i64, i64, i64, i32, i32, i32, i32, i32]
+    lib.tpmlp_attn_workspace_size.argtypes = [i64, i64, i64, i32, i32, i32, i32, i32, i32]
     lib.tpmlp_attn_forward.restype = i32
-    lib.tpmlp_attn_forward.argtypes = [i64, i64, i64, i32, i32, i32, i32, i32,
+    lib.tpmlp_attn_forward.argtypes = [i64, i64, i64, i32, i32, i32, i32, i32, i32,
                                        vpp, vp, vp, vp, vp, vp, vpp, vp, sz, vp]
     lib.tpmlp_attn_backward.restype = i32
-    lib.tpmlp_attn_backward.argtypes = [i64, i64, i64, i32, i32, i32, i32, i32,
+    lib.tpmlp_attn_backward.argtypes = [i64, i64, i64, i32, i32, i32, i32, i32, i32,
                                         vpp, vp, vp, vp, vp, vp, vpp, vpp, vp, vp, vp, vp, vp, sz, vp]
     lib.tpmlp_profile_start.restype = i32
     lib.tpmlp_profile_start.argtypes = []
@@ -442,26 +442,30 @@ class MLPBlock:
 # ---------------------------------------------------------------- attention block
 
 
-def attn_workspace_size(s, b, h, heads, tp, sp, dtype, causal) -> int:
-    return int(load().tpmlp_attn_workspace_size(s, b, h, heads, tp, int(bool(sp)), _dtype_code(dtype),
+def attn_workspace_size(s, b, h, heads, tp, sp, dtype, causal, kv_heads=None) -> int:
+    kv = heads if kv_heads is None else kv_heads
+    return int(load().tpmlp_attn_workspace_size(s, b, h, heads, kv, tp, int(bool(sp)), _dtype_code(dtype),
                                                  int(bool(causal))))
 
 
-def attn_forward(x, wqkv, wo, qkv, o, lse, z, *, s, b, h, heads, tp, sp, causal, workspace=None, dtype=None,
-                 stream=None) -> None:
-    """tpmlp_attn_forward.  x, z: lists of tp chunks under sp, else single tensors."""
+def attn_forward(x, wqkv, wo, qkv, o, lse, z, *, s, b, h, heads, tp, sp, causal, kv_heads=None, workspace=None,
+                 dtype=None, stream=None) -> None:
+    """tpmlp_attn_forward.  x, z: lists of tp chunks under sp, else single tensors;
+    kv_heads None = one key/value head per query head."""
     dt = _dtype_code(dtype if dtype is not None else wqkv.dtype)
-    _check(load().tpmlp_attn_forward(s, b, h, heads, tp, int(bool(sp)), dt, int(bool(causal)), _ptrs(x), _ptr(wqkv),
-                                     _ptr(wo), _ptr(qkv), _ptr(o), _ptr(lse), _ptrs(z), _ptr(workspace),
+    kv = heads if kv_heads is None else kv_heads
+    _check(load().tpmlp_attn_forward(s, b, h, heads, kv, tp, int(bool(sp)), dt, int(bool(causal)), _ptrs(x),
+                                     _ptr(wqkv), _ptr(wo), _ptr(qkv), _ptr(o), _ptr(lse), _ptrs(z), _ptr(workspace),
                                      0 if workspace is None else workspace.numel() * workspace.element_size(),
                                      _stream(stream)))
 
 
 def attn_backward(x, wqkv, wo, qkv, o, lse, dz, dx, dwqkv, dwo, dqkv, dout, *, s, b, h, heads, tp, sp, causal,
-                  workspace, dtype=None, stream=None) -> None:
+                  workspace, kv_heads=None, dtype=None, stream=None) -> None:
     """tpmlp_attn_backward.  x, dz, dx: lists of tp chunks under sp, else single tensors."""
     dt = _dtype_code(dtype if dtype is not None else wqkv.dtype)
-    _check(load().tpmlp_attn_backward(s, b, h, heads, tp, int(bool(sp)), dt, int(bool(causal)), _ptrs(x),
+    kv = heads if kv_heads is None else kv_heads
+    _check(load().tpmlp_attn_backward(s, b, h, heads, kv, tp, int(bool(sp)), dt, int(bool(causal)), _ptrs(x),
                                       _ptr(wqkv), _ptr(wo), _ptr(qkv), _ptr(o), _ptr(lse), _ptrs(dz), _ptrs(dx),
                                       _ptr(dwqkv), _ptr(dwo), _ptr(dqkv), _ptr(dout), _ptr(workspace),
                                       workspace.numel() * workspace.element_size(), _stream(stream)))
@@ -471,12 +475,14 @@ class AttnBlock:
     """One attention-block configuration; allocates outputs, saved activations and
     workspace with torch.empty (the library itself allocates nothing)."""
 
-    def __init__(self, s, b, h, heads, tp, sp, dtype, causal, device="cuda"):
+    def __init__(self, s, b, h, heads, tp, sp, dtype, causal, device="cuda", kv_heads=None):
         self.s, self.b, self.h, self.heads, self.tp, self.sp = s, b, h, heads, tp, bool(sp)
+        self.kv_heads = heads if kv_heads is None else kv_heads
         self.dtype, self.causal, self.device = dtype, bool(causal), device
         self.M = s * b
         self.s_pad = (s + 127) // 128 * 128
-        n = attn_workspace_size(s, b, h, heads, tp, sp, dtype, causal)
+        self.qkv_w = h + 2 * self.kv_heads * (h // heads)  # fused projection width h + 2·h_kv
+        n = attn_workspace_size(s, b, h, heads, tp, sp, dtype, causal, self.kv_heads)
         self.ws = torch.empty(max(n, 256), dtype=torch.uint8, device=device)
 
     def _act(self):
@@ -486,10 +492,11 @@ class AttnBlock:
         return torch.empty(self.s, self.b, self.h, dtype=self.dtype, device=self.device)
 
     def _kw(self):
-        return dict(s=self.s, b=self.b, h=self.h, heads=self.heads, tp=self.tp, sp=self.sp, causal=self.causal)
+        return dict(s=self.s, b=self.b, h=self.h, heads=self.heads, tp=self.tp, sp=self.sp, causal=self.causal,
+                    kv_heads=self.kv_heads)
 
     def forward(self, x, wqkv, wo, stream=None):
-        qkv = torch.empty(self.M, 3 * self.h, dtype=self.dtype, device=self.device)
+        qkv = torch.empty(self.M, self.qkv_w, dtype=self.dtype, device=self.device)
         o = torch.empty(self.M, self.h, dtype=self.dtype, device=self.device)
         lse = torch.empty(self.b, self.heads, self.s_pad, dtype=torch.float32, device=self.device)
         z = self._act()
@@ -498,9 +505,9 @@ class AttnBlock:
 
     def backward(self, x, wqkv, wo, fw, dz, stream=None):
         dx = self._act()
-        dwqkv = torch.empty(3 * self.h, self.h, dtype=self.dtype, device=self.device)
+        dwqkv = torch.empty(self.qkv_w, self.h, dtype=self.dtype, device=self.device)
         dwo = torch.empty(self.h, self.h, dtype=self.dtype, device=self.device)
-        dqkv = torch.empty(self.M, 3 * self.h, dtype=self.dtype, device=self.device)
+        dqkv = torch.empty(self.M, self.qkv_w, dtype=self.dtype, device=self.device)
         dout = torch.empty(self.M, self.h, dtype=self.dtype, device=self.device)
         attn_backward(x, wqkv, wo, fw["qkv"], fw["o"], fw["lse"], dz, dx, dwqkv, dwo, dqkv, dout,
                       workspace=self.ws, stream=stream, **self._kw())

@@ -46,7 +46,11 @@
 namespace tpmlp {
 namespace attn {
 
-constexpr int HD = 128;  // head width (d)
+// Head widths d: 128 and 96 (template parameter HDIM of the kernels).  A head's
+// q, k, v or o tile is loaded as two 64-column boxes whatever d is; with d = 96
+// the second box's upper 32 columns (the next head's, or TMA's zero fill past
+// the tensor) are never read by an MMA, whose K steps (S = Q·Kᵀ) and N extent
+// (P·V, dV, dK, dQ) stop at d.
 constexpr int ATT_THREADS = 384;  // warps 0-3: TMA, MMA, TMEM, idle; warps 4-11: two compute groups
 constexpr int COMPUTE_THREADS = 256;
 constexpr uint32_t HALF_ROW_BYTES = 128;  // one 64-column half row of 16-bit elements
@@ -115,13 +119,54 @@ __device__ __forceinline__ void mma8_ss(uint32_t d, const uint64_t* a, const uin
       "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7]), "r"(idesc), "r"(acc0)
       : "memory");
 }
+// The same over 6 K steps (a head width of 96).
+__device__ __forceinline__ void mma6_ss(uint32_t d, const uint64_t* a, const uint64_t* b, uint32_t idesc,
+                                        uint32_t acc0) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.b32 p, %14, 0;\n\t"
+      "setp.eq.b32 q, %14, %14;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %7, %13, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %2, %8, %13, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %9, %13, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %10, %13, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %11, %13, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %6, %12, %13, q;\n\t}" ::"r"(d),
+      "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(a[4]), "l"(a[5]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]),
+      "l"(b[4]), "l"(b[5]), "r"(idesc), "r"(acc0)
+      : "memory");
+}
+// D (+)= Σ_ks A_ks·B_ks over NK (6 or 8) K steps of shared-memory operands.
+template <int NK>
+__device__ __forceinline__ void mma_ss(uint32_t d, const uint64_t* a, const uint64_t* b, uint32_t idesc,
+                                       uint32_t acc0) {
+  static_assert(NK == 6 || NK == 8, "K steps");
+  if constexpr (NK == 8)
+    mma8_ss(d, a, b, idesc, acc0);
+  else
+    mma6_ss(d, a, b, idesc, acc0);
+}
 // Same with A in tensor memory (M = 128 lanes × K 16-bit elements, two per
-// 32-bit column, element 2j in the low half of column j): NK K steps (4 or 8),
-// A columns a, a+8, a+16, ….
+// 32-bit column, element 2j in the low half of column j): NK K steps (4, 6 or
+// 8), A columns a, a+8, a+16, ….
 template <int NK>
 __device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, const uint64_t* b, uint32_t idesc, uint32_t acc0) {
-  static_assert(NK == 4 || NK == 8, "K steps");
-  if constexpr (NK == 4) {
+  static_assert(NK == 4 || NK == 6 || NK == 8, "K steps");
+  if constexpr (NK == 6) {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.b32 p, %14, 0;\n\t"
+        "setp.eq.b32 q, %14, %14;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %7, %13, p;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], %8, %13, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %9, %13, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%4], %10, %13, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], %11, %13, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%6], %12, %13, q;\n\t}" ::"r"(d),
+        "r"(a), "r"(a + 8), "r"(a + 16), "r"(a + 24), "r"(a + 32), "r"(a + 40), "l"(b[0]), "l"(b[1]), "l"(b[2]),
+        "l"(b[3]), "l"(b[4]), "l"(b[5]), "r"(idesc), "r"(acc0)
+        : "memory");
+  } else if constexpr (NK == 4) {
     asm volatile(
         "{\n\t.reg .pred p, q;\n\t"
         "setp.ne.b32 p, %10, 0;\n\t"
@@ -151,10 +196,11 @@ __device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, const uint64_t* b
         : "memory");
   }
 }
-// The 8 K-step descriptors of a K-major [rows × 128] tile / an MN-major tile.
-__device__ __forceinline__ void kdescs(uint64_t base, int rows, uint64_t* o) {
+// The K-step descriptors (8, or nk) of a K-major [rows × 128] tile / an MN-major tile.
+__device__ __forceinline__ void kdescs(uint64_t base, int rows, uint64_t* o, int nk = 8) {
 #pragma unroll
-  for (int ks = 0; ks < 8; ++ks) o[ks] = base + koff(rows, ks);
+  for (int ks = 0; ks < 8; ++ks)
+    if (ks < nk) o[ks] = base + koff(rows, ks);
 }
 __device__ __forceinline__ void mndescs(uint64_t base, int nk, uint64_t* o) {
 #pragma unroll
@@ -222,11 +268,23 @@ struct AttnParams {
   int64_t ds_head_tiles;  // dSᵀ tiles per (sequence, head)
   int nqt64;           // 64-query tiles per sequence, ⌈s/64⌉
   int s, b, h, heads, s_pad, causal;
+  int kv_heads;        // key/value heads (query groups); query head j is in group j / qpg
+  int qpg;             // query heads per group
+  int d;               // head width
+  int64_t ldqkv;       // columns of QKV: (heads + 2·kv_heads)·d
   float scale_log2;    // log2(e)/√d
   float scale;         // 1/√d
   unsigned* status;
   uint64_t timeout_ns;
 };
+
+// Columns of QKV (the fused projection's output, group-interleaved: group g
+// holds its qpg query heads' q, then its k, then its v, d columns each).
+__device__ __forceinline__ int col_q(const AttnParams& p, int head) {
+  const int g = head / p.qpg;
+  return (g * (p.qpg + 2) + (head - g * p.qpg)) * p.d;
+}
+__device__ __forceinline__ int col_k(const AttnParams& p, int group) { return (group * (p.qpg + 2) + p.qpg) * p.d; }
 
 // dSᵀ is kept in HBM as [128 keys × 64 queries] tiles, each the 16 KB image of
 // the 128-byte-swizzled shared-memory operand (one 64-column half).  Per
@@ -306,8 +364,10 @@ __device__ __forceinline__ void tmem_wait_ld_tied(uint32_t* r) {
       : "memory");
 }
 
-template <int DT>
+template <int DT, int HDIM>
 __global__ void __launch_bounds__(ATT_THREADS, 1) attn_fwd_kernel(const __grid_constant__ AttnParams p) {
+  static_assert(HDIM == 128 || HDIM == 96, "head width");
+  constexpr int NK = HDIM / 16;  // K steps of S = Q·Kᵀ
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   Tail* tail = reinterpret_cast<Tail*>(smem + F_END);
@@ -315,8 +375,8 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_fwd_kernel(const __grid_c
   volatile int* abort_flag = &tail->abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // grid (256-row query pairs, heads, b): a head's pairs run side by side and
-  // share its K and V through L2; under the causal mask the longest pairs (the
+  // grid (256-row query pairs, query heads, b): a head's pairs run side by side
+  // and share its group's K and V through L2; under the causal mask the longest pairs (the
   // last ones) are dispatched first
   const int npt = (p.s + 2 * F_BQ - 1) / (2 * F_BQ);
   const int pt = p.causal ? npt - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x);
@@ -326,7 +386,6 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_fwd_kernel(const __grid_c
   // key tiles each query tile sees (up to its diagonal under the mask); NA ≤ NB ≤ NA + 1
   const int NA = p.causal ? min(nkt, 2 * pt + 1) : nkt;
   const int NB = p.causal ? min(nkt, 2 * pt + 2) : nkt;
-  const int colq = 3 * HD * head, colk = colq + HD, colv = colq + 2 * HD;
 
   if (threadIdx.x == 0) {
     mbar_init(bar(FB_Q), 1);
@@ -357,6 +416,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_fwd_kernel(const __grid_c
 
   if (warp == 0) {
     if (lane == 0) {
+      const int colq = col_q(p, head), colk = col_k(p, head / p.qpg), colv = colk + HDIM;
       tma_prefetch_map(&p.qkv128);
       uint32_t issued = 0;  // K/V tiles with copies that may still be in flight
       mbar_arrive_expect_tx(bar(FB_Q), 2 * F_TILE);
@@ -390,7 +450,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_fwd_kernel(const __grid_c
     // tiles fall into step and their softmaxes contend; measured slower).
     if (lane == 0) {
       constexpr uint32_t idesc_s = make_idesc_f16(DT == DT_BF16, false, false, 128, F_BK);
-      constexpr uint32_t idesc_o = make_idesc_f16(DT == DT_BF16, false, true, 128, HD);
+      constexpr uint32_t idesc_o = make_idesc_f16(DT == DT_BF16, false, true, 128, HDIM);
       const uint64_t dQA = sdesc_k(sQA), dQB = sdesc_k(sQB);
       const uint64_t dK0 = sdesc_k(sK0), dK1 = sdesc_k(sK0 + F_TILE);
       const uint64_t dV0 = sdesc_mn(sV0, 128), dV1 = sdesc_mn(sV0 + F_TILE, 128);
@@ -399,9 +459,9 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_fwd_kernel(const __grid_c
       };
       auto issue_s = [&](int t, int n) {  // S_t = Q_t·K(n)ᵀ
         uint64_t a[8], b[8];
-        kdescs(t ? dQB : dQA, 128, a);
-        kdescs((n & 1) ? dK1 : dK0, 128, b);
-        mma8_ss(tmem + t * 128, a, b, idesc_s, 0u);
+        kdescs(t ? dQB : dQA, 128, a, NK);
+        kdescs((n & 1) ? dK1 : dK0, 128, b, NK);
+        mma_ss<NK>(tmem + t * 128, a, b, idesc_s, 0u);
         tc_commit(bar(FB_SF + t));
       };
       auto issue_pv = [&](int t, int n) {  // O_t += P_t·V(n), P_t from tensor memory
@@ -561,7 +621,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_fwd_kernel(const __grid_c
         // brought to the new reference before this tile's P·V is issued
         const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll 1
-        for (int cc = 0; cc < 4; ++cc) {
+        for (int cc = 0; cc < HDIM / 32; ++cc) {
           float o[32];
           tmem_ld32(tO + cc * 32, o);
 #pragma unroll
@@ -586,7 +646,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_fwd_kernel(const __grid_c
       const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
       const int64_t mrow = static_cast<int64_t>(q) * p.b + bi;
 #pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
+      for (int cc = 0; cc < HDIM / 32; ++cc) {
         float o[32];
         tmem_ld32(tO + cc * 32, o);
         if (q < p.s) {
@@ -594,7 +654,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_fwd_kernel(const __grid_c
           for (int j = 0; j < 32; ++j) o[j] *= inv_l;
 #pragma unroll
           for (int k4 = 0; k4 < 4; ++k4)
-            store_row_chunk<DT>(p.o, mrow * p.h + head * HD + cc * 32 + k4 * 8, o + k4 * 8);
+            store_row_chunk<DT>(p.o, mrow * p.h + head * HDIM + cc * 32 + k4 * 8, o + k4 * 8);
         }
       }
       // rows past s (the padded tail of the last 128-row tile) get 0: the
@@ -616,9 +676,9 @@ template <int DT>
 __global__ void __launch_bounds__(256) attn_bwd_delta_kernel(const void* __restrict__ dout,
                                                              const void* __restrict__ o, const float* __restrict__ lse,
                                                              float* __restrict__ delta, float* __restrict__ nlse,
-                                                             int s, int b, int h, int heads, int s_pad) {
-  // one half-warp per (token row, head); each lane takes 8 of the 128 columns
-  // with 16-byte loads
+                                                             int s, int b, int h, int heads, int s_pad, int d) {
+  // one half-warp per (token row, head); lane i takes columns [8i, 8i+8) of
+  // the d (≤ 128) with 16-byte loads
   const int64_t pid = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 4;
   const int sub = threadIdx.x & 15;
   const int64_t total = static_cast<int64_t>(s_pad) * b * heads;
@@ -628,9 +688,9 @@ __global__ void __launch_bounds__(256) attn_bwd_delta_kernel(const void* __restr
   const int bi = static_cast<int>(rest % b);
   const int q = static_cast<int>(rest / b);
   float acc = 0.0f;
-  if (q < s) {
+  if (q < s && sub * 8 < d) {
     using T = typename Storage<DT>::T;
-    const int64_t off = (static_cast<int64_t>(q) * b + bi) * h + head * HD + sub * 8;
+    const int64_t off = (static_cast<int64_t>(q) * b + bi) * h + static_cast<int64_t>(head) * d + sub * 8;
     float a[8], c[8];
     unpack8<DT>(ldg_nc_v4(static_cast<const T*>(dout) + off), a);
     unpack8<DT>(ldg_nc_v4(static_cast<const T*>(o) + off), c);
@@ -648,7 +708,8 @@ __global__ void __launch_bounds__(256) attn_bwd_delta_kernel(const void* __restr
 }
 
 // ================================================================== backward: dK, dV
-// Per (128-key tile, head, sequence) over 64-query tiles.  K and V never change
+// Per (128-key tile, key/value head, sequence) over the 64-query tiles of the
+// group's query heads.  K and V never change
 // within a CTA, so after TMA lands them the element-wise warps copy them into
 // tensor memory (16-bit, two per column), where they are the A operands of
 // Sᵀ = K·Qᵀ and dPᵀ = V·dOᵀ: those MMAs (N = 64) then read only Q or dO from
@@ -691,8 +752,10 @@ __device__ __forceinline__ void mma4_ss(uint32_t d, const uint64_t* a, const uin
       : "memory");
 }
 
-template <int DT>
+template <int DT, int HDIM>
 __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dkdv_kernel(const __grid_constant__ AttnParams p) {
+  static_assert(HDIM == 128 || HDIM == 96, "head width");
+  constexpr int NK = HDIM / 16;  // K steps of Sᵀ = K·Qᵀ and dPᵀ = V·dOᵀ
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   Tail* tail = reinterpret_cast<Tail*>(smem + KV_END);
@@ -700,21 +763,29 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dkdv_kernel(const __g
   volatile int* abort_flag = &tail->abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // grid (key tiles, heads, b): the tiles of one head share its Q and dO through
-  // L2; under the causal mask the first key tiles see the most query tiles and
-  // are dispatched first
+  // grid (key tiles, key/value heads, b): the tiles of one group share its
+  // query heads' Q and dO through L2; under the causal mask the first key tiles
+  // see the most query tiles and are dispatched first.  The CTA's steps run over
+  // the group's query heads and, for each, the 64-query tiles the key tile
+  // sees: step it is query head grp·qpg + it / Nh, query tile qt_first + it % Nh,
+  // and dK, dV accumulate over all of them (a key/value head shared by several
+  // query heads collects their gradients).
   const int kt = static_cast<int>(blockIdx.x);
-  const int head = blockIdx.y, bi = blockIdx.z;
+  const int grp = blockIdx.y, bi = blockIdx.z;
   const int k0 = kt * KV_BK;
   const int nqt = (p.s + KV_BQ - 1) / KV_BQ;
   const int qt_first = p.causal ? k0 / KV_BQ : 0;
-  const int N = nqt - qt_first;
-  const int colq = 3 * HD * head, colk = colq + HD, colv = colq + 2 * HD;
-  const float* lse_row = p.nlse + (static_cast<int64_t>(bi) * p.heads + head) * p.s_pad;  // −lse2
-  const float* delta_row = p.delta + (static_cast<int64_t>(bi) * p.heads + head) * p.s_pad;
-  // this key tile's dSᵀ tiles in HBM, one per 64-query tile it visits
-  uint8_t* ds_out = p.ds + ((static_cast<int64_t>(bi) * p.heads + head) * p.ds_head_tiles +
-                            ds_tile_index(kt, p.nqt64, p.causal)) * DS_TILE;
+  const int Nh = nqt - qt_first;  // query tiles per query head
+  const int N = p.qpg * Nh;       // steps
+  const int colk = col_k(p, grp), colv = colk + HDIM;
+  auto step_head = [&](int it) { return grp * p.qpg + it / Nh; };
+  auto step_qtile = [&](int it) { return qt_first + it % Nh; };
+  auto head_row = [&](int head) { return (static_cast<int64_t>(bi) * p.heads + head) * p.s_pad; };
+  // dSᵀ tile of step it in HBM: key tile kt's tiles of its query head, one per 64-query tile
+  auto ds_out = [&](int it) {
+    return p.ds + ((static_cast<int64_t>(bi) * p.heads + step_head(it)) * p.ds_head_tiles +
+                   ds_tile_index(kt, p.nqt64, p.causal) + it % Nh) * DS_TILE;
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(bar(KB_KV), 1);
@@ -757,14 +828,15 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dkdv_kernel(const __g
         const int st = n % KV_ST;
         const uint32_t par = ((n / KV_ST) & 1) ^ 1u;
         if (!(ok = mbar_wait_bounded(bar(KB_E + st), par, abort_flag, p.status, p.timeout_ns))) break;
-        const int qq = (qt_first + n) * KV_BQ;
+        const int head = step_head(n);
+        const int qq = step_qtile(n) * KV_BQ;
         uint8_t* sb = stage_base(st);
         const uint32_t f = bar(KB_F + st);
         mbar_arrive_expect_tx(f, KV_STAGE);
-        load_tile(smem_u32(sb), &p.qkv64, f, colq, bi, qq, 64);
-        load_tile(smem_u32(sb + KV_QTILE), &p.do64, f, head * HD, bi, qq, 64);
-        bulk_load(smem_u32(sb + 2 * KV_QTILE), lse_row + qq, 256, f);
-        bulk_load(smem_u32(sb + 2 * KV_QTILE + 256), delta_row + qq, 256, f);
+        load_tile(smem_u32(sb), &p.qkv64, f, col_q(p, head), bi, qq, 64);
+        load_tile(smem_u32(sb + KV_QTILE), &p.do64, f, head * HDIM, bi, qq, 64);
+        bulk_load(smem_u32(sb + 2 * KV_QTILE), p.nlse + head_row(head) + qq, 256, f);  // −lse2
+        bulk_load(smem_u32(sb + 2 * KV_QTILE + 256), p.delta + head_row(head) + qq, 256, f);
         issued = n + 1;
       }
       if (!ok) {
@@ -777,7 +849,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dkdv_kernel(const __g
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t idesc_s = make_idesc_f16(DT == DT_BF16, false, false, 128, KV_BQ);
-      constexpr uint32_t idesc_acc = make_idesc_f16(DT == DT_BF16, false, true, 128, HD);
+      constexpr uint32_t idesc_acc = make_idesc_f16(DT == DT_BF16, false, true, 128, HDIM);
       // K and V are in tensor memory
       bool ok = mbar_wait_bounded(bar(KB_KVT), 0u, abort_flag, p.status, p.timeout_ns);
       // Sᵀ = K·Qᵀ and dPᵀ = V·dOᵀ of query tile n, K and V from tensor memory
@@ -787,10 +859,10 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dkdv_kernel(const __g
         tc_fence_after();
         const uint32_t sQ = smem_u32(stage_base(st)), sDO = sQ + KV_QTILE;
         uint64_t b[8];
-        kdescs(sdesc_k(sQ), 64, b);
-        mma_ts<8>(tmem + KT_S, tmem + KT_K, b, idesc_s, 0u);
-        kdescs(sdesc_k(sDO), 64, b);
-        mma_ts<8>(tmem + KT_DP, tmem + KT_V, b, idesc_s, 0u);
+        kdescs(sdesc_k(sQ), 64, b, NK);
+        mma_ts<NK>(tmem + KT_S, tmem + KT_K, b, idesc_s, 0u);
+        kdescs(sdesc_k(sDO), 64, b, NK);
+        mma_ts<NK>(tmem + KT_DP, tmem + KT_V, b, idesc_s, 0u);
         tc_commit(bar(KB_SF));
         return true;
       };
@@ -809,7 +881,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dkdv_kernel(const __g
         tc_fence_after();
         const uint32_t sQ = smem_u32(stage_base(st)), sDO = sQ + KV_QTILE;
         const uint32_t sDSn = sDST + (n % KV_DSB) * DS_TILE;
-        bulk_store(ds_out + static_cast<int64_t>(n) * DS_TILE, sDSn, DS_TILE);  // dSᵀ for the dQ kernel
+        bulk_store(ds_out(n), sDSn, DS_TILE);  // dSᵀ for the dQ kernel
         // dV += Pᵀ·dO and dK += dSᵀ·Q: A a [128 keys × 64 queries] K-major half,
         // K step ks 32 bytes along it; B MN-major from the stage
         uint64_t a[4], bd[8];
@@ -837,7 +909,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dkdv_kernel(const __g
     __syncwarp();
   } else if (warp >= 4) {
     // Two groups of four warps; group g takes query columns [32g, 32g+32) of
-    // every 64-query tile and columns [64g, 64g+64) of dV and dK.
+    // every 64-query tile and the 32-column chunks g, g + 2, … of dV and dK.
     const int g = (warp - 4) >> 2;
     const int qw = warp & 3;
     const int r = qw * 32 + lane;
@@ -886,7 +958,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dkdv_kernel(const __g
       mbar_arrive(bar(KB_SC));  // Sᵀ/dPᵀ may be overwritten by the next tile's
       const float4* lse4 = reinterpret_cast<const float4*>(stage_base(st) + 2 * KV_QTILE) + g * 8;
       const float4* del4 = lse4 + 16;
-      const int qq = (qt_first + n) * KV_BQ + g * 32;
+      const int qq = step_qtile(n) * KV_BQ + g * 32;
       const bool masked = qq + 32 > p.s || k0 + KV_BK > p.s || (p.causal && k0 + KV_BK - 1 > qq);
       float lj[32], dj[32];
 #pragma unroll
@@ -938,10 +1010,9 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dkdv_kernel(const __g
     if (ok) {
       tc_fence_after();
       const int64_t mrow = static_cast<int64_t>(key) * p.b + bi;
-      const int64_t ld = 3 * static_cast<int64_t>(p.h);
+      const int64_t ld = p.ldqkv;
 #pragma unroll 1
-      for (int cc = 0; cc < 2; ++cc) {
-        const int col = g * 64 + cc * 32;
+      for (int col = g * 32; col < HDIM; col += 64) {
         float dv[32], dk[32];
         tmem_ld32(tl + KT_DV + col, dv);
         tmem_ld32(tl + KT_DK + col, dk);
@@ -979,8 +1050,9 @@ enum { QB_F = 0, QB_E = QB_F + DQ_ST, QB_MM = QB_E + DQ_ST, QB_DRAIN = QB_MM + 1
 static_assert(QB_COUNT <= 24, "barrier slots");
 static_assert(DQ_SMEM <= 232448 && KV_SMEM <= 232448 && F_SMEM <= 232448, "shared memory per CTA");
 
-template <int DT>
+template <int DT, int HDIM>
 __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dq_kernel(const __grid_constant__ AttnParams p) {
+  static_assert(HDIM == 128 || HDIM == 96, "head width");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   Tail* tail = reinterpret_cast<Tail*>(smem + DQ_END);
@@ -988,7 +1060,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dq_kernel(const __gri
   volatile int* abort_flag = &tail->abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // grid (query tiles, heads, b); under the causal mask the last query tiles see
+  // grid (query tiles, query heads, b); under the causal mask the last query tiles see
   // the most key tiles and are dispatched first
   const int ntq = (p.s + 127) / 128;
   const int qt = p.causal ? ntq - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x);
@@ -998,7 +1070,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dq_kernel(const __gri
   // query rows 64–127 of this tile exist (else that half of A is never loaded:
   // it only feeds output rows past s, which are not stored)
   const bool upper = 2 * qt + 1 < p.nqt64;
-  const int colq = 3 * HD * head, colk = colq + HD;
+  const int colq = col_q(p, head), colk = col_k(p, head / p.qpg);  // K of the head's group
   const uint8_t* ds_head = p.ds + (static_cast<int64_t>(bi) * p.heads + head) * p.ds_head_tiles * DS_TILE;
 
   if (threadIdx.x == 0) {
@@ -1045,7 +1117,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dq_kernel(const __gri
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idesc = make_idesc_f16(DT == DT_BF16, true, true, 128, HD);
+      constexpr uint32_t idesc = make_idesc_f16(DT == DT_BF16, true, true, 128, HDIM);
       bool ok = true;
       for (int n = 0; ok && n < N; ++n) {
         const int st = n % DQ_ST;
@@ -1063,7 +1135,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dq_kernel(const __gri
     }
     __syncwarp();
   } else if (warp >= 4) {
-    // Two groups of four warps; group g stores columns [64g, 64g+64) of dQ.
+    // Two groups of four warps; group g stores the 32-column chunks g, g + 2, … of dQ.
     const int g = (warp - 4) >> 2;
     const int qw = warp & 3;
     const int r = qw * 32 + lane;
@@ -1073,10 +1145,9 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dq_kernel(const __gri
     if (__all_sync(0xffffffffu, ok)) {
       tc_fence_after();
       const int64_t mrow = static_cast<int64_t>(q) * p.b + bi;
-      const int64_t ld = 3 * static_cast<int64_t>(p.h);
+      const int64_t ld = p.ldqkv;
 #pragma unroll 1
-      for (int cc = 0; cc < 2; ++cc) {
-        const int col = g * 64 + cc * 32;
+      for (int col = g * 32; col < HDIM; col += 64) {
         float dq[32];
         tmem_ld32(tl + col, dq);
         if (q < p.s) {
@@ -1141,6 +1212,8 @@ int make_map3(CUtensorMap* m, int dtype, const void* base, int64_t cols, int64_t
 struct Shape {
   int64_t s, b, h;
   int heads, tp, sp, dtype, causal;
+  int kv_heads, d;        // key/value heads (groups), head width
+  int64_t qkv_w;          // columns of QKV / rows of Wqkv: h + 2·h_kv
   int64_t M, s_pad, rpc;  // tokens, s rounded up to 128, rows per SP chunk
   size_t e;
   bool fused_ag;          // SP chunks read in place by the GEMMs
@@ -1150,24 +1223,36 @@ const uint8_t* cb(const void* p) { return static_cast<const uint8_t*>(p); }
 uint8_t* wb(void* p) { return static_cast<uint8_t*>(p); }
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-int check_shape(int64_t s, int64_t b, int64_t h, int heads, int tp, int sp, int dtype, int causal, Shape* out) {
+int check_shape(int64_t s, int64_t b, int64_t h, int heads, int kv_heads, int tp, int sp, int dtype, int causal,
+                Shape* out) {
   if (s < 0 || b < 1 || h < 1) return set_error(TPMLP_ERR_INVALID_ARG, "s >= 0, b >= 1 and h >= 1 required");
   if (heads < 1 || tp < 1 || tp > TPMLP_MAX_TP) return set_error(TPMLP_ERR_INVALID_ARG, "heads >= 1 and tp in [1, 64]");
+  if (kv_heads < 1 || kv_heads > heads) return set_error(TPMLP_ERR_INVALID_ARG, "kv_heads must be in [1, heads]");
   if (sp != 0 && sp != 1) return set_error(TPMLP_ERR_INVALID_ARG, "sp must be 0 or 1");
   if (causal != 0 && causal != 1) return set_error(TPMLP_ERR_INVALID_ARG, "causal must be 0 or 1");
   if (dtype != DT_F16 && dtype != DT_BF16)
     return set_error(TPMLP_ERR_UNSUPPORTED, "the attention block runs in float16 or bfloat16 storage");
-  if (h != static_cast<int64_t>(heads) * HD) return set_error(TPMLP_ERR_UNSUPPORTED, "head width must be 128 (h = 128·heads)");
-  if (heads % tp != 0) return set_error(TPMLP_ERR_NOT_DIVISIBLE, "the number of heads must be divisible by tensor parallel size");
+  if (h % heads != 0 || (h / heads != 128 && h / heads != 96))
+    return set_error(TPMLP_ERR_UNSUPPORTED, "head width h/heads must be 128 or 96");
+  if (heads % kv_heads != 0)
+    return set_error(TPMLP_ERR_NOT_DIVISIBLE, "the number of heads must be divisible by the number of kv heads");
+  if (kv_heads % tp != 0)
+    return set_error(TPMLP_ERR_NOT_DIVISIBLE,
+                     "the number of kv heads (query groups) must be divisible by tensor parallel size");
   if (sp && s % tp != 0)
     return set_error(TPMLP_ERR_NOT_DIVISIBLE, "First dimension of the tensor should be divisible by tensor parallel size");
-  if (s > 65535ll * 128 || s * b >= (1ll << 31) || 3 * h >= (1ll << 31) || b >= 65536 || heads > 65535)
+  const int64_t d = h / heads;
+  const int64_t qkv_w = (static_cast<int64_t>(heads) + 2 * kv_heads) * d;
+  if (s > 65535ll * 128 || s * b >= (1ll << 31) || qkv_w >= (1ll << 31) || b >= 65536 || heads > 65535)
     return set_error(TPMLP_ERR_UNSUPPORTED, "extent too large");
   Shape k;
   k.s = s;
   k.b = b;
   k.h = h;
   k.heads = heads;
+  k.kv_heads = kv_heads;
+  k.d = static_cast<int>(d);
+  k.qkv_w = qkv_w;
   k.tp = tp;
   k.sp = sp;
   k.dtype = dtype;
@@ -1247,35 +1332,71 @@ int base_params(const Shape& k, AttnParams* p) {
   p->b = static_cast<int>(k.b);
   p->h = static_cast<int>(k.h);
   p->heads = k.heads;
+  p->kv_heads = k.kv_heads;
+  p->qpg = k.heads / k.kv_heads;
+  p->d = k.d;
+  p->ldqkv = k.qkv_w;
   p->s_pad = static_cast<int>(k.s_pad);
   p->causal = k.causal;
-  p->scale = 1.0f / std::sqrt(static_cast<float>(HD));
-  p->scale_log2 = 1.4426950408889634f / std::sqrt(static_cast<float>(HD));
+  p->scale = 1.0f / std::sqrt(static_cast<float>(k.d));
+  p->scale_log2 = 1.4426950408889634f / std::sqrt(static_cast<float>(k.d));
   p->status = dev->status;
   p->timeout_ns = wait_timeout_ns();
   return TPMLP_OK;
+}
+
+template <int DT, int HDIM>
+void fwd_kernel_launch(dim3 grid, const AttnParams& p, cudaStream_t st) {
+  attn_fwd_kernel<DT, HDIM><<<grid, ATT_THREADS, F_SMEM, st>>>(p);
+}
+template <int DT, int HDIM>
+const void* fwd_kernel_fn() {
+  return reinterpret_cast<const void*>(attn_fwd_kernel<DT, HDIM>);
 }
 
 int launch_core_forward(const Shape& k, const void* qkv, void* o, float* lse, cudaStream_t st) {
   AttnParams p;
   int rc = base_params(k, &p);
   if (rc) return rc;
-  if ((rc = make_map3(&p.qkv128, k.dtype, qkv, 3 * k.h, k.b, k.s, 128))) return rc;
+  if ((rc = make_map3(&p.qkv128, k.dtype, qkv, k.qkv_w, k.b, k.s, 128))) return rc;
   p.o = o;
   p.lse = lse;
   const dim3 grid(static_cast<unsigned>((k.s + 2 * F_BQ - 1) / (2 * F_BQ)), static_cast<unsigned>(k.heads),
                   static_cast<unsigned>(k.b));
-  const void* fn = k.dtype == DT_BF16 ? reinterpret_cast<const void*>(attn_fwd_kernel<DT_BF16>)
-                                      : reinterpret_cast<const void*>(attn_fwd_kernel<DT_F16>);
+  const bool bf = k.dtype == DT_BF16, wide = k.d == 128;
+  const void* fn = bf ? (wide ? fwd_kernel_fn<DT_BF16, 128>() : fwd_kernel_fn<DT_BF16, 96>())
+                      : (wide ? fwd_kernel_fn<DT_F16, 128>() : fwd_kernel_fn<DT_F16, 96>());
   if ((rc = set_smem(fn, F_SMEM))) return rc;
   const int ph = prof_begin(PROF_ATTN, st);
-  if (k.dtype == DT_BF16) attn_fwd_kernel<DT_BF16><<<grid, ATT_THREADS, F_SMEM, st>>>(p);
-  else attn_fwd_kernel<DT_F16><<<grid, ATT_THREADS, F_SMEM, st>>>(p);
-  // QKᵀ and P·V over the visible (query, key) pairs
+  if (bf) {
+    if (wide) fwd_kernel_launch<DT_BF16, 128>(grid, p, st);
+    else fwd_kernel_launch<DT_BF16, 96>(grid, p, st);
+  } else {
+    if (wide) fwd_kernel_launch<DT_F16, 128>(grid, p, st);
+    else fwd_kernel_launch<DT_F16, 96>(grid, p, st);
+  }
+  // QKᵀ and P·V over the visible (query, key) pairs of every query head
   const double pairs = k.causal ? static_cast<double>(k.s) * (k.s + 1) / 2 : static_cast<double>(k.s) * k.s;
-  prof_end(ph, 4.0 * pairs * HD * k.heads * k.b, st);
+  prof_end(ph, 4.0 * pairs * k.d * k.heads * k.b, st);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return set_error(TPMLP_ERR_CUDA, std::string("attention forward launch: ") + cudaGetErrorString(e));
+  return TPMLP_OK;
+}
+
+template <int DT, int HDIM>
+int bwd_kernels_launch(const Shape& k, const AttnParams& p, const void* dout, const void* o, const float* lse,
+                       float* delta, float* nlse, cudaStream_t st) {
+  const void* fkv = reinterpret_cast<const void*>(attn_bwd_dkdv_kernel<DT, HDIM>);
+  const void* fq = reinterpret_cast<const void*>(attn_bwd_dq_kernel<DT, HDIM>);
+  int rc;
+  if ((rc = set_smem(fkv, KV_SMEM)) || (rc = set_smem(fq, DQ_SMEM))) return rc;
+  const int64_t row_heads = k.s_pad * k.b * k.heads;  // (row, query head) pairs, a half-warp each
+  const unsigned gd = static_cast<unsigned>((row_heads * 16 + 255) / 256);
+  attn_bwd_delta_kernel<DT><<<gd, 256, 0, st>>>(dout, o, lse, delta, nlse, p.s, p.b, p.h, p.heads, p.s_pad, p.d);
+  const dim3 gkv(static_cast<unsigned>(k.s_pad / 128), static_cast<unsigned>(k.kv_heads), static_cast<unsigned>(k.b));
+  attn_bwd_dkdv_kernel<DT, HDIM><<<gkv, ATT_THREADS, KV_SMEM, st>>>(p);
+  const dim3 gq(static_cast<unsigned>(k.s_pad / 128), static_cast<unsigned>(k.heads), static_cast<unsigned>(k.b));
+  attn_bwd_dq_kernel<DT, HDIM><<<gq, ATT_THREADS, DQ_SMEM, st>>>(p);
   return TPMLP_OK;
 }
 
@@ -1284,8 +1405,8 @@ int launch_core_backward(const Shape& k, const void* qkv, const void* o, const f
   AttnParams p;
   int rc = base_params(k, &p);
   if (rc) return rc;
-  if ((rc = make_map3(&p.qkv128, k.dtype, qkv, 3 * k.h, k.b, k.s, 128)) ||
-      (rc = make_map3(&p.qkv64, k.dtype, qkv, 3 * k.h, k.b, k.s, 64)) ||
+  if ((rc = make_map3(&p.qkv128, k.dtype, qkv, k.qkv_w, k.b, k.s, 128)) ||
+      (rc = make_map3(&p.qkv64, k.dtype, qkv, k.qkv_w, k.b, k.s, 64)) ||
       (rc = make_map3(&p.do64, k.dtype, dout, k.h, k.b, k.s, 64)))
     return rc;
   p.lse = const_cast<float*>(lse);
@@ -1294,29 +1415,20 @@ int launch_core_backward(const Shape& k, const void* qkv, const void* o, const f
   p.ds = ds;
   p.ds_head_tiles = ds_head_tiles(k);
   p.nqt64 = static_cast<int>((k.s + 63) / 64);
-  const bool bf = k.dtype == DT_BF16;
-  const void* fkv = bf ? reinterpret_cast<const void*>(attn_bwd_dkdv_kernel<DT_BF16>)
-                       : reinterpret_cast<const void*>(attn_bwd_dkdv_kernel<DT_F16>);
-  const void* fq = bf ? reinterpret_cast<const void*>(attn_bwd_dq_kernel<DT_BF16>)
-                      : reinterpret_cast<const void*>(attn_bwd_dq_kernel<DT_F16>);
-  if ((rc = set_smem(fkv, KV_SMEM)) || (rc = set_smem(fq, DQ_SMEM))) return rc;
-  const int ph = prof_begin(PROF_ATTN, st);
-  const int64_t row_heads = k.s_pad * k.b * k.heads;  // (row, head) pairs, a half-warp each
-  const unsigned gd = static_cast<unsigned>((row_heads * 16 + 255) / 256);
   float* nlse = delta + static_cast<int64_t>(k.b) * k.heads * k.s_pad;
   p.nlse = nlse;
+  const bool bf = k.dtype == DT_BF16, wide = k.d == 128;
+  const int ph = prof_begin(PROF_ATTN, st);
   if (bf)
-    attn_bwd_delta_kernel<DT_BF16><<<gd, 256, 0, st>>>(dout, o, lse, delta, nlse, p.s, p.b, p.h, p.heads, p.s_pad);
+    rc = wide ? bwd_kernels_launch<DT_BF16, 128>(k, p, dout, o, lse, delta, nlse, st)
+              : bwd_kernels_launch<DT_BF16, 96>(k, p, dout, o, lse, delta, nlse, st);
   else
-    attn_bwd_delta_kernel<DT_F16><<<gd, 256, 0, st>>>(dout, o, lse, delta, nlse, p.s, p.b, p.h, p.heads, p.s_pad);
-  const dim3 gkv(static_cast<unsigned>(k.s_pad / 128), static_cast<unsigned>(k.heads), static_cast<unsigned>(k.b));
-  if (bf) attn_bwd_dkdv_kernel<DT_BF16><<<gkv, ATT_THREADS, KV_SMEM, st>>>(p);
-  else attn_bwd_dkdv_kernel<DT_F16><<<gkv, ATT_THREADS, KV_SMEM, st>>>(p);
-  if (bf) attn_bwd_dq_kernel<DT_BF16><<<gkv, ATT_THREADS, DQ_SMEM, st>>>(p);
-  else attn_bwd_dq_kernel<DT_F16><<<gkv, ATT_THREADS, DQ_SMEM, st>>>(p);
-  // dV, dP, dQ, dK over the visible pairs (the recomputed S is not counted)
+    rc = wide ? bwd_kernels_launch<DT_F16, 128>(k, p, dout, o, lse, delta, nlse, st)
+              : bwd_kernels_launch<DT_F16, 96>(k, p, dout, o, lse, delta, nlse, st);
+  if (rc) return rc;
+  // dV, dP, dQ, dK over the visible pairs of every query head (the recomputed S is not counted)
   const double pairs = k.causal ? static_cast<double>(k.s) * (k.s + 1) / 2 : static_cast<double>(k.s) * k.s;
-  prof_end(ph, 8.0 * pairs * HD * k.heads * k.b, st, 3);
+  prof_end(ph, 8.0 * pairs * k.d * k.heads * k.b, st, 3);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return set_error(TPMLP_ERR_CUDA, std::string("attention backward launch: ") + cudaGetErrorString(e));
   return TPMLP_OK;
@@ -1351,18 +1463,18 @@ using namespace tpmlp::attn;
 
 extern "C" {
 
-size_t tpmlp_attn_workspace_size(int64_t s, int64_t b, int64_t h, int heads, int tp, int sp, int dtype,
+size_t tpmlp_attn_workspace_size(int64_t s, int64_t b, int64_t h, int heads, int kv_heads, int tp, int sp, int dtype,
                                  int causal) {
   Shape k;
-  if (check_shape(s, b, h, heads, tp, sp, dtype, causal, &k) != TPMLP_OK) return 0;
+  if (check_shape(s, b, h, heads, kv_heads, tp, sp, dtype, causal, &k) != TPMLP_OK) return 0;
   return ws_layout(k).total;
 }
 
-int tpmlp_attn_forward(int64_t s, int64_t b, int64_t h, int heads, int tp, int sp, int dtype, int causal,
+int tpmlp_attn_forward(int64_t s, int64_t b, int64_t h, int heads, int kv_heads, int tp, int sp, int dtype, int causal,
                        const void* const* x, const void* wqkv, const void* wo, void* qkv, void* o, float* lse,
                        void* const* z, void* ws, size_t ws_bytes, void* stream) {
   Shape k;
-  int rc = check_shape(s, b, h, heads, tp, sp, dtype, causal, &k);
+  int rc = check_shape(s, b, h, heads, kv_heads, tp, sp, dtype, causal, &k);
   if (rc) return rc;
   const int nio = sp ? tp : 1;
   if ((rc = check_ptrs(x, nio, "x")) || (rc = check_ptr(wqkv, 16, "wqkv")) || (rc = check_ptr(wo, 16, "wo")) ||
@@ -1383,14 +1495,14 @@ int tpmlp_attn_forward(int64_t s, int64_t b, int64_t h, int heads, int tp, int s
     if ((rc = gather_chunks(k, x, wb(ws) + W.x_off, st))) return rc;
     X = wb(ws) + W.x_off;
   }
-  // QKV = X·Wqkvᵀ: column-parallel, every shard's heads in one launch.
+  // QKV = X·Wqkvᵀ: column-parallel, every shard's groups in one launch.
   {
     GemmDesc g = gemm(k);
     g.M = k.M;
-    g.N = 3 * h;
+    g.N = k.qkv_w;
     g.lda = h;
     g.ldb = h;
-    g.b_rows = 3 * h;
+    g.b_rows = k.qkv_w;
     g.segs.push_back(GemmSeg{X, wqkv, h, 0});
     if (k.fused_ag) {
       g.a_chunks.assign(x, x + tp);
@@ -1398,7 +1510,7 @@ int tpmlp_attn_forward(int64_t s, int64_t b, int64_t h, int heads, int tp, int s
     }
     g.epi.kind = EPI_STORE;
     g.epi.out = qkv;
-    g.epi.ldo = 3 * h;
+    g.epi.ldo = k.qkv_w;
     if ((rc = launch_gemm_tc(g, st))) return rc;
   }
   if ((rc = launch_core_forward(k, qkv, o, lse, st))) return rc;
@@ -1415,12 +1527,12 @@ int tpmlp_attn_forward(int64_t s, int64_t b, int64_t h, int heads, int tp, int s
   return launch_gemm_tc(g, st);
 }
 
-int tpmlp_attn_backward(int64_t s, int64_t b, int64_t h, int heads, int tp, int sp, int dtype, int causal,
-                        const void* const* x, const void* wqkv, const void* wo, const void* qkv, const void* o,
-                        const float* lse, const void* const* dz, void* const* dx, void* dwqkv, void* dwo, void* dqkv,
-                        void* dout, void* ws, size_t ws_bytes, void* stream) {
+int tpmlp_attn_backward(int64_t s, int64_t b, int64_t h, int heads, int kv_heads, int tp, int sp, int dtype,
+                        int causal, const void* const* x, const void* wqkv, const void* wo, const void* qkv,
+                        const void* o, const float* lse, const void* const* dz, void* const* dx, void* dwqkv,
+                        void* dwo, void* dqkv, void* dout, void* ws, size_t ws_bytes, void* stream) {
   Shape k;
-  int rc = check_shape(s, b, h, heads, tp, sp, dtype, causal, &k);
+  int rc = check_shape(s, b, h, heads, kv_heads, tp, sp, dtype, causal, &k);
   if (rc) return rc;
   const int nio = sp ? tp : 1;
   if ((rc = check_ptrs(x, nio, "x")) || (rc = check_ptr(wqkv, 16, "wqkv")) || (rc = check_ptr(wo, 16, "wo")) ||
@@ -1435,7 +1547,7 @@ int tpmlp_attn_backward(int64_t s, int64_t b, int64_t h, int heads, int tp, int 
   if ((rc = check_ptr(ws, 256, "ws"))) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (k.M == 0) {
-    cudaError_t e = cudaMemsetAsync(dwqkv, 0, static_cast<size_t>(3 * h) * h * k.e, st);
+    cudaError_t e = cudaMemsetAsync(dwqkv, 0, static_cast<size_t>(k.qkv_w) * h * k.e, st);
     if (e == cudaSuccess) e = cudaMemsetAsync(dwo, 0, static_cast<size_t>(h) * h * k.e, st);
     if (e != cudaSuccess) return set_error(TPMLP_ERR_CUDA, std::string("cudaMemsetAsync: ") + cudaGetErrorString(e));
     return TPMLP_OK;
@@ -1494,15 +1606,15 @@ int tpmlp_attn_backward(int64_t s, int64_t b, int64_t h, int heads, int tp, int 
   // dWqkv = dQKVᵀ·X.
   {
     GemmDesc g = gemm(k);
-    g.M = 3 * h;
+    g.M = k.qkv_w;
     g.N = h;
     g.a_mn = true;
     g.b_mn = true;
-    g.lda = 3 * h;
+    g.lda = k.qkv_w;
     g.ldb = h;
     g.b_rows = h;
     if (k.fused_ag) {
-      for (int j = 0; j < tp; ++j) g.segs.push_back(GemmSeg{cb(dqkv) + j * k.rpc * 3 * h * k.e, x[j], k.rpc, 0});
+      for (int j = 0; j < tp; ++j) g.segs.push_back(GemmSeg{cb(dqkv) + j * k.rpc * k.qkv_w * k.e, x[j], k.rpc, 0});
     } else {
       g.segs.push_back(GemmSeg{dqkv, X, k.M, 0});
     }
@@ -1516,10 +1628,10 @@ int tpmlp_attn_backward(int64_t s, int64_t b, int64_t h, int heads, int tp, int 
   g.M = k.M;
   g.N = h;
   g.b_mn = true;  // B(n, k) = Wqkv[k, n]
-  g.lda = 3 * h;
+  g.lda = k.qkv_w;
   g.ldb = h;
-  g.b_rows = 3 * h;
-  g.segs.push_back(GemmSeg{dqkv, wqkv, 3 * h, 0});
+  g.b_rows = k.qkv_w;
+  g.segs.push_back(GemmSeg{dqkv, wqkv, k.qkv_w, 0});
   scatter_to(k, dx, &g);
   return launch_gemm_tc(g, st);
 }

@@ -39,7 +39,7 @@ def test_header_declares_the_boundary():
 def test_library_exports_every_declared_symbol(lib):
     missing = [n for n in declared_functions() if not hasattr(lib, n)]
     assert not missing, missing
-    assert lib.tpmlp_abi_version() == 3
+    assert lib.tpmlp_abi_version() == 4
 
 
 def _ws(lib, *a):
@@ -168,23 +168,31 @@ def test_binding_refuses_to_run_without_the_library(tmp_path):
 
 
 def _attn_fwd(lib, s=256, b=1, h=256, heads=2, tp=2, sp=1, dt=2, causal=0, wqkv=FAKE, lse=FAKE, ws=None,
-              ws_bytes=0):
+              ws_bytes=0, kv=None):
     n = tp if sp else 1
     x = _vp(*([FAKE] * n))
     z = _vp(*([FAKE] * n))
     f = lib.tpmlp_attn_forward
     f.restype = ctypes.c_int
-    f.argtypes = [ctypes.c_int64] * 3 + [ctypes.c_int] * 5 + [ctypes.c_void_p] * 7 + [ctypes.c_void_p,
+    f.argtypes = [ctypes.c_int64] * 3 + [ctypes.c_int] * 6 + [ctypes.c_void_p] * 7 + [ctypes.c_void_p,
                                                                                        ctypes.c_size_t,
                                                                                        ctypes.c_void_p]
-    return f(s, b, h, heads, tp, sp, dt, causal, x, wqkv, FAKE, FAKE, FAKE, lse, z, ws, ws_bytes, None)
+    return f(s, b, h, heads, heads if kv is None else kv, tp, sp, dt, causal, x, wqkv, FAKE, FAKE, FAKE, lse, z, ws,
+             ws_bytes, None)
 
 
 def test_attention_rejects_bad_arguments_on_the_host(lib):
     assert _attn_fwd(lib, heads=3, h=384, tp=2) == NOT_DIV  # heads % tp
     assert b"heads" in lib.tpmlp_last_error()
     assert _attn_fwd(lib, s=255) == NOT_DIV  # s % tp under SP
-    assert _attn_fwd(lib, h=320) == UNSUP  # head width must be 128
+    assert _attn_fwd(lib, h=320) == UNSUP  # head width 160: only 128 and 96
+    assert _attn_fwd(lib, h=128, heads=2) == UNSUP  # head width 64
+    assert _attn_fwd(lib, heads=4, h=512, kv=3) == NOT_DIV  # heads % kv_heads
+    assert b"kv heads" in lib.tpmlp_last_error()
+    assert _attn_fwd(lib, heads=4, h=512, kv=1, tp=2) == NOT_DIV  # kv_heads % tp: a shard needs whole groups
+    assert b"query groups" in lib.tpmlp_last_error()
+    assert _attn_fwd(lib, heads=4, h=512, kv=0) == INVALID
+    assert _attn_fwd(lib, heads=4, h=512, kv=8) == INVALID
     assert _attn_fwd(lib, dt=0) == UNSUP  # float32 storage
     assert _attn_fwd(lib, causal=2) == INVALID
     assert _attn_fwd(lib, tp=0) == INVALID
@@ -198,25 +206,31 @@ def test_attention_rejects_bad_arguments_on_the_host(lib):
 def test_attention_workspace_formula(lib):
     f = lib.tpmlp_attn_workspace_size
     f.restype = ctypes.c_size_t
-    f.argtypes = [ctypes.c_int64] * 3 + [ctypes.c_int] * 5
+    f.argtypes = [ctypes.c_int64] * 3 + [ctypes.c_int] * 6
 
     def a256(x):
         return (x + 255) // 256 * 256
 
     def ds_tiles(s, causal):
-        """16 KB dSᵀ tiles per (sequence, head): key tile kt visits the 64-query
-        tiles from 2·kt (causal) or 0 to the last, counted here one by one."""
+        """16 KB dSᵀ tiles per (sequence, query head): key tile kt visits the
+        64-query tiles from 2·kt (causal) or 0 to the last, counted here one by one."""
         nk, nq = -(-s // 128), -(-s // 64)
         return sum(nq - (2 * kt if causal else 0) for kt in range(nk))
 
     # 128-row chunks read in place: Δ and −lse2, each [b][heads][s_pad] float32, then dSᵀ
     for causal in (0, 1):
-        assert f(256, 1, 256, 2, 2, 1, 2, causal) == a256(2 * 1 * 2 * 256 * 4) + 2 * ds_tiles(256, causal) * 16384
+        assert f(256, 1, 256, 2, 2, 2, 1, 2, causal) == a256(2 * 1 * 2 * 256 * 4) + 2 * ds_tiles(256, causal) * 16384
     # 96-row chunks: gathered X and dZ, then Δ and −lse2 (s_pad = 256), then dSᵀ
-    assert f(192, 1, 256, 2, 2, 1, 2, 1) == (2 * a256(192 * 256 * 2) + a256(2 * 2 * 256 * 4)
-                                             + 2 * ds_tiles(192, True) * 16384)
+    assert f(192, 1, 256, 2, 2, 2, 1, 2, 1) == (2 * a256(192 * 256 * 2) + a256(2 * 2 * 256 * 4)
+                                                + 2 * ds_tiles(192, True) * 16384)
     # ragged s = 100 (one key tile, two query tiles), b = 3, 2 heads, no SP
-    assert f(100, 3, 256, 2, 1, 0, 2, 1) == a256(2 * 3 * 2 * 128 * 4) + 3 * 2 * 2 * 16384
+    assert f(100, 3, 256, 2, 2, 1, 0, 2, 1) == a256(2 * 3 * 2 * 128 * 4) + 3 * 2 * 2 * 16384
     assert ds_tiles(4096, True) == 1056 and ds_tiles(4096, False) == 2048
-    assert f(192, 1, 320, 2, 2, 1, 2, 0) == 0  # invalid (h != 128·heads) -> 0
-    assert f(192, 1, 256, 2, 2, 1, 2, 2) == 0  # invalid causal flag -> 0
+    # grouped-query attention: the per-query-head statistics and dSᵀ tiles do not
+    # depend on the number of key/value heads
+    assert f(256, 1, 512, 4, 2, 2, 1, 2, 1) == f(256, 1, 512, 4, 4, 2, 1, 2, 1)
+    # head width 96 (h = 96·heads) is accepted and sized like 128
+    assert f(256, 1, 384, 4, 4, 2, 1, 2, 1) == f(256, 1, 512, 4, 4, 2, 1, 2, 1)
+    assert f(192, 1, 320, 2, 2, 2, 1, 2, 0) == 0  # invalid (head width 160) -> 0
+    assert f(192, 1, 256, 2, 2, 2, 1, 2, 2) == 0  # invalid causal flag -> 0
+    assert f(192, 1, 512, 4, 3, 2, 1, 2, 0) == 0  # kv_heads does not divide heads -> 0

@@ -3,7 +3,9 @@ fp64 oracle (oracle/attn_fp64.py): Z, dX, dWqkv, dWo and the saved
 intermediates (QKV, O, lse2, dO, dQKV), both masks, both 16-bit storage types,
 SP chunks read in place (whole 128-row chunks) or gathered (ragged chunks),
 ragged sequence lengths, several sequences per batch, and bit-identical
-repeats.  Tolerance ‖GPU − oracle‖∞ / ‖oracle‖∞ ≤ 2e-2 per tensor."""
+repeats; grouped-query attention (several query heads per key/value head, and
+one key/value head for all) and the head width 96 as well as 128.  Tolerance
+‖GPU − oracle‖∞ / ‖oracle‖∞ ≤ 2e-2 per tensor."""
 import numpy as np
 import pytest
 import torch
@@ -23,7 +25,8 @@ def _run(tpmlp, cfg, t=None):
     X, Wqkv, Wo, dZ = (t[k].to(dev) for k in ("X", "Wqkv", "Wo", "dZ"))
     x = chunks(X, cfg.tp) if cfg.sp else X
     dz = chunks(dZ, cfg.tp) if cfg.sp else dZ
-    blk = tpmlp.AttnBlock(cfg.s, cfg.b, cfg.h, cfg.heads, cfg.tp, cfg.sp, cfg.torch_dtype, cfg.causal)
+    blk = tpmlp.AttnBlock(cfg.s, cfg.b, cfg.h, cfg.heads, cfg.tp, cfg.sp, cfg.torch_dtype, cfg.causal,
+                          kv_heads=cfg.groups)
     fw = blk.forward(x, Wqkv, Wo)
     bw = blk.backward(x, Wqkv, Wo, fw, dz)
     torch.cuda.synchronize()
@@ -45,6 +48,16 @@ CASES = [
     AttnConfig("short-ragged", 100, 3, 256, 2, 1, False, "bf16", True),
     AttnConfig("ragged-tiles", 320, 1, 512, 4, 4, True, "bf16", True),
     AttnConfig("multi-tile-in-place", 1024, 1, 512, 4, 2, True, "bf16", False),
+    # grouped-query attention: 2 query heads per group, one group per shard, in place, causal
+    AttnConfig("gqa-2-per-group", 256, 1, 512, 4, 2, True, "bf16", True, kv_heads=2),
+    # 4 query heads per group, gathered SP chunks (96 tokens × 2 sequences), unmasked
+    AttnConfig("gqa-4-per-group-gathered", 192, 2, 1024, 8, 2, True, "bf16", False, kv_heads=2),
+    # one key/value head for all query heads, ragged sequence, fp16
+    AttnConfig("mqa-ragged-f16", 320, 1, 512, 4, 1, False, "f16", True, kv_heads=1),
+    # head width 96 (the 22B and 8.3B models' heads)
+    AttnConfig("d96-in-place-causal", 256, 1, 384, 4, 2, True, "bf16", True),
+    AttnConfig("d96-ragged-f16", 100, 3, 192, 2, 1, False, "f16", False),
+    AttnConfig("d96-gqa-multi-tile", 640, 1, 768, 8, 2, True, "bf16", True, kv_heads=2),
 ]
 
 
@@ -54,8 +67,8 @@ def test_attention_block_matches_the_oracle(cuda_lib, cfg):
     t, blk, fw, bw, cat = _run(tpmlp, cfg)
     M, s, b, heads = cfg.M, cfg.s, cfg.b, cfg.heads
     X, Wqkv, Wo, dZ = (to_np(t[k]).reshape(-1, t[k].shape[-1]) for k in ("X", "Wqkv", "Wo", "dZ"))
-    ref = O.attn_forward(X, Wqkv, Wo, s, b, heads, cfg.causal)
-    g = O.attn_backward(X, Wqkv, Wo, dZ, s, b, heads, cfg.causal)
+    ref = O.attn_forward(X, Wqkv, Wo, s, b, heads, cfg.causal, cfg.groups)
+    g = O.attn_backward(X, Wqkv, Wo, dZ, s, b, heads, cfg.causal, cfg.groups)
     lse = to_np(fw["lse"])[:, :, :s]
     errs = {
         "QKV": rel_err(to_np(fw["qkv"]), ref["QKV"]),
@@ -73,27 +86,36 @@ def test_attention_block_matches_the_oracle(cuda_lib, cfg):
     assert np.abs(lse - ref["lse2"]).max() <= 2e-2 * max(1.0, np.abs(ref["lse2"]).max())
 
 
-def test_attention_core_alone_on_the_gpu_s_own_qkv(cuda_lib):
+CORE_CASES = [
+    AttnConfig("core", 384, 2, 512, 4, 2, True, "bf16", True),
+    AttnConfig("core-gqa", 384, 2, 1024, 8, 2, True, "bf16", True, kv_heads=2),
+    AttnConfig("core-d96-gqa", 384, 1, 768, 8, 2, True, "bf16", False, kv_heads=4),
+]
+
+
+@pytest.mark.parametrize("cfg", CORE_CASES, ids=[c.name for c in CORE_CASES])
+def test_attention_core_alone_on_the_gpu_s_own_qkv(cuda_lib, cfg):
     """The core's O, lse2 and dQ/dK/dV against the oracle's core evaluated on the
     GPU's own (rounded) QKV and dO: isolates the flash kernels from the
-    projections."""
+    projections (with grouped-query attention, dK and dV sum over the query
+    heads of a group)."""
     tpmlp = cuda_lib
-    cfg = AttnConfig("core", 384, 2, 512, 4, 2, True, "bf16", True)
     t, blk, fw, bw, cat = _run(tpmlp, cfg)
-    Q, K, V = O.split_qkv(to_np(fw["qkv"]), cfg.heads)
-    core = O.attention_core_forward(Q, K, V, cfg.s, cfg.b, cfg.heads, True)
+    Q, K, V = O.split_qkv(to_np(fw["qkv"]), cfg.heads, cfg.groups)
+    core = O.attention_core_forward(Q, K, V, cfg.s, cfg.b, cfg.heads, cfg.causal, cfg.groups)
     assert rel_err(to_np(fw["o"]), core["O"]) <= 1e-2
     assert np.abs(to_np(fw["lse"])[:, :, :cfg.s] - core["lse2"]).max() <= 1e-3 * np.abs(core["lse2"]).max()
-    gc = O.attention_core_backward(Q, K, V, to_np(bw["dout"]), cfg.s, cfg.b, cfg.heads, True)
-    dq, dk, dv = O.split_qkv(to_np(bw["dqkv"]), cfg.heads)
+    gc = O.attention_core_backward(Q, K, V, to_np(bw["dout"]), cfg.s, cfg.b, cfg.heads, cfg.causal, cfg.groups)
+    dq, dk, dv = O.split_qkv(to_np(bw["dqkv"]), cfg.heads, cfg.groups)
     assert rel_err(dq, gc["dQ"]) <= TOL
     assert rel_err(dk, gc["dK"]) <= TOL
     assert rel_err(dv, gc["dV"]) <= TOL
 
 
-def test_attention_is_deterministic(cuda_lib):
+@pytest.mark.parametrize("kv", [4, 2], ids=["mha", "gqa"])
+def test_attention_is_deterministic(cuda_lib, kv):
     tpmlp = cuda_lib
-    cfg = AttnConfig("det", 256, 1, 512, 4, 2, True, "bf16", True)
+    cfg = AttnConfig("det", 256, 1, 512, 4, 2, True, "bf16", True, kv_heads=kv)
     t = attn_inputs(cfg)
     _, _, fw1, bw1, cat = _run(tpmlp, cfg, t)
     _, _, fw2, bw2, _ = _run(tpmlp, cfg, t)
@@ -156,6 +178,57 @@ def test_llama70b_width_attention_sampled(cuda_lib):
     dwqkv = to_np(bw["dwqkv"])
     qrows = np.array([0, 383, 12288, 24575])
     assert rel_err(dwqkv[qrows], dqkv[:, qrows].T @ X) <= TOL
+
+
+def _sampled_projections(cfg, t, fw, bw, cat, rows, feats, qrows):
+    """QKV, Z, dO, dX on sampled token rows and dWo, dWqkv on sampled features,
+    against the oracle's fp64 products of the GPU's own inputs."""
+    X = to_np(t["X"]).reshape(-1, cfg.h)
+    Wqkv, Wo = to_np(t["Wqkv"]), to_np(t["Wo"])
+    qkv, o, do, dqkv = to_np(fw["qkv"]), to_np(fw["o"]), to_np(bw["dout"]), to_np(bw["dqkv"])
+    assert rel_err(qkv[rows], X[rows] @ Wqkv.T) <= TOL
+    z = to_np(cat(fw["z"])).reshape(-1, cfg.h)
+    assert rel_err(z[rows], o[rows] @ Wo.T) <= TOL
+    dZ = to_np(t["dZ"]).reshape(-1, cfg.h)
+    assert rel_err(do[rows], dZ[rows] @ Wo) <= TOL
+    dx = to_np(cat(bw["dx"])).reshape(-1, cfg.h)
+    assert rel_err(dx[rows], dqkv[rows] @ Wqkv) <= TOL
+    dwo = to_np(bw["dwo"])
+    assert rel_err(dwo[feats], dZ[:, feats].T @ o) <= TOL
+    dwqkv = to_np(bw["dwqkv"])
+    assert rel_err(dwqkv[qrows], dqkv[:, qrows].T @ X) <= TOL
+
+
+@pytest.mark.parametrize("name,heads_checked", [("llama70b_gqa_attn_tpsp8_bf16", (3, 60)),
+                                                 ("w22b_attn_tpsp8_bf16", (5, 62))])
+def test_gqa_and_d96_widths_sampled(cuda_lib, name, heads_checked):
+    """The Llama-70B-like grouped-query workload ([4096, 1, 8192], 64 query heads
+    and 8 key/value heads of 128, tp 8, SP, causal) and the 22B model's
+    attention ([4096, 1, 6144], 64 heads of 96) at full size: the core of two
+    query heads (first and last shard) against the oracle's core on the GPU's own
+    QKV and dO — for GQA with the whole group, whose dK/dV sum over its eight
+    query heads — and the projections on sampled rows and features."""
+    tpmlp = cuda_lib
+    cfg = ATTN_CONFIGS[name]
+    t, blk, fw, bw, cat = _run(tpmlp, cfg)
+    s, b, d, heads, G = cfg.s, cfg.b, cfg.d, cfg.heads, cfg.groups
+    r = heads // G
+    qkv, o, do, dqkv = to_np(fw["qkv"]), to_np(fw["o"]), to_np(bw["dout"]), to_np(bw["dqkv"])
+    for j in heads_checked:
+        g = j // r
+        cols = slice(g * (r + 2) * d, (g + 1) * (r + 2) * d)  # the whole group: its r query heads, k, v
+        hcols = slice(g * r * d, (g + 1) * r * d)
+        Q, K, V = O.split_qkv(qkv[:, cols], r, 1)
+        core = O.attention_core_forward(Q, K, V, s, b, r, True, 1)
+        assert rel_err(o[:, hcols], core["O"]) <= 1e-2
+        gc = O.attention_core_backward(Q, K, V, do[:, hcols], s, b, r, True, 1)
+        dq, dk, dv = O.split_qkv(dqkv[:, cols], r, 1)
+        for nm, got, want in (("dQ", dq, gc["dQ"]), ("dK", dk, gc["dK"]), ("dV", dv, gc["dV"])):
+            assert rel_err(got, want) <= TOL, (j, nm)
+    rows = np.array([0, 1, 511, 512, 2047, 4095])
+    feats = np.array([0, 127, cfg.h // 2, cfg.h - 1])
+    qrows = np.array([0, d - 1, cfg.qkv_rows // 2, cfg.qkv_rows - 1])
+    _sampled_projections(cfg, t, fw, bw, cat, rows, feats, qrows)
 
 
 @pytest.mark.parametrize("causal", [True, False], ids=["causal", "unmasked"])
