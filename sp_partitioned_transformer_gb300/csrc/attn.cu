@@ -778,13 +778,18 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dkdv_kernel(const __g
   const int Nh = nqt - qt_first;  // query tiles per query head
   const int N = p.qpg * Nh;       // steps
   const int colk = col_k(p, grp), colv = colk + HDIM;
-  auto step_head = [&](int it) { return grp * p.qpg + it / Nh; };
-  auto step_qtile = [&](int it) { return qt_first + it % Nh; };
   auto head_row = [&](int head) { return (static_cast<int64_t>(bi) * p.heads + head) * p.s_pad; };
-  // dSᵀ tile of step it in HBM: key tile kt's tiles of its query head, one per 64-query tile
-  auto ds_out = [&](int it) {
-    return p.ds + ((static_cast<int64_t>(bi) * p.heads + step_head(it)) * p.ds_head_tiles +
-                   ds_tile_index(kt, p.nqt64, p.causal) + it % Nh) * DS_TILE;
+  // Each role walks the steps with counters (no division on the issuing lanes):
+  // (head, query tile) advances as (grp·qpg, qt_first) → … → (…, nqt − 1) →
+  // (head + 1, qt_first) → ….
+  struct Walk {
+    int head, qt;
+    __device__ void next(int qt_first, int nqt) {
+      if (++qt == nqt) {
+        qt = qt_first;
+        ++head;
+      }
+    }
   };
 
   if (threadIdx.x == 0) {
@@ -824,12 +829,13 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dkdv_kernel(const __g
       load_tile(sV, &p.qkv128, bar(KB_KV), colv, bi, k0, 128);
       bool ok = true;
       int issued = 0;
-      for (int n = 0; ok && n < N; ++n) {
+      Walk w{grp * p.qpg, qt_first};
+      for (int n = 0; ok && n < N; ++n, w.next(qt_first, nqt)) {
         const int st = n % KV_ST;
         const uint32_t par = ((n / KV_ST) & 1) ^ 1u;
         if (!(ok = mbar_wait_bounded(bar(KB_E + st), par, abort_flag, p.status, p.timeout_ns))) break;
-        const int head = step_head(n);
-        const int qq = step_qtile(n) * KV_BQ;
+        const int head = w.head;
+        const int qq = w.qt * KV_BQ;
         uint8_t* sb = stage_base(st);
         const uint32_t f = bar(KB_F + st);
         mbar_arrive_expect_tx(f, KV_STAGE);
@@ -869,6 +875,12 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dkdv_kernel(const __g
       if (ok) tc_fence_after();
       if (ok) ok = issue_sdp(0);
       const uint64_t dPT = sdesc_k(sPT);
+      // dSᵀ tile of the current step in HBM (key tile kt's tiles of its query
+      // head, one per 64-query tile), advanced per step
+      uint8_t* ds_next = p.ds + ((static_cast<int64_t>(bi) * p.heads + grp * p.qpg) * p.ds_head_tiles +
+                                 ds_tile_index(kt, p.nqt64, p.causal)) * DS_TILE;
+      const int64_t ds_head_skip = (p.ds_head_tiles - Nh) * static_cast<int64_t>(DS_TILE);
+      int in_head = 0;
       for (int n = 0; ok && n < N; ++n) {
         const int st = n % KV_ST;
         if (n + 1 < N) {
@@ -881,7 +893,12 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dkdv_kernel(const __g
         tc_fence_after();
         const uint32_t sQ = smem_u32(stage_base(st)), sDO = sQ + KV_QTILE;
         const uint32_t sDSn = sDST + (n % KV_DSB) * DS_TILE;
-        bulk_store(ds_out(n), sDSn, DS_TILE);  // dSᵀ for the dQ kernel
+        bulk_store(ds_next, sDSn, DS_TILE);  // dSᵀ for the dQ kernel
+        ds_next += DS_TILE;
+        if (++in_head == Nh) {  // the group's next query head
+          in_head = 0;
+          ds_next += ds_head_skip;
+        }
         // dV += Pᵀ·dO and dK += dSᵀ·Q: A a [128 keys × 64 queries] K-major half,
         // K step ks 32 bytes along it; B MN-major from the stage
         uint64_t a[4], bd[8];
@@ -944,7 +961,8 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dkdv_kernel(const __g
     asm volatile("bar.sync 1, %0;" ::"n"(COMPUTE_THREADS) : "memory");
     tc_fence_before();
     mbar_arrive(bar(KB_KVT));
-    for (int n = 0; ok && n < N; ++n) {
+    Walk w{grp * p.qpg, qt_first};
+    for (int n = 0; ok && n < N; ++n, w.next(qt_first, nqt)) {
       const int st = n % KV_ST;
       ok = mbar_wait_bounded(bar(KB_SF), n & 1, abort_flag, p.status, p.timeout_ns);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
@@ -958,7 +976,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dkdv_kernel(const __g
       mbar_arrive(bar(KB_SC));  // Sᵀ/dPᵀ may be overwritten by the next tile's
       const float4* lse4 = reinterpret_cast<const float4*>(stage_base(st) + 2 * KV_QTILE) + g * 8;
       const float4* del4 = lse4 + 16;
-      const int qq = step_qtile(n) * KV_BQ + g * 32;
+      const int qq = w.qt * KV_BQ + g * 32;
       const bool masked = qq + 32 > p.s || k0 + KV_BK > p.s || (p.causal && k0 + KV_BK - 1 > qq);
       float lj[32], dj[32];
 #pragma unroll

@@ -14,7 +14,7 @@
 //                         statistics, normalise + affine, save mean/rstd;
 //   ln_fwd_stream_kernel  float32 rows (h >= 1024, 16-byte aligned): persistent
 //                         CTAs stream rows through a TMA-bulk shared-memory ring;
-//   ln_bwd_stream_kernel  the same ring over (x, dy) rows:
+//   ln_bwd_stream_kernel  the same ring over (x, dy[, dx]) rows:
 //                         dx = rstd·(g − mean(g) − x̂·mean(g·x̂)), g = dy·γ, written
 //                         or added to the residual gradient, and each CTA's dγ, dβ
 //                         partial sums over its rows; ln_bwd_reduce_parts_kernel
@@ -143,14 +143,15 @@ __global__ void __launch_bounds__(256) ln_fwd_kernel(ChunkSet cs, const void* __
 // vectors l, l + 32, …), kept packed: at most 128 data registers a thread.
 constexpr int REG_MAX_NV = 32;
 
-// 8 packed 16-bit values -> 4 float pairs.
+// 8 packed 16-bit values -> 4 float pairs (a bf16 is the upper half of the
+// float with the same value: one shift and one mask per pair).
 template <int DT>
 __device__ __forceinline__ void unpack8_pairs(const uint4& r, float2* f) {
   const uint32_t w[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     if constexpr (DT == DT_BF16)
-      f[i] = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+      f[i] = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
     else
       f[i] = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
   }
@@ -177,6 +178,38 @@ __device__ __forceinline__ void unpack8_pairs_v(const uint4& r, float2* f) {
       f[i] = make_float2(a, b);
     }
   }
+}
+
+// A 16-byte shared-memory load issued where it stands (volatile: not hoisted
+// ahead of the loop that uses it, which would hold every vector's γ and β in
+// registers at once).
+__device__ __forceinline__ uint4 lds_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(smem_u32(p)));
+  return v;
+}
+
+// y = x·γ + β on 8 packed 16-bit values, two per fused multiply-add.
+template <int DT>
+__device__ __forceinline__ uint4 affine8_packed(const uint4& x, const uint4& g, const uint4& b) {
+  const uint32_t xw[4] = {x.x, x.y, x.z, x.w}, gw[4] = {g.x, g.y, g.z, g.w}, bw[4] = {b.x, b.y, b.z, b.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if constexpr (DT == DT_BF16) {
+      const __nv_bfloat162 r = __hfma2(*reinterpret_cast<const __nv_bfloat162*>(&xw[i]),
+                                       *reinterpret_cast<const __nv_bfloat162*>(&gw[i]),
+                                       *reinterpret_cast<const __nv_bfloat162*>(&bw[i]));
+      o[i] = *reinterpret_cast<const uint32_t*>(&r);
+    } else {
+      const __half2 r = __hfma2(*reinterpret_cast<const __half2*>(&xw[i]), *reinterpret_cast<const __half2*>(&gw[i]),
+                                *reinterpret_cast<const __half2*>(&bw[i]));
+      o[i] = *reinterpret_cast<const uint32_t*>(&r);
+    }
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 // An optimisation barrier on a row held in registers: the compiler must assume
@@ -308,8 +341,11 @@ __host__ __device__ __forceinline__ uint32_t pad128(uint32_t x) { return (x + 12
 // block barrier).  Statistics take one pass over the registers:
 // the shifted sums Σ(x − c), Σ(x − c)² with c the row's first element (which
 // keeps the variance when the mean is large against the spread), two warp
-// reductions, then y = (x − μ)·rstd·γ + β.  EXACT: h = 256·NV, so every lane
-// owns exactly NV vectors and no vector is predicated.
+// reductions, then y = x̂·γ + β with x̂ = (x − μ)·rstd computed in float32 and
+// rounded once to the storage type, the affine step a packed 16-bit fused
+// multiply-add (one more rounding of the storage type's order than an all-float32
+// evaluation).  EXACT: every lane owns exactly NV vectors (h = 256·NV) and no
+// vector is predicated.
 template <int NV>
 struct LnFwdShape {
   static constexpr int MAX_WARPS = NV <= 24 ? 16 : 8;  // registers: 128 (NV ≤ 24) or 255 a thread
@@ -409,13 +445,13 @@ __global__ void __launch_bounds__(32 * LnFwdShape<NV>::MAX_WARPS, 1)
     for (int kk = 0; kk < NV; ++kk) {
       const int vi = lane + 32 * kk;
       if (EXACT || vi < nv) {
-        float2 f[4], gg[4], bbv[4], o[4];
+        // x̂ = (x − μ)·rstd in float32, rounded once to 16 bits; y = x̂·γ + β as
+        // one packed 16-bit fused multiply-add (a single rounding of the result)
+        float2 f[4], xh[4];
         unpack8_pairs<DT>(v[kk], f);
-        unpack8_pairs<DT>(gs[vi], gg);
-        unpack8_pairs<DT>(bs[vi], bbv);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) o[i] = __ffma2_rn(__ffma2_rn(f[i], r2, nmr2), gg[i], bbv[i]);
-        y[vi] = pack8_pairs<DT>(o);
+        for (int i = 0; i < 4; ++i) xh[i] = __ffma2_rn(f[i], r2, nmr2);
+        y[vi] = affine8_packed<DT>(pack8_pairs<DT>(xh), lds_v4(gs + vi), lds_v4(bs + vi));
       }
     }
     if (lane == 0) {
@@ -437,8 +473,9 @@ bool ln_fwd_warp_nv(const ChunkSet& cs, const void* gamma, const void* beta, flo
   const int wpc = static_cast<int>(std::min<size_t>(LnFwdShape<NV>::MAX_WARPS, (cap - fixed) / slot));
   if (wpc < 1) return false;
   const size_t smem = fixed + static_cast<size_t>(wpc) * slot;
-  const bool exact = h == 256 * NV;
-  auto* fn = exact ? ln_fwd_warp_kernel<DT, NV, true> : ln_fwd_warp_kernel<DT, NV, false>;
+  // (a variant without the per-vector predicate for h = 256·NV held more
+  // registers and spilled)
+  auto* fn = ln_fwd_warp_kernel<DT, NV, false>;
   // (always set: the kernel's static shared memory counts against the default 48 KB too)
   if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess) {
     cudaGetLastError();
@@ -567,12 +604,12 @@ __global__ void __launch_bounds__(STREAM_THREADS) ln_fwd_stream_kernel(ChunkSet 
 // dx = rstd·(g − mean(g) − x̂·mean(g·x̂)), g = dy·γ, written or added to dx; and
 // this CTA's partial sums of dγ = Σ dy·x̂ and dβ = Σ dy over its rows, in row
 // order, stored as part[blockIdx.x][:] and part[G + blockIdx.x][:].
-// Shared memory: a ring of S slots of (x, dy) rows; thread 0 keeps S − 1 rows
-// in flight while one is computed.  Each thread keeps its vectors of γ in
-// registers for the whole kernel and, per row, its vectors of x and dy (copied
-// out of the slot once) and of the dx being accumulated into (read from global
-// memory at the start of the row, so the load overlaps the row's first barrier
-// and its reduction); the element-wise math runs on float pairs.
+// Shared memory: a ring of S slots of (x, dy[, dx being accumulated into])
+// rows; thread 0 keeps S − 1 rows in flight while one is computed.  Each thread
+// keeps its vectors of γ in registers for the whole kernel and, per row, its
+// vectors of x and dy (copied out of the slot once); the dx it accumulates into
+// is read from the slot in the second pass; the element-wise math runs on float
+// pairs.
 template <int DT>
 __device__ __forceinline__ void raw_to_pairs(const uint4* raw, float2* f) {
   if constexpr (DT == DT_F32) {
@@ -612,7 +649,7 @@ __global__ void __launch_bounds__(THREADS, (THREADS == 256 ? 2 : 1)) ln_bwd_stre
   const int tid = threadIdx.x;
   const int nv = static_cast<int>(h / 8);
   const uint32_t rb = static_cast<uint32_t>(h * sizeof(T));
-  const RowRing ring{smem, rb, pad128(rb), 2, S};
+  const RowRing ring{smem, rb, pad128(rb), accumulate ? 3 : 2, S};
   const int64_t G = gridDim.x;
   const int64_t cnt = (M - blockIdx.x + G - 1) / G;
   uint4 graw[V][RAW];  // this thread's vectors of γ
@@ -647,16 +684,6 @@ __global__ void __launch_bounds__(THREADS, (THREADS == 256 ? 2 : 1)) ln_bwd_stre
     }
     const int64_t j = m / rpc;
     uint4* dx = reinterpret_cast<uint4*>(static_cast<T*>(cs.out[j]) + (m - j * rpc) * h);
-    // the dx being accumulated into: loaded now, used after the row's reduction
-    uint4 oraw[V][RAW];
-    if (accumulate) {
-#pragma unroll
-      for (int kk = 0; kk < V; ++kk) {
-        const int vi = tid + kk * THREADS;
-#pragma unroll
-        for (int u = 0; u < RAW; ++u) oraw[kk][u] = vi < nv ? dx[vi * RAW + u] : make_uint4(0, 0, 0, 0);
-      }
-    }
     if (tid == 0 &&
         !mbar_wait_bounded(smem_u32(&full[s]), static_cast<uint32_t>((k / S) & 1), nullptr, status, timeout_ns))
       abort_flag = 1;
@@ -667,6 +694,7 @@ __global__ void __launch_bounds__(THREADS, (THREADS == 256 ? 2 : 1)) ln_bwd_stre
     }
     const uint8_t* xs = ring.base + static_cast<size_t>(s) * ring.nin * ring.rb_al;
     const uint8_t* ds = xs + ring.rb_al;
+    const uint8_t* os = xs + 2 * ring.rb_al;  // the dx being accumulated into (accumulate only)
     uint4 xraw[V][RAW], draw[V][RAW];
 #pragma unroll
     for (int kk = 0; kk < V; ++kk) {
@@ -713,7 +741,12 @@ __global__ void __launch_bounds__(THREADS, (THREADS == 256 ? 2 : 1)) ln_bwd_stre
         raw_to_pairs<DT>(xraw[kk], xv);
         raw_to_pairs<DT>(draw[kk], d);
         raw_to_pairs<DT>(graw[kk], g);
-        if (accumulate) raw_to_pairs<DT>(oraw[kk], o);
+        if (accumulate) {
+          uint4 oraw[RAW];
+#pragma unroll
+          for (int u = 0; u < RAW; ++u) oraw[u] = reinterpret_cast<const uint4*>(os)[vi * RAW + u];
+          raw_to_pairs<DT>(oraw, o);
+        }
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const float2 xh = __ffma2_rn(xv[i], r2, nmr2);
@@ -1100,7 +1133,8 @@ bool ln_bwd_streamed_v(const ChunkSet& cs, const void* gamma, const float* mean,
                        cudaStream_t st) {
   const void* fn = reinterpret_cast<const void*>(ln_bwd_stream_kernel<DT, V, THREADS>);
   const size_t rb = pad128(static_cast<uint32_t>(h * sizeof(typename Storage<DT>::T)));
-  const StreamPlan p = plan_stream(fn, 0, 2 * rb, THREADS == 256 ? 2 : 1, std::min(M, max_parts), THREADS);
+  const StreamPlan p = plan_stream(fn, 0, (accumulate ? 3 : 2) * rb, THREADS == 256 ? 2 : 1, std::min(M, max_parts),
+                                   THREADS);
   if (!p.ok) return false;
   DeviceInfo* dev = nullptr;
   current_device(&dev);
