@@ -760,7 +760,22 @@ def run_ours(args) -> int:
                              "share_of_step": v["ms"] / args.steps / ms_prof}
     region_s = ms_max * args.steps / 1e3
     peak, regime, peak_key = choose_peak(peaks, region_s)
-    achieved = g["work"] / (g["ms"] / 1e3) / 1e12 if g["ms"] > 0 else None
+    # When every launch of the step is this kernel (the fused block), the timed
+    # region is nothing but its launches back to back: their average duration is
+    # the region's time over the launches, in the same window as `value`.  Else
+    # (shard sums, SP-region kernels) the event pairs of the second region split
+    # the step by kernel.
+    only_kernel = launches_total == g["launches"]
+    if only_kernel and g["launches"]:
+        kernel_ms = ms_max * args.steps
+        timing_note = (f"the timed region itself: the step runs only this kernel ({g['launches'] // args.steps} "
+                       f"launches a step), so its launch durations are the region's {ms_max:.4f} ms/step "
+                       f"(gaps between launches included)")
+    else:
+        kernel_ms = g["ms"]
+        timing_note = (f"event pairs around every launch over a second region of the same {args.steps} steps "
+                       f"({ms_prof:.4f} ms/step with the events; the line's ms_per_step is the region without them)")
+    achieved = g["work"] / (kernel_ms / 1e3) / 1e12 if kernel_ms > 0 else None
     traffic = ncu_traffic(cfg.name, args.mode)
     roofline = {
         "bound": "tensor",
@@ -774,9 +789,8 @@ def run_ours(args) -> int:
         "frac": (achieved / peak) if achieved else None,
         "traffic": traffic.get("dram_bytes_per_launch") if traffic else None,
         "flops_per_launch": g["work"] / max(1, g["launches"]),
-        "avg_launch_ms": g["ms"] / max(1, g["launches"]),
-        "timing": f"event pairs around every launch over a second region of the same {args.steps} steps "
-                  f"({ms_prof:.4f} ms/step with the events; the line's ms_per_step is the region without them)",
+        "avg_launch_ms": kernel_ms / max(1, g["launches"]),
+        "timing": timing_note,
         "frac_of_burst_peak": (achieved / peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])) if achieved else None,
         "frac_of_sustained_peak": (achieved / (peaks.get("bf16_tflops_sustained")
                                                or FALLBACK_PEAKS["bf16_tflops_sustained"])) if achieved else None,

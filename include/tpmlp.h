@@ -364,7 +364,10 @@ int tpmlp_wait_timeout_selftest(uint64_t timeout_ns, void* stream);
  * needs only the gathered X), then Δ and −lse2, each [b][heads][s_pad] float32,
  * then the backward's 16-bit dSᵀ tiles: b·heads·T tiles of 16 KB (128 keys × 64
  * queries), T = nk·nq − nk·(nk−1) under the causal mask, else nk·nq, with
- * nk = ⌈s/128⌉ and nq = ⌈s/64⌉ (≈ b·heads·s²·2 bytes unmasked, half causal).
+ * nk = ⌈s/128⌉ and nq = ⌈s/64⌉ (≈ b·heads·s²·2 bytes unmasked, half causal),
+ * then with grouped-query attention (kv_heads < heads) the float32 dK/dV
+ * partials of every group's r query heads, r·s·b·kv_heads·2·d·4 bytes, added in
+ * query-head order by the backward (so results stay deterministic).
  * Every on-chip wait is bounded (tpmlp_set_wait_timeout_ns): an expired wait
  * is reported through tpmlp_device_status() as TPMLP_ERR_TIMEOUT.  Results
  * are deterministic (no atomics).

@@ -272,6 +272,9 @@ struct AttnParams {
   int qpg;             // query heads per group
   int d;               // head width
   int64_t ldqkv;       // columns of QKV: (heads + 2·kv_heads)·d
+  int kv_split;        // dK/dV CTAs per (key tile, group): the group's query heads in chunks of qpc
+  int qpc;             // query heads per chunk
+  float* dkv_part;     // kv_split > 1: float32 partial [dK | dV] [kv_split][s·b][kv_heads][2][d]
   float scale_log2;    // log2(e)/√d
   float scale;         // 1/√d
   unsigned* status;
@@ -763,24 +766,29 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dkdv_kernel(const __g
   volatile int* abort_flag = &tail->abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // grid (key tiles, key/value heads, b): the tiles of one group share its
-  // query heads' Q and dO through L2; under the causal mask the first key tiles
-  // see the most query tiles and are dispatched first.  The CTA's steps run over
-  // the group's query heads and, for each, the 64-query tiles the key tile
-  // sees: step it is query head grp·qpg + it / Nh, query tile qt_first + it % Nh,
-  // and dK, dV accumulate over all of them (a key/value head shared by several
-  // query heads collects their gradients).
+  // grid (key tiles, key/value heads × kv_split, b): the tiles of one group
+  // share its query heads' Q and dO through L2; under the causal mask the first
+  // key tiles see the most query tiles and are dispatched first.  The CTA takes
+  // chunk `chunk` of its group's query heads (qpc of them) and runs over them
+  // and, for each, the 64-query tiles the key tile sees; dK, dV accumulate over
+  // all of them.  A key/value head shared by several query heads collects their
+  // gradients: in this CTA's accumulators when one chunk holds the whole group
+  // (kv_split = 1), else as float32 partials that attn_dkv_reduce_kernel adds in
+  // chunk order.
   const int kt = static_cast<int>(blockIdx.x);
-  const int grp = blockIdx.y, bi = blockIdx.z;
+  const int grp = static_cast<int>(blockIdx.y) / p.kv_split;
+  const int chunk = static_cast<int>(blockIdx.y) - grp * p.kv_split;
+  const int bi = blockIdx.z;
   const int k0 = kt * KV_BK;
   const int nqt = (p.s + KV_BQ - 1) / KV_BQ;
   const int qt_first = p.causal ? k0 / KV_BQ : 0;
   const int Nh = nqt - qt_first;  // query tiles per query head
-  const int N = p.qpg * Nh;       // steps
+  const int N = p.qpc * Nh;       // steps
+  const int head0 = grp * p.qpg + chunk * p.qpc;  // the chunk's first query head
   const int colk = col_k(p, grp), colv = colk + HDIM;
   auto head_row = [&](int head) { return (static_cast<int64_t>(bi) * p.heads + head) * p.s_pad; };
   // Each role walks the steps with counters (no division on the issuing lanes):
-  // (head, query tile) advances as (grp·qpg, qt_first) → … → (…, nqt − 1) →
+  // (head, query tile) advances as (head0, qt_first) → … → (…, nqt − 1) →
   // (head + 1, qt_first) → ….
   struct Walk {
     int head, qt;
@@ -829,7 +837,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dkdv_kernel(const __g
       load_tile(sV, &p.qkv128, bar(KB_KV), colv, bi, k0, 128);
       bool ok = true;
       int issued = 0;
-      Walk w{grp * p.qpg, qt_first};
+      Walk w{head0, qt_first};
       for (int n = 0; ok && n < N; ++n, w.next(qt_first, nqt)) {
         const int st = n % KV_ST;
         const uint32_t par = ((n / KV_ST) & 1) ^ 1u;
@@ -877,7 +885,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dkdv_kernel(const __g
       const uint64_t dPT = sdesc_k(sPT);
       // dSᵀ tile of the current step in HBM (key tile kt's tiles of its query
       // head, one per 64-query tile), advanced per step
-      uint8_t* ds_next = p.ds + ((static_cast<int64_t>(bi) * p.heads + grp * p.qpg) * p.ds_head_tiles +
+      uint8_t* ds_next = p.ds + ((static_cast<int64_t>(bi) * p.heads + head0) * p.ds_head_tiles +
                                  ds_tile_index(kt, p.nqt64, p.causal)) * DS_TILE;
       const int64_t ds_head_skip = (p.ds_head_tiles - Nh) * static_cast<int64_t>(DS_TILE);
       int in_head = 0;
@@ -961,7 +969,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dkdv_kernel(const __g
     asm volatile("bar.sync 1, %0;" ::"n"(COMPUTE_THREADS) : "memory");
     tc_fence_before();
     mbar_arrive(bar(KB_KVT));
-    Walk w{grp * p.qpg, qt_first};
+    Walk w{head0, qt_first};
     for (int n = 0; ok && n < N; ++n, w.next(qt_first, nqt)) {
       const int st = n % KV_ST;
       ok = mbar_wait_bounded(bar(KB_SF), n & 1, abort_flag, p.status, p.timeout_ns);
@@ -1029,12 +1037,22 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dkdv_kernel(const __g
       tc_fence_after();
       const int64_t mrow = static_cast<int64_t>(key) * p.b + bi;
       const int64_t ld = p.ldqkv;
+      // kv_split > 1: this chunk's float32 partial row [dK | dV] (unscaled)
+      float* part = p.dkv_part + ((static_cast<int64_t>(chunk) * p.s * p.b + mrow) * p.kv_heads + grp) * 2 * HDIM;
 #pragma unroll 1
       for (int col = g * 32; col < HDIM; col += 64) {
         float dv[32], dk[32];
         tmem_ld32(tl + KT_DV + col, dv);
         tmem_ld32(tl + KT_DK + col, dk);
-        if (key < p.s) {
+        if (key < p.s && p.kv_split > 1) {
+#pragma unroll
+          for (int k4 = 0; k4 < 8; ++k4) {
+            reinterpret_cast<float4*>(part + col)[k4] =
+                make_float4(dk[4 * k4], dk[4 * k4 + 1], dk[4 * k4 + 2], dk[4 * k4 + 3]);
+            reinterpret_cast<float4*>(part + HDIM + col)[k4] =
+                make_float4(dv[4 * k4], dv[4 * k4 + 1], dv[4 * k4 + 2], dv[4 * k4 + 3]);
+          }
+        } else if (key < p.s) {
 #pragma unroll
           for (int j = 0; j < 32; ++j) dk[j] *= p.scale;
 #pragma unroll
@@ -1052,6 +1070,44 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dkdv_kernel(const __g
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+}
+
+// ================================================================== backward: dK/dV chunk sum
+// dK_g, dV_g = Σ over chunks c = 0…kv_split−1, in order, of the float32 partials
+// the dK/dV kernel wrote (dK then scaled by 1/√d), rounded once into dQKV's k
+// and v columns of group g.  One thread per 4 consecutive values of a row's
+// [kv_heads][2][d] block.
+template <int DT, int HDIM>
+__global__ void __launch_bounds__(256) attn_dkv_reduce_kernel(const __grid_constant__ AttnParams p) {
+  const int64_t per_row = static_cast<int64_t>(p.kv_heads) * 2 * HDIM;
+  const int64_t rows = static_cast<int64_t>(p.s) * p.b;
+  const int64_t i4 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i4 * 4 >= rows * per_row) return;
+  const int64_t m = (i4 * 4) / per_row;
+  const int e = static_cast<int>(i4 * 4 - m * per_row);  // offset within the row's block
+  const int g = e / (2 * HDIM);
+  const int kv = (e / HDIM) & 1;  // 0: dK, 1: dV
+  const int col = e % HDIM;
+  const int64_t stride = rows * per_row;  // floats between consecutive chunks
+  const float4* src = reinterpret_cast<const float4*>(p.dkv_part + m * per_row + e);
+  float4 acc = __ldcs(src);
+  for (int c = 1; c < p.kv_split; ++c) {
+    const float4 v = __ldcs(src + c * (stride / 4));
+    acc.x += v.x;
+    acc.y += v.y;
+    acc.z += v.z;
+    acc.w += v.w;
+  }
+  if (kv == 0) {
+    acc.x *= p.scale;
+    acc.y *= p.scale;
+    acc.z *= p.scale;
+    acc.w *= p.scale;
+  }
+  using T = typename Storage<DT>::T;
+  T o[4] = {Storage<DT>::from(acc.x), Storage<DT>::from(acc.y), Storage<DT>::from(acc.z), Storage<DT>::from(acc.w)};
+  T* dst = static_cast<T*>(p.dqkv) + m * p.ldqkv + col_k(p, g) + kv * HDIM + col;
+  *reinterpret_cast<uint2*>(dst) = *reinterpret_cast<const uint2*>(o);
 }
 
 // ================================================================== backward: dQ
@@ -1290,10 +1346,18 @@ int64_t ds_head_tiles(const Shape& k) {
   return ds_tile_index(nkt, nqt64, k.causal);
 }
 
+// dK/dV CTAs per (key tile, group): with grouped-query attention one per query
+// head of the group (a whole group in one CTA would leave the causal mask's
+// first key tiles with r times the work of the others; with eight query heads a
+// group that made the backward 45% slower than multi-head attention), their
+// float32 partials added by attn_dkv_reduce_kernel.
+int kv_split_of(const Shape& k) { return k.heads / k.kv_heads; }
+
 // workspace: [X gathered | dZ gathered] when SP chunks are not read in place
-// (all the forward needs), then Δ and −lse2, then the dSᵀ tiles (backward).
+// (all the forward needs), then Δ and −lse2, then the dSᵀ tiles, then (grouped-
+// query attention) the dK/dV partials (backward).
 struct Ws {
-  size_t x_off, dz_off, delta_off, ds_off, fwd_total, total;
+  size_t x_off, dz_off, delta_off, ds_off, dkv_off, fwd_total, total;
 };
 Ws ws_layout(const Shape& k) {
   Ws w{};
@@ -1309,6 +1373,9 @@ Ws ws_layout(const Shape& k) {
   off += align256(2 * static_cast<size_t>(k.b) * k.heads * k.s_pad * sizeof(float));
   w.ds_off = off;
   off += static_cast<size_t>(k.b) * k.heads * ds_head_tiles(k) * DS_TILE;
+  w.dkv_off = off;
+  if (kv_split_of(k) > 1)
+    off += static_cast<size_t>(kv_split_of(k)) * k.M * k.kv_heads * 2 * k.d * sizeof(float);
   w.total = off;
   return w;
 }
@@ -1354,6 +1421,8 @@ int base_params(const Shape& k, AttnParams* p) {
   p->qpg = k.heads / k.kv_heads;
   p->d = k.d;
   p->ldqkv = k.qkv_w;
+  p->kv_split = kv_split_of(k);
+  p->qpc = p->qpg / p->kv_split;
   p->s_pad = static_cast<int>(k.s_pad);
   p->causal = k.causal;
   p->scale = 1.0f / std::sqrt(static_cast<float>(k.d));
@@ -1411,15 +1480,20 @@ int bwd_kernels_launch(const Shape& k, const AttnParams& p, const void* dout, co
   const int64_t row_heads = k.s_pad * k.b * k.heads;  // (row, query head) pairs, a half-warp each
   const unsigned gd = static_cast<unsigned>((row_heads * 16 + 255) / 256);
   attn_bwd_delta_kernel<DT><<<gd, 256, 0, st>>>(dout, o, lse, delta, nlse, p.s, p.b, p.h, p.heads, p.s_pad, p.d);
-  const dim3 gkv(static_cast<unsigned>(k.s_pad / 128), static_cast<unsigned>(k.kv_heads), static_cast<unsigned>(k.b));
+  const dim3 gkv(static_cast<unsigned>(k.s_pad / 128), static_cast<unsigned>(k.kv_heads * p.kv_split),
+                 static_cast<unsigned>(k.b));
   attn_bwd_dkdv_kernel<DT, HDIM><<<gkv, ATT_THREADS, KV_SMEM, st>>>(p);
+  if (p.kv_split > 1) {
+    const int64_t n4 = k.M * k.kv_heads * 2 * k.d / 4;
+    attn_dkv_reduce_kernel<DT, HDIM><<<static_cast<unsigned>((n4 + 255) / 256), 256, 0, st>>>(p);
+  }
   const dim3 gq(static_cast<unsigned>(k.s_pad / 128), static_cast<unsigned>(k.heads), static_cast<unsigned>(k.b));
   attn_bwd_dq_kernel<DT, HDIM><<<gq, ATT_THREADS, DQ_SMEM, st>>>(p);
   return TPMLP_OK;
 }
 
 int launch_core_backward(const Shape& k, const void* qkv, const void* o, const float* lse, const void* dout,
-                         float* delta, uint8_t* ds, void* dqkv, cudaStream_t st) {
+                         float* delta, uint8_t* ds, float* dkv_part, void* dqkv, cudaStream_t st) {
   AttnParams p;
   int rc = base_params(k, &p);
   if (rc) return rc;
@@ -1431,6 +1505,7 @@ int launch_core_backward(const Shape& k, const void* qkv, const void* o, const f
   p.delta = delta;
   p.dqkv = dqkv;
   p.ds = ds;
+  p.dkv_part = dkv_part;
   p.ds_head_tiles = ds_head_tiles(k);
   p.nqt64 = static_cast<int>((k.s + 63) / 64);
   float* nlse = delta + static_cast<int64_t>(k.b) * k.heads * k.s_pad;
@@ -1446,7 +1521,7 @@ int launch_core_backward(const Shape& k, const void* qkv, const void* o, const f
   if (rc) return rc;
   // dV, dP, dQ, dK over the visible pairs of every query head (the recomputed S is not counted)
   const double pairs = k.causal ? static_cast<double>(k.s) * (k.s + 1) / 2 : static_cast<double>(k.s) * k.s;
-  prof_end(ph, 8.0 * pairs * k.d * k.heads * k.b, st, 3);
+  prof_end(ph, 8.0 * pairs * k.d * k.heads * k.b, st, p.kv_split > 1 ? 4 : 3);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return set_error(TPMLP_ERR_CUDA, std::string("attention backward launch: ") + cudaGetErrorString(e));
   return TPMLP_OK;
@@ -1619,7 +1694,7 @@ int tpmlp_attn_backward(int64_t s, int64_t b, int64_t h, int heads, int kv_heads
     if ((rc = launch_gemm_tc(g, st))) return rc;
   }
   if ((rc = launch_core_backward(k, qkv, o, lse, dout, reinterpret_cast<float*>(wb(ws) + W.delta_off),
-                                 wb(ws) + W.ds_off, dqkv, st)))
+                                 wb(ws) + W.ds_off, reinterpret_cast<float*>(wb(ws) + W.dkv_off), dqkv, st)))
     return rc;
   // dWqkv = dQKVᵀ·X.
   {

@@ -227,8 +227,10 @@ def test_attention_workspace_formula(lib):
     assert f(100, 3, 256, 2, 2, 1, 0, 2, 1) == a256(2 * 3 * 2 * 128 * 4) + 3 * 2 * 2 * 16384
     assert ds_tiles(4096, True) == 1056 and ds_tiles(4096, False) == 2048
     # grouped-query attention: the per-query-head statistics and dSᵀ tiles do not
-    # depend on the number of key/value heads
-    assert f(256, 1, 512, 4, 2, 2, 1, 2, 1) == f(256, 1, 512, 4, 4, 2, 1, 2, 1)
+    # depend on the number of key/value heads; the dK/dV partials of the r query
+    # heads of every group follow, float32 [r][s·b][kv_heads][2][d]
+    r, kv, d = 2, 2, 128
+    assert f(256, 1, 512, 4, kv, 2, 1, 2, 1) == f(256, 1, 512, 4, 4, 2, 1, 2, 1) + r * 256 * kv * 2 * d * 4
     # head width 96 (h = 96·heads) is accepted and sized like 128
     assert f(256, 1, 384, 4, 4, 2, 1, 2, 1) == f(256, 1, 512, 4, 4, 2, 1, 2, 1)
     assert f(192, 1, 320, 2, 2, 2, 1, 2, 0) == 0  # invalid (head width 160) -> 0
