@@ -196,6 +196,81 @@ __device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, const uint64_t* b
         : "memory");
   }
 }
+// Two independent accumulations issued K step by K step in alternation,
+// D1 (+)= Σ A1_k·B1_k and D2 (+)= Σ A2_k·B2_k: consecutive instructions of one
+// chain update the same accumulator, so alternating two chains gives the pipe
+// an independent instruction between them.  A in tensor memory (columns a,
+// a+8, … as in mma_ts), KS K steps per call starting at the given columns and
+// descriptors; `first` != 0 overwrites both accumulators on the first step.
+__device__ __forceinline__ void mma_ts_2x3(uint32_t d1, uint32_t a1, const uint64_t* b1, uint32_t d2, uint32_t a2,
+                                           const uint64_t* b2, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.b32 p, %15, 0;\n\t"
+      "setp.eq.b32 q, %15, %15;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], %8, %14, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%1], [%5], %11, %14, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %9, %14, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%1], [%6], %12, %14, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%4], %10, %14, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%1], [%7], %13, %14, q;\n\t}" ::"r"(d1),
+      "r"(d2), "r"(a1), "r"(a1 + 8), "r"(a1 + 16), "r"(a2), "r"(a2 + 8), "r"(a2 + 16), "l"(b1[0]), "l"(b1[1]),
+      "l"(b1[2]), "l"(b2[0]), "l"(b2[1]), "l"(b2[2]), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void mma_ts_2x4(uint32_t d1, uint32_t a1, const uint64_t* b1, uint32_t d2, uint32_t a2,
+                                           const uint64_t* b2, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.b32 p, %19, 0;\n\t"
+      "setp.eq.b32 q, %19, %19;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], %10, %18, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%1], [%6], %14, %18, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %11, %18, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%1], [%7], %15, %18, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%4], %12, %18, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%1], [%8], %16, %18, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], %13, %18, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%1], [%9], %17, %18, q;\n\t}" ::"r"(d1),
+      "r"(d2), "r"(a1), "r"(a1 + 8), "r"(a1 + 16), "r"(a1 + 24), "r"(a2), "r"(a2 + 8), "r"(a2 + 16), "r"(a2 + 24),
+      "l"(b1[0]), "l"(b1[1]), "l"(b1[2]), "l"(b1[3]), "l"(b2[0]), "l"(b2[1]), "l"(b2[2]), "l"(b2[3]), "r"(idesc),
+      "r"(acc)
+      : "memory");
+}
+// NK K steps (6 or 8) of two tensor-memory-A chains, alternating.
+template <int NK>
+__device__ __forceinline__ void mma_ts_2(uint32_t d1, uint32_t a1, const uint64_t* b1, uint32_t d2, uint32_t a2,
+                                         const uint64_t* b2, uint32_t idesc, uint32_t acc0) {
+  static_assert(NK == 6 || NK == 8, "K steps");
+  constexpr int H = NK / 2;
+  if constexpr (H == 4) {
+    mma_ts_2x4(d1, a1, b1, d2, a2, b2, idesc, acc0);
+    mma_ts_2x4(d1, a1 + 8 * H, b1 + H, d2, a2 + 8 * H, b2 + H, idesc, 1u);
+  } else {
+    mma_ts_2x3(d1, a1, b1, d2, a2, b2, idesc, acc0);
+    mma_ts_2x3(d1, a1 + 8 * H, b1 + H, d2, a2 + 8 * H, b2 + H, idesc, 1u);
+  }
+}
+// Four K steps of two shared-memory chains, alternating.
+__device__ __forceinline__ void mma4_ss_2(uint32_t d1, const uint64_t* a1, const uint64_t* b1, uint32_t d2,
+                                          const uint64_t* a2, const uint64_t* b2, uint32_t idesc, uint32_t acc0) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.b32 p, %19, 0;\n\t"
+      "setp.eq.b32 q, %19, %19;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %2, %6, %18, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%1], %10, %14, %18, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %7, %18, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%1], %11, %15, %18, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %8, %18, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%1], %12, %16, %18, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %9, %18, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%1], %13, %17, %18, q;\n\t}" ::"r"(d1),
+      "r"(d2), "l"(a1[0]), "l"(a1[1]), "l"(a1[2]), "l"(a1[3]), "l"(b1[0]), "l"(b1[1]), "l"(b1[2]), "l"(b1[3]),
+      "l"(a2[0]), "l"(a2[1]), "l"(a2[2]), "l"(a2[3]), "l"(b2[0]), "l"(b2[1]), "l"(b2[2]), "l"(b2[3]), "r"(idesc),
+      "r"(acc0)
+      : "memory");
+}
 // The K-step descriptors (8, or nk) of a K-major [rows × 128] tile / an MN-major tile.
 __device__ __forceinline__ void kdescs(uint64_t base, int rows, uint64_t* o, int nk = 8) {
 #pragma unroll
@@ -711,8 +786,10 @@ __global__ void __launch_bounds__(256) attn_bwd_delta_kernel(const void* __restr
 }
 
 // ================================================================== backward: dK, dV
-// Per (128-key tile, key/value head, sequence) over the 64-query tiles of the
-// group's query heads.  K and V never change
+// Per (128-key tile, chunk of a group's query heads, sequence) over the 64-query
+// tiles of those query heads (one query head a chunk when a group has several:
+// the chunks' float32 partials are added by attn_dkv_reduce_kernel; the whole
+// group, i.e. the one head, otherwise).  K and V never change
 // within a CTA, so after TMA lands them the element-wise warps copy them into
 // tensor memory (16-bit, two per column), where they are the A operands of
 // Sᵀ = K·Qᵀ and dPᵀ = V·dOᵀ: those MMAs (N = 64) then read only Q or dO from
@@ -872,11 +949,10 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dkdv_kernel(const __g
         if (!mbar_wait_bounded(bar(KB_F + st), (n / KV_ST) & 1u, abort_flag, p.status, p.timeout_ns)) return false;
         tc_fence_after();
         const uint32_t sQ = smem_u32(stage_base(st)), sDO = sQ + KV_QTILE;
-        uint64_t b[8];
-        kdescs(sdesc_k(sQ), 64, b, NK);
-        mma_ts<NK>(tmem + KT_S, tmem + KT_K, b, idesc_s, 0u);
-        kdescs(sdesc_k(sDO), 64, b, NK);
-        mma_ts<NK>(tmem + KT_DP, tmem + KT_V, b, idesc_s, 0u);
+        uint64_t bq[8], bo[8];
+        kdescs(sdesc_k(sQ), 64, bq, NK);
+        kdescs(sdesc_k(sDO), 64, bo, NK);
+        mma_ts_2<NK>(tmem + KT_S, tmem + KT_K, bq, tmem + KT_DP, tmem + KT_V, bo, idesc_s, 0u);
         tc_commit(bar(KB_SF));
         return true;
       };
@@ -909,16 +985,16 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dkdv_kernel(const __g
         }
         // dV += Pᵀ·dO and dK += dSᵀ·Q: A a [128 keys × 64 queries] K-major half,
         // K step ks 32 bytes along it; B MN-major from the stage
-        uint64_t a[4], bd[8];
+        uint64_t ap[4], ad[4], bd[8], bq[8];
         const uint64_t dDS = sdesc_k(sDSn);
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks) a[ks] = dPT + 2u * ks;
+        for (int ks = 0; ks < 4; ++ks) {
+          ap[ks] = dPT + 2u * ks;
+          ad[ks] = dDS + 2u * ks;
+        }
         mndescs(sdesc_mn(sDO, KV_BQ), 4, bd);
-        mma4_ss(tmem + KT_DV, a, bd, idesc_acc, n > 0 ? 1u : 0u);
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) a[ks] = dDS + 2u * ks;
-        mndescs(sdesc_mn(sQ, KV_BQ), 4, bd);
-        mma4_ss(tmem + KT_DK, a, bd, idesc_acc, n > 0 ? 1u : 0u);
+        mndescs(sdesc_mn(sQ, KV_BQ), 4, bq);
+        mma4_ss_2(tmem + KT_DV, ap, bd, tmem + KT_DK, ad, bq, idesc_acc, n > 0 ? 1u : 0u);
         // the element-wise warps rewrite Pᵀ and dSᵀ buffer (n+1)%3 once MM of
         // this step completes; the store of step n−2 (that buffer) must have read it
         bulk_wait_read<1>();

@@ -303,13 +303,32 @@ struct RowRing {
   int S;           // slots
 };
 
-// Thread 0: start the bulk copies of the CTA's k-th row into slot k % S.
-__device__ __forceinline__ void ring_issue(const RowRing& ring, uint64_t* full, const ChunkSet& cs, int64_t k,
-                                          int64_t h, int64_t rpc, size_t esz) {
-  const int64_t m = blockIdx.x + k * gridDim.x;
-  const int64_t j = m / rpc;
-  const int64_t off = (m - j * rpc) * h * static_cast<int64_t>(esz);
-  const int s = static_cast<int>(k % ring.S);
+// Where row m = m0 + k·G lies, as (chunk j, row r of the chunk), stepped from
+// one k to the next without a division (G = qG·rpc + rG): a 64-bit division
+// is a long software sequence on the GPU, and these kernels advance a row at a
+// time.
+struct RowStep {
+  int64_t qG, rG, rpc;
+  __device__ __forceinline__ RowStep(int64_t G, int64_t rpc_) : qG(G / rpc_), rG(G - (G / rpc_) * rpc_), rpc(rpc_) {}
+};
+struct RowPos {
+  int64_t j, r;
+  __device__ __forceinline__ RowPos(int64_t m0, const RowStep& st) : j(m0 / st.rpc), r(m0 - (m0 / st.rpc) * st.rpc) {}
+  __device__ __forceinline__ void next(const RowStep& st) {
+    j += st.qG;
+    r += st.rG;
+    if (r >= st.rpc) {
+      r -= st.rpc;
+      ++j;
+    }
+  }
+};
+
+// Thread 0: start the bulk copies of the row at `pos` into slot s.
+__device__ __forceinline__ void ring_issue(const RowRing& ring, uint64_t* full, const ChunkSet& cs, int s,
+                                          const RowPos& pos, int64_t h, size_t esz) {
+  const int64_t j = pos.j;
+  const int64_t off = pos.r * h * static_cast<int64_t>(esz);
   const uint32_t bar = smem_u32(&full[s]);
   const uint32_t dst = smem_u32(ring.base + static_cast<size_t>(s) * ring.nin * ring.rb_al);
   mbar_arrive_expect_tx(bar, ring.rb * ring.nin);
@@ -338,14 +357,14 @@ __host__ __device__ __forceinline__ uint32_t pad128(uint32_t x) { return (x + 12
 // into it, the lanes copy the row into registers (NV packed vectors a lane) and
 // at once lane 0 refills the slot with row k + 1, whose load then overlaps row
 // k's arithmetic.  γ and β are staged in shared memory once per CTA (the only
-// block barrier).  Statistics take one pass over the registers:
-// the shifted sums Σ(x − c), Σ(x − c)² with c the row's first element (which
-// keeps the variance when the mean is large against the spread), two warp
-// reductions, then y = x̂·γ + β with x̂ = (x − μ)·rstd computed in float32 and
-// rounded once to the storage type, the affine step a packed 16-bit fused
-// multiply-add (one more rounding of the storage type's order than an all-float32
-// evaluation).  EXACT: every lane owns exactly NV vectors (h = 256·NV) and no
-// vector is predicated.
+// block barrier).  Statistics take one pass over the registers: the shifted
+// sums Σ(x − c), Σ(x − c)² with c the row's first element (which keeps the
+// variance when the mean is large against the spread) in two independent pairs
+// of accumulators, both warp reductions interleaved; then y = x̂·γ + β with
+// x̂ = (x − μ)·rstd computed in float32 and rounded once to the storage type,
+// the affine step a packed 16-bit fused multiply-add (one more rounding of the
+// storage type's order than an all-float32 evaluation).  EXACT: every lane owns
+// exactly NV vectors (h = 256·NV) and no vector is predicated.
 template <int NV>
 struct LnFwdShape {
   static constexpr int MAX_WARPS = NV <= 24 ? 16 : 8;  // registers: 128 (NV ≤ 24) or 255 a thread
@@ -371,17 +390,17 @@ __global__ void __launch_bounds__(32 * LnFwdShape<NV>::MAX_WARPS, 1)
   const int64_t W = static_cast<int64_t>(gridDim.x) * wpc;
   const int64_t g = static_cast<int64_t>(blockIdx.x) * wpc + w;
   const int64_t cnt = g < M ? (M - g + W - 1) / W : 0;
-  auto issue = [&](int64_t k) {  // lane 0: row g + k·W into the slot
-    const int64_t m = g + k * W;
-    const int64_t jj = m / rpc;
+  const RowStep step(W, rpc);
+  RowPos cur(g, step);  // the row computed
+  auto issue = [&](const RowPos& at) {  // lane 0: the row at `at` into the slot
     mbar_arrive_expect_tx(bar, rb);
-    bulk_g2s(smem_u32(slot), static_cast<const uint8_t*>(cs.in[jj]) + (m - jj * rpc) * h * static_cast<int64_t>(sizeof(T)),
+    bulk_g2s(smem_u32(slot), static_cast<const uint8_t*>(cs.in[at.j]) + at.r * h * static_cast<int64_t>(sizeof(T)),
              rb, bar);
   };
   if (lane == 0) {
     mbar_init(bar, 1);
     fence_barrier_init();
-    if (cnt > 0) issue(0);
+    if (cnt > 0) issue(cur);
   }
   for (int vi = threadIdx.x; vi < nv; vi += blockDim.x) {
     gs[vi] = __ldg(static_cast<const uint4*>(gamma) + vi);
@@ -406,7 +425,9 @@ __global__ void __launch_bounds__(32 * LnFwdShape<NV>::MAX_WARPS, 1)
     __syncwarp();  // every lane has copied the row out of the slot
     if (lane == 0 && k + 1 < cnt) {
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      issue(k + 1);
+      RowPos at = cur;
+      at.next(step);
+      issue(at);
     }
     // c = the row's first element (lane 0's first value)
     float c;
@@ -416,7 +437,11 @@ __global__ void __launch_bounds__(32 * LnFwdShape<NV>::MAX_WARPS, 1)
       c = __shfl_sync(0xffffffffu, f0[0].x, 0);
     }
     const float2 nc2 = make_float2(-c, -c);
-    float2 s1 = make_float2(0.0f, 0.0f), s2 = make_float2(0.0f, 0.0f);
+    // two independent pairs of accumulators (for the even and the odd float
+    // pairs of a vector): the sums' dependency chains are half as long
+    float2 s1[2], s2[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) s1[i] = s2[i] = make_float2(0.0f, 0.0f);
 #pragma unroll
     for (int kk = 0; kk < NV; ++kk) {
       if (EXACT || lane + 32 * kk < nv) {
@@ -425,13 +450,21 @@ __global__ void __launch_bounds__(32 * LnFwdShape<NV>::MAX_WARPS, 1)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const float2 d = __fadd2_rn(f[i], nc2);
-          s1 = __fadd2_rn(s1, d);
-          s2 = __ffma2_rn(d, d, s2);
+          s1[i & 1] = __fadd2_rn(s1[i & 1], d);
+          s2[i & 1] = __ffma2_rn(d, d, s2[i & 1]);
         }
       }
     }
-    const float dm = warp_sum(s1.x + s1.y) * inv_h;
-    const float var = fmaxf(warp_sum(s2.x + s2.y) * inv_h - dm * dm, 0.0f);
+    const float2 t1 = __fadd2_rn(s1[0], s1[1]);
+    const float2 t2 = __fadd2_rn(s2[0], s2[1]);
+    float q1 = t1.x + t1.y, q2 = t2.x + t2.y;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {  // both warp sums, interleaved
+      q1 += __shfl_xor_sync(0xffffffffu, q1, o);
+      q2 += __shfl_xor_sync(0xffffffffu, q2, o);
+    }
+    const float dm = q1 * inv_h;
+    const float var = fmaxf(q2 * inv_h - dm * dm, 0.0f);
     const float mu = c + dm;
     const float r = 1.0f / sqrtf(var + eps);
     reg_fence(v);
@@ -439,8 +472,7 @@ __global__ void __launch_bounds__(32 * LnFwdShape<NV>::MAX_WARPS, 1)
     const float2 r2 = make_float2(r, r);
     const float2 nmr2 = make_float2(-mu * r, -mu * r);
     const int64_t m = g + k * W;
-    const int64_t jj = m / rpc;
-    uint4* y = reinterpret_cast<uint4*>(static_cast<T*>(cs.out[jj]) + (m - jj * rpc) * h);
+    uint4* y = reinterpret_cast<uint4*>(static_cast<T*>(cs.out[cur.j]) + cur.r * h);
 #pragma unroll
     for (int kk = 0; kk < NV; ++kk) {
       const int vi = lane + 32 * kk;
@@ -458,6 +490,7 @@ __global__ void __launch_bounds__(32 * LnFwdShape<NV>::MAX_WARPS, 1)
       mean[m] = mu;
       rstd[m] = r;
     }
+    cur.next(step);
   }
 }
 
@@ -530,18 +563,22 @@ __global__ void __launch_bounds__(STREAM_THREADS) ln_fwd_stream_kernel(ChunkSet 
       stage8<DT>(sb, beta, vi);
     }
   }
+  const RowStep step(G, rpc);
+  RowPos cur(blockIdx.x, step), nxt = cur;  // the row computed, and (thread 0) the next row to load
   if (tid == 0) {
     abort_flag = 0;
     for (int s = 0; s < S; ++s) mbar_init(smem_u32(&full[s]), 1);
     fence_barrier_init();
-    for (int64_t k = 0; k < S && k < cnt; ++k) ring_issue(ring, full, cs, k, h, rpc, sizeof(T));
+    for (int64_t k = 0; k < S && k < cnt; ++k) {
+      ring_issue(ring, full, cs, static_cast<int>(k), nxt, h, sizeof(T));
+      nxt.next(step);
+    }
   }
   const float inv_h = 1.0f / static_cast<float>(h);
+  int s = 0, s_prev = S - 1;  // slots of rows k and k − 1
+  uint32_t ph = 0;            // phase parity of row k's slot
   for (int64_t k = 0; k < cnt; ++k) {
-    const int s = static_cast<int>(k % S);
-    if (tid == 0 &&
-        !mbar_wait_bounded(smem_u32(&full[s]), static_cast<uint32_t>((k / S) & 1), nullptr, status, timeout_ns))
-      abort_flag = 1;
+    if (tid == 0 && !mbar_wait_bounded(smem_u32(&full[s]), ph, nullptr, status, timeout_ns)) abort_flag = 1;
     __syncthreads();  // row k is in slot s; every thread is done with row k - 1
     if (abort_flag) {
       if (tid == 0) ring_drain(ring, full, k, cnt, status, timeout_ns);
@@ -549,7 +586,8 @@ __global__ void __launch_bounds__(STREAM_THREADS) ln_fwd_stream_kernel(ChunkSet 
     }
     if (tid == 0 && k >= 1 && k - 1 + S < cnt) {
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      ring_issue(ring, full, cs, k - 1 + S, h, rpc, sizeof(T));
+      ring_issue(ring, full, cs, s_prev, nxt, h, sizeof(T));
+      nxt.next(step);
     }
     const uint8_t* row = ring.base + static_cast<size_t>(s) * ring.rb_al;
     // Mean and variance from one block reduction of the shifted sums
@@ -579,8 +617,7 @@ __global__ void __launch_bounds__(STREAM_THREADS) ln_fwd_stream_kernel(ChunkSet 
     const float mu = c + dm;
     const float r = 1.0f / sqrtf(fmaxf(st.y * inv_h - dm * dm, 0.0f) + eps);
     const int64_t m = blockIdx.x + k * G;
-    const int64_t j = m / rpc;
-    T* y = static_cast<T*>(cs.out[j]) + (m - j * rpc) * h;
+    T* y = static_cast<T*>(cs.out[cur.j]) + cur.r * h;
 #pragma unroll
     for (int kk = 0; kk < V; ++kk) {
       const int vi = tid + kk * STREAM_THREADS;
@@ -597,6 +634,12 @@ __global__ void __launch_bounds__(STREAM_THREADS) ln_fwd_stream_kernel(ChunkSet 
     if (tid == 0) {
       mean[m] = mu;
       rstd[m] = r;
+    }
+    cur.next(step);
+    s_prev = s;
+    if (++s == S) {
+      s = 0;
+      ph ^= 1u;
     }
   }
 }
@@ -660,11 +703,16 @@ __global__ void __launch_bounds__(THREADS, (THREADS == 256 ? 2 : 1)) ln_bwd_stre
     for (int u = 0; u < RAW; ++u)
       graw[kk][u] = vi < nv ? __ldg(reinterpret_cast<const uint4*>(gamma) + vi * RAW + u) : make_uint4(0, 0, 0, 0);
   }
+  const RowStep step(G, rpc);
+  RowPos cur(blockIdx.x, step), nxt = cur;  // the row computed, and (thread 0) the next row to load
   if (tid == 0) {
     abort_flag = 0;
     for (int s = 0; s < S; ++s) mbar_init(smem_u32(&full[s]), 1);
     fence_barrier_init();
-    for (int64_t k = 0; k < S && k < cnt; ++k) ring_issue(ring, full, cs, k, h, rpc, sizeof(T));
+    for (int64_t k = 0; k < S && k < cnt; ++k) {
+      ring_issue(ring, full, cs, static_cast<int>(k), nxt, h, sizeof(T));
+      nxt.next(step);
+    }
   }
   float2 ag[V][4], ab[V][4];
 #pragma unroll
@@ -674,19 +722,17 @@ __global__ void __launch_bounds__(THREADS, (THREADS == 256 ? 2 : 1)) ln_bwd_stre
   const float inv_h = 1.0f / static_cast<float>(h);
   float mu_next = cnt > 0 ? mean[blockIdx.x] : 0.0f;
   float r_next = cnt > 0 ? rstd[blockIdx.x] : 0.0f;
+  int s = 0, s_prev = S - 1;  // slots of rows k and k − 1
+  uint32_t ph = 0;            // phase parity of row k's slot
   for (int64_t k = 0; k < cnt; ++k) {
-    const int s = static_cast<int>(k % S);
     const int64_t m = blockIdx.x + k * G;
     const float mu = mu_next, r = r_next;
     if (k + 1 < cnt) {  // the next row's statistics, one row ahead
       mu_next = mean[m + G];
       r_next = rstd[m + G];
     }
-    const int64_t j = m / rpc;
-    uint4* dx = reinterpret_cast<uint4*>(static_cast<T*>(cs.out[j]) + (m - j * rpc) * h);
-    if (tid == 0 &&
-        !mbar_wait_bounded(smem_u32(&full[s]), static_cast<uint32_t>((k / S) & 1), nullptr, status, timeout_ns))
-      abort_flag = 1;
+    uint4* dx = reinterpret_cast<uint4*>(static_cast<T*>(cs.out[cur.j]) + cur.r * h);
+    if (tid == 0 && !mbar_wait_bounded(smem_u32(&full[s]), ph, nullptr, status, timeout_ns)) abort_flag = 1;
     __syncthreads();  // row k is in slot s; every thread is done with row k − 1
     if (abort_flag) {
       if (tid == 0) ring_drain(ring, full, k, cnt, status, timeout_ns);
@@ -707,7 +753,8 @@ __global__ void __launch_bounds__(THREADS, (THREADS == 256 ? 2 : 1)) ln_bwd_stre
     }
     if (tid == 0 && k >= 1 && k - 1 + S < cnt) {  // row k − 1's slot is free
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      ring_issue(ring, full, cs, k - 1 + S, h, rpc, sizeof(T));
+      ring_issue(ring, full, cs, s_prev, nxt, h, sizeof(T));
+      nxt.next(step);
     }
     const float2 r2 = make_float2(r, r), nmr2 = make_float2(-mu * r, -mu * r);
     float2 sg1 = make_float2(0.0f, 0.0f), sgx = make_float2(0.0f, 0.0f);
@@ -758,6 +805,12 @@ __global__ void __launch_bounds__(THREADS, (THREADS == 256 ? 2 : 1)) ln_bwd_stre
 #pragma unroll
         for (int u = 0; u < RAW; ++u) dx[vi * RAW + u] = out[u];
       }
+    }
+    cur.next(step);
+    s_prev = s;
+    if (++s == S) {
+      s = 0;
+      ph ^= 1u;
     }
   }
   float* pg = part + static_cast<int64_t>(blockIdx.x) * h;
