@@ -371,6 +371,10 @@ int tpmlp_wait_timeout_selftest(uint64_t timeout_ns, void* stream);
  * Every on-chip wait is bounded (tpmlp_set_wait_timeout_ns): an expired wait
  * is reported through tpmlp_device_status() as TPMLP_ERR_TIMEOUT.  Results
  * are deterministic (no atomics).
+ * Environment: TPMLP_ATTN_FWD_PAIR=1 (read at every forward call) runs the
+ * forward's core for head width 128 as CTA pairs (2-SM MMAs, 512 query rows a
+ * pair) instead of one CTA per 256 query rows; same results within rounding,
+ * measured slower, off by default.
  * ------------------------------------------------------------------------- */
 size_t tpmlp_attn_workspace_size(int64_t s, int64_t b, int64_t h, int heads, int kv_heads, int tp, int sp,
                                  int dtype, int causal);

@@ -24,7 +24,10 @@
 //                     O += P·V from there; O is rescaled in TMEM only when a
 //                     tile's probabilities would pass 2^15 against the running
 //                     reference maximum; O and the row log-sum-exp (lse2) are
-//                     written at the end.
+//                     written at the end.  With head width 128 the same
+//                     kernel can run as CTA pairs (2-SM MMAs, each SM loading
+//                     half of every K and V tile; TPMLP_ATTN_FWD_PAIR=1): correct,
+//                     but slower than one CTA per pair of tiles, so not the default.
 //   attn_bwd_dkdv_kernel  per (128-key tile, head, sequence), over 64-query tiles:
 //                     Sᵀ = K·Qᵀ and dPᵀ = V·dOᵀ, Pᵀ = 2^(Sᵀ·c − lse2),
 //                     dSᵀ = Pᵀ ⊙ (dPᵀ − Δ), dV += Pᵀ·dO, dK += dSᵀ·Q; each
@@ -36,6 +39,7 @@
 // No atomics anywhere: every output element is written by one CTA, so results
 // are the same bits on every run.
 #include <algorithm>
+#include <cstdlib>
 #include <cmath>
 #include <mutex>
 
@@ -77,6 +81,22 @@ __device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* map, 
                                           int row0, int rows) {
   tma_load_3d(dst, map, bar, col, bi, row0);
   tma_load_3d(dst + static_cast<uint32_t>(rows) * HALF_ROW_BYTES, map, bar, col + 64, bi, row0);
+}
+
+// The same into this CTA's shared memory, completing on an mbarrier that may
+// be the even CTA's of the pair (shared::cluster address).
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster,
+                                                 int32_t c0, int32_t c1, int32_t c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ void load_tile_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster, int col,
+                                               int bi, int row0, int rows) {
+  tma_load_3d_pair(dst, map, bar_cluster, col, bi, row0);
+  tma_load_3d_pair(dst + static_cast<uint32_t>(rows) * HALF_ROW_BYTES, map, bar_cluster, col + 64, bi, row0);
 }
 
 // Batched MMA issue.  The lane that issues the MMAs shares its sub-partition
@@ -271,6 +291,46 @@ __device__ __forceinline__ void mma4_ss_2(uint32_t d1, const uint64_t* a1, const
       "r"(acc0)
       : "memory");
 }
+// 2-SM forms (cta_group::2, M = 256 across the CTA pair, issued by the even
+// CTA): A rows [0, 128) from the even CTA, [128, 256) from the odd one (its
+// shared memory, or its tensor memory at the same column); B's N extent in
+// halves, the even CTA's first.  8 K steps; the first accumulates iff acc0.
+__device__ __forceinline__ void mma8_ss_pair(uint32_t d, const uint64_t* a, const uint64_t* b, uint32_t idesc,
+                                             uint32_t acc0) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.b32 p, %18, 0;\n\t"
+      "setp.eq.b32 q, %18, %18;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %9, %17, p;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %2, %10, %17, q;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %3, %11, %17, q;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %4, %12, %17, q;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %5, %13, %17, q;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %6, %14, %17, q;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %7, %15, %17, q;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %8, %16, %17, q;\n\t}" ::"r"(d),
+      "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(a[4]), "l"(a[5]), "l"(a[6]), "l"(a[7]), "l"(b[0]), "l"(b[1]),
+      "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7]), "r"(idesc), "r"(acc0)
+      : "memory");
+}
+__device__ __forceinline__ void mma8_ts_pair(uint32_t d, uint32_t a, const uint64_t* b, uint32_t idesc,
+                                             uint32_t acc0) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.b32 p, %18, 0;\n\t"
+      "setp.eq.b32 q, %18, %18;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %9, %17, p;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%2], %10, %17, q;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%3], %11, %17, q;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%4], %12, %17, q;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%5], %13, %17, q;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%6], %14, %17, q;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%7], %15, %17, q;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%8], %16, %17, q;\n\t}" ::"r"(d),
+      "r"(a), "r"(a + 8), "r"(a + 16), "r"(a + 24), "r"(a + 32), "r"(a + 40), "r"(a + 48), "r"(a + 56),
+      "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7]), "r"(idesc), "r"(acc0)
+      : "memory");
+}
 // The K-step descriptors (8, or nk) of a K-major [rows × 128] tile / an MN-major tile.
 __device__ __forceinline__ void kdescs(uint64_t base, int rows, uint64_t* o, int nk = 8) {
 #pragma unroll
@@ -313,6 +373,16 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
       : "memory");
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Arrive on a barrier of the even CTA of the pair, relaxed: what the arrival
+// announces (P in tensor memory) is ordered by tcgen05.wait::st and
+// tcgen05.fence::before_thread_sync on this side and fence::after_thread_sync
+// after the wait on the issuing side, not by the arrival's memory semantics —
+// and a release at cluster scope waits for this thread's earlier memory
+// operations to become visible to the cluster, hundreds of cycles a tile.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -442,28 +512,44 @@ __device__ __forceinline__ void tmem_wait_ld_tied(uint32_t* r) {
       : "memory");
 }
 
-template <int DT, int HDIM>
+// PAIR: a cluster of two CTAs computes the tiles as 2-SM MMAs (cta_group::2,
+// M = 256): tile A is the 256 query rows [q0, q0 + 256), the even CTA holding
+// the first 128 and the odd CTA the next 128 in its own shared and tensor
+// memory, tile B the following 256.  Each CTA loads half of every K tile (64
+// keys, the B operand of S = Q·Kᵀ split along N) and half of every V tile (64
+// of the head's columns, the B operand of O += P·V split along N), so the
+// shared-memory traffic per MMA is 6 KB (S) and 2 KB (P·V) instead of 8 and 4;
+// both CTAs' copies complete on the even CTA's barriers, the even CTA's lane
+// issues every MMA and multicasts its commits to both CTAs, and the softmax
+// warps of both CTAs report P ready on the even CTA's barrier.  Head width 128.
+template <int DT, int HDIM, bool PAIR>
 __global__ void __launch_bounds__(ATT_THREADS, 1) attn_fwd_kernel(const __grid_constant__ AttnParams p) {
   static_assert(HDIM == 128 || HDIM == 96, "head width");
+  static_assert(!PAIR || HDIM == 128, "the 2-SM forward splits the head's 128 columns into two 64-column halves");
   constexpr int NK = HDIM / 16;  // K steps of S = Q·Kᵀ
+  constexpr int TQ = PAIR ? 2 * F_BQ : F_BQ;  // query rows of tile A (or B) across the CTA(s)
+  constexpr uint32_t KV_TX = PAIR ? F_TILE / 2 : F_TILE;  // bytes of K (or V) one CTA loads per key tile
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   Tail* tail = reinterpret_cast<Tail*>(smem + F_END);
   auto bar = [&](int i) { return smem_u32(&tail->bars[i]); };
   volatile int* abort_flag = &tail->abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;  // within the pair; 0 issues the MMAs
+  const bool leader = rank == 0;
 
-  // grid (256-row query pairs, query heads, b): a head's pairs run side by side
-  // and share its group's K and V through L2; under the causal mask the longest pairs (the
-  // last ones) are dispatched first
-  const int npt = (p.s + 2 * F_BQ - 1) / (2 * F_BQ);
-  const int pt = p.causal ? npt - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x);
+  // grid (query-row blocks of 2·TQ [× 2 CTAs], query heads, b): a head's blocks
+  // run side by side and share its group's K and V through L2; under the causal
+  // mask the longest blocks (the last ones) are dispatched first
+  const int npt = (p.s + 2 * TQ - 1) / (2 * TQ);
+  const int bx = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int pt = p.causal ? npt - 1 - bx : bx;
   const int head = blockIdx.y, bi = blockIdx.z;
-  const int q0 = pt * 2 * F_BQ;
+  const int q0 = pt * 2 * TQ;
   const int nkt = (p.s + F_BK - 1) / F_BK;
-  // key tiles each query tile sees (up to its diagonal under the mask); NA ≤ NB ≤ NA + 1
-  const int NA = p.causal ? min(nkt, 2 * pt + 1) : nkt;
-  const int NB = p.causal ? min(nkt, 2 * pt + 2) : nkt;
+  // key tiles each query tile sees (up to its last row's diagonal under the mask)
+  const int NA = p.causal ? min(nkt, (q0 + TQ) / F_BK) : nkt;
+  const int NB = p.causal ? min(nkt, (q0 + 2 * TQ) / F_BK) : nkt;
 
   if (threadIdx.x == 0) {
     mbar_init(bar(FB_Q), 1);
@@ -473,7 +559,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_fwd_kernel(const __grid_c
       mbar_init(bar(FB_VF + i), 1);
       mbar_init(bar(FB_VE + i), 1);
       mbar_init(bar(FB_SF + i), 1);
-      mbar_init(bar(FB_P + i), 128);
+      mbar_init(bar(FB_P + i), PAIR ? 8 : 128);  // pair: one arrival per softmax warp of both CTAs
       mbar_init(bar(FB_O + i), 1);
     }
     mbar_init(bar(FB_DRAIN), 1);
@@ -481,12 +567,24 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_fwd_kernel(const __grid_c
     fence_barrier_init();
   }
   if (warp == 2) {
-    tmem_alloc(smem_u32(&tail->tmem_slot), 512);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(smem_u32(&tail->tmem_slot), 512);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(&tail->tmem_slot), 512);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR) cluster_sync_all();  // both CTAs' barriers exist before any cross-CTA signal
+  else __syncthreads();
   tc_fence_after();
+  // a barrier of the even CTA (shared::cluster address) / a commit to this and the peer CTA
+  auto lead_bar = [&](int i) { return PAIR ? mapa_shared(bar(i), 0u) : bar(i); };
+  auto commit_all = [&](int i) {
+    if constexpr (PAIR) tc_commit_pair_mc(bar(i), 0x3);
+    else tc_commit(bar(i));
+  };
   const uint32_t tmem = tail->tmem_slot;
   // TMEM columns: S_A (later P_A) at 0, S_B (P_B) at 128, O_A at 256, O_B at 384.
   const uint32_t sQA = smem_u32(smem + F_QA), sQB = smem_u32(smem + F_QB);
@@ -496,28 +594,49 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_fwd_kernel(const __grid_c
     if (lane == 0) {
       const int colq = col_q(p, head), colk = col_k(p, head / p.qpg), colv = colk + HDIM;
       tma_prefetch_map(&p.qkv128);
+      if (PAIR) tma_prefetch_map(&p.qkv64);
       uint32_t issued = 0;  // K/V tiles with copies that may still be in flight
-      mbar_arrive_expect_tx(bar(FB_Q), 2 * F_TILE);
-      load_tile(sQA, &p.qkv128, bar(FB_Q), colq, bi, q0, 128);
-      load_tile(sQB, &p.qkv128, bar(FB_Q), colq, bi, q0 + F_BQ, 128);
+      // this CTA's 128 rows of tiles A and B; both CTAs' copies complete on the even CTA's barriers
+      const int qa = q0 + static_cast<int>(rank) * F_BQ, qb = qa + TQ;
+      if (leader) mbar_arrive_expect_tx(bar(FB_Q), (PAIR ? 4 : 2) * F_TILE);
+      if constexpr (PAIR) {
+        load_tile_pair(sQA, &p.qkv128, lead_bar(FB_Q), colq, bi, qa, 128);
+        load_tile_pair(sQB, &p.qkv128, lead_bar(FB_Q), colq, bi, qb, 128);
+      } else {
+        load_tile(sQA, &p.qkv128, bar(FB_Q), colq, bi, qa, 128);
+        load_tile(sQB, &p.qkv128, bar(FB_Q), colq, bi, qb, 128);
+      }
       bool ok = true;
       for (int n = 0; ok && n < NB; ++n) {
         const int st = n & 1;
         const uint32_t par = ((n >> 1) & 1) ^ 1u;
         if (!(ok = mbar_wait_bounded(bar(FB_KE + st), par, abort_flag, p.status, p.timeout_ns))) break;
-        mbar_arrive_expect_tx(bar(FB_KF + st), F_TILE);
-        load_tile(sK0 + st * F_TILE, &p.qkv128, bar(FB_KF + st), colk, bi, n * F_BK, 128);
+        if (leader) mbar_arrive_expect_tx(bar(FB_KF + st), (PAIR ? 2 : 1) * KV_TX);
+        if constexpr (PAIR)  // keys [64·rank, 64·rank + 64) of the tile, all 128 columns
+          load_tile_pair(sK0 + st * F_TILE, &p.qkv64, lead_bar(FB_KF + st), colk, bi, n * F_BK + 64 * rank, 64);
+        else
+          load_tile(sK0 + st * F_TILE, &p.qkv128, bar(FB_KF + st), colk, bi, n * F_BK, 128);
         if (!(ok = mbar_wait_bounded(bar(FB_VE + st), par, abort_flag, p.status, p.timeout_ns))) break;
-        mbar_arrive_expect_tx(bar(FB_VF + st), F_TILE);
-        load_tile(sV0 + st * F_TILE, &p.qkv128, bar(FB_VF + st), colv, bi, n * F_BK, 128);
+        if (leader) mbar_arrive_expect_tx(bar(FB_VF + st), (PAIR ? 2 : 1) * KV_TX);
+        if constexpr (PAIR)  // columns [64·rank, 64·rank + 64) of the head, all 128 keys
+          tma_load_3d_pair(sV0 + st * F_TILE, &p.qkv128, lead_bar(FB_VF + st), colv + 64 * rank, bi, n * F_BK);
+        else
+          load_tile(sV0 + st * F_TILE, &p.qkv128, bar(FB_VF + st), colv, bi, n * F_BK, 128);
         issued = static_cast<uint32_t>(n + 1);
       }
       if (!ok) {
-        // let the copies already issued land before the CTA exits
-        (void)mbar_wait_bounded(bar(FB_Q), 0u, nullptr, nullptr, p.timeout_ns);
-        for (uint32_t n = issued > 2 ? issued - 2 : 0; n < issued; ++n) {
-          (void)mbar_wait_bounded(bar(FB_KF + (n & 1)), (n >> 1) & 1u, nullptr, nullptr, p.timeout_ns);
-          (void)mbar_wait_bounded(bar(FB_VF + (n & 1)), (n >> 1) & 1u, nullptr, nullptr, p.timeout_ns);
+        // let the copies already issued land before the CTA exits: the even CTA
+        // watches its barriers, where the odd CTA's copies complete too, so the
+        // odd CTA waits a fixed time instead
+        if (leader) {
+          (void)mbar_wait_bounded(bar(FB_Q), 0u, nullptr, nullptr, p.timeout_ns);
+          for (uint32_t n = issued > 2 ? issued - 2 : 0; n < issued; ++n) {
+            (void)mbar_wait_bounded(bar(FB_KF + (n & 1)), (n >> 1) & 1u, nullptr, nullptr, p.timeout_ns);
+            (void)mbar_wait_bounded(bar(FB_VF + (n & 1)), (n >> 1) & 1u, nullptr, nullptr, p.timeout_ns);
+          }
+        } else {
+          const uint64_t t0 = globaltimer_ns();
+          while (globaltimer_ns() - t0 < 2000000ull) __nanosleep(1000);
         }
       }
     }
@@ -526,9 +645,10 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_fwd_kernel(const __grid_c
     // One issuing lane for both tiles, alternating between them: its order is
     // what staggers the two tiles' softmax by half a period (two issuers let the
     // tiles fall into step and their softmaxes contend; measured slower).
-    if (lane == 0) {
-      constexpr uint32_t idesc_s = make_idesc_f16(DT == DT_BF16, false, false, 128, F_BK);
-      constexpr uint32_t idesc_o = make_idesc_f16(DT == DT_BF16, false, true, 128, HDIM);
+    if (lane == 0 && leader) {
+      constexpr uint32_t idesc_s = make_idesc_f16(DT == DT_BF16, false, false, PAIR ? 256 : 128, F_BK);
+      constexpr uint32_t idesc_o = make_idesc_f16(DT == DT_BF16, false, true, PAIR ? 256 : 128, HDIM);
+      constexpr int KROWS = PAIR ? 64 : 128;  // rows of K in this CTA's shared memory
       const uint64_t dQA = sdesc_k(sQA), dQB = sdesc_k(sQB);
       const uint64_t dK0 = sdesc_k(sK0), dK1 = sdesc_k(sK0 + F_TILE);
       const uint64_t dV0 = sdesc_mn(sV0, 128), dV1 = sdesc_mn(sV0 + F_TILE, 128);
@@ -538,21 +658,23 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_fwd_kernel(const __grid_c
       auto issue_s = [&](int t, int n) {  // S_t = Q_t·K(n)ᵀ
         uint64_t a[8], b[8];
         kdescs(t ? dQB : dQA, 128, a, NK);
-        kdescs((n & 1) ? dK1 : dK0, 128, b, NK);
-        mma_ss<NK>(tmem + t * 128, a, b, idesc_s, 0u);
-        tc_commit(bar(FB_SF + t));
+        kdescs((n & 1) ? dK1 : dK0, KROWS, b, NK);
+        if constexpr (PAIR) mma8_ss_pair(tmem + t * 128, a, b, idesc_s, 0u);
+        else mma_ss<NK>(tmem + t * 128, a, b, idesc_s, 0u);
+        commit_all(FB_SF + t);
       };
       auto issue_pv = [&](int t, int n) {  // O_t += P_t·V(n), P_t from tensor memory
         uint64_t b[8];
         mndescs((n & 1) ? dV1 : dV0, 8, b);
-        mma_ts<8>(tmem + 256 + t * 128, tmem + t * 128, b, idesc_o, n > 0 ? 1u : 0u);
+        if constexpr (PAIR) mma8_ts_pair(tmem + 256 + t * 128, tmem + t * 128, b, idesc_o, n > 0 ? 1u : 0u);
+        else mma_ts<8>(tmem + 256 + t * 128, tmem + t * 128, b, idesc_o, n > 0 ? 1u : 0u);
       };
       bool ok = mbar_wait_bounded(bar(FB_Q), 0u, abort_flag, p.status, p.timeout_ns) && wait_k(0);
       if (ok) {
         tc_fence_after();
         issue_s(0, 0);
         issue_s(1, 0);
-        tc_commit(bar(FB_KE + 0));
+        commit_all(FB_KE + 0);
       }
       for (int n = 0; ok && n < NB; ++n) {
         const int st = n & 1;
@@ -569,7 +691,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_fwd_kernel(const __grid_c
             tc_fence_after();
             issue_s(0, n + 1);
           } else {
-            tc_commit(bar(FB_O + 0));
+            commit_all(FB_O + 0);
           }
         }
         if (!(ok = mbar_wait_bounded(bar(FB_P + 1), n & 1, abort_flag, p.status, p.timeout_ns))) break;
@@ -578,18 +700,19 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_fwd_kernel(const __grid_c
           break;
         tc_fence_after();
         issue_pv(1, n);
-        tc_commit(bar(FB_VE + st));  // V(n) is free once both tiles' P·V have run
+        commit_all(FB_VE + st);  // V(n) is free once both tiles' P·V have run
         if (n + 1 < NB) {
           if (!k_ready && !(ok = wait_k(n + 1))) break;
           tc_fence_after();
           issue_s(1, n + 1);
-          tc_commit(bar(FB_KE + ((n + 1) & 1)));  // K(n+1) is free once both tiles' S have run
+          commit_all(FB_KE + ((n + 1) & 1));  // K(n+1) is free once both tiles' S have run
         } else {
-          tc_commit(bar(FB_O + 1));
+          commit_all(FB_O + 1);
         }
       }
       if (!ok) {
-        tc_commit(bar(FB_DRAIN));
+        if constexpr (PAIR) tc_commit_pair_mc(bar(FB_DRAIN), 0x1);
+        else tc_commit(bar(FB_DRAIN));
         (void)mbar_wait_bounded(bar(FB_DRAIN), 0u, nullptr, nullptr, p.timeout_ns);
       }
     }
@@ -600,7 +723,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_fwd_kernel(const __grid_c
     const int t = (warp - 4) >> 2;
     const int qw = warp & 3;
     const int r = qw * 32 + lane;
-    const int q0t = q0 + t * F_BQ;
+    const int q0t = q0 + t * TQ + static_cast<int>(rank) * F_BQ;  // this CTA's first row of tile t
     const int q = q0t + r;
     const int N = t ? NB : NA;
     const uint32_t tl = tmem + (static_cast<uint32_t>(qw * 32) << 16);
@@ -713,7 +836,12 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_fwd_kernel(const __grid_c
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar(FB_P + t));
+      if constexpr (PAIR) {  // one arrival per warp, on the even CTA's barrier
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster_relaxed(lead_bar(FB_P + t));
+      } else {
+        mbar_arrive(bar(FB_P + t));
+      }
     }
     if (ok) {
       ok = mbar_wait_bounded(bar(FB_O + t), 0u, abort_flag, p.status, p.timeout_ns);
@@ -742,10 +870,12 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_fwd_kernel(const __grid_c
     }
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR) cluster_sync_all();  // the pair's MMAs and cross-CTA arrivals are all done
+  else __syncthreads();
   if (warp == 2) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    if constexpr (PAIR) tmem_dealloc_pair(tmem, 512);
+    else tmem_dealloc(tmem, 512);
   }
 }
 
@@ -1508,42 +1638,57 @@ int base_params(const Shape& k, AttnParams* p) {
   return TPMLP_OK;
 }
 
-template <int DT, int HDIM>
-void fwd_kernel_launch(dim3 grid, const AttnParams& p, cudaStream_t st) {
-  attn_fwd_kernel<DT, HDIM><<<grid, ATT_THREADS, F_SMEM, st>>>(p);
+// The one-CTA forward; with TPMLP_ATTN_FWD_PAIR=1 in the environment (read at
+// every call) and head width 128, the 2-SM (CTA pair) forward instead.
+bool fwd_pair_requested() {
+  const char* e = std::getenv("TPMLP_ATTN_FWD_PAIR");
+  return e != nullptr && e[0] == '1';
 }
-template <int DT, int HDIM>
-const void* fwd_kernel_fn() {
-  return reinterpret_cast<const void*>(attn_fwd_kernel<DT, HDIM>);
+template <int DT, int HDIM, bool PAIR>
+int fwd_kernel_launch(const Shape& k, const AttnParams& p, cudaStream_t st) {
+  const void* fn = reinterpret_cast<const void*>(attn_fwd_kernel<DT, HDIM, PAIR>);
+  if (const int rc = set_smem(fn, F_SMEM)) return rc;
+  constexpr int rows = PAIR ? 4 * F_BQ : 2 * F_BQ;  // query rows of one CTA (pair)
+  const unsigned blocks = static_cast<unsigned>((k.s + rows - 1) / rows);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((PAIR ? 2u : 1u) * blocks, static_cast<unsigned>(k.heads), static_cast<unsigned>(k.b));
+  cfg.blockDim = dim3(ATT_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = F_SMEM;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = PAIR ? 2 : 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, attn_fwd_kernel<DT, HDIM, PAIR>, p);
+  if (e != cudaSuccess) return set_error(TPMLP_ERR_CUDA, std::string("attention forward launch: ") + cudaGetErrorString(e));
+  return TPMLP_OK;
 }
 
 int launch_core_forward(const Shape& k, const void* qkv, void* o, float* lse, cudaStream_t st) {
   AttnParams p;
   int rc = base_params(k, &p);
   if (rc) return rc;
-  if ((rc = make_map3(&p.qkv128, k.dtype, qkv, k.qkv_w, k.b, k.s, 128))) return rc;
+  if ((rc = make_map3(&p.qkv128, k.dtype, qkv, k.qkv_w, k.b, k.s, 128)) ||
+      (rc = make_map3(&p.qkv64, k.dtype, qkv, k.qkv_w, k.b, k.s, 64)))
+    return rc;
   p.o = o;
   p.lse = lse;
-  const dim3 grid(static_cast<unsigned>((k.s + 2 * F_BQ - 1) / (2 * F_BQ)), static_cast<unsigned>(k.heads),
-                  static_cast<unsigned>(k.b));
-  const bool bf = k.dtype == DT_BF16, wide = k.d == 128;
-  const void* fn = bf ? (wide ? fwd_kernel_fn<DT_BF16, 128>() : fwd_kernel_fn<DT_BF16, 96>())
-                      : (wide ? fwd_kernel_fn<DT_F16, 128>() : fwd_kernel_fn<DT_F16, 96>());
-  if ((rc = set_smem(fn, F_SMEM))) return rc;
+  const bool bf = k.dtype == DT_BF16, wide = k.d == 128, pair = wide && fwd_pair_requested();
   const int ph = prof_begin(PROF_ATTN, st);
   if (bf) {
-    if (wide) fwd_kernel_launch<DT_BF16, 128>(grid, p, st);
-    else fwd_kernel_launch<DT_BF16, 96>(grid, p, st);
+    if (pair) rc = fwd_kernel_launch<DT_BF16, 128, true>(k, p, st);
+    else rc = wide ? fwd_kernel_launch<DT_BF16, 128, false>(k, p, st) : fwd_kernel_launch<DT_BF16, 96, false>(k, p, st);
   } else {
-    if (wide) fwd_kernel_launch<DT_F16, 128>(grid, p, st);
-    else fwd_kernel_launch<DT_F16, 96>(grid, p, st);
+    if (pair) rc = fwd_kernel_launch<DT_F16, 128, true>(k, p, st);
+    else rc = wide ? fwd_kernel_launch<DT_F16, 128, false>(k, p, st) : fwd_kernel_launch<DT_F16, 96, false>(k, p, st);
   }
   // QKᵀ and P·V over the visible (query, key) pairs of every query head
   const double pairs = k.causal ? static_cast<double>(k.s) * (k.s + 1) / 2 : static_cast<double>(k.s) * k.s;
   prof_end(ph, 4.0 * pairs * k.d * k.heads * k.b, st);
-  const cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return set_error(TPMLP_ERR_CUDA, std::string("attention forward launch: ") + cudaGetErrorString(e));
-  return TPMLP_OK;
+  return rc;
 }
 
 template <int DT, int HDIM>

@@ -288,3 +288,34 @@ def test_empty_sequence(cuda_lib):
     torch.cuda.synchronize()
     assert tpmlp.device_status() == 0
     assert not dwqkv.any() and not dwo.any()
+
+
+PAIR_CASES = [
+    # s = 1024 is two 512-row pair blocks; 320 leaves the last block mostly past s
+    AttnConfig("pair-causal-gqa", 1024, 1, 1024, 8, 2, True, "bf16", True, kv_heads=2),
+    AttnConfig("pair-unmasked-ragged-f16", 320, 2, 512, 4, 1, False, "f16", False),
+]
+
+
+@pytest.mark.parametrize("cfg", PAIR_CASES, ids=[c.name for c in PAIR_CASES])
+def test_two_sm_forward_matches_the_one_cta_forward_and_the_oracle(cuda_lib, cfg, monkeypatch):
+    """The 2-SM (CTA pair) forward, selected with TPMLP_ATTN_FWD_PAIR=1: O and
+    lse2 against the oracle's core on the GPU's own QKV, O close to the one-CTA
+    forward's, and the backward run on the pair forward's O and lse2 against
+    the oracle's core gradients."""
+    tpmlp = cuda_lib
+    t = attn_inputs(cfg)
+    monkeypatch.setenv("TPMLP_ATTN_FWD_PAIR", "1")
+    _, _, fp, bp, cat = _run(tpmlp, cfg, t)
+    monkeypatch.setenv("TPMLP_ATTN_FWD_PAIR", "0")
+    _, _, f1, b1, _ = _run(tpmlp, cfg, t)
+    assert torch.equal(fp["qkv"], f1["qkv"])
+    Q, K, V = O.split_qkv(to_np(fp["qkv"]), cfg.heads, cfg.groups)
+    core = O.attention_core_forward(Q, K, V, cfg.s, cfg.b, cfg.heads, cfg.causal, cfg.groups)
+    assert rel_err(to_np(fp["o"]), core["O"]) <= 1e-2
+    assert np.abs(to_np(fp["lse"])[:, :, :cfg.s] - core["lse2"]).max() <= 1e-3 * np.abs(core["lse2"]).max()
+    assert rel_err(to_np(fp["o"]), to_np(f1["o"])) <= 1e-2
+    g = O.attention_core_backward(Q, K, V, to_np(bp["dout"]), cfg.s, cfg.b, cfg.heads, cfg.causal, cfg.groups)
+    dq, dk, dv = O.split_qkv(to_np(bp["dqkv"]), cfg.heads, cfg.groups)
+    for name, got, want in (("dQ", dq, g["dQ"]), ("dK", dk, g["dK"]), ("dV", dv, g["dV"])):
+        assert rel_err(got, want) <= TOL, name
