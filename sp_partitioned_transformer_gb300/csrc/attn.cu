@@ -1318,12 +1318,17 @@ __global__ void __launch_bounds__(256) attn_dkv_reduce_kernel(const __grid_const
 
 // ================================================================== backward: dQ
 // dQ = (dS·K)/√d per 128-query tile, over the key tiles it sees, reading the dSᵀ
-// tiles the dK/dV kernel stored: two [128 keys × 64 queries] tiles side by side
-// are the [K = 128 keys] × [M = 128 queries] MN-major A operand, and the K tile
-// [128 keys × 128 d] as TMA lands it is the MN-major B operand.  Nothing is
-// recomputed; the kernel streams dSᵀ from HBM once.
+// tiles the dK/dV kernel stored, 64 keys at a time: the first or second 64 rows
+// (8 KB, contiguous) of the two [128 keys × 64 queries] tiles side by side are
+// the [K = 64 keys] × [M = 128 queries] MN-major A operand, and the K rows
+// [64 keys × 128 d] as TMA lands them are the MN-major B operand.  Nothing is
+// recomputed; the kernel streams dSᵀ from HBM once.  Two CTAs of 8 warps per SM
+// (32 KB stages, 128 tensor-memory columns each), so one CTA's start and
+// epilogue overlap the other's streaming.
 constexpr int DQ_ST = 3;
-constexpr uint32_t DQ_STAGE = 2 * DS_TILE + KV_TILE;  // dSᵀ for query rows 0–63 and 64–127, K
+constexpr int DQ_THREADS = 256;  // warps 0–3: TMA, MMA, TMEM, idle; warps 4–7: epilogue
+constexpr uint32_t DQ_HALF = DS_TILE / 2;                    // 64 key rows of a dSᵀ tile, 8 KB
+constexpr uint32_t DQ_STAGE = 2 * DQ_HALF + KV_TILE / 2;     // dSᵀ for query rows 0–63 and 64–127, K
 constexpr uint32_t DQ_END = DQ_ST * DQ_STAGE;
 constexpr size_t DQ_SMEM = 1024 + DQ_END + sizeof(Tail);
 enum { QB_F = 0, QB_E = QB_F + DQ_ST, QB_MM = QB_E + DQ_ST, QB_DRAIN = QB_MM + 1, QB_COUNT = QB_DRAIN + 1 };
@@ -1331,7 +1336,7 @@ static_assert(QB_COUNT <= 24, "barrier slots");
 static_assert(DQ_SMEM <= 232448 && KV_SMEM <= 232448 && F_SMEM <= 232448, "shared memory per CTA");
 
 template <int DT, int HDIM>
-__global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dq_kernel(const __grid_constant__ AttnParams p) {
+__global__ void __launch_bounds__(DQ_THREADS, 2) attn_bwd_dq_kernel(const __grid_constant__ AttnParams p) {
   static_assert(HDIM == 128 || HDIM == 96, "head width");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -1346,7 +1351,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dq_kernel(const __gri
   const int qt = p.causal ? ntq - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x);
   const int head = blockIdx.y, bi = blockIdx.z;
   const int q0 = qt * 128;
-  const int N = p.causal ? qt + 1 : ntq;  // key tiles of 128
+  const int N = 2 * (p.causal ? qt + 1 : ntq);  // steps of 64 keys
   // query rows 64–127 of this tile exist (else that half of A is never loaded:
   // it only feeds output rows past s, which are not stored)
   const bool upper = 2 * qt + 1 < p.nqt64;
@@ -1375,7 +1380,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dq_kernel(const __gri
 
   if (warp == 0) {
     if (lane == 0) {
-      tma_prefetch_map(&p.qkv128);
+      tma_prefetch_map(&p.qkv64);
       bool ok = true;
       int issued = 0;
       for (int n = 0; ok && n < N; ++n) {
@@ -1383,11 +1388,13 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dq_kernel(const __gri
         const uint32_t par = ((n / DQ_ST) & 1) ^ 1u;
         if (!(ok = mbar_wait_bounded(bar(QB_E + st), par, abort_flag, p.status, p.timeout_ns))) break;
         const uint32_t f = bar(QB_F + st), sa = stage_addr(st);
-        mbar_arrive_expect_tx(f, (upper ? 2 : 1) * DS_TILE + KV_TILE);
-        const uint8_t* src = ds_head + (ds_tile_index(n, p.nqt64, p.causal) + 2 * qt - (p.causal ? 2 * n : 0)) * DS_TILE;
-        bulk_load(sa, src, DS_TILE, f);
-        if (upper) bulk_load(sa + DS_TILE, src + DS_TILE, DS_TILE, f);
-        load_tile(sa + 2 * DS_TILE, &p.qkv128, f, colk, bi, n * 128, 128);
+        const int kt = n >> 1, hk = n & 1;  // key tile, and which 64 of its keys
+        mbar_arrive_expect_tx(f, (upper ? 2 : 1) * DQ_HALF + KV_TILE / 2);
+        const uint8_t* src =
+            ds_head + (ds_tile_index(kt, p.nqt64, p.causal) + 2 * qt - (p.causal ? 2 * kt : 0)) * DS_TILE + hk * DQ_HALF;
+        bulk_load(sa, src, DQ_HALF, f);
+        if (upper) bulk_load(sa + DQ_HALF, src + DS_TILE, DQ_HALF, f);
+        load_tile(sa + 2 * DQ_HALF, &p.qkv64, f, colk, bi, kt * 128 + hk * 64, 64);
         issued = n + 1;
       }
       if (!ok)
@@ -1403,11 +1410,11 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dq_kernel(const __gri
         const int st = n % DQ_ST;
         if (!(ok = mbar_wait_bounded(bar(QB_F + st), (n / DQ_ST) & 1u, abort_flag, p.status, p.timeout_ns))) break;
         tc_fence_after();
-        const uint32_t sa = stage_addr(st), sk = sa + 2 * DS_TILE;
+        const uint32_t sa = stage_addr(st), sk = sa + 2 * DQ_HALF;
         uint64_t a[8], b[8];
-        mndescs(sdesc_mn(sa, 128), 8, a);
-        mndescs(sdesc_mn(sk, 128), 8, b);
-        mma8_ss(tmem, a, b, idesc, n > 0 ? 1u : 0u);
+        mndescs(sdesc_mn(sa, 64), 4, a);  // the two query halves 8 KB apart
+        mndescs(sdesc_mn(sk, 64), 4, b);  // K's two 64-column halves 8 KB apart
+        mma4_ss(tmem, a, b, idesc, n > 0 ? 1u : 0u);
         tc_commit(bar(QB_E + st));
       }
       tc_commit(bar(ok ? QB_MM : QB_DRAIN));
@@ -1415,8 +1422,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dq_kernel(const __gri
     }
     __syncwarp();
   } else if (warp >= 4) {
-    // Two groups of four warps; group g stores the 32-column chunks g, g + 2, … of dQ.
-    const int g = (warp - 4) >> 2;
+    // Four warps, a row per thread, the 32-column chunks of dQ in turn.
     const int qw = warp & 3;
     const int r = qw * 32 + lane;
     const int q = q0 + r;
@@ -1427,7 +1433,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_bwd_dq_kernel(const __gri
       const int64_t mrow = static_cast<int64_t>(q) * p.b + bi;
       const int64_t ld = p.ldqkv;
 #pragma unroll 1
-      for (int col = g * 32; col < HDIM; col += 64) {
+      for (int col = 0; col < HDIM; col += 32) {
         float dq[32];
         tmem_ld32(tl + col, dq);
         if (q < p.s) {
@@ -1709,7 +1715,7 @@ int bwd_kernels_launch(const Shape& k, const AttnParams& p, const void* dout, co
     attn_dkv_reduce_kernel<DT, HDIM><<<static_cast<unsigned>((n4 + 255) / 256), 256, 0, st>>>(p);
   }
   const dim3 gq(static_cast<unsigned>(k.s_pad / 128), static_cast<unsigned>(k.heads), static_cast<unsigned>(k.b));
-  attn_bwd_dq_kernel<DT, HDIM><<<gq, ATT_THREADS, DQ_SMEM, st>>>(p);
+  attn_bwd_dq_kernel<DT, HDIM><<<gq, DQ_THREADS, DQ_SMEM, st>>>(p);
   return TPMLP_OK;
 }
 
