@@ -885,33 +885,42 @@ __global__ void __launch_bounds__(256) attn_bwd_delta_kernel(const void* __restr
                                                              const void* __restrict__ o, const float* __restrict__ lse,
                                                              float* __restrict__ delta, float* __restrict__ nlse,
                                                              int s, int b, int h, int heads, int s_pad, int d) {
-  // one half-warp per (token row, head); lane i takes columns [8i, 8i+8) of
-  // the d (≤ 128) with 16-byte loads
-  const int64_t pid = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 4;
+  // grid (⌈s_pad/64⌉, heads, b): a half-warp per token row, the rows
+  // q0 + 16j (j < 4) of one head; lane i takes columns [8i, 8i+8) of the
+  // d (≤ 128) with 16-byte loads, all four rows' loads issued before any is used
+  using T = typename Storage<DT>::T;
+  constexpr int R = 4;
+  const int head = blockIdx.y, bi = blockIdx.z;
   const int sub = threadIdx.x & 15;
-  const int64_t total = static_cast<int64_t>(s_pad) * b * heads;
-  if (pid >= total) return;  // whole half-warps leave together (total pairs fill them)
-  const int head = static_cast<int>(pid % heads);
-  const int64_t rest = pid / heads;
-  const int bi = static_cast<int>(rest % b);
-  const int q = static_cast<int>(rest / b);
-  float acc = 0.0f;
-  if (q < s && sub * 8 < d) {
-    using T = typename Storage<DT>::T;
-    const int64_t off = (static_cast<int64_t>(q) * b + bi) * h + static_cast<int64_t>(head) * d + sub * 8;
-    float a[8], c[8];
-    unpack8<DT>(ldg_nc_v4(static_cast<const T*>(dout) + off), a);
-    unpack8<DT>(ldg_nc_v4(static_cast<const T*>(o) + off), c);
+  const int q0 = blockIdx.x * 16 * R + (threadIdx.x >> 4);
+  uint4 av[R], cv[R];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc += a[i] * c[i];
+  for (int j = 0; j < R; ++j) {
+    const int q = q0 + 16 * j;
+    if (q < s && sub * 8 < d) {
+      const int64_t off = (static_cast<int64_t>(q) * b + bi) * h + static_cast<int64_t>(head) * d + sub * 8;
+      av[j] = ldg_nc_v4(static_cast<const T*>(dout) + off);
+      cv[j] = ldg_nc_v4(static_cast<const T*>(o) + off);
+    } else {
+      av[j] = cv[j] = make_uint4(0u, 0u, 0u, 0u);
+    }
   }
   const unsigned mask = (threadIdx.x & 16) ? 0xffff0000u : 0x0000ffffu;
+  const int64_t row0 = (static_cast<int64_t>(bi) * heads + head) * s_pad;
 #pragma unroll
-  for (int off = 8; off > 0; off >>= 1) acc += __shfl_xor_sync(mask, acc, off);
-  if (sub == 0) {
-    const int64_t i = (static_cast<int64_t>(bi) * heads + head) * s_pad + q;
-    delta[i] = acc;
-    nlse[i] = -lse[i];  // the dK/dV kernel's exponent argument is S·c + (−lse2)
+  for (int j = 0; j < R; ++j) {
+    float a[8], c[8], acc = 0.0f;
+    unpack8<DT>(av[j], a);
+    unpack8<DT>(cv[j], c);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc += a[i] * c[i];
+#pragma unroll
+    for (int off = 8; off > 0; off >>= 1) acc += __shfl_xor_sync(mask, acc, off);
+    const int q = q0 + 16 * j;
+    if (sub == 0 && q < s_pad) {
+      delta[row0 + q] = acc;
+      nlse[row0 + q] = -lse[row0 + q];  // the dK/dV kernel's exponent argument is S·c + (−lse2)
+    }
   }
 }
 
@@ -1704,8 +1713,7 @@ int bwd_kernels_launch(const Shape& k, const AttnParams& p, const void* dout, co
   const void* fq = reinterpret_cast<const void*>(attn_bwd_dq_kernel<DT, HDIM>);
   int rc;
   if ((rc = set_smem(fkv, KV_SMEM)) || (rc = set_smem(fq, DQ_SMEM))) return rc;
-  const int64_t row_heads = k.s_pad * k.b * k.heads;  // (row, query head) pairs, a half-warp each
-  const unsigned gd = static_cast<unsigned>((row_heads * 16 + 255) / 256);
+  const dim3 gd(static_cast<unsigned>((k.s_pad + 63) / 64), static_cast<unsigned>(k.heads), static_cast<unsigned>(k.b));
   attn_bwd_delta_kernel<DT><<<gd, 256, 0, st>>>(dout, o, lse, delta, nlse, p.s, p.b, p.h, p.heads, p.s_pad, p.d);
   const dim3 gkv(static_cast<unsigned>(k.s_pad / 128), static_cast<unsigned>(k.kv_heads * p.kv_split),
                  static_cast<unsigned>(k.b));
