@@ -479,9 +479,9 @@ constexpr uint32_t F_TILE = 128 * 128 * 2;  // 32 KB
 constexpr uint32_t F_QA = 0, F_QB = F_TILE, F_K0 = 2 * F_TILE, F_V0 = 4 * F_TILE;
 constexpr uint32_t F_END = 6 * F_TILE;
 constexpr size_t F_SMEM = 1024 + F_END + sizeof(Tail);
-// barriers: Q; K full/empty [2]; V full/empty [2]; S full, P ready, O done per tile
-enum { FB_Q = 0, FB_KF = 1, FB_KE = 3, FB_VF = 5, FB_VE = 7, FB_SF = 9, FB_P = 11, FB_O = 13, FB_DRAIN = 15,
-       FB_COUNT = 16 };
+// barriers: Q; K+V full [2] (both tensors of a stage land on one barrier); K
+// empty, V empty [2]; S full, P ready, O done per tile
+enum { FB_Q = 0, FB_KVF = 1, FB_KE = 3, FB_VE = 5, FB_SF = 7, FB_P = 9, FB_O = 11, FB_DRAIN = 13, FB_COUNT = 14 };
 static_assert(FB_COUNT <= 24, "barrier slots");
 
 // 32 columns of this warp's lane quarter into registers, without waiting.
@@ -554,9 +554,8 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_fwd_kernel(const __grid_c
   if (threadIdx.x == 0) {
     mbar_init(bar(FB_Q), 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(FB_KF + i), 1);
+      mbar_init(bar(FB_KVF + i), 1);
       mbar_init(bar(FB_KE + i), 1);
-      mbar_init(bar(FB_VF + i), 1);
       mbar_init(bar(FB_VE + i), 1);
       mbar_init(bar(FB_SF + i), 1);
       mbar_init(bar(FB_P + i), PAIR ? 8 : 128);  // pair: one arrival per softmax warp of both CTAs
@@ -610,18 +609,20 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_fwd_kernel(const __grid_c
       for (int n = 0; ok && n < NB; ++n) {
         const int st = n & 1;
         const uint32_t par = ((n >> 1) & 1) ^ 1u;
+        // K(n) and V(n) complete on one barrier, so the issuing lane waits once per
+        // key tile (each wait on that lane idles the tensor pipe); each is loaded
+        // as soon as its own buffer is free (K after both tiles' S, V after both P·V)
         if (!(ok = mbar_wait_bounded(bar(FB_KE + st), par, abort_flag, p.status, p.timeout_ns))) break;
-        if (leader) mbar_arrive_expect_tx(bar(FB_KF + st), (PAIR ? 2 : 1) * KV_TX);
+        if (leader) mbar_arrive_expect_tx(bar(FB_KVF + st), (PAIR ? 2 : 1) * 2 * KV_TX);
         if constexpr (PAIR)  // keys [64·rank, 64·rank + 64) of the tile, all 128 columns
-          load_tile_pair(sK0 + st * F_TILE, &p.qkv64, lead_bar(FB_KF + st), colk, bi, n * F_BK + 64 * rank, 64);
+          load_tile_pair(sK0 + st * F_TILE, &p.qkv64, lead_bar(FB_KVF + st), colk, bi, n * F_BK + 64 * rank, 64);
         else
-          load_tile(sK0 + st * F_TILE, &p.qkv128, bar(FB_KF + st), colk, bi, n * F_BK, 128);
+          load_tile(sK0 + st * F_TILE, &p.qkv128, bar(FB_KVF + st), colk, bi, n * F_BK, 128);
         if (!(ok = mbar_wait_bounded(bar(FB_VE + st), par, abort_flag, p.status, p.timeout_ns))) break;
-        if (leader) mbar_arrive_expect_tx(bar(FB_VF + st), (PAIR ? 2 : 1) * KV_TX);
         if constexpr (PAIR)  // columns [64·rank, 64·rank + 64) of the head, all 128 keys
-          tma_load_3d_pair(sV0 + st * F_TILE, &p.qkv128, lead_bar(FB_VF + st), colv + 64 * rank, bi, n * F_BK);
+          tma_load_3d_pair(sV0 + st * F_TILE, &p.qkv128, lead_bar(FB_KVF + st), colv + 64 * rank, bi, n * F_BK);
         else
-          load_tile(sV0 + st * F_TILE, &p.qkv128, bar(FB_VF + st), colv, bi, n * F_BK, 128);
+          load_tile(sV0 + st * F_TILE, &p.qkv128, bar(FB_KVF + st), colv, bi, n * F_BK, 128);
         issued = static_cast<uint32_t>(n + 1);
       }
       if (!ok) {
@@ -630,10 +631,8 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_fwd_kernel(const __grid_c
         // odd CTA waits a fixed time instead
         if (leader) {
           (void)mbar_wait_bounded(bar(FB_Q), 0u, nullptr, nullptr, p.timeout_ns);
-          for (uint32_t n = issued > 2 ? issued - 2 : 0; n < issued; ++n) {
-            (void)mbar_wait_bounded(bar(FB_KF + (n & 1)), (n >> 1) & 1u, nullptr, nullptr, p.timeout_ns);
-            (void)mbar_wait_bounded(bar(FB_VF + (n & 1)), (n >> 1) & 1u, nullptr, nullptr, p.timeout_ns);
-          }
+          for (uint32_t n = issued > 2 ? issued - 2 : 0; n < issued; ++n)
+            (void)mbar_wait_bounded(bar(FB_KVF + (n & 1)), (n >> 1) & 1u, nullptr, nullptr, p.timeout_ns);
         } else {
           const uint64_t t0 = globaltimer_ns();
           while (globaltimer_ns() - t0 < 2000000ull) __nanosleep(1000);
@@ -653,7 +652,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_fwd_kernel(const __grid_c
       const uint64_t dK0 = sdesc_k(sK0), dK1 = sdesc_k(sK0 + F_TILE);
       const uint64_t dV0 = sdesc_mn(sV0, 128), dV1 = sdesc_mn(sV0 + F_TILE, 128);
       auto wait_k = [&](int n) {
-        return mbar_wait_bounded(bar(FB_KF + (n & 1)), (n >> 1) & 1u, abort_flag, p.status, p.timeout_ns);
+        return mbar_wait_bounded(bar(FB_KVF + (n & 1)), (n >> 1) & 1u, abort_flag, p.status, p.timeout_ns);
       };
       auto issue_s = [&](int t, int n) {  // S_t = Q_t·K(n)ᵀ
         uint64_t a[8], b[8];
@@ -678,11 +677,9 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_fwd_kernel(const __grid_c
       }
       for (int n = 0; ok && n < NB; ++n) {
         const int st = n & 1;
-        bool v_ready = false, k_ready = false;
+        bool k_ready = false;  // K(n + 1) and V(n + 1) landed (V(n) did with K(n))
         if (n < NA) {
           if (!(ok = mbar_wait_bounded(bar(FB_P + 0), n & 1, abort_flag, p.status, p.timeout_ns))) break;
-          if (!(ok = mbar_wait_bounded(bar(FB_VF + st), (n >> 1) & 1u, abort_flag, p.status, p.timeout_ns))) break;
-          v_ready = true;
           tc_fence_after();
           issue_pv(0, n);
           if (n + 1 < NA) {
@@ -695,9 +692,6 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_fwd_kernel(const __grid_c
           }
         }
         if (!(ok = mbar_wait_bounded(bar(FB_P + 1), n & 1, abort_flag, p.status, p.timeout_ns))) break;
-        if (!v_ready &&
-            !(ok = mbar_wait_bounded(bar(FB_VF + st), (n >> 1) & 1u, abort_flag, p.status, p.timeout_ns)))
-          break;
         tc_fence_after();
         issue_pv(1, n);
         commit_all(FB_VE + st);  // V(n) is free once both tiles' P·V have run
