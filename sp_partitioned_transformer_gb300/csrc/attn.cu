@@ -8,34 +8,43 @@
 // 道理是一样的").
 //
 // The projections run on the tcgen05 GEMM (gemm_tc.cu).  The attention core is
-// three tcgen05 kernels (head width 128, 16-bit storage, float32 accumulation in
-// tensor memory) and a small Δ kernel.  Each tcgen05 CTA has 12 warps: warp 0
-// issues TMA loads, warp 1 issues the MMAs, warp 2 owns the tensor-memory
-// allocation and warps 4–11 are two groups of four element-wise warps, one
-// thread per row of a 128-row tile (in the forward each group owns one of the
-// CTA's two query tiles; in dK/dV the groups split a tile's columns).
+// three tcgen05 kernels (head width 128 or 96, 16-bit storage, float32
+// accumulation in tensor memory), a small Δ kernel and, for grouped-query
+// attention, a fixed-order reduce of the per-query-head dK, dV partials.  The
+// forward and dK/dV CTAs have 12 warps: warp 0 issues TMA loads, warp 1 issues
+// the MMAs, warp 2 owns the tensor-memory allocation and warps 4–11 are two
+// groups of four element-wise warps, one thread per row of a 128-row tile (in
+// the forward each group owns one of the CTA's two query tiles; in dK/dV the
+// groups split a tile's columns).
 //
 //   attn_fwd_kernel   per (pair of 128-query tiles A and B, head, sequence):
-//                     K and V tiles stream through 2-deep TMA rings; the issuing
-//                     lane alternates S_A = Q_A·Kᵀ, P_B·V, S_B = Q_B·Kᵀ, P_A·V,
-//                     so one element-wise group's softmax (base 2, streaming)
-//                     overlaps the other tile's MMAs; P is written back into
-//                     TMEM over its own S columns and is the A operand of
-//                     O += P·V from there; O is rescaled in TMEM only when a
-//                     tile's probabilities would pass 2^15 against the running
+//                     K and V tiles stream through a 2-stage TMA ring (K and V
+//                     of a stage complete on one barrier: the issuing lane
+//                     waits once per key tile); the issuing lane alternates
+//                     S_A = Q_A·Kᵀ, P_B·V, S_B = Q_B·Kᵀ, P_A·V, so one
+//                     element-wise group's softmax (base 2, streaming) overlaps
+//                     the other tile's MMAs; P is written back into TMEM over
+//                     its own S columns and is the A operand of O += P·V from
+//                     there; O is rescaled in TMEM only when a tile's
+//                     probabilities would pass 2^15 against the running
 //                     reference maximum; O and the row log-sum-exp (lse2) are
 //                     written at the end.  With head width 128 the same
 //                     kernel can run as CTA pairs (2-SM MMAs, each SM loading
 //                     half of every K and V tile; TPMLP_ATTN_FWD_PAIR=1): correct,
 //                     but slower than one CTA per pair of tiles, so not the default.
-//   attn_bwd_dkdv_kernel  per (128-key tile, head, sequence), over 64-query tiles:
-//                     Sᵀ = K·Qᵀ and dPᵀ = V·dOᵀ, Pᵀ = 2^(Sᵀ·c − lse2),
-//                     dSᵀ = Pᵀ ⊙ (dPᵀ − Δ), dV += Pᵀ·dO, dK += dSᵀ·Q; each
-//                     16-bit dSᵀ tile is also bulk-stored to HBM.
-//   attn_bwd_dq_kernel    per (128-query tile, head, sequence), over 128-key
-//                     tiles: dQ += dS·K from the stored dSᵀ tiles (a streaming
-//                     contraction; S and dP are not recomputed).
-//   attn_bwd_delta_kernel Δ = rowsum(dO ⊙ O) per query row and head.
+//   attn_bwd_dkdv_kernel  per (128-key tile, query head or chunk of a group's
+//                     query heads, sequence), over 64-query tiles, K and V in
+//                     tensor memory as the A operands: Sᵀ = K·Qᵀ and
+//                     dPᵀ = V·dOᵀ, Pᵀ = 2^(Sᵀ·c − lse2), dSᵀ = Pᵀ ⊙ (dPᵀ − Δ),
+//                     dV += Pᵀ·dO, dK += dSᵀ·Q; each 16-bit dSᵀ tile is also
+//                     bulk-stored to HBM.
+//   attn_dkv_reduce_kernel  (grouped-query attention) adds the float32 dK, dV
+//                     partials of a group's query-head chunks in chunk order.
+//   attn_bwd_dq_kernel    per (128-query tile, head, sequence), two CTAs per
+//                     SM, over the keys it sees 64 at a time: dQ += dS·K from
+//                     the stored dSᵀ tiles (a streaming contraction; S and dP
+//                     are not recomputed).
+//   attn_bwd_delta_kernel Δ = rowsum(dO ⊙ O) per query row and head, and −lse2.
 // No atomics anywhere: every output element is written by one CTA, so results
 // are the same bits on every run.
 #include <algorithm>
