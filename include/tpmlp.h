@@ -374,7 +374,12 @@ int tpmlp_wait_timeout_selftest(uint64_t timeout_ns, void* stream);
  * Environment: TPMLP_ATTN_FWD_PAIR=1 (read at every forward call) runs the
  * forward's core for head width 128 as CTA pairs (2-SM MMAs, 512 query rows a
  * pair) instead of one CTA per 256 query rows; same results within rounding,
- * measured slower, off by default.
+ * measured slower, off by default.  With grouped-query attention the backward
+ * splits each group's query heads over kv_split CTAs per key tile (the
+ * smallest divisor of heads/kv_heads giving six waves of CTAs on the device)
+ * and adds their float32 dK, dV partials in chunk order; TPMLP_ATTN_KV_SPLIT=n
+ * (read at every backward call) sets the split when n divides heads/kv_heads.
+ * tpmlp_attn_workspace_size covers the largest split.
  * ------------------------------------------------------------------------- */
 size_t tpmlp_attn_workspace_size(int64_t s, int64_t b, int64_t h, int heads, int kv_heads, int tp, int sp,
                                  int dtype, int causal);

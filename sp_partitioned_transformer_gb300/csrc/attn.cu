@@ -1570,12 +1570,29 @@ int64_t ds_head_tiles(const Shape& k) {
   return ds_tile_index(nkt, nqt64, k.causal);
 }
 
-// dK/dV CTAs per (key tile, group): with grouped-query attention one per query
-// head of the group (a whole group in one CTA would leave the causal mask's
-// first key tiles with r times the work of the others; with eight query heads a
-// group that made the backward 45% slower than multi-head attention), their
-// float32 partials added by attn_dkv_reduce_kernel.
-int kv_split_of(const Shape& k) { return k.heads / k.kv_heads; }
+// dK/dV CTAs per (key tile, group) with grouped-query attention: the group's
+// query heads in kv_split chunks, one chunk a CTA (its heads one after the
+// other), the chunks' float32 partials added by attn_dkv_reduce_kernel.  Too
+// few CTAs leave SMs idle behind the causal mask's long first key tiles (a
+// whole group of eight heads per CTA made the backward 45% slower than
+// multi-head attention); one head per CTA doubles the partial traffic and the
+// CTAs' fixed cost.  The split is the smallest divisor of the group size that
+// gives at least six waves of CTAs — at the Llama-70B width (8 heads a group, 32
+// key tiles, 8 groups) splits 8, 4 and 2 measured dK/dV 626, 595 and 635 µs
+// with the reduce 45, 25 and 14 µs.
+// TPMLP_ATTN_KV_SPLIT=n in the environment (read at every backward call) sets
+// the split when n divides the group size.
+int kv_split_of(const Shape& k, int num_sms) {
+  const int qpg = k.heads / k.kv_heads;
+  if (const char* e = std::getenv("TPMLP_ATTN_KV_SPLIT")) {
+    const int n = std::atoi(e);
+    if (n >= 1 && n <= qpg && qpg % n == 0) return n;
+  }
+  const int64_t per_split = (k.s_pad / 128) * k.kv_heads * k.b;  // CTAs of one chunk per group
+  for (int d = 1; d < qpg; ++d)
+    if (qpg % d == 0 && per_split * d >= 6LL * num_sms) return d;
+  return qpg;
+}
 
 // workspace: [X gathered | dZ gathered] when SP chunks are not read in place
 // (all the forward needs), then Δ and −lse2, then the dSᵀ tiles, then (grouped-
@@ -1598,8 +1615,9 @@ Ws ws_layout(const Shape& k) {
   w.ds_off = off;
   off += static_cast<size_t>(k.b) * k.heads * ds_head_tiles(k) * DS_TILE;
   w.dkv_off = off;
-  if (kv_split_of(k) > 1)
-    off += static_cast<size_t>(kv_split_of(k)) * k.M * k.kv_heads * 2 * k.d * sizeof(float);
+  // room for the largest split (one chunk a query head); the launch may use fewer
+  const int qpg = k.heads / k.kv_heads;
+  if (qpg > 1) off += static_cast<size_t>(qpg) * k.M * k.kv_heads * 2 * k.d * sizeof(float);
   w.total = off;
   return w;
 }
@@ -1645,7 +1663,7 @@ int base_params(const Shape& k, AttnParams* p) {
   p->qpg = k.heads / k.kv_heads;
   p->d = k.d;
   p->ldqkv = k.qkv_w;
-  p->kv_split = kv_split_of(k);
+  p->kv_split = kv_split_of(k, dev->num_sms);
   p->qpc = p->qpg / p->kv_split;
   p->s_pad = static_cast<int>(k.s_pad);
   p->causal = k.causal;

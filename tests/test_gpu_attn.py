@@ -86,6 +86,32 @@ def test_attention_block_matches_the_oracle(cuda_lib, cfg):
     assert np.abs(lse - ref["lse2"]).max() <= 2e-2 * max(1.0, np.abs(ref["lse2"]).max())
 
 
+SPLIT_CASES = [c for c in CASES if c.name in ("gqa-4-per-group-gathered", "d96-gqa-multi-tile")]
+
+
+@pytest.mark.parametrize("split", ["1", "2"])
+@pytest.mark.parametrize("cfg", SPLIT_CASES, ids=[c.name for c in SPLIT_CASES])
+def test_grouped_query_split_of_the_key_value_gradients(cuda_lib, cfg, split, monkeypatch):
+    """The dK/dV kernel with a group's 4 query heads split over 1 or 2 CTAs per
+    key tile (each CTA running its heads one after the other; with 2, float32
+    partials added by the reduce kernel) instead of one head per CTA: the
+    backward against the oracle (the large-shape split is chosen by the CTA
+    count, so small shapes take one head per CTA unless told otherwise)."""
+    tpmlp = cuda_lib
+    monkeypatch.setenv("TPMLP_ATTN_KV_SPLIT", split)
+    t, blk, fw, bw, cat = _run(tpmlp, cfg)
+    M, s, b, heads = cfg.M, cfg.s, cfg.b, cfg.heads
+    X, Wqkv, Wo, dZ = (to_np(t[k]).reshape(-1, t[k].shape[-1]) for k in ("X", "Wqkv", "Wo", "dZ"))
+    g = O.attn_backward(X, Wqkv, Wo, dZ, s, b, heads, cfg.causal, cfg.groups)
+    errs = {
+        "dQKV": rel_err(to_np(bw["dqkv"]), g["dQKV"]),
+        "dX": rel_err(_flat(to_np(cat(bw["dx"])), M), g["dX"]),
+        "dWqkv": rel_err(to_np(bw["dwqkv"]), g["dWqkv"]),
+    }
+    bad = {k: e for k, e in errs.items() if not e <= TOL}
+    assert not bad, bad
+
+
 CORE_CASES = [
     AttnConfig("core", 384, 2, 512, 4, 2, True, "bf16", True),
     AttnConfig("core-gqa", 384, 2, 1024, 8, 2, True, "bf16", True, kv_heads=2),
