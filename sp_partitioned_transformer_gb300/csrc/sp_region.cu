@@ -8,8 +8,8 @@
 // The LayerNorm's outputs are the chunks the block's fc1 reads in place (the
 // all-gather fused into its loads), so no gathered copy of the activation is
 // ever made.  Everything here is token-wise and HBM-bound:
-//   ln_fwd_pair_kernel    16-bit rows of 2k < h/8 ≤ 6k vectors (h up to 6144):
-//                         two warps per row sharing one TMA-filled slot, each
+//   ln_fwd_pair_kernel    16-bit rows of an even number of vectors, 2k < h/8 ≤ 8k
+//                         (h up to 8192): two warps per row sharing one TMA-filled slot, each
 //                         holding half the row in registers, their shifted sums
 //                         combined through shared memory;
 //   ln_fwd_warp_kernel    other 16-bit rows up to h = 8192: one warp per row, each
@@ -506,10 +506,11 @@ __global__ void __launch_bounds__(32 * LnFwdShape<NV>::MAX_WARPS, 1)
 // have copied the row out by then).  With half the registers a warp, a CTA
 // holds 24 warps where the one-warp-per-row kernel holds 16, for 12 rows in
 // flight: 18.2 against 20.5 µs at h = 6144 (4096 rows), the extra warps hiding
-// the arithmetic's latency.
+// the arithmetic's latency; at h = 8192, 16 warps (8 rows) where the one-warp
+// form holds 8: 27.9 against 28.9 µs back to back.
 template <int NVH>
 struct LnPairShape {
-  static constexpr int MAX_PAIRS = 12;  // 24 warps, ≤ 85 registers a thread
+  static constexpr int MAX_PAIRS = NVH <= 12 ? 12 : 8;  // 24 warps at ≤ 85 registers, or 16 at ≤ 128
 };
 
 template <int DT, int NVH>
@@ -706,6 +707,8 @@ bool ln_fwd_registers(const ChunkSet& cs, const void* gamma, const void* beta, f
   }
   if (per_lane <= 16) return ln_fwd_warp_nv<DT, 16>(cs, gamma, beta, eps, mean, rstd, M, h, rpc, st);
   if (per_lane <= 24) return ln_fwd_warp_nv<DT, 24>(cs, gamma, beta, eps, mean, rstd, M, h, rpc, st);
+  if ((h / 8) % 2 == 0 && (h / 16 + 31) / 32 <= 16)
+    return ln_fwd_pair_nv<DT, 16>(cs, gamma, beta, eps, mean, rstd, M, h, rpc, st);
   if (per_lane <= REG_MAX_NV) return ln_fwd_warp_nv<DT, 32>(cs, gamma, beta, eps, mean, rstd, M, h, rpc, st);
   return false;
 }
