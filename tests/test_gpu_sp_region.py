@@ -23,9 +23,12 @@ def _flat(t):
 # Shapes: warp-per-row kernels (h < 1024, or rows not a whole number of
 # 8-element vectors) and the streamed kernels (h >= 1024) with 1..4 vectors per
 # thread, a ragged last vector column (h = 2056: 257 vectors), fewer rows than
-# CTAs, and the widest ring (h = 8192).
+# CTAs, and the widest ring (h = 8192); the 16-bit forward's two-warps-per-row
+# kernel with 8, 10 (predicated), 12 and 16 vectors a lane (h = 4096, 5120,
+# 6144, 8192).
 LN_SHAPES = [(64, 2, 136, 2), (9, 1, 5, 3), (512, 4, 1024, 4), (16, 2, 64, 1), (24, 1, 64, 2),
-             (40, 2, 2056, 4), (48, 1, 6144, 2), (9, 1, 1032, 3), (24, 1, 8192, 3), (6, 1, 1030, 3)]
+             (40, 2, 2056, 4), (48, 1, 6144, 2), (9, 1, 1032, 3), (24, 1, 8192, 3), (6, 1, 1030, 3),
+             (32, 2, 4096, 2), (24, 1, 5120, 4)]
 
 
 @pytest.mark.parametrize("dt", ["f32", "bf16", "f16"])
